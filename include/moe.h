@@ -1,0 +1,207 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts layer library
+ * (libmoe.so): forward and backward of one MoE expert layer on one GPU.
+ *
+ * The layer (per dispatch chunk of T tokens, model width d, expert FFN width
+ * f, E experts, k experts per token):
+ *
+ *   A1  L      = x Wg^T + beta                     router logits      [T,E]
+ *   A2  idx, w = softmax top-k gate of L                             [T,k]
+ *   A3  counts, offsets, pos, perm                 stable dispatch by expert
+ *   A4  X_perm[pos[t,j]] = x[t]                    permute            [T*k,d]
+ *   A5  per expert e over its segment of X_perm:
+ *         H = X W1[e]^T + b1[e],  A = GELU(H),  Y_perm = A W2[e]^T + b2[e]
+ *   A6  y[t] = sum_j w[t,j] Y_perm[pos[t,j]]       combine            [T,d]
+ *   and the backward of each step (A7 combine, A8 expert FFN, A9 permute,
+ *   A10 router).
+ *
+ * Sources for the method: the gating network's output decides each token's
+ * experts, tokens are permuted and then assigned to their target experts in
+ * order, and the experts run one after another over only their own tokens,
+ * with no dispatch mask and no zero padding ("ES-MoE: Scaling Beyond the GPU
+ * Memory Limit for Large Mixture-of-Experts Model Training", review, section
+ * 3 "expert-wise offloading and processing" and "dynamic expert placement",
+ * section 4 table row "sequential processing"); a dedicated FFN with a
+ * per-expert linear over a scatter/gather layout that batches inputs by expert
+ * ("FastMoE: A Fast Mixture-of-Expert Training System", review, "proposed
+ * method"); dispatch in chunks with a cap on tokens per chunk ("Flattening
+ * Every Memory Peak in Long-Context Mixture-of-Experts Training", abstract,
+ * PipelinedLLEP).  The pages give no gate formula, GELU variant, tie rule or
+ * precision; this library takes: softmax over all E logits, the k largest
+ * logits (equal logits -> lower expert index; slot j = 0 is the largest),
+ * w = softmax probability (k = 1 or renorm = 0) or the k probabilities divided
+ * by their sum (renorm = 1); GELU(x) = x * Phi(x) (erf form).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Every pointer is a DEVICE pointer (cudaMalloc / torch CUDA memory) on the
+ *    current device, 16-byte aligned, row-major and densely packed, unless
+ *    stated otherwise.  Shapes come from `moe_shape`.
+ *  - Ownership: the caller allocates and frees every buffer, including the
+ *    workspace (size from moe_workspace_size).  The library never allocates,
+ *    frees or synchronises, and keeps no state between calls other than
+ *    cached device attributes.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  Calls on one stream run in order; the same
+ *    workspace must not be used by calls that may overlap.
+ *  - Return value: MOE_OK, or MOE_ERR_INVALID / MOE_ERR_UNSUPPORTED for bad
+ *    arguments (nothing is launched), or MOE_ERR_CUDA when a launch fails.
+ *    Errors that happen on the device after launch (a bounded wait that ran
+ *    out, non-finite logits) are written to `*dev_status` (an int32 in device
+ *    memory that the caller zeroes and reads after synchronising); the first
+ *    error wins.  Kernels never trap and every device-side wait is bounded
+ *    (default 1 s, environment variable MOE_WAIT_TIMEOUT_NS overrides).
+ *  - dtype MOE_BF16: x, weights, biases and activations are bf16, arithmetic
+ *    accumulates in fp32; the expert GEMMs run on the tcgen05 tensor cores and
+ *    need d % 64 == 0 and f % 64 == 0.  dtype MOE_F32: everything fp32 with
+ *    fp32 arithmetic on CUDA cores (no TF32).  Logits, gate weights, dw and
+ *    every weight / bias gradient are fp32 in both.
+ *  - Limits: T * k < 2^31, 1 <= k <= min(E, 16), 1 <= E <= 256.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__) || defined(__clang__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID = 1,     /* bad argument: null / misaligned pointer, bad size */
+    MOE_ERR_UNSUPPORTED = 2, /* valid but unsupported shape or dtype */
+    MOE_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
+    MOE_ERR_TIMEOUT = 4,     /* device: a bounded wait ran out */
+    MOE_ERR_NONFINITE = 5    /* device: a router logit was NaN or infinite */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef struct {
+    int64_t T;      /* tokens in this call (one dispatch chunk), >= 0 */
+    int32_t d;      /* model width */
+    int32_t f;      /* expert FFN hidden width */
+    int32_t E;      /* number of experts */
+    int32_t k;      /* experts per token */
+    int32_t dtype;  /* moe_dtype of x, weights, biases and activations */
+    int32_t renorm; /* 1: divide the k gate probabilities by their sum */
+} moe_shape;
+
+/* Human-readable name of a status code (static string, never NULL). */
+MOE_API const char* moe_status_string(moe_status s);
+
+/* Bytes of device workspace that every entry point below may use for a call
+ * with this shape (the maximum over all of them; 0 on invalid shape).  The
+ * workspace holds transient data only (per-block histograms, dH of the expert
+ * backward, router-gradient partial sums); its contents need no
+ * initialisation and are garbage after the call. */
+MOE_API size_t moe_workspace_size(const moe_shape* s);
+
+/* A1 + A2 + A3: router logits, softmax top-k gate and stable dispatch.
+ *   x       [T,d] dtype            tokens
+ *   Wg      [E,d] dtype            router weight
+ *   logit_bias [E] fp32 or NULL    fixed per-expert additive logit shift
+ *   logits  [T,E] fp32             written when compute_logits != 0 (then
+ *                                  x and Wg are read); READ as the given
+ *                                  logits when compute_logits == 0 (then x,
+ *                                  Wg and logit_bias are ignored and may be
+ *                                  NULL)
+ *   idx     [T,k] int32  out       selected experts, slot 0 = largest logit,
+ *                                  equal logits -> lower expert index
+ *   w       [T,k] fp32   out       gate weights
+ *   counts  [E]   int32  out       tokens routed to each expert
+ *   offsets [E+1] int32  out       exclusive prefix sum of counts; offsets[E] = T*k
+ *   pos     [T,k] int32  out       row of slot (t,j) in the expert-sorted order:
+ *                                  offsets[e] + number of tokens t' < t routed to e
+ *   perm    [T*k] int32  out       inverse of pos: perm[pos[t*k+j]] = t*k+j
+ *   ws      workspace, dev_status  see above (MOE_ERR_NONFINITE on NaN/Inf
+ *                                  logits; the outputs then stay in range but
+ *                                  are otherwise unspecified)
+ * Deterministic: identical logits give bit-identical idx, counts, offsets,
+ * pos and perm. */
+MOE_API moe_status moe_route(const moe_shape* s, const void* x, const void* Wg,
+                     const float* logit_bias, float* logits, int compute_logits,
+                     int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
+                     int32_t* pos, int32_t* perm, void* ws, int32_t* dev_status,
+                     moe_stream_t stream);
+
+/* A4: X_perm[pos[t*k+j]] = x[t].   x [T,d], X_perm [T*k,d], dtype. */
+MOE_API moe_status moe_permute(const moe_shape* s, const void* x, const int32_t* pos,
+                       void* x_perm, moe_stream_t stream);
+
+/* A5: expert FFN forward over the contiguous expert segments
+ * [offsets[e], offsets[e+1]) of X_perm (offsets as produced by moe_route).
+ *   W1 [E,f,d], b1 [E,f] (or NULL = 0), W2 [E,d,f], b2 [E,d] (or NULL), dtype
+ *   H  [T*k,f] out  pre-activation (kept for the backward)
+ *   A  [T*k,f] out  GELU(H), computed from the unrounded pre-activation
+ *   y_perm [T*k,d] out
+ * Experts with no tokens read no weights. */
+MOE_API moe_status moe_expert_ffn_fwd(const moe_shape* s, const void* x_perm,
+                              const int32_t* offsets, const void* W1, const void* b1,
+                              const void* W2, const void* b2, void* H, void* A,
+                              void* y_perm, void* ws, int32_t* dev_status,
+                              moe_stream_t stream);
+
+/* A6 (w != NULL): y[t] = sum_j w[t,j] * y_perm[pos[t,j]], j ascending, fp32
+ * accumulation.  A9 (w == NULL): the permute backward, y[t] = sum_j
+ * y_perm[pos[t,j]].   y_perm [T*k,d], y [T,d], dtype. */
+MOE_API moe_status moe_combine_fwd(const moe_shape* s, const void* y_perm, const int32_t* pos,
+                           const float* w, void* y, moe_stream_t stream);
+
+/* A7: combine backward.
+ *   dy_perm[pos[t,j]] = w[t,j] * dy[t]            [T*k,d] dtype out
+ *   dw[t,j]           = <dy[t], y_perm[pos[t,j]]> [T,k]   fp32  out */
+MOE_API moe_status moe_combine_bwd(const moe_shape* s, const void* dy, const void* y_perm,
+                           const int32_t* pos, const float* w, void* dy_perm, float* dw,
+                           moe_stream_t stream);
+
+/* A8: expert FFN backward over the same segments.
+ *   dA = dY W2[e];  dH = dA * GELU'(H);  dx_perm = dH W1[e]
+ *   dW2[e] (+)= dY^T A,  db2[e] (+)= sum_rows dY
+ *   dW1[e] (+)= dH^T X,  db1[e] (+)= sum_rows dH
+ * dy_perm, x_perm [T*k,d], H, A [T*k,f] dtype; dx_perm [T*k,d] dtype out;
+ * dW1 [E,f,d], db1 [E,f], dW2 [E,d,f], db2 [E,d] fp32.  accumulate == 0
+ * overwrites the weight/bias gradients (experts with no tokens get zeros);
+ * accumulate != 0 adds to them (used across dispatch chunks).  The row sums
+ * are taken in a fixed order: results are deterministic. */
+MOE_API moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const void* x_perm,
+                              const void* H, const void* A, const int32_t* offsets,
+                              const void* W1, const void* W2, void* dx_perm, float* dW1,
+                              float* db1, float* dW2, float* db2, int accumulate, void* ws,
+                              int32_t* dev_status, moe_stream_t stream);
+
+/* A10: router backward.  dL = d(gate weights)/d(logits)^T dw:
+ *   renorm: dL[idx_j] = w_j (dw_j - sum_i w_i dw_i), zero elsewhere;
+ *   else:   dL[e] = sum_j dw_j p[idx_j] (delta(e, idx_j) - p[e]), p = softmax(L).
+ *   dx[t]  += sum_e dL[t,e] Wg[e]     (dx [T,d] dtype, read-modify-write)
+ *   dWg    (+)= dL^T x                (dWg [E,d] fp32; accumulate as above)
+ * perm / offsets are the dispatch of this chunk (used to sum each expert's
+ * tokens in a fixed order).  The logit shift has no gradient. */
+MOE_API moe_status moe_route_bwd(const moe_shape* s, const float* dw, const float* logits,
+                         const int32_t* idx, const float* w, const int32_t* perm,
+                         const int32_t* offsets, const void* x, const void* Wg, void* dx,
+                         float* dWg, int accumulate, void* ws, int32_t* dev_status,
+                         moe_stream_t stream);
+
+/* Diagnostics: launch one kernel that waits on a device flag that nothing
+ * sets, with the library's bounded wait (limit_ns nanoseconds), then writes
+ * MOE_ERR_TIMEOUT to *dev_status and returns.  It exercises the timeout path
+ * every pipelined kernel uses, without hanging the GPU. */
+MOE_API moe_status moe_debug_bounded_wait(uint64_t limit_ns, int32_t* dev_status,
+                                  moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,298 @@
+// dispatch.cu -- permute (scatter into expert-sorted rows), weighted combine
+// back to token order, their backward, and per-expert column sums (bias
+// gradients).  Steps A4, A6, A7, A9 of the layer and the bias part of A8.
+//
+// The expert-sorted layout is FastMoE's scatter/gather-by-expert layout
+// ("FastMoE: A Fast Mixture-of-Expert Training System", review, "proposed
+// method"); the permutation stage precedes the per-expert processing in
+// ES-MoE (review, section 3 "expert-wise offloading and processing").
+//
+// All of these are bandwidth-bound row copies / reductions: one warp per
+// token row, 16-byte vector accesses, every row read or written once.  The
+// combine is a gather (no atomics), so results are deterministic.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMaxK = 16;
+
+template <typename T> struct V16;  // 16 bytes of T as fp32 lanes
+template <> struct V16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    static __device__ __forceinline__ void unpack(const uint4& u, float* v) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+        #pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ uint4 pack(const float* v) {
+        uint4 u;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+        #pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        return u;
+    }
+};
+template <> struct V16<float> {
+    static constexpr int N = 4;
+    static __device__ __forceinline__ void unpack(const uint4& u, float* v) {
+        v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+        v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+    }
+    static __device__ __forceinline__ uint4 pack(const float* v) {
+        return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                          __float_as_uint(v[3]));
+    }
+};
+
+__device__ __forceinline__ uint4 ldg16(const void* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void stg16(void* p, const uint4& v) {
+    *reinterpret_cast<uint4*>(p) = v;
+}
+
+inline unsigned grid_for_rows(int64_t rows) {
+    // 8 warps per block, one row per warp per iteration; enough blocks to
+    // fill every SM several times over, grid-striding beyond that.
+    const int64_t want = (rows + 7) / 8;
+    const int64_t cap = (int64_t)device_sm_count() * 16;
+    return (unsigned)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+// ---- A4: X_perm[pos[t,j]] = x[t] ------------------------------------------------
+// nv = row length in 16-byte vectors.
+__global__ void __launch_bounds__(256) permute_kernel(int64_t T, int nv, int k,
+                                                      const uint4* __restrict__ x,
+                                                      const int32_t* __restrict__ pos,
+                                                      uint4* __restrict__ xp) {
+    const int lane = threadIdx.x & 31;
+    const int64_t wstride = (int64_t)gridDim.x * 8;
+    for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += wstride) {
+        int32_t p[kMaxK];
+        #pragma unroll
+        for (int j = 0; j < kMaxK; ++j) p[j] = (j < k) ? __ldg(pos + t * k + j) : 0;
+        const uint4* src = x + t * nv;
+        int c = lane;
+        for (; c + 96 < nv; c += 128) {
+            const uint4 v0 = ldg16(src + c), v1 = ldg16(src + c + 32), v2 = ldg16(src + c + 64),
+                        v3 = ldg16(src + c + 96);
+            #pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                if (j >= k) break;
+                uint4* dst = xp + (int64_t)p[j] * nv + c;
+                dst[0] = v0; dst[32] = v1; dst[64] = v2; dst[96] = v3;
+            }
+        }
+        for (; c < nv; c += 32) {
+            const uint4 v = ldg16(src + c);
+            #pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                if (j >= k) break;
+                xp[(int64_t)p[j] * nv + c] = v;
+            }
+        }
+    }
+}
+
+// ---- A6 / A9: y[t] = sum_j w[t,j] Y[pos[t,j]] (w == null: weights 1) -------------
+template <typename T>
+__global__ void __launch_bounds__(256) combine_kernel(int64_t Tn, int nv, int k,
+                                                      const uint4* __restrict__ Y,
+                                                      const int32_t* __restrict__ pos,
+                                                      const float* __restrict__ w,
+                                                      uint4* __restrict__ y) {
+    using V = V16<T>;
+    const int lane = threadIdx.x & 31;
+    const int64_t wstride = (int64_t)gridDim.x * 8;
+    for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < Tn; t += wstride) {
+        int32_t p[kMaxK];
+        float wj[kMaxK];
+        #pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            p[j] = (j < k) ? __ldg(pos + t * k + j) : 0;
+            wj[j] = (j < k) ? (w ? __ldg(w + t * k + j) : 1.f) : 0.f;
+        }
+        for (int c = lane; c < nv; c += 32) {
+            float acc[V::N], v[V::N];
+            #pragma unroll
+            for (int u = 0; u < V::N; ++u) acc[u] = 0.f;
+            #pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                if (j >= k) break;
+                V::unpack(ldg16(Y + (int64_t)p[j] * nv + c), v);
+                #pragma unroll
+                for (int u = 0; u < V::N; ++u) acc[u] = fmaf(wj[j], v[u], acc[u]);
+            }
+            stg16(y + t * nv + c, V::pack(acc));
+        }
+    }
+}
+
+// ---- A7: dY[pos[t,j]] = w[t,j] dy[t];  dw[t,j] = <dy[t], Y[pos[t,j]]> -------------
+template <typename T>
+__global__ void __launch_bounds__(256) combine_bwd_kernel(int64_t Tn, int nv, int k,
+                                                          const uint4* __restrict__ dy,
+                                                          const uint4* __restrict__ Y,
+                                                          const int32_t* __restrict__ pos,
+                                                          const float* __restrict__ w,
+                                                          uint4* __restrict__ dY,
+                                                          float* __restrict__ dw) {
+    using V = V16<T>;
+    const int lane = threadIdx.x & 31;
+    const int64_t wstride = (int64_t)gridDim.x * 8;
+    for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < Tn; t += wstride) {
+        int32_t p[kMaxK];
+        float wj[kMaxK], part[kMaxK];
+        #pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            p[j] = (j < k) ? __ldg(pos + t * k + j) : 0;
+            wj[j] = (j < k) ? __ldg(w + t * k + j) : 0.f;
+            part[j] = 0.f;
+        }
+        for (int c = lane; c < nv; c += 32) {
+            float g[V::N], v[V::N], o[V::N];
+            V::unpack(ldg16(dy + t * nv + c), g);
+            #pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                if (j >= k) break;
+                V::unpack(ldg16(Y + (int64_t)p[j] * nv + c), v);
+                #pragma unroll
+                for (int u = 0; u < V::N; ++u) {
+                    part[j] = fmaf(g[u], v[u], part[j]);
+                    o[u] = wj[j] * g[u];
+                }
+                stg16(dY + (int64_t)p[j] * nv + c, V::pack(o));
+            }
+        }
+        #pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j >= k) break;
+            float s = part[j];
+            #pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+            if (lane == 0) dw[t * k + j] = s;
+        }
+    }
+}
+
+// ---- per-expert column sums (bias gradients) -------------------------------------
+// Phase 1: one partial per (expert, chunk of kDwgChunk rows of its segment);
+// phase 2: partials added in chunk order.  Deterministic.
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_partial_kernel(int n, int E,
+                                                             const int32_t* __restrict__ offsets,
+                                                             const T* __restrict__ g,
+                                                             float* __restrict__ partial) {
+    using V = V16<T>;
+    int e = 0, acc = 0, sub = -1;
+    for (; e < E; ++e) {
+        const int cnt = offsets[e + 1] - offsets[e];
+        const int nc = (cnt + kDwgChunk - 1) / kDwgChunk;
+        if ((int)blockIdx.x < acc + nc) { sub = blockIdx.x - acc; break; }
+        acc += nc;
+    }
+    if (sub < 0) return;
+    const int c = (blockIdx.y * 256 + threadIdx.x) * V::N;
+    if (c >= n) return;
+    const int p0 = offsets[e] + sub * kDwgChunk;
+    const int p1 = min(offsets[e + 1], p0 + kDwgChunk);
+    float a[V::N], v[V::N];
+    #pragma unroll
+    for (int u = 0; u < V::N; ++u) a[u] = 0.f;
+    for (int p = p0; p < p1; ++p) {
+        V::unpack(ldg16(g + (int64_t)p * n + c), v);
+        #pragma unroll
+        for (int u = 0; u < V::N; ++u) a[u] += v[u];
+    }
+    float* out = partial + (int64_t)blockIdx.x * n + c;
+    #pragma unroll
+    for (int u = 0; u < V::N; ++u) out[u] = a[u];
+}
+
+__global__ void __launch_bounds__(256) colsum_reduce_kernel(int n, int E,
+                                                            const int32_t* __restrict__ offsets,
+                                                            const float* __restrict__ partial,
+                                                            float* __restrict__ out,
+                                                            int accumulate) {
+    const int e = blockIdx.x;
+    const int c = blockIdx.y * 256 + threadIdx.x;
+    if (c >= n) return;
+    int start = 0;
+    for (int q = 0; q < e; ++q) {
+        const int cnt = offsets[q + 1] - offsets[q];
+        start += (cnt + kDwgChunk - 1) / kDwgChunk;
+    }
+    const int cnt = offsets[e + 1] - offsets[e];
+    const int nc = (cnt + kDwgChunk - 1) / kDwgChunk;
+    float s = 0.f;
+    for (int i = 0; i < nc; ++i) s += partial[(int64_t)(start + i) * n + c];
+    float* o = out + (int64_t)e * n + c;
+    *o = accumulate ? *o + s : s;
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const moe_shape& s, const void* x, const int32_t* pos, void* x_perm,
+                           cudaStream_t st) {
+    const int esz = s.dtype == MOE_BF16 ? 2 : 4;
+    const int nv = s.d * esz / 16;
+    permute_kernel<<<grid_for_rows(s.T), 256, 0, st>>>(s.T, nv, s.k, (const uint4*)x, pos,
+                                                       (uint4*)x_perm);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const moe_shape& s, const void* y_perm, const int32_t* pos,
+                           const float* w, void* y, cudaStream_t st) {
+    const unsigned g = grid_for_rows(s.T);
+    if (s.dtype == MOE_BF16)
+        combine_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(s.T, s.d / 8, s.k, (const uint4*)y_perm,
+                                                          pos, w, (uint4*)y);
+    else
+        combine_kernel<float><<<g, 256, 0, st>>>(s.T, s.d / 4, s.k, (const uint4*)y_perm, pos, w,
+                                                  (uint4*)y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const moe_shape& s, const void* dy, const void* y_perm,
+                               const int32_t* pos, const float* w, void* dy_perm, float* dw,
+                               cudaStream_t st) {
+    const unsigned g = grid_for_rows(s.T);
+    if (s.dtype == MOE_BF16)
+        combine_bwd_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(
+            s.T, s.d / 8, s.k, (const uint4*)dy, (const uint4*)y_perm, pos, w, (uint4*)dy_perm, dw);
+    else
+        combine_bwd_kernel<float><<<g, 256, 0, st>>>(s.T, s.d / 4, s.k, (const uint4*)dy,
+                                                      (const uint4*)y_perm, pos, w,
+                                                      (uint4*)dy_perm, dw);
+    return cudaGetLastError();
+}
+
+size_t segment_colsum_workspace(const moe_shape& s, int n) {
+    return (size_t)((s.T * s.k + kDwgChunk - 1) / kDwgChunk + s.E) * (size_t)n * sizeof(float);
+}
+
+cudaError_t launch_segment_colsum(const moe_shape& s, const void* g, int n,
+                                  const int32_t* offsets, float* out, int accumulate,
+                                  float* partial, cudaStream_t st) {
+    const int64_t nchunks = (s.T * s.k + kDwgChunk - 1) / kDwgChunk + s.E;
+    const int vn = s.dtype == MOE_BF16 ? 8 : 4;
+    const unsigned gy = (unsigned)((n + 256 * vn - 1) / (256 * vn));
+    if (s.dtype == MOE_BF16)
+        colsum_partial_kernel<__nv_bfloat16><<<dim3((unsigned)nchunks, gy), 256, 0, st>>>(
+            n, s.E, offsets, (const __nv_bfloat16*)g, partial);
+    else
+        colsum_partial_kernel<float><<<dim3((unsigned)nchunks, gy), 256, 0, st>>>(
+            n, s.E, offsets, (const float*)g, partial);
+    colsum_reduce_kernel<<<dim3(s.E, (unsigned)((n + 255) / 256)), 256, 0, st>>>(
+        n, s.E, offsets, partial, out, accumulate);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,98 @@
+// kernels.h -- host-side launchers of the layer's kernels (internal to
+// libmoe.so; the public interface is include/moe.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Tokens handled by one block of the gate / rank kernels: the per-block
+// histogram is a bitmask of 256 tokens per expert.
+constexpr int kRouteBlockTokens = 256;
+// Rows summed per partial of the router weight gradient.
+constexpr int kDwgChunk = 128;
+
+inline int64_t route_blocks(int64_t T) { return (T + kRouteBlockTokens - 1) / kRouteBlockTokens; }
+
+// Default bound on every device-side wait (ns); MOE_WAIT_TIMEOUT_NS overrides.
+uint64_t wait_limit_ns();
+int device_sm_count();
+
+// A1
+cudaError_t launch_router_logits(const moe_shape& s, const void* x, const void* Wg,
+                                 const float* beta, float* logits, cudaStream_t st);
+// A2 + per-block histogram (block_counts laid out [E][nblk])
+cudaError_t launch_gate_hist(const moe_shape& s, const float* logits, int32_t* idx,
+                             float* w, int32_t* block_counts, int32_t* status,
+                             cudaStream_t st);
+// A3 scan: block_counts -> block_base in place, counts, offsets
+cudaError_t launch_dispatch_scan(const moe_shape& s, int32_t* block_counts,
+                                 int32_t* counts, int32_t* offsets, cudaStream_t st);
+// A3 stable rank: pos, perm
+cudaError_t launch_dispatch_rank(const moe_shape& s, const int32_t* idx,
+                                 const int32_t* block_base, int32_t* pos, int32_t* perm,
+                                 cudaStream_t st);
+// A10
+cudaError_t launch_route_bwd(const moe_shape& s, const float* dw, const float* logits,
+                             const int32_t* idx, const float* w, const int32_t* perm,
+                             const int32_t* offsets, const void* x, const void* Wg,
+                             void* dx, float* dWg, int accumulate, float* dL,
+                             float* partial, cudaStream_t st);
+size_t route_bwd_workspace(const moe_shape& s);  // dL + partials, bytes
+
+// A4, A6/A9, A7
+cudaError_t launch_permute(const moe_shape& s, const void* x, const int32_t* pos,
+                           void* x_perm, cudaStream_t st);
+cudaError_t launch_combine(const moe_shape& s, const void* y_perm, const int32_t* pos,
+                           const float* w, void* y, cudaStream_t st);
+cudaError_t launch_combine_bwd(const moe_shape& s, const void* dy, const void* y_perm,
+                               const int32_t* pos, const float* w, void* dy_perm,
+                               float* dw, cudaStream_t st);
+// per-expert column sums of a [T*k, n] activation: out[e][c] (+)= sum rows
+cudaError_t launch_segment_colsum(const moe_shape& s, const void* g, int n,
+                                  const int32_t* offsets, float* out, int accumulate,
+                                  float* partial, cudaStream_t st);
+size_t segment_colsum_workspace(const moe_shape& s, int n);
+
+// Grouped expert GEMMs.  Operand layouts (row-major):
+//   VarM ("fwd"/"dgrad"): for each expert e, rows [off_e, off_e+n_e) of act
+//   [P, K] times the expert's weight, giving out rows [P, N].  The weight is
+//   [E, N, K] (b_kmajor) or [E, K, N].
+//   VarK ("wgrad"): C_e [M, N] (+)= act_a[seg_e, M]^T act_b[seg_e, N], fp32.
+enum class Epi : int { BiasGelu = 0, Bias = 1, GeluGrad = 2, Plain = 3 };
+
+struct GemmVarM {
+    int E, N, K;
+    int64_t P;              // rows of act / out
+    const int32_t* offsets; // [E+1]
+    const void* act;        // [P, K]
+    const void* weight;     // [E,N,K] or [E,K,N]
+    bool weight_kmajor;     // true: [E,N,K]
+    Epi epi;
+    const void* bias;       // [E,N] or null
+    const void* aux;        // GeluGrad: H [P,N]
+    void* out0;             // [P,N]
+    void* out1;             // BiasGelu: A = GELU(out0 pre-rounding) [P,N]
+};
+struct GemmVarK {
+    int E, M, N;
+    int64_t P;
+    const int32_t* offsets;
+    const void* act_a;      // [P, M]
+    const void* act_b;      // [P, N]
+    float* out;             // [E, M, N]
+    int accumulate;
+};
+
+cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t st);
+cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t st);
+cudaError_t launch_gemm_varm_simt(const GemmVarM& g, cudaStream_t st);
+cudaError_t launch_gemm_vark_simt(const GemmVarK& g, cudaStream_t st);
+
+// Diagnostics
+cudaError_t launch_bounded_wait(uint64_t limit_ns, int32_t* status, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,271 @@
+// moe_api.cu -- the C ABI of include/moe.h: argument validation, workspace
+// carving, and the launch sequence of each step on the caller's stream.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+namespace moe {
+
+uint64_t wait_limit_ns() {
+    static uint64_t v = [] {
+        const char* s = getenv("MOE_WAIT_TIMEOUT_NS");
+        if (s && *s) {
+            const unsigned long long x = strtoull(s, nullptr, 10);
+            if (x > 0) return (uint64_t)x;
+        }
+        return (uint64_t)1000000000ull;  // 1 s
+    }();
+    return v;
+}
+
+int device_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 132;
+    }
+    return cache[dev];
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+inline bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
+// the status word is one int32: 4-byte alignment suffices
+inline bool ok_status(const int32_t* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+inline size_t esize(const moe_shape& s) { return s.dtype == MOE_BF16 ? 2 : 4; }
+
+moe_status check_shape(const moe_shape* s) {
+    if (!s) return MOE_ERR_INVALID;
+    if (s->T < 0 || s->d <= 0 || s->f <= 0 || s->E < 1 || s->E > 256 || s->k < 1 ||
+        s->k > 16 || s->k > s->E)
+        return MOE_ERR_INVALID;
+    if (s->dtype != MOE_F32 && s->dtype != MOE_BF16) return MOE_ERR_INVALID;
+    if (s->renorm != 0 && s->renorm != 1) return MOE_ERR_INVALID;
+    if (s->T * (int64_t)s->k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (s->d % 8 || s->f % 8) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status check_gemm_shape(const moe_shape* s) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->dtype == MOE_BF16 && (s->d % 64 || s->f % 64)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+inline moe_status cuda_status(cudaError_t e) {
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t route_ws(const moe_shape& s) {
+    return align_up((size_t)s.E * (size_t)route_blocks(s.T) * sizeof(int32_t));
+}
+
+size_t ffn_bwd_ws(const moe_shape& s) {
+    const size_t dh = align_up((size_t)s.T * s.k * s.f * esize(s));
+    const int n = s.d > s.f ? s.d : s.f;
+    return dh + align_up(segment_colsum_workspace(s, n));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID: return "MOE_ERR_INVALID: bad argument";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: unsupported shape or dtype";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA call or launch failed";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait ran out";
+        case MOE_ERR_NONFINITE: return "MOE_ERR_NONFINITE: non-finite router logit";
+    }
+    return "unknown moe_status";
+}
+
+size_t moe_workspace_size(const moe_shape* s) {
+    if (check_shape(s) != MOE_OK) return 0;
+    size_t m = route_ws(*s);
+    const size_t b = ffn_bwd_ws(*s);
+    if (b > m) m = b;
+    const size_t r = align_up(route_bwd_workspace(*s));
+    if (r > m) m = r;
+    return m;
+}
+
+moe_status moe_route(const moe_shape* s, const void* x, const void* Wg, const float* logit_bias,
+                     float* logits, int compute_logits, int32_t* idx, float* w, int32_t* counts,
+                     int32_t* offsets, int32_t* pos, int32_t* perm, void* ws,
+                     int32_t* dev_status, moe_stream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (!ok_ptr(counts) || !ok_ptr(offsets)) return MOE_ERR_INVALID;
+    if (s->T > 0) {
+        if (!ok_ptr(logits) || !ok_ptr(idx) || !ok_ptr(w) || !ok_ptr(pos) || !ok_ptr(perm) ||
+            !ok_ptr(ws) || !ok_status(dev_status))
+            return MOE_ERR_INVALID;
+        if (compute_logits && (!ok_ptr(x) || !ok_ptr(Wg) || !ok_opt(logit_bias)))
+            return MOE_ERR_INVALID;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t* block_counts = (int32_t*)ws;
+    cudaError_t e = cudaSuccess;
+    if (s->T > 0) {
+        if (compute_logits) e = launch_router_logits(*s, x, Wg, logit_bias, logits, st);
+        if (e == cudaSuccess) e = launch_gate_hist(*s, logits, idx, w, block_counts, dev_status, st);
+    }
+    if (e == cudaSuccess) e = launch_dispatch_scan(*s, block_counts, counts, offsets, st);
+    if (e == cudaSuccess && s->T > 0) e = launch_dispatch_rank(*s, idx, block_counts, pos, perm, st);
+    return cuda_status(e);
+}
+
+moe_status moe_permute(const moe_shape* s, const void* x, const int32_t* pos, void* x_perm,
+                       moe_stream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->T == 0) return MOE_OK;
+    if (!ok_ptr(x) || !ok_ptr(pos) || !ok_ptr(x_perm)) return MOE_ERR_INVALID;
+    return cuda_status(launch_permute(*s, x, pos, x_perm, (cudaStream_t)stream));
+}
+
+moe_status moe_expert_ffn_fwd(const moe_shape* s, const void* x_perm, const int32_t* offsets,
+                              const void* W1, const void* b1, const void* W2, const void* b2,
+                              void* H, void* A, void* y_perm, void* ws, int32_t* dev_status,
+                              moe_stream_t stream) {
+    (void)ws;
+    moe_status r = check_gemm_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->T == 0) return MOE_OK;
+    if (!ok_ptr(x_perm) || !ok_ptr(offsets) || !ok_ptr(W1) || !ok_ptr(W2) || !ok_opt(b1) ||
+        !ok_opt(b2) || !ok_ptr(H) || !ok_ptr(A) || !ok_ptr(y_perm) || !ok_status(dev_status))
+        return MOE_ERR_INVALID;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t P = s->T * s->k;
+    GemmVarM g1{s->E, s->f, s->d, P, offsets, x_perm, W1, true, Epi::BiasGelu, b1, nullptr, H, A};
+    GemmVarM g2{s->E, s->d, s->f, P, offsets, A, W2, true, Epi::Bias, b2, nullptr, y_perm, nullptr};
+    cudaError_t e;
+    if (s->dtype == MOE_BF16) {
+        e = launch_gemm_varm_tc(g1, dev_status, st);
+        if (e == cudaSuccess) e = launch_gemm_varm_tc(g2, dev_status, st);
+    } else {
+        e = launch_gemm_varm_simt(g1, st);
+        if (e == cudaSuccess) e = launch_gemm_varm_simt(g2, st);
+    }
+    return cuda_status(e);
+}
+
+moe_status moe_combine_fwd(const moe_shape* s, const void* y_perm, const int32_t* pos,
+                           const float* w, void* y, moe_stream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->T == 0) return MOE_OK;
+    if (!ok_ptr(y_perm) || !ok_ptr(pos) || !ok_opt(w) || !ok_ptr(y)) return MOE_ERR_INVALID;
+    return cuda_status(launch_combine(*s, y_perm, pos, w, y, (cudaStream_t)stream));
+}
+
+moe_status moe_combine_bwd(const moe_shape* s, const void* dy, const void* y_perm,
+                           const int32_t* pos, const float* w, void* dy_perm, float* dw,
+                           moe_stream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->T == 0) return MOE_OK;
+    if (!ok_ptr(dy) || !ok_ptr(y_perm) || !ok_ptr(pos) || !ok_ptr(w) || !ok_ptr(dy_perm) ||
+        !ok_ptr(dw))
+        return MOE_ERR_INVALID;
+    return cuda_status(launch_combine_bwd(*s, dy, y_perm, pos, w, dy_perm, dw,
+                                          (cudaStream_t)stream));
+}
+
+moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const void* x_perm,
+                              const void* H, const void* A, const int32_t* offsets,
+                              const void* W1, const void* W2, void* dx_perm, float* dW1,
+                              float* db1, float* dW2, float* db2, int accumulate, void* ws,
+                              int32_t* dev_status, moe_stream_t stream) {
+    moe_status r = check_gemm_shape(s);
+    if (r != MOE_OK) return r;
+    if (!ok_ptr(dW1) || !ok_ptr(db1) || !ok_ptr(dW2) || !ok_ptr(db2)) return MOE_ERR_INVALID;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int E = s->E, d = s->d, f = s->f;
+    if (s->T == 0) {
+        if (accumulate) return MOE_OK;
+        cudaError_t e = cudaMemsetAsync(dW1, 0, sizeof(float) * (size_t)E * f * d, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, sizeof(float) * (size_t)E * d * f, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(db1, 0, sizeof(float) * (size_t)E * f, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(db2, 0, sizeof(float) * (size_t)E * d, st);
+        return cuda_status(e);
+    }
+    if (!ok_ptr(dy_perm) || !ok_ptr(x_perm) || !ok_ptr(H) || !ok_ptr(A) || !ok_ptr(offsets) ||
+        !ok_ptr(W1) || !ok_ptr(W2) || !ok_ptr(dx_perm) || !ok_ptr(ws) || !ok_status(dev_status))
+        return MOE_ERR_INVALID;
+    const int64_t P = s->T * s->k;
+    uint8_t* wsb = (uint8_t*)ws;
+    void* dH = wsb;
+    float* partial = (float*)(wsb + align_up((size_t)P * f * esize(*s)));
+    // dA = dY W2[e] (W2 stored [E,d,f] = [E,K,N]); dH = dA * GELU'(H)
+    GemmVarM g_dh{E, f, d, P, offsets, dy_perm, W2, false, Epi::GeluGrad, nullptr, H, dH, nullptr};
+    // dX = dH W1[e] (W1 stored [E,f,d] = [E,K,N])
+    GemmVarM g_dx{E, d, f, P, offsets, dH, W1, false, Epi::Plain, nullptr, nullptr, dx_perm, nullptr};
+    // dW2[e] = dY^T A  ([d, f]);  dW1[e] = dH^T X  ([f, d])
+    GemmVarK g_w2{E, d, f, P, offsets, dy_perm, A, dW2, accumulate};
+    GemmVarK g_w1{E, f, d, P, offsets, dH, x_perm, dW1, accumulate};
+    const bool tc = s->dtype == MOE_BF16;
+    cudaError_t e = tc ? launch_gemm_varm_tc(g_dh, dev_status, st) : launch_gemm_varm_simt(g_dh, st);
+    if (e == cudaSuccess)
+        e = tc ? launch_gemm_varm_tc(g_dx, dev_status, st) : launch_gemm_varm_simt(g_dx, st);
+    if (e == cudaSuccess)
+        e = tc ? launch_gemm_vark_tc(g_w2, dev_status, st) : launch_gemm_vark_simt(g_w2, st);
+    if (e == cudaSuccess)
+        e = tc ? launch_gemm_vark_tc(g_w1, dev_status, st) : launch_gemm_vark_simt(g_w1, st);
+    if (e == cudaSuccess) e = launch_segment_colsum(*s, dy_perm, d, offsets, db2, accumulate, partial, st);
+    if (e == cudaSuccess) e = launch_segment_colsum(*s, dH, f, offsets, db1, accumulate, partial, st);
+    return cuda_status(e);
+}
+
+moe_status moe_route_bwd(const moe_shape* s, const float* dw, const float* logits,
+                         const int32_t* idx, const float* w, const int32_t* perm,
+                         const int32_t* offsets, const void* x, const void* Wg, void* dx,
+                         float* dWg, int accumulate, void* ws, int32_t* dev_status,
+                         moe_stream_t stream) {
+    (void)dev_status;
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (!ok_ptr(dWg)) return MOE_ERR_INVALID;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (s->T == 0) {
+        if (accumulate) return MOE_OK;
+        return cuda_status(cudaMemsetAsync(dWg, 0, sizeof(float) * (size_t)s->E * s->d, st));
+    }
+    if (!ok_ptr(dw) || !ok_ptr(logits) || !ok_ptr(idx) || !ok_ptr(w) || !ok_ptr(perm) ||
+        !ok_ptr(offsets) || !ok_ptr(x) || !ok_ptr(Wg) || !ok_ptr(dx) || !ok_ptr(ws))
+        return MOE_ERR_INVALID;
+    float* dL = (float*)ws;
+    const size_t dl_bytes = (size_t)s->T * (size_t)(s->renorm ? s->k : s->E) * sizeof(float);
+    float* partial = (float*)((uint8_t*)ws + align_up(dl_bytes));
+    return cuda_status(launch_route_bwd(*s, dw, logits, idx, w, perm, offsets, x, Wg, dx, dWg,
+                                        accumulate, dL, partial, st));
+}
+
+moe_status moe_debug_bounded_wait(uint64_t limit_ns, int32_t* dev_status, moe_stream_t stream) {
+    if (dev_status == nullptr || !ok_status(dev_status)) return MOE_ERR_INVALID;
+    return cuda_status(launch_bounded_wait(limit_ns, dev_status, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,657 @@
+// route.cu -- router logits, softmax top-k gate, stable dispatch by expert,
+// and the router backward (steps A1, A2, A3, A10 of the layer).
+//
+// The gating network's output decides each token's experts; tokens are then
+// assigned to their target experts in token order, so that each expert sees
+// one contiguous segment and no dispatch mask is built ("ES-MoE: Scaling
+// Beyond the GPU Memory Limit for Large Mixture-of-Experts Model Training",
+// review, section 3 "expert-wise offloading and processing"; "FastMoE",
+// review, "proposed method": scatter/gather layout batching inputs by expert).
+//
+// Dispatch design: each block of 256 tokens records, per expert, a 256-bit
+// mask of the tokens routed there (8 words of 32 bits).  Popcounts of those
+// masks give the block's histogram; one single-block scan over the
+// expert-major (expert, block) table gives every block's base row per expert;
+// a token's rank inside its block is a popcount of the mask bits below it.
+// Positions are therefore a pure function of idx: deterministic and stable.
+#include <float.h>
+#include <limits.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float warp_max(float v) {
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// ---- vector load / store of 8 (bf16) or 4 (fp32) elements as fp32 ----------------
+
+template <typename T> struct Vec;
+template <> struct Vec<__nv_bfloat16> {
+    static constexpr int N = 8;
+    static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* v) {
+        uint4 u = *reinterpret_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+        #pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(h[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, const float* v) {
+        uint4 u;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+        #pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        *reinterpret_cast<uint4*>(p) = u;
+    }
+};
+template <> struct Vec<float> {
+    static constexpr int N = 4;
+    static __device__ __forceinline__ void load(const float* p, float* v) {
+        float4 u = *reinterpret_cast<const float4*>(p);
+        v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+    }
+    static __device__ __forceinline__ void store(float* p, const float* v) {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+};
+
+// ---- A1: router logits, SIMT GEMM with fp32 accumulation ------------------------
+//
+// logits[t][e] = sum_c x[t][c] Wg[e][c] + beta[e].  Block tile BM tokens x BN
+// experts, K staged through shared memory 32 at a time; thread (tx, ty) owns
+// tokens ty + NTY*i and experts tx + NTX*j (interleaved: conflict-free shared
+// reads, coalesced stores).
+
+template <typename TIn, int BM, int BN, int TM, int TN>
+__global__ void __launch_bounds__(256) router_logits_kernel(
+    int64_t T, int d, int E, const TIn* __restrict__ x, const TIn* __restrict__ Wg,
+    const float* __restrict__ beta, float* __restrict__ logits) {
+    constexpr int BK = 32;
+    constexpr int NTX = BN / TN;
+    constexpr int NTY = BM / TM;
+    static_assert(NTX * NTY == 256, "256 threads");
+    __shared__ float xs[BK][BM + 1];
+    __shared__ float ws[BK][BN + 1];
+    const int tid = threadIdx.x;
+    const int tx = tid % NTX, ty = tid / NTX;
+    const int64_t m0 = (int64_t)blockIdx.x * BM;
+    const int n0 = blockIdx.y * BN;
+    float acc[TM][TN];
+    #pragma unroll
+    for (int i = 0; i < TM; ++i)
+        #pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+
+    for (int k0 = 0; k0 < d; k0 += BK) {
+        for (int i = tid; i < BM * BK; i += 256) {
+            const int r = i / BK, c = i % BK;
+            const int64_t gm = m0 + r;
+            const int gk = k0 + c;
+            xs[c][r] = (gm < T && gk < d) ? to_f32(x[gm * d + gk]) : 0.f;
+        }
+        for (int i = tid; i < BN * BK; i += 256) {
+            const int r = i / BK, c = i % BK;
+            const int gn = n0 + r;
+            const int gk = k0 + c;
+            ws[c][r] = (gn < E && gk < d) ? to_f32(Wg[(int64_t)gn * d + gk]) : 0.f;
+        }
+        __syncthreads();
+        #pragma unroll 4
+        for (int kk = 0; kk < BK; ++kk) {
+            float a[TM], b[TN];
+            #pragma unroll
+            for (int i = 0; i < TM; ++i) a[i] = xs[kk][ty + NTY * i];
+            #pragma unroll
+            for (int j = 0; j < TN; ++j) b[j] = ws[kk][tx + NTX * j];
+            #pragma unroll
+            for (int i = 0; i < TM; ++i)
+                #pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+    #pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int64_t t = m0 + ty + NTY * i;
+        if (t >= T) continue;
+        #pragma unroll
+        for (int j = 0; j < TN; ++j) {
+            const int e = n0 + tx + NTX * j;
+            if (e < E) logits[t * E + e] = acc[i][j] + (beta ? beta[e] : 0.f);
+        }
+    }
+}
+
+template <typename TIn>
+cudaError_t router_logits_dispatch(const moe_shape& s, const TIn* x, const TIn* Wg,
+                                   const float* beta, float* logits, cudaStream_t st) {
+    const int64_t T = s.T;
+    if (s.E <= 16) {
+        dim3 grid((unsigned)((T + 255) / 256), 1);
+        router_logits_kernel<TIn, 256, 16, 16, 1><<<grid, 256, 0, st>>>(T, s.d, s.E, x, Wg, beta, logits);
+    } else if (s.E <= 32) {
+        dim3 grid((unsigned)((T + 127) / 128), 1);
+        router_logits_kernel<TIn, 128, 32, 8, 2><<<grid, 256, 0, st>>>(T, s.d, s.E, x, Wg, beta, logits);
+    } else if (s.E <= 64) {
+        dim3 grid((unsigned)((T + 127) / 128), 1);
+        router_logits_kernel<TIn, 128, 64, 8, 4><<<grid, 256, 0, st>>>(T, s.d, s.E, x, Wg, beta, logits);
+    } else {
+        dim3 grid((unsigned)((T + 63) / 64), (unsigned)((s.E + 127) / 128));
+        router_logits_kernel<TIn, 64, 128, 4, 8><<<grid, 256, 0, st>>>(T, s.d, s.E, x, Wg, beta, logits);
+    }
+    return cudaGetLastError();
+}
+
+// ---- A2: softmax top-k gate + per-block expert bitmask histogram ----------------
+//
+// One warp per token; lane l holds logits of experts l, l+32, ...  Top-k by k
+// rounds of a warp arg-max on (logit desc, expert index asc).  A NaN logit is
+// ranked below every number (so k distinct valid experts are always chosen)
+// and, like an infinite one, raises MOE_ERR_NONFINITE.
+
+template <int EPL>
+__global__ void __launch_bounds__(256) gate_hist_kernel(
+    int64_t T, int E, int k, int renorm, int nblk, const float* __restrict__ logits,
+    int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ block_counts,
+    int32_t* status) {
+    __shared__ uint32_t bits[256][8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < E * 8; i += 256) bits[i >> 3][i & 7] = 0u;
+    __syncthreads();
+
+    const int64_t tbase = (int64_t)blockIdx.x * kRouteBlockTokens + warp * 32;
+    for (int tt = 0; tt < 32; ++tt) {
+        const int64_t t = tbase + tt;
+        if (t >= T) break;
+        float L[EPL];
+        bool bad = false;
+        #pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+            const int e = lane + 32 * q;
+            float v = -INFINITY;
+            if (e < E) {
+                v = logits[t * E + e];
+                if (!isfinite(v)) bad = true;
+                if (isnan(v)) v = -INFINITY;
+            }
+            L[q] = v;
+        }
+        if (__any_sync(kFull, bad) && lane == 0) report(status, MOE_ERR_NONFINITE);
+        float m = L[0];
+        #pragma unroll
+        for (int q = 1; q < EPL; ++q) m = fmaxf(m, L[q]);
+        m = warp_max(m);
+        float z = 0.f;
+        #pragma unroll
+        for (int q = 0; q < EPL; ++q)
+            if (lane + 32 * q < E) z += expf(L[q] - m);
+        z = warp_sum(z);
+
+        uint32_t taken = 0u;
+        int my_e = 0;
+        float my_p = 0.f, psum = 0.f;
+        for (int j = 0; j < k; ++j) {
+            float bv = -INFINITY;
+            int be = INT_MAX;
+            #pragma unroll
+            for (int q = 0; q < EPL; ++q) {
+                const int e = lane + 32 * q;
+                if (e < E && !((taken >> q) & 1u) && (be == INT_MAX || L[q] > bv)) {
+                    bv = L[q];
+                    be = e;
+                }
+            }
+            #pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(kFull, bv, o);
+                const int oe = __shfl_xor_sync(kFull, be, o);
+                if (oe != INT_MAX &&
+                    (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+            const float p = expf(bv - m) / z;
+            if (lane == j) { my_e = be; my_p = p; }
+            psum += p;
+            if (lane == 0) bits[be][warp] |= 1u << tt;
+        }
+        if (lane < k) {
+            idx[t * k + lane] = my_e;
+            w[t * k + lane] = renorm ? my_p / psum : my_p;
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += 256) {
+        int c = 0;
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) c += __popc(bits[e][q]);
+        block_counts[(int64_t)e * nblk + blockIdx.x] = c;
+    }
+}
+
+// ---- A3: scan of the expert-major (expert, block) histogram ---------------------
+
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nblk, int32_t* data,
+                                                            int32_t* counts,
+                                                            int32_t* offsets) {
+    __shared__ int warp_tot[32];
+    __shared__ int grand;
+    const int n = E * nblk;
+    const int per = (n + 1023) / 1024;
+    const int b = threadIdx.x * per;
+    const int e_ = min(n, b + per);
+    int s = 0;
+    for (int i = b; i < e_; ++i) s += data[i];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = s;
+    #pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        const int v = warp_tot[lane];
+        int iv = v;
+        #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(kFull, iv, o);
+            if (lane >= o) iv += u;
+        }
+        warp_tot[lane] = iv - v;
+        if (lane == 31) grand = iv;
+    }
+    __syncthreads();
+    int run = warp_tot[wid] + incl - s;
+    for (int i = b; i < e_; ++i) {
+        const int c = data[i];
+        data[i] = run;
+        run += c;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e <= E; e += 1024) {
+        const int off = (e == E) ? grand : data[e * nblk];
+        offsets[e] = off;
+        if (e < E) {
+            const int nxt = (e + 1 == E) ? grand : data[(e + 1) * nblk];
+            counts[e] = nxt - off;
+        }
+    }
+}
+
+// ---- A3: stable rank inside each block -> pos, perm ------------------------------
+
+__global__ void __launch_bounds__(256) dispatch_rank_kernel(
+    int64_t T, int E, int k, int nblk, const int32_t* __restrict__ idx,
+    const int32_t* __restrict__ block_base, int32_t* __restrict__ pos,
+    int32_t* __restrict__ perm) {
+    __shared__ uint32_t bits[256][8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < E * 8; i += 256) bits[i >> 3][i & 7] = 0u;
+    __syncthreads();
+    const int64_t t = (int64_t)blockIdx.x * kRouteBlockTokens + threadIdx.x;
+    if (t < T)
+        for (int j = 0; j < k; ++j) atomicOr(&bits[idx[t * k + j]][warp], 1u << lane);
+    __syncthreads();
+    if (t >= T) return;
+    const uint32_t below = (1u << lane) - 1u;
+    for (int j = 0; j < k; ++j) {
+        const int e = idx[t * k + j];
+        int r = __popc(bits[e][warp] & below);
+        for (int q = 0; q < warp; ++q) r += __popc(bits[e][q]);
+        const int32_t p = block_base[(int64_t)e * nblk + blockIdx.x] + r;
+        pos[t * k + j] = p;
+        perm[p] = (int32_t)(t * k + j);
+    }
+}
+
+// ---- A10: router backward ----------------------------------------------------------
+//
+// Warp per token.  renorm: dL_j = w_j (dw_j - sum_i w_i dw_i) on the k selected
+// experts (stored [T][k]).  Otherwise the full softmax Jacobian (stored
+// [T][E]).  dx[t] += sum_e dL[t][e] Wg[e] (read-modify-write in the storage
+// dtype, fp32 arithmetic).
+
+template <typename TIn, int EPL>
+__global__ void __launch_bounds__(256) route_bwd_dx_kernel(
+    int64_t T, int d, int E, int k, int renorm, const float* __restrict__ dw,
+    const float* __restrict__ logits, const int32_t* __restrict__ idx,
+    const float* __restrict__ w, const TIn* __restrict__ Wg, TIn* __restrict__ dx,
+    float* __restrict__ dL) {
+    __shared__ float g_s[8][256];
+    __shared__ int e_s[8][256];
+    using V = Vec<TIn>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    int ng;  // number of (expert, dL) terms for this token
+    if (renorm) {
+        float wj = 0.f, dwj = 0.f;
+        int ej = 0;
+        if (lane < k) {
+            wj = w[t * k + lane];
+            dwj = dw[t * k + lane];
+            ej = idx[t * k + lane];
+        }
+        const float sdot = warp_sum(wj * dwj);
+        if (lane < k) {
+            const float g = wj * (dwj - sdot);
+            dL[t * k + lane] = g;
+            g_s[warp][lane] = g;
+            e_s[warp][lane] = ej;
+        }
+        ng = k;
+    } else {
+        float L[EPL], p[EPL];
+        #pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+            const int e = lane + 32 * q;
+            L[q] = (e < E) ? logits[t * E + e] : -INFINITY;
+        }
+        float m = L[0];
+        #pragma unroll
+        for (int q = 1; q < EPL; ++q) m = fmaxf(m, L[q]);
+        m = warp_max(m);
+        float z = 0.f;
+        #pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+            p[q] = (lane + 32 * q < E) ? expf(L[q] - m) : 0.f;
+            z += p[q];
+        }
+        z = warp_sum(z);
+        #pragma unroll
+        for (int q = 0; q < EPL; ++q) p[q] /= z;
+        // c_j = dw_j * p[idx_j];  dL_e = -p_e * sum_j c_j + sum_j c_j [e == idx_j]
+        float add[EPL];
+        #pragma unroll
+        for (int q = 0; q < EPL; ++q) add[q] = 0.f;
+        float csum = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int a = idx[t * k + j];
+            float pa_l = 0.f;
+            #pragma unroll
+            for (int q = 0; q < EPL; ++q)
+                if (q == (a >> 5)) pa_l = p[q];
+            const float pa = __shfl_sync(kFull, pa_l, a & 31);
+            const float c = dw[t * k + j] * pa;
+            csum += c;
+            #pragma unroll
+            for (int q = 0; q < EPL; ++q)
+                if (lane + 32 * q == a) add[q] += c;
+        }
+        #pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+            const int e = lane + 32 * q;
+            if (e < E) {
+                const float g = add[q] - p[q] * csum;
+                dL[t * E + e] = g;
+                g_s[warp][e] = g;
+                e_s[warp][e] = e;
+            }
+        }
+        ng = E;
+    }
+    __syncwarp();
+    constexpr int VN = V::N;
+    for (int c = lane * VN; c < d; c += 32 * VN) {
+        float acc[VN], wv[VN];
+        V::load(dx + t * d + c, acc);
+        for (int i = 0; i < ng; ++i) {
+            const float g = g_s[warp][i];
+            V::load(Wg + (int64_t)e_s[warp][i] * d + c, wv);
+            #pragma unroll
+            for (int u = 0; u < VN; ++u) acc[u] = fmaf(g, wv[u], acc[u]);
+        }
+        V::store(dx + t * d + c, acc);
+    }
+}
+
+// Sparse (renorm) partial sums of dWg: one partial per (expert, chunk of
+// kDwgChunk consecutive rows of the expert's segment), rows in segment order.
+template <typename TIn>
+__global__ void __launch_bounds__(256) dwg_partial_sparse_kernel(
+    int d, int E, int k, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ perm, const float* __restrict__ dLsel,
+    const TIn* __restrict__ x, float* __restrict__ partial) {
+    using V = Vec<TIn>;
+    constexpr int VN = V::N;
+    // locate (expert, chunk) of this block
+    int e = 0, acc = 0, sub = -1;
+    for (; e < E; ++e) {
+        const int n = offsets[e + 1] - offsets[e];
+        const int nc = (n + kDwgChunk - 1) / kDwgChunk;
+        if ((int)blockIdx.x < acc + nc) { sub = blockIdx.x - acc; break; }
+        acc += nc;
+    }
+    if (sub < 0) return;
+    const int c = (blockIdx.y * 256 + threadIdx.x) * VN;
+    if (c >= d) return;
+    const int p0 = offsets[e] + sub * kDwgChunk;
+    const int p1 = min(offsets[e + 1], p0 + kDwgChunk);
+    float a[VN], xv[VN];
+    #pragma unroll
+    for (int u = 0; u < VN; ++u) a[u] = 0.f;
+    for (int p = p0; p < p1; ++p) {
+        const int s = perm[p];
+        const float g = dLsel[s];
+        V::load(x + (int64_t)(s / k) * d + c, xv);
+        #pragma unroll
+        for (int u = 0; u < VN; ++u) a[u] = fmaf(g, xv[u], a[u]);
+    }
+    float* out = partial + (int64_t)blockIdx.x * d + c;
+    #pragma unroll
+    for (int u = 0; u < VN; ++u) out[u] = a[u];
+}
+
+__global__ void __launch_bounds__(256) dwg_reduce_sparse_kernel(
+    int d, int E, const int32_t* __restrict__ offsets, const float* __restrict__ partial,
+    float* __restrict__ dWg, int accumulate) {
+    const int e = blockIdx.x;
+    const int c = blockIdx.y * 256 + threadIdx.x;
+    if (c >= d) return;
+    int start = 0;
+    for (int q = 0; q < e; ++q) {
+        const int n = offsets[q + 1] - offsets[q];
+        start += (n + kDwgChunk - 1) / kDwgChunk;
+    }
+    const int n = offsets[e + 1] - offsets[e];
+    const int nc = (n + kDwgChunk - 1) / kDwgChunk;
+    float s = 0.f;
+    for (int i = 0; i < nc; ++i) s += partial[(int64_t)(start + i) * d + c];
+    float* o = dWg + (int64_t)e * d + c;
+    *o = accumulate ? *o + s : s;
+}
+
+// Dense (softmax Jacobian) partial sums: partial[tc][e][c] over kDwgChunk
+// consecutive tokens, 8 experts per block.
+template <typename TIn>
+__global__ void __launch_bounds__(256) dwg_partial_dense_kernel(
+    int64_t T, int d, int E, const float* __restrict__ dL, const TIn* __restrict__ x,
+    float* __restrict__ partial) {
+    using V = Vec<TIn>;
+    constexpr int VN = V::N;
+    const int tc = blockIdx.x;
+    const int e0 = blockIdx.z * 8;
+    const int c = (blockIdx.y * 256 + threadIdx.x) * VN;
+    if (c >= d) return;
+    const int64_t t0 = (int64_t)tc * kDwgChunk;
+    const int64_t t1 = min(T, t0 + kDwgChunk);
+    float a[8][VN], xv[VN];
+    #pragma unroll
+    for (int i = 0; i < 8; ++i)
+        #pragma unroll
+        for (int u = 0; u < VN; ++u) a[i][u] = 0.f;
+    for (int64_t t = t0; t < t1; ++t) {
+        V::load(x + t * d + c, xv);
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float g = (e0 + i < E) ? dL[t * E + e0 + i] : 0.f;
+            #pragma unroll
+            for (int u = 0; u < VN; ++u) a[i][u] = fmaf(g, xv[u], a[i][u]);
+        }
+    }
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (e0 + i >= E) break;
+        float* out = partial + ((int64_t)tc * E + e0 + i) * d + c;
+        #pragma unroll
+        for (int u = 0; u < VN; ++u) out[u] = a[i][u];
+    }
+}
+
+__global__ void __launch_bounds__(256) dwg_reduce_dense_kernel(int d, int E, int ntc,
+                                                              const float* __restrict__ partial,
+                                                              float* __restrict__ dWg,
+                                                              int accumulate) {
+    const int e = blockIdx.x;
+    const int c = blockIdx.y * 256 + threadIdx.x;
+    if (c >= d) return;
+    float s = 0.f;
+    for (int i = 0; i < ntc; ++i) s += partial[((int64_t)i * E + e) * d + c];
+    float* o = dWg + (int64_t)e * d + c;
+    *o = accumulate ? *o + s : s;
+}
+
+template <typename TIn>
+cudaError_t route_bwd_typed(const moe_shape& s, const float* dw, const float* logits,
+                            const int32_t* idx, const float* w, const int32_t* perm,
+                            const int32_t* offsets, const TIn* x, const TIn* Wg, TIn* dx,
+                            float* dWg, int accumulate, float* dL, float* partial,
+                            cudaStream_t st) {
+    const int64_t T = s.T;
+    const int d = s.d, E = s.E, k = s.k;
+    const unsigned gx = (unsigned)((T + 7) / 8);
+    if (E <= 32)
+        route_bwd_dx_kernel<TIn, 1><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx, dL);
+    else if (E <= 64)
+        route_bwd_dx_kernel<TIn, 2><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx, dL);
+    else if (E <= 128)
+        route_bwd_dx_kernel<TIn, 4><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx, dL);
+    else
+        route_bwd_dx_kernel<TIn, 8><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx, dL);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    constexpr int VN = Vec<TIn>::N;
+    const unsigned gy = (unsigned)((d + 256 * VN - 1) / (256 * VN));
+    const unsigned gy_red = (unsigned)((d + 255) / 256);
+    if (s.renorm) {
+        const int64_t nchunks = (T * k + kDwgChunk - 1) / kDwgChunk + E;
+        dwg_partial_sparse_kernel<TIn><<<dim3((unsigned)nchunks, gy), 256, 0, st>>>(
+            d, E, k, offsets, perm, dL, x, partial);
+        dwg_reduce_sparse_kernel<<<dim3(E, gy_red), 256, 0, st>>>(d, E, offsets, partial, dWg,
+                                                                 accumulate);
+    } else {
+        const int ntc = (int)((T + kDwgChunk - 1) / kDwgChunk);
+        dwg_partial_dense_kernel<TIn><<<dim3(ntc, gy, (E + 7) / 8), 256, 0, st>>>(T, d, E, dL, x,
+                                                                                  partial);
+        dwg_reduce_dense_kernel<<<dim3(E, gy_red), 256, 0, st>>>(d, E, ntc, partial, dWg,
+                                                                accumulate);
+    }
+    return cudaGetLastError();
+}
+
+__global__ void bounded_wait_kernel(uint64_t limit_ns, int32_t* status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);  // nothing ever arrives on it
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (!mbar_wait_bounded(smem_u32(&bar), 0, limit_ns, &abort_flag))
+            report(status, MOE_ERR_TIMEOUT);
+    }
+}
+
+}  // namespace
+
+// ---- launchers -----------------------------------------------------------------------
+
+cudaError_t launch_router_logits(const moe_shape& s, const void* x, const void* Wg,
+                                 const float* beta, float* logits, cudaStream_t st) {
+    if (s.dtype == MOE_BF16)
+        return router_logits_dispatch(s, (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg,
+                                      beta, logits, st);
+    return router_logits_dispatch(s, (const float*)x, (const float*)Wg, beta, logits, st);
+}
+
+cudaError_t launch_gate_hist(const moe_shape& s, const float* logits, int32_t* idx, float* w,
+                             int32_t* block_counts, int32_t* status, cudaStream_t st) {
+    const int nblk = (int)route_blocks(s.T);
+    const int E = s.E;
+    if (E <= 32)
+        gate_hist_kernel<1><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+    else if (E <= 64)
+        gate_hist_kernel<2><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+    else if (E <= 128)
+        gate_hist_kernel<4><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+    else
+        gate_hist_kernel<8><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_scan(const moe_shape& s, int32_t* block_counts, int32_t* counts,
+                                 int32_t* offsets, cudaStream_t st) {
+    dispatch_scan_kernel<<<1, 1024, 0, st>>>(s.E, (int)route_blocks(s.T), block_counts, counts,
+                                             offsets);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_rank(const moe_shape& s, const int32_t* idx,
+                                 const int32_t* block_base, int32_t* pos, int32_t* perm,
+                                 cudaStream_t st) {
+    const int nblk = (int)route_blocks(s.T);
+    dispatch_rank_kernel<<<nblk, 256, 0, st>>>(s.T, s.E, s.k, nblk, idx, block_base, pos, perm);
+    return cudaGetLastError();
+}
+
+size_t route_bwd_workspace(const moe_shape& s) {
+    const int64_t T = s.T;
+    const size_t dl = (size_t)T * (size_t)(s.renorm ? s.k : s.E) * sizeof(float);
+    size_t part;
+    if (s.renorm)
+        part = (size_t)((T * s.k + kDwgChunk - 1) / kDwgChunk + s.E) * s.d * sizeof(float);
+    else
+        part = (size_t)((T + kDwgChunk - 1) / kDwgChunk) * s.E * s.d * sizeof(float);
+    return ((dl + 255) & ~(size_t)255) + part;
+}
+
+cudaError_t launch_route_bwd(const moe_shape& s, const float* dw, const float* logits,
+                             const int32_t* idx, const float* w, const int32_t* perm,
+                             const int32_t* offsets, const void* x, const void* Wg, void* dx,
+                             float* dWg, int accumulate, float* dL, float* partial,
+                             cudaStream_t st) {
+    if (s.dtype == MOE_BF16)
+        return route_bwd_typed(s, dw, logits, idx, w, perm, offsets, (const __nv_bfloat16*)x,
+                               (const __nv_bfloat16*)Wg, (__nv_bfloat16*)dx, dWg, accumulate,
+                               dL, partial, st);
+    return route_bwd_typed(s, dw, logits, idx, w, perm, offsets, (const float*)x,
+                           (const float*)Wg, (float*)dx, dWg, accumulate, dL, partial, st);
+}
+
+cudaError_t launch_bounded_wait(uint64_t limit_ns, int32_t* status, cudaStream_t st) {
+    bounded_wait_kernel<<<1, 32, 0, st>>>(limit_ns, status);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,167 @@
+"""Thin Python binding of libmoe.so (include/moe.h): same entry-point names,
+argument marshalling only.  Every step of the layer runs in the library's CUDA
+kernels; there is no Python or CPU fallback.  If the library has not been
+built, the first call raises.
+
+Tensors are torch CUDA tensors (any pointer-like argument may also be a raw
+device address as an int, or None where the C ABI allows NULL).  Work is
+enqueued on the current torch CUDA stream unless ``stream`` is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_NONFINITE = range(6)
+MOE_F32, MOE_BF16 = 0, 1
+
+ENTRY_POINTS = ("moe_status_string", "moe_workspace_size", "moe_route", "moe_permute",
+                "moe_expert_ffn_fwd", "moe_combine_fwd", "moe_combine_bwd",
+                "moe_expert_ffn_bwd", "moe_route_bwd", "moe_debug_bounded_wait")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn}: {msg}")
+        self.code = code
+
+
+class moe_shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("f", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("renorm", ctypes.c_int32)]
+
+
+def make_shape(T: int, d: int, f: int, E: int, k: int, dtype, renorm: int) -> moe_shape:
+    if isinstance(dtype, torch.dtype):
+        dt = MOE_BF16 if dtype == torch.bfloat16 else MOE_F32
+    elif isinstance(dtype, str):
+        dt = MOE_BF16 if dtype == "bf16" else MOE_F32
+    else:
+        dt = int(dtype)
+    return moe_shape(int(T), int(d), int(f), int(E), int(k), dt, int(renorm))
+
+
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_SP = ctypes.POINTER(moe_shape)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            L.moe_status_string.restype = ctypes.c_char_p
+            L.moe_status_string.argtypes = [ctypes.c_int]
+            L.moe_workspace_size.restype = ctypes.c_size_t
+            L.moe_workspace_size.argtypes = [_SP]
+            L.moe_route.argtypes = [_SP, _P, _P, _P, _P, ctypes.c_int, _P, _P, _P, _P, _P, _P,
+                                    _P, _P, _P]
+            L.moe_permute.argtypes = [_SP, _P, _P, _P, _P]
+            L.moe_expert_ffn_fwd.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+            L.moe_combine_fwd.argtypes = [_SP, _P, _P, _P, _P, _P]
+            L.moe_combine_bwd.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P]
+            L.moe_expert_ffn_bwd.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                             _P, ctypes.c_int, _P, _P, _P]
+            L.moe_route_bwd.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        ctypes.c_int, _P, _P, _P]
+            L.moe_debug_bounded_wait.argtypes = [ctypes.c_uint64, _P, _P]
+            for fn in ENTRY_POINTS[2:]:
+                getattr(L, fn).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, code: int):
+    if code != MOE_OK:
+        raise MoEError(fn, code, moe_status_string(code))
+
+
+def moe_status_string(code: int) -> str:
+    return lib().moe_status_string(int(code)).decode()
+
+
+def moe_workspace_size(s: moe_shape) -> int:
+    return int(lib().moe_workspace_size(ctypes.byref(s)))
+
+
+def moe_route(s, x, Wg, logit_bias, logits, compute_logits, idx, w, counts, offsets, pos, perm,
+              ws, dev_status, stream=None):
+    _check("moe_route", lib().moe_route(
+        ctypes.byref(s), _ptr(x), _ptr(Wg), _ptr(logit_bias), _ptr(logits), int(compute_logits),
+        _ptr(idx), _ptr(w), _ptr(counts), _ptr(offsets), _ptr(pos), _ptr(perm), _ptr(ws),
+        _ptr(dev_status), _stream(stream)))
+
+
+def moe_permute(s, x, pos, x_perm, stream=None):
+    _check("moe_permute", lib().moe_permute(ctypes.byref(s), _ptr(x), _ptr(pos), _ptr(x_perm),
+                                            _stream(stream)))
+
+
+def moe_expert_ffn_fwd(s, x_perm, offsets, W1, b1, W2, b2, H, A, y_perm, ws, dev_status,
+                       stream=None):
+    _check("moe_expert_ffn_fwd", lib().moe_expert_ffn_fwd(
+        ctypes.byref(s), _ptr(x_perm), _ptr(offsets), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2),
+        _ptr(H), _ptr(A), _ptr(y_perm), _ptr(ws), _ptr(dev_status), _stream(stream)))
+
+
+def moe_combine_fwd(s, y_perm, pos, w, y, stream=None):
+    _check("moe_combine_fwd", lib().moe_combine_fwd(ctypes.byref(s), _ptr(y_perm), _ptr(pos),
+                                                    _ptr(w), _ptr(y), _stream(stream)))
+
+
+def moe_combine_bwd(s, dy, y_perm, pos, w, dy_perm, dw, stream=None):
+    _check("moe_combine_bwd", lib().moe_combine_bwd(
+        ctypes.byref(s), _ptr(dy), _ptr(y_perm), _ptr(pos), _ptr(w), _ptr(dy_perm), _ptr(dw),
+        _stream(stream)))
+
+
+def moe_expert_ffn_bwd(s, dy_perm, x_perm, H, A, offsets, W1, W2, dx_perm, dW1, db1, dW2, db2,
+                       accumulate, ws, dev_status, stream=None):
+    _check("moe_expert_ffn_bwd", lib().moe_expert_ffn_bwd(
+        ctypes.byref(s), _ptr(dy_perm), _ptr(x_perm), _ptr(H), _ptr(A), _ptr(offsets), _ptr(W1),
+        _ptr(W2), _ptr(dx_perm), _ptr(dW1), _ptr(db1), _ptr(dW2), _ptr(db2), int(accumulate),
+        _ptr(ws), _ptr(dev_status), _stream(stream)))
+
+
+def moe_route_bwd(s, dw, logits, idx, w, perm, offsets, x, Wg, dx, dWg, accumulate, ws,
+                  dev_status, stream=None):
+    _check("moe_route_bwd", lib().moe_route_bwd(
+        ctypes.byref(s), _ptr(dw), _ptr(logits), _ptr(idx), _ptr(w), _ptr(perm), _ptr(offsets),
+        _ptr(x), _ptr(Wg), _ptr(dx), _ptr(dWg), int(accumulate), _ptr(ws), _ptr(dev_status),
+        _stream(stream)))
+
+
+def moe_debug_bounded_wait(limit_ns: int, dev_status, stream=None):
+    _check("moe_debug_bounded_wait", lib().moe_debug_bounded_wait(
+        int(limit_ns), _ptr(dev_status), _stream(stream)))
