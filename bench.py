@@ -1,0 +1,364 @@
+"""Benchmark: one MoE layer forward + backward per step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+A step is one pass of the whole path over one batch of synthetic input:
+router logits, top-k gate, dispatch, permute, expert FFN, combine, and the
+backward of each (all dispatch chunks of the workload).  Inputs are resident
+in HBM before the timed region; L2 is flushed (a 256 MiB write) between
+steps, outside the per-step CUDA-event brackets.  Prints ONE JSON line on
+rank 0.
+
+Multi-GPU: the layer does not shard (one GPU per layer pass, no collective in
+the data path), so N ranks run N independent replicas; the timed region is
+bracketed by a barrier and the slowest rank's time is taken ("scaling":
+"weak").
+
+--impl reference times the CPU oracle (the plain definition of the layer, in
+double precision) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from mixture_experts_layer_11_gb300 import synth  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd tokens/s and TFLOP/s on 1 GB300; % of bf16 peak and HBM roofline"
+DEFAULT_CONFIG = "moe_s_bf16"
+L2_FLUSH_BYTES = 256 << 20
+
+# kernels each C-ABI call launches (route with logits computed)
+LAUNCHES = {"route": 4, "permute": 1, "ffn_fwd": 2, "combine": 1, "combine_bwd": 1,
+            "ffn_bwd": 8, "permute_bwd": 1, "route_bwd": 3}
+
+
+def workload_desc(cfg) -> str:
+    s = (f"{cfg.name}: T={cfg.T} d_model={cfg.d} d_ffn={cfg.f} E={cfg.E} top-{cfg.k}"
+         f"{' renorm' if cfg.renorm else ''} {cfg.dtype}")
+    if cfg.zipf_s:
+        s += f" zipf_s={cfg.zipf_s} logit shift"
+    if cfg.chunk:
+        s += f" dispatch chunks of {cfg.chunk}"
+    return s
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---- clocks sampled during the timed region ------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index: int):
+        self.proc = None
+        self.dev = dev_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = max(smax, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- CPU oracle timing ------------------------------------------------------------------
+
+def oracle_tokens_per_s(cfg, budget_s: float = 15.0, seed: int = 0):
+    """Time the oracle's full forward + backward on growing token samples of
+    the workload (same sizes d, f, E, k) until one run takes a few seconds or
+    the cumulative budget is spent.  Returns (tokens/s, sample description,
+    cores)."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    oracle.build()
+    Ts, spent, best = 64, 0.0, None
+    while True:
+        Ts = min(Ts, cfg.T)
+        sub = cfg.scaled(T=Ts, chunk=None)
+        inp = synth.make_inputs(sub, seed=seed)
+        t0 = time.perf_counter()
+        oracle.layer(inp, sub.k, sub.renorm, sub.dtype == "bf16")
+        dt = time.perf_counter() - t0
+        spent += dt
+        best = (Ts / dt, Ts, dt)
+        if dt > budget_s / 4 or Ts >= cfg.T or spent + 4 * dt > budget_s:
+            break
+        Ts *= 2
+    tps, Ts, dt = best
+    desc = (f"oracle fwd+bwd on the first {Ts} of {cfg.T} tokens (same d_model, d_ffn, E, k, "
+            f"weights drawn with the same recipe) took {dt:.2f} s; tokens/s scales linearly")
+    return tps, desc, cores
+
+
+# ---- reference arm: the oracle as the baseline implementation --------------------------
+
+def run_reference(args, cfg):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    vals, desc, cores = [], "", 1
+    budget = max(5.0, 120.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        tps, desc, cores = oracle_tokens_per_s(cfg, budget_s=budget, seed=i)
+        if i >= args.warmup:
+            vals.append(tps)
+    v = statistics.median(vals)
+    flops_per_token = (cfg.expert_flops() + cfg.router_flops()) / cfg.T
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": cfg.T / v * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "tflops": v * flops_per_token / 1e12,
+        "config": {"workload": workload_desc(cfg), "T": cfg.T},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- our arm -----------------------------------------------------------------------------
+
+def run_ours(args, cfg):
+    from mixture_experts_layer_11_gb300 import ops
+    from mixture_experts_layer_11_gb300.layer import LayerPass
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ops.lib()  # fail loudly if the library is missing
+
+    inp = synth.make_inputs(cfg, seed=rank, device=str(dev))
+    lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
+                   chunk=cfg.chunk, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def fwd(x):
+        return lp.forward(x, inp["Wg"], inp["W1"], inp["b1"], inp["W2"], inp["b2"], inp["beta"])
+
+    def bwd(x, dy):
+        return lp.backward(dy, x, inp["Wg"], inp["W1"], inp["W2"])
+
+    # ffn timing hooks: events around the expert GEMM calls on the launching stream
+    ffn_events = []
+    orig_fwd, orig_bwd = ops.moe_expert_ffn_fwd, ops.moe_expert_ffn_bwd
+
+    def timed(fn, kind):
+        def wrapper(*a, **kw):
+            if not recording[0]:
+                return fn(*a, **kw)
+            e0, e1 = ev(), ev()
+            e0.record(st)
+            r = fn(*a, **kw)
+            e1.record(st)
+            ffn_events.append((kind, e0, e1))
+            return r
+        return wrapper
+
+    recording = [False]
+    import mixture_experts_layer_11_gb300.layer as layer_mod
+    layer_mod.ops.moe_expert_ffn_fwd = timed(orig_fwd, "fwd")
+    layer_mod.ops.moe_expert_ffn_bwd = timed(orig_bwd, "bwd")
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        fwd(inp["x"])
+        bwd(inp["x"], inp["dy"])
+    torch.cuda.synchronize()
+    lp.check_status()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    recording[0] = True
+    steps = []
+    wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0, e1 = ev(), ev()
+        e0.record(st)
+        fwd(inp["x"])
+        bwd(inp["x"], inp["dy"])
+        e1.record(st)
+        steps.append((e0, e1))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    recording[0] = False
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    lp.check_status()
+    step_ms = [a.elapsed_time(b) for a, b in steps]
+    total_ms = sum(step_ms)
+    ffn_ms = {"fwd": 0.0, "bwd": 0.0}
+    n_ffn = {"fwd": 0, "bwd": 0}
+    for kind, a, b in ffn_events:
+        ffn_ms[kind] += a.elapsed_time(b)
+        n_ffn[kind] += 1
+    layer_mod.ops.moe_expert_ffn_fwd, layer_mod.ops.moe_expert_ffn_bwd = orig_fwd, orig_bwd
+
+    # ---- end to end through the public API with host buffers ----
+    x_h = inp["x"].cpu().pin_memory()
+    dy_h = inp["dy"].cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    dx_h = torch.empty_like(x_h).pin_memory()
+    x_d = torch.empty_like(inp["x"])
+    dy_d = torch.empty_like(inp["dy"])
+    e2e_steps = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        e0, e1 = ev(), ev()
+        e0.record(st)
+        x_d.copy_(x_h, non_blocking=True)
+        dy_d.copy_(dy_h, non_blocking=True)
+        y = fwd(x_d)
+        dx = bwd(x_d, dy_d)
+        y_h.copy_(y, non_blocking=True)
+        dx_h.copy_(dx, non_blocking=True)
+        e1.record(st)
+        if i >= args.warmup:
+            e2e_steps.append((e0, e1))
+    torch.cuda.synchronize()
+    lp.check_status()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_steps)
+
+    # max over ranks
+    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    tokens = cfg.T * args.steps * world
+    value = tokens / (total_ms / 1e3)
+    flops = cfg.expert_flops() + cfg.router_flops()
+    pk, pk_kind = peaks()
+    gemm_flops = cfg.expert_flops() * args.steps
+    gemm_ms = ffn_ms["fwd"] + ffn_ms["bwd"]
+    achieved = gemm_flops / (gemm_ms / 1e3) / 1e12
+    peak = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    chunks = len(lp.chunks)
+    launches = sum(LAUNCHES.values()) * chunks * args.steps
+    elem = 2 if cfg.dtype == "bf16" else 4
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg.dtype, "data": "synthetic (seeded N(0,1) inputs, N(0,1/fan_in) weights)",
+        "tflops": flops * args.steps * world / (total_ms / 1e3) / 1e12,
+        "config": {"workload": workload_desc(cfg), "T": cfg.T, "d_model": cfg.d,
+                   "d_ffn": cfg.f, "E": cfg.E, "k": cfg.k,
+                   "l2": "flushed between steps (256 MiB write, outside the step timing)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {
+            "bound": "tensor", "kernel": "grouped expert GEMM (tcgen05), all expert FFN calls",
+            "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_kind": f"bf16 dense cuBLAS, sustained ({pk_kind})",
+            "traffic": None,
+            "algorithmic_flops_per_step": cfg.expert_flops(),
+            "ffn_ms_per_step": {k: v / args.steps for k, v in ffn_ms.items()},
+        },
+        "gpu_launches": launches,
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * cfg.T * cfg.d * elem,
+                "d2h_bytes_per_step": 2 * cfg.T * cfg.d * elem},
+        "wall_s_timed_region": wall,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        tps, desc, cores = oracle_tokens_per_s(cfg)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores,
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    cfg = synth.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
