@@ -200,6 +200,15 @@ MOE_API moe_status moe_route_bwd(const moe_shape* s, const float* dw, const floa
 MOE_API moe_status moe_debug_bounded_wait(uint64_t limit_ns, int32_t* dev_status,
                                   moe_stream_t stream);
 
+/* Diagnostics: GELU(x) = x Phi(x) and GELU'(x) = Phi(x) + x phi(x) of n fp32
+ * values, as the kernels evaluate them: fast != 0 selects the approximation
+ * the bf16 expert-GEMM epilogues use (erf by Abramowitz & Stegun, "Handbook
+ * of Mathematical Functions", formula 7.1.26, |error| <= 1.5e-7), fast == 0
+ * the CUDA erff / expf form the fp32 path uses.  x, gelu, gelu_grad: [n]
+ * fp32 device arrays. */
+MOE_API moe_status moe_debug_gelu(int64_t n, const float* x, float* gelu, float* gelu_grad,
+                                  int fast, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

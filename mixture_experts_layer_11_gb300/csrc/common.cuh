@@ -51,6 +51,34 @@ __device__ __forceinline__ float gelu_grad_f(float x) {
     return Phi + x * phi;
 }
 
+// Fast GELU for bf16 outputs.  erf from the rational approximation of
+// Abramowitz & Stegun, "Handbook of Mathematical Functions" (1964), formula
+// 7.1.26: erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2),
+// t = 1 / (1 + p z), z >= 0, |error| <= 1.5e-7.  With z = |x|/sqrt(2) the
+// factor exp(-z^2) = exp(-x^2/2) is also sqrt(2 pi) phi(x), so one exponential
+// serves Phi(x) and phi(x).  Used only where the result is rounded to bf16
+// (relative spacing 2^-8), far above the approximation error.
+struct PhiFast {
+    float Phi;   // standard normal CDF at x
+    float g;     // exp(-x^2 / 2)
+};
+__device__ __forceinline__ PhiFast phi_fast(float x) {
+    const float z = fabsf(x) * 0.70710678118654752f;
+    const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
+    const float g = __expf(-0.5f * x * x);
+    const float poly =
+        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f),
+                         -0.284496736f),
+                 0.254829592f);
+    const float q = 0.5f * poly * g;  // 0.5 * (1 - erf(z)) = Phi(-|x|)
+    return {x >= 0.f ? 1.0f - q : q, g};
+}
+__device__ __forceinline__ float gelu_fast(float x) { return x * phi_fast(x).Phi; }
+__device__ __forceinline__ float gelu_grad_fast(float x) {
+    const PhiFast r = phi_fast(x);
+    return fmaf(x * 0.39894228040143268f, r.g, r.Phi);
+}
+
 // ---- shared-memory addresses and mbarriers ---------------------------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

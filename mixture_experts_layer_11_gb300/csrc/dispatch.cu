@@ -66,77 +66,89 @@ inline unsigned grid_for_rows(int64_t rows) {
     return (unsigned)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
+// Vectors per lane kept in flight: U * KMAX 16-byte loads before any use.
+template <int KMAX> struct Unroll { static constexpr int U = KMAX >= 8 ? 1 : 8 / KMAX; };
+
 // ---- A4: X_perm[pos[t,j]] = x[t] ------------------------------------------------
-// nv = row length in 16-byte vectors.
+// nv = row length in 16-byte vectors.  One warp per token row: read once,
+// written to its k positions.
+template <int KMAX>
 __global__ void __launch_bounds__(256) permute_kernel(int64_t T, int nv, int k,
                                                       const uint4* __restrict__ x,
                                                       const int32_t* __restrict__ pos,
                                                       uint4* __restrict__ xp) {
+    constexpr int U = KMAX >= 8 ? 2 : 4;
     const int lane = threadIdx.x & 31;
     const int64_t wstride = (int64_t)gridDim.x * 8;
     for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += wstride) {
-        int32_t p[kMaxK];
+        int32_t p[KMAX];
         #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) p[j] = (j < k) ? __ldg(pos + t * k + j) : 0;
+        for (int j = 0; j < KMAX; ++j) p[j] = (j < k) ? __ldg(pos + t * k + j) : 0;
         const uint4* src = x + t * nv;
-        int c = lane;
-        for (; c + 96 < nv; c += 128) {
-            const uint4 v0 = ldg16(src + c), v1 = ldg16(src + c + 32), v2 = ldg16(src + c + 64),
-                        v3 = ldg16(src + c + 96);
+        for (int c0 = lane; c0 < nv; c0 += 32 * U) {
+            uint4 v[U];
             #pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
-                if (j >= k) break;
-                uint4* dst = xp + (int64_t)p[j] * nv + c;
-                dst[0] = v0; dst[32] = v1; dst[64] = v2; dst[96] = v3;
-            }
-        }
-        for (; c < nv; c += 32) {
-            const uint4 v = ldg16(src + c);
+            for (int u = 0; u < U; ++u)
+                if (c0 + 32 * u < nv) v[u] = ldg16(src + c0 + 32 * u);
             #pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
+            for (int j = 0; j < KMAX; ++j) {
                 if (j >= k) break;
-                xp[(int64_t)p[j] * nv + c] = v;
+                uint4* dst = xp + (int64_t)p[j] * nv + c0;
+                #pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (c0 + 32 * u < nv) dst[32 * u] = v[u];
             }
         }
     }
 }
 
 // ---- A6 / A9: y[t] = sum_j w[t,j] Y[pos[t,j]] (w == null: weights 1) -------------
-template <typename T>
+template <typename T, int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(int64_t Tn, int nv, int k,
                                                       const uint4* __restrict__ Y,
                                                       const int32_t* __restrict__ pos,
                                                       const float* __restrict__ w,
                                                       uint4* __restrict__ y) {
     using V = V16<T>;
+    constexpr int U = Unroll<KMAX>::U;
     const int lane = threadIdx.x & 31;
     const int64_t wstride = (int64_t)gridDim.x * 8;
     for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < Tn; t += wstride) {
-        int32_t p[kMaxK];
-        float wj[kMaxK];
+        int32_t p[KMAX];
+        float wj[KMAX];
         #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
+        for (int j = 0; j < KMAX; ++j) {
             p[j] = (j < k) ? __ldg(pos + t * k + j) : 0;
             wj[j] = (j < k) ? (w ? __ldg(w + t * k + j) : 1.f) : 0.f;
         }
-        for (int c = lane; c < nv; c += 32) {
-            float acc[V::N], v[V::N];
+        for (int c0 = lane; c0 < nv; c0 += 32 * U) {
+            uint4 r[U][KMAX];
             #pragma unroll
-            for (int u = 0; u < V::N; ++u) acc[u] = 0.f;
-            #pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
-                if (j >= k) break;
-                V::unpack(ldg16(Y + (int64_t)p[j] * nv + c), v);
+            for (int u = 0; u < U; ++u)
                 #pragma unroll
-                for (int u = 0; u < V::N; ++u) acc[u] = fmaf(wj[j], v[u], acc[u]);
+                for (int j = 0; j < KMAX; ++j)
+                    if (j < k && c0 + 32 * u < nv) r[u][j] = ldg16(Y + (int64_t)p[j] * nv + c0 + 32 * u);
+            #pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (c0 + 32 * u >= nv) break;
+                float acc[V::N], v[V::N];
+                #pragma unroll
+                for (int e = 0; e < V::N; ++e) acc[e] = 0.f;
+                #pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j >= k) break;
+                    V::unpack(r[u][j], v);
+                    #pragma unroll
+                    for (int e = 0; e < V::N; ++e) acc[e] = fmaf(wj[j], v[e], acc[e]);
+                }
+                stg16(y + t * nv + c0 + 32 * u, V::pack(acc));
             }
-            stg16(y + t * nv + c, V::pack(acc));
         }
     }
 }
 
 // ---- A7: dY[pos[t,j]] = w[t,j] dy[t];  dw[t,j] = <dy[t], Y[pos[t,j]]> -------------
-template <typename T>
+template <typename T, int KMAX>
 __global__ void __launch_bounds__(256) combine_bwd_kernel(int64_t Tn, int nv, int k,
                                                           const uint4* __restrict__ dy,
                                                           const uint4* __restrict__ Y,
@@ -145,34 +157,47 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int64_t Tn, int nv, in
                                                           uint4* __restrict__ dY,
                                                           float* __restrict__ dw) {
     using V = V16<T>;
+    constexpr int U = Unroll<KMAX>::U;
     const int lane = threadIdx.x & 31;
     const int64_t wstride = (int64_t)gridDim.x * 8;
     for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < Tn; t += wstride) {
-        int32_t p[kMaxK];
-        float wj[kMaxK], part[kMaxK];
+        int32_t p[KMAX];
+        float wj[KMAX], part[KMAX];
         #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
+        for (int j = 0; j < KMAX; ++j) {
             p[j] = (j < k) ? __ldg(pos + t * k + j) : 0;
             wj[j] = (j < k) ? __ldg(w + t * k + j) : 0.f;
             part[j] = 0.f;
         }
-        for (int c = lane; c < nv; c += 32) {
-            float g[V::N], v[V::N], o[V::N];
-            V::unpack(ldg16(dy + t * nv + c), g);
+        for (int c0 = lane; c0 < nv; c0 += 32 * U) {
+            uint4 gr[U], r[U][KMAX];
             #pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
-                if (j >= k) break;
-                V::unpack(ldg16(Y + (int64_t)p[j] * nv + c), v);
+            for (int u = 0; u < U; ++u) {
+                if (c0 + 32 * u < nv) gr[u] = ldg16(dy + t * nv + c0 + 32 * u);
                 #pragma unroll
-                for (int u = 0; u < V::N; ++u) {
-                    part[j] = fmaf(g[u], v[u], part[j]);
-                    o[u] = wj[j] * g[u];
+                for (int j = 0; j < KMAX; ++j)
+                    if (j < k && c0 + 32 * u < nv) r[u][j] = ldg16(Y + (int64_t)p[j] * nv + c0 + 32 * u);
+            }
+            #pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (c0 + 32 * u >= nv) break;
+                float g[V::N], v[V::N], o[V::N];
+                V::unpack(gr[u], g);
+                #pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j >= k) break;
+                    V::unpack(r[u][j], v);
+                    #pragma unroll
+                    for (int e = 0; e < V::N; ++e) {
+                        part[j] = fmaf(g[e], v[e], part[j]);
+                        o[e] = wj[j] * g[e];
+                    }
+                    stg16(dY + (int64_t)p[j] * nv + c0 + 32 * u, V::pack(o));
                 }
-                stg16(dY + (int64_t)p[j] * nv + c, V::pack(o));
             }
         }
         #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
+        for (int j = 0; j < KMAX; ++j) {
             if (j >= k) break;
             float s = part[j];
             #pragma unroll
@@ -206,7 +231,19 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(int n, int E,
     float a[V::N], v[V::N];
     #pragma unroll
     for (int u = 0; u < V::N; ++u) a[u] = 0.f;
-    for (int p = p0; p < p1; ++p) {
+    int p = p0;
+    for (; p + 8 <= p1; p += 8) {       // 8 loads in flight, summed in row order
+        uint4 r[8];
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) r[q] = ldg16(g + (int64_t)(p + q) * n + c);
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            V::unpack(r[q], v);
+            #pragma unroll
+            for (int u = 0; u < V::N; ++u) a[u] += v[u];
+        }
+    }
+    for (; p < p1; ++p) {
         V::unpack(ldg16(g + (int64_t)p * n + c), v);
         #pragma unroll
         for (int u = 0; u < V::N; ++u) a[u] += v[u];
@@ -237,41 +274,68 @@ __global__ void __launch_bounds__(256) colsum_reduce_kernel(int n, int E,
     *o = accumulate ? *o + s : s;
 }
 
+
+template <template <int> class F, typename... Args>
+cudaError_t by_k(int k, Args... args) {
+    if (k <= 1) return F<1>::run(args...);
+    if (k <= 2) return F<2>::run(args...);
+    if (k <= 4) return F<4>::run(args...);
+    if (k <= 8) return F<8>::run(args...);
+    return F<16>::run(args...);
+}
+
+template <int KM> struct PermuteL {
+    static cudaError_t run(const moe_shape& s, const void* x, const int32_t* pos, void* xp,
+                           cudaStream_t st) {
+        const int esz = s.dtype == MOE_BF16 ? 2 : 4;
+        permute_kernel<KM><<<grid_for_rows(s.T), 256, 0, st>>>(s.T, s.d * esz / 16, s.k,
+                                                               (const uint4*)x, pos, (uint4*)xp);
+        return cudaGetLastError();
+    }
+};
+template <int KM> struct CombineL {
+    static cudaError_t run(const moe_shape& s, const void* Y, const int32_t* pos, const float* w,
+                           void* y, cudaStream_t st) {
+        const unsigned g = grid_for_rows(s.T);
+        if (s.dtype == MOE_BF16)
+            combine_kernel<__nv_bfloat16, KM><<<g, 256, 0, st>>>(s.T, s.d / 8, s.k, (const uint4*)Y,
+                                                                 pos, w, (uint4*)y);
+        else
+            combine_kernel<float, KM><<<g, 256, 0, st>>>(s.T, s.d / 4, s.k, (const uint4*)Y, pos,
+                                                         w, (uint4*)y);
+        return cudaGetLastError();
+    }
+};
+template <int KM> struct CombineBwdL {
+    static cudaError_t run(const moe_shape& s, const void* dy, const void* Y, const int32_t* pos,
+                           const float* w, void* dY, float* dw, cudaStream_t st) {
+        const unsigned g = grid_for_rows(s.T);
+        if (s.dtype == MOE_BF16)
+            combine_bwd_kernel<__nv_bfloat16, KM><<<g, 256, 0, st>>>(
+                s.T, s.d / 8, s.k, (const uint4*)dy, (const uint4*)Y, pos, w, (uint4*)dY, dw);
+        else
+            combine_bwd_kernel<float, KM><<<g, 256, 0, st>>>(
+                s.T, s.d / 4, s.k, (const uint4*)dy, (const uint4*)Y, pos, w, (uint4*)dY, dw);
+        return cudaGetLastError();
+    }
+};
+
 }  // namespace
 
 cudaError_t launch_permute(const moe_shape& s, const void* x, const int32_t* pos, void* x_perm,
                            cudaStream_t st) {
-    const int esz = s.dtype == MOE_BF16 ? 2 : 4;
-    const int nv = s.d * esz / 16;
-    permute_kernel<<<grid_for_rows(s.T), 256, 0, st>>>(s.T, nv, s.k, (const uint4*)x, pos,
-                                                       (uint4*)x_perm);
-    return cudaGetLastError();
+    return by_k<PermuteL>(s.k, s, x, pos, x_perm, st);
 }
 
 cudaError_t launch_combine(const moe_shape& s, const void* y_perm, const int32_t* pos,
                            const float* w, void* y, cudaStream_t st) {
-    const unsigned g = grid_for_rows(s.T);
-    if (s.dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(s.T, s.d / 8, s.k, (const uint4*)y_perm,
-                                                          pos, w, (uint4*)y);
-    else
-        combine_kernel<float><<<g, 256, 0, st>>>(s.T, s.d / 4, s.k, (const uint4*)y_perm, pos, w,
-                                                  (uint4*)y);
-    return cudaGetLastError();
+    return by_k<CombineL>(s.k, s, y_perm, pos, w, y, st);
 }
 
 cudaError_t launch_combine_bwd(const moe_shape& s, const void* dy, const void* y_perm,
                                const int32_t* pos, const float* w, void* dy_perm, float* dw,
                                cudaStream_t st) {
-    const unsigned g = grid_for_rows(s.T);
-    if (s.dtype == MOE_BF16)
-        combine_bwd_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(
-            s.T, s.d / 8, s.k, (const uint4*)dy, (const uint4*)y_perm, pos, w, (uint4*)dy_perm, dw);
-    else
-        combine_bwd_kernel<float><<<g, 256, 0, st>>>(s.T, s.d / 4, s.k, (const uint4*)dy,
-                                                      (const uint4*)y_perm, pos, w,
-                                                      (uint4*)dy_perm, dw);
-    return cudaGetLastError();
+    return by_k<CombineBwdL>(s.k, s, dy, y_perm, pos, w, dy_perm, dw, st);
 }
 
 size_t segment_colsum_workspace(const moe_shape& s, int n) {

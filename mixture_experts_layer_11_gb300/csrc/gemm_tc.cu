@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         __syncwarp();
                         if (EPI == (int)Epi::BiasGelu) {
                             #pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+                            for (int i = 0; i < 32; ++i) v[i] = gelu_fast(v[i]);
                             stage_row_bf16(stg, lane, v);
                             __syncwarp();
                             store_tile_bf16(stg, lane, (__nv_bfloat16*)p.out1, grow0, valid, N, col0);
@@ -445,8 +445,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const float2 f = __bfloat1622float2(h[i]);
-                                v[cc * 8 + 2 * i] *= gelu_grad_f(f.x);
-                                v[cc * 8 + 2 * i + 1] *= gelu_grad_f(f.y);
+                                v[cc * 8 + 2 * i] *= gelu_grad_fast(f.x);
+                                v[cc * 8 + 2 * i + 1] *= gelu_grad_fast(f.y);
                             }
                         }
                         __syncwarp();

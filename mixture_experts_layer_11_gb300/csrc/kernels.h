@@ -21,13 +21,11 @@ inline int64_t route_blocks(int64_t T) { return (T + kRouteBlockTokens - 1) / kR
 uint64_t wait_limit_ns();
 int device_sm_count();
 
-// A1
-cudaError_t launch_router_logits(const moe_shape& s, const void* x, const void* Wg,
-                                 const float* beta, float* logits, cudaStream_t st);
-// A2 + per-block histogram (block_counts laid out [E][nblk])
-cudaError_t launch_gate_hist(const moe_shape& s, const float* logits, int32_t* idx,
-                             float* w, int32_t* block_counts, int32_t* status,
-                             cudaStream_t st);
+// A1 (when compute_logits) + A2 + per-block histogram (block_counts laid out
+// [E][nblk]).  E <= 32 fuses all three in one kernel.
+cudaError_t launch_route_gate(const moe_shape& s, const void* x, const void* Wg,
+                             const float* beta, float* logits, int compute_logits, int32_t* idx,
+                             float* w, int32_t* block_counts, int32_t* status, cudaStream_t st);
 // A3 scan: block_counts -> block_base in place, counts, offsets
 cudaError_t launch_dispatch_scan(const moe_shape& s, int32_t* block_counts,
                                  int32_t* counts, int32_t* offsets, cudaStream_t st);
@@ -94,5 +92,7 @@ cudaError_t launch_gemm_vark_simt(const GemmVarK& g, cudaStream_t st);
 
 // Diagnostics
 cudaError_t launch_bounded_wait(uint64_t limit_ns, int32_t* status, cudaStream_t st);
+cudaError_t launch_debug_gelu(int64_t n, const float* x, float* g, float* gd, int fast,
+                              cudaStream_t st);
 
 }  // namespace moe

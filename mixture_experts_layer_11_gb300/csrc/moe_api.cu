@@ -128,10 +128,9 @@ moe_status moe_route(const moe_shape* s, const void* x, const void* Wg, const fl
     cudaStream_t st = (cudaStream_t)stream;
     int32_t* block_counts = (int32_t*)ws;
     cudaError_t e = cudaSuccess;
-    if (s->T > 0) {
-        if (compute_logits) e = launch_router_logits(*s, x, Wg, logit_bias, logits, st);
-        if (e == cudaSuccess) e = launch_gate_hist(*s, logits, idx, w, block_counts, dev_status, st);
-    }
+    if (s->T > 0)
+        e = launch_route_gate(*s, x, Wg, logit_bias, logits, compute_logits, idx, w, block_counts,
+                              dev_status, st);
     if (e == cudaSuccess) e = launch_dispatch_scan(*s, block_counts, counts, offsets, st);
     if (e == cudaSuccess && s->T > 0) e = launch_dispatch_rank(*s, idx, block_counts, pos, perm, st);
     return cuda_status(e);
@@ -266,6 +265,14 @@ moe_status moe_route_bwd(const moe_shape* s, const float* dw, const float* logit
 moe_status moe_debug_bounded_wait(uint64_t limit_ns, int32_t* dev_status, moe_stream_t stream) {
     if (dev_status == nullptr || !ok_status(dev_status)) return MOE_ERR_INVALID;
     return cuda_status(launch_bounded_wait(limit_ns, dev_status, (cudaStream_t)stream));
+}
+
+moe_status moe_debug_gelu(int64_t n, const float* x, float* gelu, float* gelu_grad, int fast,
+                          moe_stream_t stream) {
+    if (n < 0) return MOE_ERR_INVALID;
+    if (n == 0) return MOE_OK;
+    if (!ok_ptr(x) || !ok_ptr(gelu) || !ok_ptr(gelu_grad)) return MOE_ERR_INVALID;
+    return cuda_status(launch_debug_gelu(n, x, gelu, gelu_grad, fast, (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -70,69 +70,128 @@ template <> struct Vec<float> {
     }
 };
 
-// ---- A1: router logits, SIMT GEMM with fp32 accumulation ------------------------
+// ---- A1: router logits for many experts: register-tiled SIMT GEMM ------------------
 //
-// logits[t][e] = sum_c x[t][c] Wg[e][c] + beta[e].  Block tile BM tokens x BN
-// experts, K staged through shared memory 32 at a time; thread (tx, ty) owns
-// tokens ty + NTY*i and experts tx + NTX*j (interleaved: conflict-free shared
-// reads, coalesced stores).
+// logits[t][e] = sum_c x[t][c] Wg[e][c] + beta[e] with fp32 accumulation on the
+// CUDA cores.  Block tile 128 tokens x BN experts, K in steps of 16 through
+// double-buffered shared memory (fp32, K-major so that a thread reads 4
+// consecutive rows / columns as one float4); each of the 256 threads owns an
+// 8 x (BN/16) register tile: rows ty*4+i and 64+ty*4+i, columns tx*4+j (and
+// 64+tx*4+j when BN = 128).  Summation over K runs in index order.
 
-template <typename TIn, int BM, int BN, int TM, int TN>
-__global__ void __launch_bounds__(256) router_logits_kernel(
+template <typename TIn, int BN>
+__global__ void __launch_bounds__(256, 2) router_logits_tiled_kernel(
     int64_t T, int d, int E, const TIn* __restrict__ x, const TIn* __restrict__ Wg,
     const float* __restrict__ beta, float* __restrict__ logits) {
-    constexpr int BK = 32;
-    constexpr int NTX = BN / TN;
-    constexpr int NTY = BM / TM;
-    static_assert(NTX * NTY == 256, "256 threads");
-    __shared__ float xs[BK][BM + 1];
-    __shared__ float ws[BK][BN + 1];
+    constexpr int BM = 128, BK = 16;
+    constexpr int TN = BN / 16;          // 8 or 4 columns per thread
+    constexpr int VN = Vec<TIn>::N;      // elements per 16-byte load
+    constexpr int LA = BM * BK / VN / 256;  // 16-byte loads per thread per tile
+    constexpr int LB = BN * BK / VN / 256 > 0 ? BN * BK / VN / 256 : 1;
+    __shared__ __align__(16) float As[2][BK][BM];
+    __shared__ __align__(16) float Bs[2][BK][BN];
     const int tid = threadIdx.x;
-    const int tx = tid % NTX, ty = tid / NTX;
+    const int tx = tid & 15, ty = tid >> 4;
     const int64_t m0 = (int64_t)blockIdx.x * BM;
     const int n0 = blockIdx.y * BN;
-    float acc[TM][TN];
+    constexpr int CPR = BK / VN;         // 16-byte chunks per row of a tile
+
+    float ra[LA][VN], rb[LB][VN];
+    auto load_tiles = [&](int k0) {
+        #pragma unroll
+        for (int l = 0; l < LA; ++l) {
+            const int i = tid + 256 * l;
+            const int r = i / CPR, c = (i % CPR) * VN;
+            const int64_t gm = m0 + r;
+            if (gm < T && k0 + c < d) Vec<TIn>::load(x + gm * d + k0 + c, ra[l]);
+            else
+                #pragma unroll
+                for (int u = 0; u < VN; ++u) ra[l][u] = 0.f;
+        }
+        #pragma unroll
+        for (int l = 0; l < LB; ++l) {
+            const int i = tid + 256 * l;
+            const int r = i / CPR, c = (i % CPR) * VN;
+            const int gn = n0 + r;
+            if (r < BN && gn < E && k0 + c < d) Vec<TIn>::load(Wg + (int64_t)gn * d + k0 + c, rb[l]);
+            else
+                #pragma unroll
+                for (int u = 0; u < VN; ++u) rb[l][u] = 0.f;
+        }
+    };
+    auto store_tiles = [&](int buf) {
+        #pragma unroll
+        for (int l = 0; l < LA; ++l) {
+            const int i = tid + 256 * l;
+            const int r = i / CPR, c = (i % CPR) * VN;
+            #pragma unroll
+            for (int u = 0; u < VN; ++u) As[buf][c + u][r] = ra[l][u];
+        }
+        #pragma unroll
+        for (int l = 0; l < LB; ++l) {
+            const int i = tid + 256 * l;
+            const int r = i / CPR, c = (i % CPR) * VN;
+            if (r < BN)
+                #pragma unroll
+                for (int u = 0; u < VN; ++u) Bs[buf][c + u][r] = rb[l][u];
+        }
+    };
+
+    float acc[8][TN];
     #pragma unroll
-    for (int i = 0; i < TM; ++i)
+    for (int i = 0; i < 8; ++i)
         #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
+    load_tiles(0);
+    store_tiles(0);
+    __syncthreads();
+    int buf = 0;
     for (int k0 = 0; k0 < d; k0 += BK) {
-        for (int i = tid; i < BM * BK; i += 256) {
-            const int r = i / BK, c = i % BK;
-            const int64_t gm = m0 + r;
-            const int gk = k0 + c;
-            xs[c][r] = (gm < T && gk < d) ? to_f32(x[gm * d + gk]) : 0.f;
-        }
-        for (int i = tid; i < BN * BK; i += 256) {
-            const int r = i / BK, c = i % BK;
-            const int gn = n0 + r;
-            const int gk = k0 + c;
-            ws[c][r] = (gn < E && gk < d) ? to_f32(Wg[(int64_t)gn * d + gk]) : 0.f;
-        }
-        __syncthreads();
-        #pragma unroll 4
+        const bool more = k0 + BK < d;
+        if (more) load_tiles(k0 + BK);
+        #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
-            float a[TM], b[TN];
+            float a[8], b[TN];
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+            a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
+            a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+            b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+            if (TN == 8) {
+                const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
+                b[TN - 4] = b1.x; b[TN - 3] = b1.y; b[TN - 2] = b1.z; b[TN - 1] = b1.w;
+            }
             #pragma unroll
-            for (int i = 0; i < TM; ++i) a[i] = xs[kk][ty + NTY * i];
-            #pragma unroll
-            for (int j = 0; j < TN; ++j) b[j] = ws[kk][tx + NTX * j];
-            #pragma unroll
-            for (int i = 0; i < TM; ++i)
+            for (int i = 0; i < 8; ++i)
                 #pragma unroll
                 for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
-        __syncthreads();
+        if (more) {
+            store_tiles(buf ^ 1);
+            __syncthreads();
+            buf ^= 1;
+        }
     }
     #pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        const int64_t t = m0 + ty + NTY * i;
+    for (int i = 0; i < 8; ++i) {
+        const int64_t t = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
         if (t >= T) continue;
         #pragma unroll
-        for (int j = 0; j < TN; ++j) {
-            const int e = n0 + tx + NTX * j;
-            if (e < E) logits[t * E + e] = acc[i][j] + (beta ? beta[e] : 0.f);
+        for (int jj = 0; jj < TN; jj += 4) {
+            const int e0 = n0 + (jj < 4 ? tx * 4 : 64 + tx * 4);
+            float o[4];
+            #pragma unroll
+            for (int j = 0; j < 4; ++j)
+                o[j] = acc[i][jj + j] + ((beta && e0 + j < E) ? beta[e0 + j] : 0.f);
+            if ((E & 3) == 0 && e0 + 3 < E) {
+                *reinterpret_cast<float4*>(logits + t * E + e0) = make_float4(o[0], o[1], o[2], o[3]);
+            } else {
+                #pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (e0 + j < E) logits[t * E + e0 + j] = o[j];
+            }
         }
     }
 }
@@ -141,19 +200,13 @@ template <typename TIn>
 cudaError_t router_logits_dispatch(const moe_shape& s, const TIn* x, const TIn* Wg,
                                    const float* beta, float* logits, cudaStream_t st) {
     const int64_t T = s.T;
-    if (s.E <= 16) {
-        dim3 grid((unsigned)((T + 255) / 256), 1);
-        router_logits_kernel<TIn, 256, 16, 16, 1><<<grid, 256, 0, st>>>(T, s.d, s.E, x, Wg, beta, logits);
-    } else if (s.E <= 32) {
-        dim3 grid((unsigned)((T + 127) / 128), 1);
-        router_logits_kernel<TIn, 128, 32, 8, 2><<<grid, 256, 0, st>>>(T, s.d, s.E, x, Wg, beta, logits);
-    } else if (s.E <= 64) {
-        dim3 grid((unsigned)((T + 127) / 128), 1);
-        router_logits_kernel<TIn, 128, 64, 8, 4><<<grid, 256, 0, st>>>(T, s.d, s.E, x, Wg, beta, logits);
-    } else {
-        dim3 grid((unsigned)((T + 63) / 64), (unsigned)((s.E + 127) / 128));
-        router_logits_kernel<TIn, 64, 128, 4, 8><<<grid, 256, 0, st>>>(T, s.d, s.E, x, Wg, beta, logits);
-    }
+    const unsigned gx = (unsigned)((T + 127) / 128);
+    if (s.E <= 64)
+        router_logits_tiled_kernel<TIn, 64><<<dim3(gx, (s.E + 63) / 64), 256, 0, st>>>(
+            T, s.d, s.E, x, Wg, beta, logits);
+    else
+        router_logits_tiled_kernel<TIn, 128><<<dim3(gx, (s.E + 127) / 128), 256, 0, st>>>(
+            T, s.d, s.E, x, Wg, beta, logits);
     return cudaGetLastError();
 }
 
@@ -162,88 +215,197 @@ cudaError_t router_logits_dispatch(const moe_shape& s, const TIn* x, const TIn* 
 // One warp per token; lane l holds logits of experts l, l+32, ...  Top-k by k
 // rounds of a warp arg-max on (logit desc, expert index asc).  A NaN logit is
 // ranked below every number (so k distinct valid experts are always chosen)
-// and, like an infinite one, raises MOE_ERR_NONFINITE.
+// and, like an infinite one, raises MOE_ERR_NONFINITE.  Blocks hold 256 tokens
+// (the bitmask histogram) and 32 warps, 8 tokens per warp.
 
 template <int EPL>
-__global__ void __launch_bounds__(256) gate_hist_kernel(
-    int64_t T, int E, int k, int renorm, int nblk, const float* __restrict__ logits,
-    int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ block_counts,
-    int32_t* status) {
-    __shared__ uint32_t bits[256][8];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < E * 8; i += 256) bits[i >> 3][i & 7] = 0u;
-    __syncthreads();
+__device__ __forceinline__ void gate_token(int64_t t, int E, int k, int renorm, float (&L)[EPL],
+                                           int lane, int tok, uint32_t (*bits)[8],
+                                           int32_t* __restrict__ idx, float* __restrict__ w,
+                                           int32_t* status) {
+    bool bad = false;
+    #pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+        const int e = lane + 32 * q;
+        if (e < E) {
+            if (!isfinite(L[q])) bad = true;
+            if (isnan(L[q])) L[q] = -INFINITY;
+        } else {
+            L[q] = -INFINITY;
+        }
+    }
+    if (__any_sync(kFull, bad) && lane == 0) report(status, MOE_ERR_NONFINITE);
+    float m = L[0];
+    #pragma unroll
+    for (int q = 1; q < EPL; ++q) m = fmaxf(m, L[q]);
+    m = warp_max(m);
+    float z = 0.f;
+    #pragma unroll
+    for (int q = 0; q < EPL; ++q)
+        if (lane + 32 * q < E) z += expf(L[q] - m);
+    z = warp_sum(z);
 
-    const int64_t tbase = (int64_t)blockIdx.x * kRouteBlockTokens + warp * 32;
-    for (int tt = 0; tt < 32; ++tt) {
-        const int64_t t = tbase + tt;
-        if (t >= T) break;
-        float L[EPL];
-        bool bad = false;
+    uint32_t taken = 0u;
+    int my_e = 0;
+    float my_p = 0.f, psum = 0.f;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int be = INT_MAX;
         #pragma unroll
         for (int q = 0; q < EPL; ++q) {
             const int e = lane + 32 * q;
-            float v = -INFINITY;
-            if (e < E) {
-                v = logits[t * E + e];
-                if (!isfinite(v)) bad = true;
-                if (isnan(v)) v = -INFINITY;
+            if (e < E && !((taken >> q) & 1u) && (be == INT_MAX || L[q] > bv)) {
+                bv = L[q];
+                be = e;
             }
-            L[q] = v;
         }
-        if (__any_sync(kFull, bad) && lane == 0) report(status, MOE_ERR_NONFINITE);
-        float m = L[0];
         #pragma unroll
-        for (int q = 1; q < EPL; ++q) m = fmaxf(m, L[q]);
-        m = warp_max(m);
-        float z = 0.f;
-        #pragma unroll
-        for (int q = 0; q < EPL; ++q)
-            if (lane + 32 * q < E) z += expf(L[q] - m);
-        z = warp_sum(z);
-
-        uint32_t taken = 0u;
-        int my_e = 0;
-        float my_p = 0.f, psum = 0.f;
-        for (int j = 0; j < k; ++j) {
-            float bv = -INFINITY;
-            int be = INT_MAX;
-            #pragma unroll
-            for (int q = 0; q < EPL; ++q) {
-                const int e = lane + 32 * q;
-                if (e < E && !((taken >> q) & 1u) && (be == INT_MAX || L[q] > bv)) {
-                    bv = L[q];
-                    be = e;
-                }
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(kFull, bv, o);
+            const int oe = __shfl_xor_sync(kFull, be, o);
+            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
             }
-            #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(kFull, bv, o);
-                const int oe = __shfl_xor_sync(kFull, be, o);
-                if (oe != INT_MAX &&
-                    (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            const float p = expf(bv - m) / z;
-            if (lane == j) { my_e = be; my_p = p; }
-            psum += p;
-            if (lane == 0) bits[be][warp] |= 1u << tt;
         }
-        if (lane < k) {
-            idx[t * k + lane] = my_e;
-            w[t * k + lane] = renorm ? my_p / psum : my_p;
-        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        const float p = expf(bv - m) / z;
+        if (lane == j) { my_e = be; my_p = p; }
+        psum += p;
+        if (lane == 0) atomicOr(&bits[be][tok >> 5], 1u << (tok & 31));
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += 256) {
+    if (lane < k) {
+        idx[t * k + lane] = my_e;
+        w[t * k + lane] = renorm ? my_p / psum : my_p;
+    }
+}
+
+__device__ __forceinline__ void zero_bits(uint32_t (*bits)[8], int E) {
+    for (int i = threadIdx.x; i < E * 8; i += blockDim.x) bits[i >> 3][i & 7] = 0u;
+}
+
+__device__ __forceinline__ void write_block_counts(uint32_t (*bits)[8], int E, int nblk,
+                                                   int32_t* block_counts) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int c = 0;
         #pragma unroll
         for (int q = 0; q < 8; ++q) c += __popc(bits[e][q]);
         block_counts[(int64_t)e * nblk + blockIdx.x] = c;
     }
+}
+
+// Gate on logits already in memory (given, or from the tiled GEMM).
+template <int EPL>
+__global__ void __launch_bounds__(1024) gate_hist_kernel(
+    int64_t T, int E, int k, int renorm, int nblk, const float* __restrict__ logits,
+    int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ block_counts,
+    int32_t* status) {
+    __shared__ uint32_t bits[256][8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    zero_bits(bits, E);
+    __syncthreads();
+    for (int tt = 0; tt < 8; ++tt) {
+        const int tok = warp * 8 + tt;
+        const int64_t t = (int64_t)blockIdx.x * kRouteBlockTokens + tok;
+        if (t >= T) break;
+        float L[EPL];
+        #pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+            const int e = lane + 32 * q;
+            L[q] = (e < E) ? logits[t * E + e] : -INFINITY;
+        }
+        gate_token<EPL>(t, E, k, renorm, L, lane, tok, bits, idx, w, status);
+    }
+    __syncthreads();
+    write_block_counts(bits, E, nblk, block_counts);
+}
+
+// Few experts (E <= 32): router logits, gate and histogram fused, one warp per
+// token.  Each lane accumulates EP (= E rounded up to a power of two) partial
+// dot products over its share of the row (16-byte loads of x and Wg, Wg
+// staying in L1), then a reduce-scatter across the warp leaves expert e's sum
+// in lanes e*32/EP ... e*32/EP + 32/EP - 1.
+template <int EP>
+__device__ __forceinline__ float reduce_scatter(float (&v)[EP], int lane) {
+    #pragma unroll
+    for (int half = EP / 2, off = 16; half >= 1; half >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+        #pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFull, send, off);
+        }
+    }
+    float r = v[0];
+    #pragma unroll
+    for (int o = 16 / EP; o >= 1; o >>= 1) r += __shfl_xor_sync(kFull, r, o);
+    return r;
+}
+
+template <typename TIn, int EP>
+__global__ void __launch_bounds__(1024) router_gate_small_kernel(
+    int64_t T, int d, int E, int k, int renorm, int nblk, const TIn* __restrict__ x,
+    const TIn* __restrict__ Wg, const float* __restrict__ beta, float* __restrict__ logits,
+    int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ block_counts,
+    int32_t* status) {
+    using V = Vec<TIn>;
+    __shared__ uint32_t bits[256][8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    zero_bits(bits, E);
+    __syncthreads();
+    const int nv = d / V::N;
+    for (int tt = 0; tt < 8; ++tt) {
+        const int tok = warp * 8 + tt;
+        const int64_t t = (int64_t)blockIdx.x * kRouteBlockTokens + tok;
+        if (t >= T) break;
+        float acc[EP];
+        #pragma unroll
+        for (int e = 0; e < EP; ++e) acc[e] = 0.f;
+        for (int c = lane; c < nv; c += 32) {
+            float xv[V::N], wv[V::N];
+            V::load(x + t * d + (int64_t)c * V::N, xv);
+            #pragma unroll
+            for (int e = 0; e < EP; ++e) {
+                if (e < E) {
+                    V::load(Wg + (int64_t)e * d + (int64_t)c * V::N, wv);
+                    #pragma unroll
+                    for (int u = 0; u < V::N; ++u) acc[e] = fmaf(xv[u], wv[u], acc[e]);
+                }
+            }
+        }
+        const float r = reduce_scatter<EP>(acc, lane);
+        // lane e (< E) takes expert e's sum
+        const float le = __shfl_sync(kFull, r, (lane % EP) * (32 / EP));
+        float L[1];
+        L[0] = -INFINITY;
+        if (lane < E) {
+            L[0] = le + (beta ? beta[lane] : 0.f);
+            logits[t * E + lane] = L[0];
+        }
+        gate_token<1>(t, E, k, renorm, L, lane, tok, bits, idx, w, status);
+    }
+    __syncthreads();
+    write_block_counts(bits, E, nblk, block_counts);
+}
+
+template <typename TIn>
+cudaError_t router_gate_small(const moe_shape& s, const TIn* x, const TIn* Wg, const float* beta,
+                              float* logits, int32_t* idx, float* w, int32_t* block_counts,
+                              int32_t* status, cudaStream_t st) {
+    const int nblk = (int)route_blocks(s.T);
+#define MOE_SMALL(EPV)                                                                        \
+    router_gate_small_kernel<TIn, EPV><<<nblk, 1024, 0, st>>>(s.T, s.d, s.E, s.k, s.renorm,  \
+                                                              nblk, x, Wg, beta, logits, idx, \
+                                                              w, block_counts, status)
+    if (s.E <= 1) MOE_SMALL(1);
+    else if (s.E <= 2) MOE_SMALL(2);
+    else if (s.E <= 4) MOE_SMALL(4);
+    else if (s.E <= 8) MOE_SMALL(8);
+    else if (s.E <= 16) MOE_SMALL(16);
+    else MOE_SMALL(32);
+#undef MOE_SMALL
+    return cudaGetLastError();
 }
 
 // ---- A3: scan of the expert-major (expert, block) histogram ---------------------
@@ -449,7 +611,23 @@ __global__ void __launch_bounds__(256) dwg_partial_sparse_kernel(
     float a[VN], xv[VN];
     #pragma unroll
     for (int u = 0; u < VN; ++u) a[u] = 0.f;
-    for (int p = p0; p < p1; ++p) {
+    int p = p0;
+    for (; p + 4 <= p1; p += 4) {       // 4 rows in flight, summed in segment order
+        int sl[4];
+        float g[4], xr[4][VN];
+        #pragma unroll
+        for (int q = 0; q < 4; ++q) sl[q] = perm[p + q];
+        #pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            g[q] = dLsel[sl[q]];
+            V::load(x + (int64_t)(sl[q] / k) * d + c, xr[q]);
+        }
+        #pragma unroll
+        for (int q = 0; q < 4; ++q)
+            #pragma unroll
+            for (int u = 0; u < VN; ++u) a[u] = fmaf(g[q], xr[q][u], a[u]);
+    }
+    for (; p < p1; ++p) {
         const int s = perm[p];
         const float g = dLsel[s];
         V::load(x + (int64_t)(s / k) * d + c, xv);
@@ -583,30 +761,56 @@ __global__ void bounded_wait_kernel(uint64_t limit_ns, int32_t* status) {
     }
 }
 
+// GELU and its derivative, exact (CUDA erff / expf) or fast (the bf16
+// epilogue's approximation), for checking the latter against its error bound.
+__global__ void debug_gelu_kernel(int64_t n, const float* __restrict__ x, float* __restrict__ g,
+                                  float* __restrict__ gd, int fast) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float v = x[i];
+    g[i] = fast ? gelu_fast(v) : gelu_f(v);
+    gd[i] = fast ? gelu_grad_fast(v) : gelu_grad_f(v);
+}
+
 }  // namespace
+
+cudaError_t launch_debug_gelu(int64_t n, const float* x, float* g, float* gd, int fast,
+                              cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    debug_gelu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(n, x, g, gd, fast);
+    return cudaGetLastError();
+}
 
 // ---- launchers -----------------------------------------------------------------------
 
-cudaError_t launch_router_logits(const moe_shape& s, const void* x, const void* Wg,
-                                 const float* beta, float* logits, cudaStream_t st) {
-    if (s.dtype == MOE_BF16)
-        return router_logits_dispatch(s, (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg,
-                                      beta, logits, st);
-    return router_logits_dispatch(s, (const float*)x, (const float*)Wg, beta, logits, st);
-}
-
-cudaError_t launch_gate_hist(const moe_shape& s, const float* logits, int32_t* idx, float* w,
-                             int32_t* block_counts, int32_t* status, cudaStream_t st) {
+cudaError_t launch_route_gate(const moe_shape& s, const void* x, const void* Wg,
+                             const float* beta, float* logits, int compute_logits, int32_t* idx,
+                             float* w, int32_t* block_counts, int32_t* status, cudaStream_t st) {
+    const bool bf = s.dtype == MOE_BF16;
+    if (compute_logits && s.E <= 32) {
+        if (bf)
+            return router_gate_small(s, (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg, beta,
+                                     logits, idx, w, block_counts, status, st);
+        return router_gate_small(s, (const float*)x, (const float*)Wg, beta, logits, idx, w,
+                                 block_counts, status, st);
+    }
+    if (compute_logits) {
+        cudaError_t e = bf ? router_logits_dispatch(s, (const __nv_bfloat16*)x,
+                                                    (const __nv_bfloat16*)Wg, beta, logits, st)
+                           : router_logits_dispatch(s, (const float*)x, (const float*)Wg, beta,
+                                                    logits, st);
+        if (e != cudaSuccess) return e;
+    }
     const int nblk = (int)route_blocks(s.T);
     const int E = s.E;
     if (E <= 32)
-        gate_hist_kernel<1><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+        gate_hist_kernel<1><<<nblk, 1024, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
     else if (E <= 64)
-        gate_hist_kernel<2><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+        gate_hist_kernel<2><<<nblk, 1024, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
     else if (E <= 128)
-        gate_hist_kernel<4><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+        gate_hist_kernel<4><<<nblk, 1024, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
     else
-        gate_hist_kernel<8><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+        gate_hist_kernel<8><<<nblk, 1024, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
     return cudaGetLastError();
 }
 

@@ -23,7 +23,8 @@ MOE_F32, MOE_BF16 = 0, 1
 
 ENTRY_POINTS = ("moe_status_string", "moe_workspace_size", "moe_route", "moe_permute",
                 "moe_expert_ffn_fwd", "moe_combine_fwd", "moe_combine_bwd",
-                "moe_expert_ffn_bwd", "moe_route_bwd", "moe_debug_bounded_wait")
+                "moe_expert_ffn_bwd", "moe_route_bwd", "moe_debug_bounded_wait",
+                "moe_debug_gelu")
 
 
 class MoEError(RuntimeError):
@@ -80,6 +81,7 @@ def lib() -> ctypes.CDLL:
             L.moe_route_bwd.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                         ctypes.c_int, _P, _P, _P]
             L.moe_debug_bounded_wait.argtypes = [ctypes.c_uint64, _P, _P]
+            L.moe_debug_gelu.argtypes = [ctypes.c_int64, _P, _P, _P, ctypes.c_int, _P]
             for fn in ENTRY_POINTS[2:]:
                 getattr(L, fn).restype = ctypes.c_int
             _lib = L
@@ -165,3 +167,8 @@ def moe_route_bwd(s, dw, logits, idx, w, perm, offsets, x, Wg, dx, dWg, accumula
 def moe_debug_bounded_wait(limit_ns: int, dev_status, stream=None):
     _check("moe_debug_bounded_wait", lib().moe_debug_bounded_wait(
         int(limit_ns), _ptr(dev_status), _stream(stream)))
+
+
+def moe_debug_gelu(x, gelu, gelu_grad, fast: int, stream=None):
+    _check("moe_debug_gelu", lib().moe_debug_gelu(
+        int(x.numel()), _ptr(x), _ptr(gelu), _ptr(gelu_grad), int(fast), _stream(stream)))
