@@ -269,7 +269,15 @@ __global__ void __launch_bounds__(256) colsum_reduce_kernel(int n, int E,
     const int cnt = offsets[e + 1] - offsets[e];
     const int nc = (cnt + kDwgChunk - 1) / kDwgChunk;
     float s = 0.f;
-    for (int i = 0; i < nc; ++i) s += partial[(int64_t)(start + i) * n + c];
+    int i = 0;
+    for (; i + 8 <= nc; i += 8) {   // 8 loads in flight, added in chunk order
+        float v[8];
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = partial[(int64_t)(start + i + q) * n + c];
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) s += v[q];
+    }
+    for (; i < nc; ++i) s += partial[(int64_t)(start + i) * n + c];
     float* o = out + (int64_t)e * n + c;
     *o = accumulate ? *o + s : s;
 }

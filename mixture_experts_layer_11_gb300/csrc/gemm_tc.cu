@@ -380,6 +380,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 continue;
             }
+            // GELU' epilogue: the saved pre-activation H of this thread's row is
+            // fetched ahead (chunk 0 before the accumulator is ready, chunk c+1
+            // while chunk c is processed), so its latency overlaps other work.
+            uint4 hnext[4];
+            const int64_t grow_lane = (int64_t)ti.row0 + q * 32 + lane;
+            const bool row_ok = (q * 32 + lane) < ti.rows;
+            if (EPI == (int)Epi::GeluGrad && !VAR_K) {
+                const int col0 = ti.nt * BN + half * 128;
+                #pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    hnext[u] = row_ok ? __ldg(reinterpret_cast<const uint4*>(
+                                            (const __nv_bfloat16*)p.aux + grow_lane * p.N + col0 + u * 8))
+                                      : make_uint4(0, 0, 0, 0);
+            }
             if (!mbar_wait_warp(smem_u32(&c.tfull[acc]), acc_phase, p.limit_ns,
                                 &c.abort_flag)) {
                 raise_abort(c, p);
@@ -427,21 +441,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                             __syncwarp();
                         }
                     } else if (EPI == (int)Epi::GeluGrad) {
-                        // bring the saved pre-activation tile in (coalesced)
-                        const __nv_bfloat16* H = (const __nv_bfloat16*)p.aux;
+                        uint4 hcur[4];
                         #pragma unroll
-                        for (int it = 0; it < 4; ++it) {
-                            const int rr = it * 8 + (lane >> 2), cc = lane & 3;
-                            uint4 hv = make_uint4(0, 0, 0, 0);
-                            if (rr < valid)
-                                hv = *reinterpret_cast<const uint4*>(H + (grow0 + rr) * N + col0 + cc * 8);
-                            *reinterpret_cast<uint4*>(stg + stg_off(rr, cc)) = hv;
+                        for (int u = 0; u < 4; ++u) hcur[u] = hnext[u];
+                        if (ch < 3 && col0 + 32 < p.N) {
+                            #pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                hnext[u] = row_ok ? __ldg(reinterpret_cast<const uint4*>(
+                                                        (const __nv_bfloat16*)p.aux + grow_lane * N +
+                                                        col0 + 32 + u * 8))
+                                                  : make_uint4(0, 0, 0, 0);
                         }
-                        __syncwarp();
                         #pragma unroll
                         for (int cc = 0; cc < 4; ++cc) {
-                            const uint4 hv = *reinterpret_cast<const uint4*>(stg + stg_off(lane, cc));
-                            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&hv);
+                            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&hcur[cc]);
                             #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const float2 f = __bfloat1622float2(h[i]);
@@ -449,7 +462,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 v[cc * 8 + 2 * i + 1] *= gelu_grad_fast(f.y);
                             }
                         }
-                        __syncwarp();
                         stage_row_bf16(stg, lane, v);
                         __syncwarp();
                         store_tile_bf16(stg, lane, (__nv_bfloat16*)p.out0, grow0, valid, N, col0);

@@ -10,10 +10,12 @@
 namespace moe {
 
 // Tokens handled by one block of the gate / rank kernels: the per-block
-// histogram is a bitmask of 256 tokens per expert.
-constexpr int kRouteBlockTokens = 256;
-// Rows summed per partial of the router weight gradient.
-constexpr int kDwgChunk = 128;
+// histogram is a bitmask of 64 tokens (two 32-bit words) per expert.
+constexpr int kRouteBlockTokens = 64;
+constexpr int kRouteWords = kRouteBlockTokens / 32;
+// Rows summed per partial of the router weight gradient and of the bias
+// gradients (column sums).
+constexpr int kDwgChunk = 32;
 
 inline int64_t route_blocks(int64_t T) { return (T + kRouteBlockTokens - 1) / kRouteBlockTokens; }
 

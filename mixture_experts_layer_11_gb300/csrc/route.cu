@@ -8,8 +8,8 @@
 // review, section 3 "expert-wise offloading and processing"; "FastMoE",
 // review, "proposed method": scatter/gather layout batching inputs by expert).
 //
-// Dispatch design: each block of 256 tokens records, per expert, a 256-bit
-// mask of the tokens routed there (8 words of 32 bits).  Popcounts of those
+// Dispatch design: each block of 64 tokens records, per expert, a 64-bit
+// mask of the tokens routed there (2 words of 32 bits).  Popcounts of those
 // masks give the block's histogram; one single-block scan over the
 // expert-major (expert, block) table gives every block's base row per expert;
 // a token's rank inside its block is a popcount of the mask bits below it.
@@ -215,12 +215,12 @@ cudaError_t router_logits_dispatch(const moe_shape& s, const TIn* x, const TIn* 
 // One warp per token; lane l holds logits of experts l, l+32, ...  Top-k by k
 // rounds of a warp arg-max on (logit desc, expert index asc).  A NaN logit is
 // ranked below every number (so k distinct valid experts are always chosen)
-// and, like an infinite one, raises MOE_ERR_NONFINITE.  Blocks hold 256 tokens
-// (the bitmask histogram) and 32 warps, 8 tokens per warp.
+// and, like an infinite one, raises MOE_ERR_NONFINITE.  Blocks hold 64 tokens
+// (the bitmask histogram) and 8 warps, 8 tokens per warp.
 
 template <int EPL>
 __device__ __forceinline__ void gate_token(int64_t t, int E, int k, int renorm, float (&L)[EPL],
-                                           int lane, int tok, uint32_t (*bits)[8],
+                                           int lane, int tok, uint32_t (*bits)[kRouteWords],
                                            int32_t* __restrict__ idx, float* __restrict__ w,
                                            int32_t* status) {
     bool bad = false;
@@ -280,27 +280,28 @@ __device__ __forceinline__ void gate_token(int64_t t, int E, int k, int renorm, 
     }
 }
 
-__device__ __forceinline__ void zero_bits(uint32_t (*bits)[8], int E) {
-    for (int i = threadIdx.x; i < E * 8; i += blockDim.x) bits[i >> 3][i & 7] = 0u;
+__device__ __forceinline__ void zero_bits(uint32_t (*bits)[kRouteWords], int E) {
+    for (int i = threadIdx.x; i < E * kRouteWords; i += blockDim.x)
+        bits[i / kRouteWords][i % kRouteWords] = 0u;
 }
 
-__device__ __forceinline__ void write_block_counts(uint32_t (*bits)[8], int E, int nblk,
+__device__ __forceinline__ void write_block_counts(uint32_t (*bits)[kRouteWords], int E, int nblk,
                                                    int32_t* block_counts) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int c = 0;
         #pragma unroll
-        for (int q = 0; q < 8; ++q) c += __popc(bits[e][q]);
+        for (int q = 0; q < kRouteWords; ++q) c += __popc(bits[e][q]);
         block_counts[(int64_t)e * nblk + blockIdx.x] = c;
     }
 }
 
 // Gate on logits already in memory (given, or from the tiled GEMM).
 template <int EPL>
-__global__ void __launch_bounds__(1024) gate_hist_kernel(
+__global__ void __launch_bounds__(256) gate_hist_kernel(
     int64_t T, int E, int k, int renorm, int nblk, const float* __restrict__ logits,
     int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ block_counts,
     int32_t* status) {
-    __shared__ uint32_t bits[256][8];
+    __shared__ uint32_t bits[256][kRouteWords];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     zero_bits(bits, E);
     __syncthreads();
@@ -344,13 +345,13 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[EP], int lane) {
 }
 
 template <typename TIn, int EP>
-__global__ void __launch_bounds__(1024) router_gate_small_kernel(
+__global__ void __launch_bounds__(256) router_gate_small_kernel(
     int64_t T, int d, int E, int k, int renorm, int nblk, const TIn* __restrict__ x,
     const TIn* __restrict__ Wg, const float* __restrict__ beta, float* __restrict__ logits,
     int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ block_counts,
     int32_t* status) {
     using V = Vec<TIn>;
-    __shared__ uint32_t bits[256][8];
+    __shared__ uint32_t bits[256][kRouteWords];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     zero_bits(bits, E);
     __syncthreads();
@@ -362,6 +363,7 @@ __global__ void __launch_bounds__(1024) router_gate_small_kernel(
         float acc[EP];
         #pragma unroll
         for (int e = 0; e < EP; ++e) acc[e] = 0.f;
+        #pragma unroll 4
         for (int c = lane; c < nv; c += 32) {
             float xv[V::N], wv[V::N];
             V::load(x + t * d + (int64_t)c * V::N, xv);
@@ -395,7 +397,7 @@ cudaError_t router_gate_small(const moe_shape& s, const TIn* x, const TIn* Wg, c
                               int32_t* status, cudaStream_t st) {
     const int nblk = (int)route_blocks(s.T);
 #define MOE_SMALL(EPV)                                                                        \
-    router_gate_small_kernel<TIn, EPV><<<nblk, 1024, 0, st>>>(s.T, s.d, s.E, s.k, s.renorm,  \
+    router_gate_small_kernel<TIn, EPV><<<nblk, 256, 0, st>>>(s.T, s.d, s.E, s.k, s.renorm,  \
                                                               nblk, x, Wg, beta, logits, idx, \
                                                               w, block_counts, status)
     if (s.E <= 1) MOE_SMALL(1);
@@ -461,13 +463,14 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nblk, in
 
 // ---- A3: stable rank inside each block -> pos, perm ------------------------------
 
-__global__ void __launch_bounds__(256) dispatch_rank_kernel(
+__global__ void __launch_bounds__(kRouteBlockTokens) dispatch_rank_kernel(
     int64_t T, int E, int k, int nblk, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ block_base, int32_t* __restrict__ pos,
     int32_t* __restrict__ perm) {
-    __shared__ uint32_t bits[256][8];
+    __shared__ uint32_t bits[256][kRouteWords];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < E * 8; i += 256) bits[i >> 3][i & 7] = 0u;
+    for (int i = threadIdx.x; i < E * kRouteWords; i += blockDim.x)
+        bits[i / kRouteWords][i % kRouteWords] = 0u;
     __syncthreads();
     const int64_t t = (int64_t)blockIdx.x * kRouteBlockTokens + threadIdx.x;
     if (t < T)
@@ -653,7 +656,15 @@ __global__ void __launch_bounds__(256) dwg_reduce_sparse_kernel(
     const int n = offsets[e + 1] - offsets[e];
     const int nc = (n + kDwgChunk - 1) / kDwgChunk;
     float s = 0.f;
-    for (int i = 0; i < nc; ++i) s += partial[(int64_t)(start + i) * d + c];
+    int i = 0;
+    for (; i + 8 <= nc; i += 8) {   // 8 loads in flight, added in chunk order
+        float v[8];
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = partial[(int64_t)(start + i + q) * d + c];
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) s += v[q];
+    }
+    for (; i < nc; ++i) s += partial[(int64_t)(start + i) * d + c];
     float* o = dWg + (int64_t)e * d + c;
     *o = accumulate ? *o + s : s;
 }
@@ -804,13 +815,13 @@ cudaError_t launch_route_gate(const moe_shape& s, const void* x, const void* Wg,
     const int nblk = (int)route_blocks(s.T);
     const int E = s.E;
     if (E <= 32)
-        gate_hist_kernel<1><<<nblk, 1024, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+        gate_hist_kernel<1><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
     else if (E <= 64)
-        gate_hist_kernel<2><<<nblk, 1024, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+        gate_hist_kernel<2><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
     else if (E <= 128)
-        gate_hist_kernel<4><<<nblk, 1024, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+        gate_hist_kernel<4><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
     else
-        gate_hist_kernel<8><<<nblk, 1024, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+        gate_hist_kernel<8><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
     return cudaGetLastError();
 }
 
@@ -825,7 +836,7 @@ cudaError_t launch_dispatch_rank(const moe_shape& s, const int32_t* idx,
                                  const int32_t* block_base, int32_t* pos, int32_t* perm,
                                  cudaStream_t st) {
     const int nblk = (int)route_blocks(s.T);
-    dispatch_rank_kernel<<<nblk, 256, 0, st>>>(s.T, s.E, s.k, nblk, idx, block_base, pos, perm);
+    dispatch_rank_kernel<<<nblk, kRouteBlockTokens, 0, st>>>(s.T, s.E, s.k, nblk, idx, block_base, pos, perm);
     return cudaGetLastError();
 }
 

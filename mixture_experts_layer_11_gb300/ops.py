@@ -88,11 +88,27 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-def _ptr(t):
+_F32, _I32 = torch.float32, torch.int32
+
+
+def _act(s: moe_shape):
+    return torch.bfloat16 if s.dtype == MOE_BF16 else torch.float32
+
+
+def _ptr(t, want=None):
+    """Device address of a tensor (None -> NULL; ints pass through).  Tensors
+    must be CUDA, contiguous, and of the element type the C ABI expects for
+    that argument: the library reads raw pointers and cannot check this."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise MoEError("argument", MOE_ERR_INVALID, "tensor is not on a CUDA device")
+    if not t.is_contiguous():
+        raise MoEError("argument", MOE_ERR_INVALID, "tensor is not contiguous")
+    if want is not None and t.dtype != want:
+        raise MoEError("argument", MOE_ERR_INVALID, f"tensor dtype {t.dtype}, expected {want}")
     return t.data_ptr()
 
 
@@ -120,55 +136,62 @@ def moe_workspace_size(s: moe_shape) -> int:
 def moe_route(s, x, Wg, logit_bias, logits, compute_logits, idx, w, counts, offsets, pos, perm,
               ws, dev_status, stream=None):
     _check("moe_route", lib().moe_route(
-        ctypes.byref(s), _ptr(x), _ptr(Wg), _ptr(logit_bias), _ptr(logits), int(compute_logits),
-        _ptr(idx), _ptr(w), _ptr(counts), _ptr(offsets), _ptr(pos), _ptr(perm), _ptr(ws),
-        _ptr(dev_status), _stream(stream)))
+        ctypes.byref(s), _ptr(x, _act(s)), _ptr(Wg, _act(s)), _ptr(logit_bias, _F32),
+        _ptr(logits, _F32), int(compute_logits), _ptr(idx, _I32), _ptr(w, _F32),
+        _ptr(counts, _I32), _ptr(offsets, _I32), _ptr(pos, _I32), _ptr(perm, _I32), _ptr(ws),
+        _ptr(dev_status, _I32), _stream(stream)))
 
 
 def moe_permute(s, x, pos, x_perm, stream=None):
-    _check("moe_permute", lib().moe_permute(ctypes.byref(s), _ptr(x), _ptr(pos), _ptr(x_perm),
-                                            _stream(stream)))
+    _check("moe_permute", lib().moe_permute(ctypes.byref(s), _ptr(x, _act(s)), _ptr(pos, _I32),
+                                            _ptr(x_perm, _act(s)), _stream(stream)))
 
 
 def moe_expert_ffn_fwd(s, x_perm, offsets, W1, b1, W2, b2, H, A, y_perm, ws, dev_status,
                        stream=None):
     _check("moe_expert_ffn_fwd", lib().moe_expert_ffn_fwd(
-        ctypes.byref(s), _ptr(x_perm), _ptr(offsets), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2),
-        _ptr(H), _ptr(A), _ptr(y_perm), _ptr(ws), _ptr(dev_status), _stream(stream)))
+        ctypes.byref(s), _ptr(x_perm, _act(s)), _ptr(offsets, _I32), _ptr(W1, _act(s)),
+        _ptr(b1, _act(s)), _ptr(W2, _act(s)), _ptr(b2, _act(s)), _ptr(H, _act(s)),
+        _ptr(A, _act(s)), _ptr(y_perm, _act(s)), _ptr(ws), _ptr(dev_status, _I32),
+        _stream(stream)))
 
 
 def moe_combine_fwd(s, y_perm, pos, w, y, stream=None):
-    _check("moe_combine_fwd", lib().moe_combine_fwd(ctypes.byref(s), _ptr(y_perm), _ptr(pos),
-                                                    _ptr(w), _ptr(y), _stream(stream)))
+    _check("moe_combine_fwd", lib().moe_combine_fwd(
+        ctypes.byref(s), _ptr(y_perm, _act(s)), _ptr(pos, _I32), _ptr(w, _F32), _ptr(y, _act(s)),
+        _stream(stream)))
 
 
 def moe_combine_bwd(s, dy, y_perm, pos, w, dy_perm, dw, stream=None):
     _check("moe_combine_bwd", lib().moe_combine_bwd(
-        ctypes.byref(s), _ptr(dy), _ptr(y_perm), _ptr(pos), _ptr(w), _ptr(dy_perm), _ptr(dw),
-        _stream(stream)))
+        ctypes.byref(s), _ptr(dy, _act(s)), _ptr(y_perm, _act(s)), _ptr(pos, _I32), _ptr(w, _F32),
+        _ptr(dy_perm, _act(s)), _ptr(dw, _F32), _stream(stream)))
 
 
 def moe_expert_ffn_bwd(s, dy_perm, x_perm, H, A, offsets, W1, W2, dx_perm, dW1, db1, dW2, db2,
                        accumulate, ws, dev_status, stream=None):
     _check("moe_expert_ffn_bwd", lib().moe_expert_ffn_bwd(
-        ctypes.byref(s), _ptr(dy_perm), _ptr(x_perm), _ptr(H), _ptr(A), _ptr(offsets), _ptr(W1),
-        _ptr(W2), _ptr(dx_perm), _ptr(dW1), _ptr(db1), _ptr(dW2), _ptr(db2), int(accumulate),
-        _ptr(ws), _ptr(dev_status), _stream(stream)))
+        ctypes.byref(s), _ptr(dy_perm, _act(s)), _ptr(x_perm, _act(s)), _ptr(H, _act(s)),
+        _ptr(A, _act(s)), _ptr(offsets, _I32), _ptr(W1, _act(s)), _ptr(W2, _act(s)),
+        _ptr(dx_perm, _act(s)), _ptr(dW1, _F32), _ptr(db1, _F32), _ptr(dW2, _F32),
+        _ptr(db2, _F32), int(accumulate), _ptr(ws), _ptr(dev_status, _I32), _stream(stream)))
 
 
 def moe_route_bwd(s, dw, logits, idx, w, perm, offsets, x, Wg, dx, dWg, accumulate, ws,
                   dev_status, stream=None):
     _check("moe_route_bwd", lib().moe_route_bwd(
-        ctypes.byref(s), _ptr(dw), _ptr(logits), _ptr(idx), _ptr(w), _ptr(perm), _ptr(offsets),
-        _ptr(x), _ptr(Wg), _ptr(dx), _ptr(dWg), int(accumulate), _ptr(ws), _ptr(dev_status),
+        ctypes.byref(s), _ptr(dw, _F32), _ptr(logits, _F32), _ptr(idx, _I32), _ptr(w, _F32),
+        _ptr(perm, _I32), _ptr(offsets, _I32), _ptr(x, _act(s)), _ptr(Wg, _act(s)),
+        _ptr(dx, _act(s)), _ptr(dWg, _F32), int(accumulate), _ptr(ws), _ptr(dev_status, _I32),
         _stream(stream)))
 
 
 def moe_debug_bounded_wait(limit_ns: int, dev_status, stream=None):
     _check("moe_debug_bounded_wait", lib().moe_debug_bounded_wait(
-        int(limit_ns), _ptr(dev_status), _stream(stream)))
+        int(limit_ns), _ptr(dev_status, _I32), _stream(stream)))
 
 
 def moe_debug_gelu(x, gelu, gelu_grad, fast: int, stream=None):
     _check("moe_debug_gelu", lib().moe_debug_gelu(
-        int(x.numel()), _ptr(x), _ptr(gelu), _ptr(gelu_grad), int(fast), _stream(stream)))
+        int(x.numel()), _ptr(x, _F32), _ptr(gelu, _F32), _ptr(gelu_grad, _F32), int(fast),
+        _stream(stream)))

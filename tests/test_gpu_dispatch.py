@@ -34,9 +34,9 @@ def test_permute_combine_and_backward(dtype, T, d, E, k):
     rb = dtype == "bf16"
     idx, w, offsets, pos, perm = _routing(T, E, k, 1, seed=T + d)
     g = torch.Generator().manual_seed(T)
-    x = torch.randn(T, d, generator=g).to(tdt)
-    Y = torch.randn(T * k, d, generator=g).to(tdt)
-    dy = torch.randn(T, d, generator=g).to(tdt)
+    x = torch.randn(T, d, generator=g, dtype=torch.float32).to(tdt)
+    Y = torch.randn(T * k, d, generator=g, dtype=torch.float32).to(tdt)
+    dy = torch.randn(T, d, generator=g, dtype=torch.float32).to(tdt)
     s = ops.make_shape(T, d, 64, E, k, dtype, 1)
     pos_d = _tensor(pos, torch.int32)
     w32 = w.astype(np.float32)

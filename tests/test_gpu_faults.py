@@ -33,7 +33,19 @@ def test_first_error_wins():
 
 def test_invalid_arguments_raise_without_launch():
     s = ops.make_shape(100, 64, 64, 4, 1, "f32", 0)
-    x = torch.zeros(100, 64, device="cuda")
+    x = torch.zeros(100, 64, dtype=torch.float32, device="cuda")
     with pytest.raises(ops.MoEError) as ei:
         ops.moe_permute(s, x, None, x)
+    assert ei.value.code == ops.MOE_ERR_INVALID
+
+
+def test_wrong_dtype_buffer_rejected_at_the_binding():
+    # an fp32 gradient slot given a float64 tensor would be written as fp32
+    # bit patterns into doubles; the binding refuses it before any launch
+    s = ops.make_shape(8, 64, 64, 4, 1, "f32", 0)
+    dw = torch.zeros(8, 1, dtype=torch.float64, device="cuda")
+    y = torch.zeros(8, 64, dtype=torch.float32, device="cuda")
+    pos = torch.zeros(8, 1, dtype=torch.int32, device="cuda")
+    with pytest.raises(ops.MoEError) as ei:
+        ops.moe_combine_bwd(s, y, y, pos, dw, y, dw)
     assert ei.value.code == ops.MOE_ERR_INVALID

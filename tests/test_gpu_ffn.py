@@ -42,8 +42,8 @@ def test_expert_ffn_fwd_bwd(dtype, T, d, f, E, k, zipf):
     cfg = synth.MoEConfig("t", T=T, d=d, f=f, E=E, k=k, renorm=1, dtype=dtype)
     inp = synth.make_inputs(cfg, seed=E + d, random_bias=True)
     g = torch.Generator().manual_seed(P)
-    X = torch.randn(P, d, generator=g).to(tdt)
-    dY = torch.randn(P, d, generator=g).to(tdt)
+    X = torch.randn(P, d, generator=g, dtype=torch.float32).to(tdt)
+    dY = torch.randn(P, d, generator=g, dtype=torch.float32).to(tdt)
     s = ops.make_shape(T, d, f, E, k, dtype, 1)
     dev = {n: inp[n].to(DEV) for n in ("W1", "b1", "W2", "b2")}
     offs = torch.from_numpy(offsets).to(DEV)
@@ -62,7 +62,7 @@ def test_expert_ffn_fwd_bwd(dtype, T, d, f, E, k, zipf):
     assert_close("Y", Y, rY, dtype)
 
     dX = torch.empty(P, d, dtype=tdt, device=DEV)
-    grads = {n: torch.full(sh, float("nan"), device=DEV) for n, sh in
+    grads = {n: torch.full(sh, float("nan"), dtype=torch.float32, device=DEV) for n, sh in
              (("dW1", (E, f, d)), ("db1", (E, f)), ("dW2", (E, d, f)), ("db2", (E, d)))}
     ops.moe_expert_ffn_bwd(s, dYd, Xd, H, A, offs, dev["W1"], dev["W2"], dX, grads["dW1"],
                            grads["db1"], grads["dW2"], grads["db2"], 0, ws, st)

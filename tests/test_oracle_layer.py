@@ -13,8 +13,6 @@ import torch.nn.functional as F
 import oracle
 from mixture_experts_layer_11_gb300 import synth
 
-torch.set_default_dtype(torch.float64)
-
 
 # ---- scalar helpers -----------------------------------------------------------
 
@@ -39,7 +37,7 @@ def test_gelu_special_values_and_library():
     xs = np.linspace(-6, 6, 241)
     for v in xs:
         assert abs(oracle.gelu(v) - oracle.gelu(-v) - v) < 1e-14 * max(1, abs(v))
-    t = torch.tensor(xs, requires_grad=True)
+    t = torch.tensor(xs, dtype=torch.float64, requires_grad=True)
     y = F.gelu(t, approximate="none")
     y.sum().backward()
     np.testing.assert_allclose([oracle.gelu(v) for v in xs], y.detach().numpy(),
