@@ -193,6 +193,36 @@ MOE_API moe_status moe_route_bwd(const moe_shape* s, const float* dw, const floa
                          float* dWg, int accumulate, void* ws, int32_t* dev_status,
                          moe_stream_t stream);
 
+/* Routing (A1 + A2 + A3) without a caller-provided workspace.
+ *
+ * For callers that cannot allocate device memory: a plug-in whose host
+ * framework owns every allocation and hands it only the tensors it reads and
+ * writes, with no room for a workspace.  This entry point needs nothing beyond
+ * those.  It is an interface convenience of this library; the MoE method
+ * itself has no counterpart for it.
+ *
+ * Same arguments and results as moe_route, minus `ws`.  The per-block expert
+ * histogram lives in a fixed scratch array inside libmoe.so (a static device
+ * array of MOE_ROUTE_NOALLOC_MAX_SCRATCH int32, 1 MiB; every GPU that loads
+ * the library keeps it until the process exits).
+ *   - Size limit: E * ceil(T / 64) must not exceed MOE_ROUTE_NOALLOC_MAX_SCRATCH;
+ *     larger shapes return MOE_ERR_UNSUPPORTED without launching anything.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.  A failure there returns MOE_ERR_CUDA.
+ *   - The library allocates and frees nothing on this path.
+ *   - All calls share the one array and leave their contents in it; every
+ *     entry a call reads is written earlier by the same call, so nothing needs
+ *     clearing.  Calls whose work may overlap on the GPU (different streams,
+ *     no ordering between them) race on the array and give wrong results:
+ *     serialise them. */
+#define MOE_ROUTE_NOALLOC_MAX_SCRATCH (1 << 18)
+MOE_API moe_status moe_route_noalloc(const moe_shape* s, const void* x, const void* Wg,
+                                     const float* logit_bias, float* logits,
+                                     int compute_logits, int32_t* idx, float* w,
+                                     int32_t* counts, int32_t* offsets, int32_t* pos,
+                                     int32_t* perm, int32_t* dev_status, moe_stream_t stream);
+
 /* Diagnostics: launch one kernel that waits on a device flag that nothing
  * sets, with the library's bounded wait (limit_ns nanoseconds), then writes
  * MOE_ERR_TIMEOUT to *dev_status and returns.  It exercises the timeout path

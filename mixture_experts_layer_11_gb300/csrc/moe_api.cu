@@ -262,6 +262,66 @@ moe_status moe_route_bwd(const moe_shape* s, const float* dw, const float* logit
                                         accumulate, dL, partial, st));
 }
 
+}  // extern "C"
+
+// ---- routing without a caller workspace ----------------------------------------
+// The histogram scratch of moe_route_noalloc: a fixed device array inside the
+// library (1 MiB on every GPU that loads it).  In host code the symbol names a
+// host-side stand-in, never a device address: the device address is looked up
+// once per device and passed to the kernels.
+static __device__ __align__(256) int32_t g_route_noalloc_scratch[MOE_ROUTE_NOALLOC_MAX_SCRATCH];
+
+namespace {
+
+// Device address of the scratch array on the current device, looked up on the
+// first call for that device (nullptr if the lookup fails).
+int32_t* route_noalloc_scratch() {
+    static std::mutex mu;
+    static int32_t* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_route_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<int32_t*>(p);
+    }
+    return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_route_noalloc(const moe_shape* s, const void* x, const void* Wg,
+                             const float* logit_bias, float* logits, int compute_logits,
+                             int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
+                             int32_t* pos, int32_t* perm, int32_t* dev_status,
+                             moe_stream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (!ok_ptr(counts) || !ok_ptr(offsets)) return MOE_ERR_INVALID;
+    if (s->T > 0) {
+        if (!ok_ptr(logits) || !ok_ptr(idx) || !ok_ptr(w) || !ok_ptr(pos) || !ok_ptr(perm) ||
+            !ok_status(dev_status))
+            return MOE_ERR_INVALID;
+        if (compute_logits && (!ok_ptr(x) || !ok_ptr(Wg) || !ok_opt(logit_bias)))
+            return MOE_ERR_INVALID;
+    }
+    if ((int64_t)s->E * route_blocks(s->T) > (int64_t)MOE_ROUTE_NOALLOC_MAX_SCRATCH)
+        return MOE_ERR_UNSUPPORTED;
+    int32_t* block_counts = route_noalloc_scratch();
+    if (block_counts == nullptr) return MOE_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    if (s->T > 0)
+        e = launch_route_gate(*s, x, Wg, logit_bias, logits, compute_logits, idx, w, block_counts,
+                              dev_status, st);
+    if (e == cudaSuccess) e = launch_dispatch_scan(*s, block_counts, counts, offsets, st);
+    if (e == cudaSuccess && s->T > 0) e = launch_dispatch_rank(*s, idx, block_counts, pos, perm, st);
+    return cuda_status(e);
+}
+
 moe_status moe_debug_bounded_wait(uint64_t limit_ns, int32_t* dev_status, moe_stream_t stream) {
     if (dev_status == nullptr || !ok_status(dev_status)) return MOE_ERR_INVALID;
     return cuda_status(launch_bounded_wait(limit_ns, dev_status, (cudaStream_t)stream));

@@ -24,7 +24,7 @@ MOE_F32, MOE_BF16 = 0, 1
 ENTRY_POINTS = ("moe_status_string", "moe_workspace_size", "moe_route", "moe_permute",
                 "moe_expert_ffn_fwd", "moe_combine_fwd", "moe_combine_bwd",
                 "moe_expert_ffn_bwd", "moe_route_bwd", "moe_debug_bounded_wait",
-                "moe_debug_gelu")
+                "moe_debug_gelu", "moe_route_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
                                         ctypes.c_int, _P, _P, _P]
             L.moe_debug_bounded_wait.argtypes = [ctypes.c_uint64, _P, _P]
             L.moe_debug_gelu.argtypes = [ctypes.c_int64, _P, _P, _P, ctypes.c_int, _P]
+            L.moe_route_noalloc.argtypes = [_SP, _P, _P, _P, _P, ctypes.c_int, _P, _P, _P, _P,
+                                            _P, _P, _P, _P]
             for fn in ENTRY_POINTS[2:]:
                 getattr(L, fn).restype = ctypes.c_int
             _lib = L
@@ -195,3 +197,17 @@ def moe_debug_gelu(x, gelu, gelu_grad, fast: int, stream=None):
     _check("moe_debug_gelu", lib().moe_debug_gelu(
         int(x.numel()), _ptr(x, _F32), _ptr(gelu, _F32), _ptr(gelu_grad, _F32), int(fast),
         _stream(stream)))
+
+
+ROUTE_NOALLOC_MAX_SCRATCH = 1 << 18  # MOE_ROUTE_NOALLOC_MAX_SCRATCH in include/moe.h
+
+
+def moe_route_noalloc(s, x, Wg, logit_bias, logits, compute_logits, idx, w, counts, offsets,
+                      pos, perm, dev_status, stream=None):
+    """moe_route without a workspace argument: for callers that cannot
+    allocate device memory (see include/moe.h)."""
+    _check("moe_route_noalloc", lib().moe_route_noalloc(
+        ctypes.byref(s), _ptr(x, _act(s)), _ptr(Wg, _act(s)), _ptr(logit_bias, _F32),
+        _ptr(logits, _F32), int(compute_logits), _ptr(idx, _I32), _ptr(w, _F32),
+        _ptr(counts, _I32), _ptr(offsets, _I32), _ptr(pos, _I32), _ptr(perm, _I32),
+        _ptr(dev_status, _I32), _stream(stream)))
