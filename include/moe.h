@@ -183,13 +183,17 @@ MOE_API moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, c
 /* A10: router backward.  dL = d(gate weights)/d(logits)^T dw:
  *   renorm: dL[idx_j] = w_j (dw_j - sum_i w_i dw_i), zero elsewhere;
  *   else:   dL[e] = sum_j dw_j p[idx_j] (delta(e, idx_j) - p[e]), p = softmax(L).
- *   dx[t]  += sum_e dL[t,e] Wg[e]     (dx [T,d] dtype, read-modify-write)
+ *   dx[t]   = [sum_j dx_perm[pos[t,j]]]  +  sum_e dL[t,e] Wg[e]
+ *             (dx [T,d] dtype).  With dx_perm and pos given, the bracketed
+ *             permute backward (A9) is fused in and dx is overwritten; with
+ *             dx_perm == NULL, dx is read and the router term added to it.
  *   dWg    (+)= dL^T x                (dWg [E,d] fp32; accumulate as above)
  * perm / offsets are the dispatch of this chunk (used to sum each expert's
  * tokens in a fixed order).  The logit shift has no gradient. */
 MOE_API moe_status moe_route_bwd(const moe_shape* s, const float* dw, const float* logits,
                          const int32_t* idx, const float* w, const int32_t* perm,
-                         const int32_t* offsets, const void* x, const void* Wg, void* dx,
+                         const int32_t* offsets, const void* x, const void* Wg,
+                         const void* dx_perm, const int32_t* pos, void* dx,
                          float* dWg, int accumulate, void* ws, int32_t* dev_status,
                          moe_stream_t stream);
 

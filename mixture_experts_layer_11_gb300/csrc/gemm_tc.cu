@@ -16,17 +16,28 @@
 //     length varies per expert.  Rows past the segment are computed from
 //     whatever TMA loads there and never stored.
 //   VarK (weight gradient): C_e[M, N] (+)= act_a[seg_e, M]^T act_b[seg_e, N];
-//     the reduction runs over the segment's rows, so rows past the segment in
-//     the last K block are zeroed in shared memory before the MMA reads them.
+//     the reduction runs over the segment's rows.  The tensor cores take the
+//     whole 16-row groups; the last n_e mod 16 rows are added by the epilogue
+//     on the CUDA cores, so no row past the segment is ever summed.
 //
-// CTA = 10 warps: warp 0 issues TMA loads into a 4-stage ring, warp 1 issues
-// tcgen05.mma (M=128, N=256, K=16 per instruction) into one of two TMEM
-// accumulators (2 x 256 fp32 columns), warps 2-9 drain the other accumulator
-// (tcgen05.ld), apply the fused epilogue (bias, GELU, GELU', fp32 accumulate)
-// and write through a swizzled shared staging buffer with coalesced stores.
-// Every wait is bounded; on expiry the CTA records MOE_ERR_TIMEOUT, waits for
-// its own copies and MMAs in flight, frees TMEM and exits.
+// Two CTA shapes (template PAIR):
+//   1 CTA: tile 128 x 256, tcgen05.mma.cta_group::1 (M 128, N 256, K 16);
+//     4 stages of 48 KB (A 128x64, B 256x64).
+//   CTA pair (cluster of 2): tile 256 x 256, tcgen05.mma.cta_group::2 (M 256,
+//     N 256, K 16) issued by the even CTA; each CTA holds its 128 rows of A
+//     and 128 columns of B, so a stage is 32 KB and 6 stages fit.  Both CTAs'
+//     TMA loads complete on the even CTA's stage barrier; MMA completion is
+//     multicast to both CTAs' barriers; each CTA drains its own TMEM rows.
+//
+// CTA = 10 warps: warp 0 issues TMA loads, warp 1 issues the MMAs into one of
+// two TMEM accumulators (2 x 256 fp32 columns), warps 2-9 drain the other
+// accumulator (tcgen05.ld), apply the fused epilogue (bias, GELU, GELU', fp32
+// accumulate) and write through a swizzled shared staging buffer with
+// coalesced stores.  Every wait is bounded; on expiry the CTA records
+// MOE_ERR_TIMEOUT, waits for its own copies and MMAs in flight, frees TMEM
+// and exits.
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 
 #include <mutex>
 
@@ -36,19 +47,25 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;            // tile rows (MMA M)
+constexpr int BM = 128;            // rows per CTA (TMEM lanes)
 constexpr int BN = 256;            // tile columns (MMA N)
 constexpr int BK = 64;             // K per stage: one 128-byte swizzle row of bf16
-constexpr int STAGES = 4;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 32 * (2 + EPI_WARPS);
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SLAB_BYTES = 64 * BK * 2;    // one 64-wide MN slab of BK rows
 constexpr int STAGING_BYTES = 32 * 64;     // per epilogue warp: 32 rows x 64 B
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_E = 256;
+
+template <bool PAIR> struct Shape {
+    static constexpr int CTAS = PAIR ? 2 : 1;
+    static constexpr int TILE_M = BM * CTAS;          // rows of one (pair) tile
+    static constexpr int BN_CTA = BN / CTAS;          // B columns this CTA holds
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN_CTA * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = PAIR ? 6 : 4;
+};
 
 struct TcParams {
     int E, M, N, K;          // VarM: N, K (M unused); VarK: M, N (K = segment)
@@ -59,12 +76,14 @@ struct TcParams {
     void* out0;
     void* out1;
     float* outf;
+    const void* act_a;       // VarK: CUDA-core tail rows
+    const void* act_b;
     int accumulate;
     int32_t* status;
     uint64_t limit_ns;
 };
 
-struct Ctrl {
+template <int STAGES> struct Ctrl {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t tfull[2];
@@ -78,17 +97,24 @@ struct Ctrl {
     int order[MAX_E];            // VarK: experts by descending row count
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES +
-                              (size_t)EPI_WARPS * STAGING_BYTES + sizeof(Ctrl);
+template <bool PAIR>
+constexpr size_t smem_bytes() {
+    using S = Shape<PAIR>;
+    return 1024 + (size_t)S::STAGES * S::STAGE_BYTES + (size_t)EPI_WARPS * STAGING_BYTES +
+           sizeof(Ctrl<S::STAGES>);
+}
 
 struct Tile {
     int e, mt, nt, num_kb;
-    int row0;     // VarM: first row of the tile; VarK: first row of the segment
-    int rows;     // VarM: valid rows in the tile; VarK: rows of the segment
+    int row0;     // VarM: first row of this CTA's part; VarK: first row of the segment
+    int rows;     // VarM: valid rows of this CTA's part (may be <= 0); VarK: segment rows
+    int kfull;    // VarK: rows taken by the tensor cores (whole 16-row groups)
 };
 
-template <bool VAR_K>
-__device__ __forceinline__ Tile get_tile(const Ctrl& c, const TcParams& p, int t, int& ecur) {
+template <bool VAR_K, bool PAIR, typename C>
+__device__ __forceinline__ Tile get_tile(const C& c, const TcParams& p, int t, int& ecur,
+                                         int rank) {
+    using S = Shape<PAIR>;
     Tile ti;
     const int NT = (p.N + BN - 1) / BN;
     if (!VAR_K) {
@@ -97,11 +123,12 @@ __device__ __forceinline__ Tile get_tile(const Ctrl& c, const TcParams& p, int t
         ti.e = ecur;
         ti.mt = local / NT;
         ti.nt = local % NT;
-        ti.row0 = c.off[ecur] + ti.mt * BM;
+        ti.row0 = c.off[ecur] + ti.mt * S::TILE_M + rank * BM;
         ti.rows = min(BM, c.off[ecur + 1] - ti.row0);
         ti.num_kb = p.K / BK;
+        ti.kfull = p.K;
     } else {
-        const int MT = (p.M + BM - 1) / BM;
+        const int MT = (p.M + S::TILE_M - 1) / S::TILE_M;
         const int per = MT * NT;
         ti.e = c.order[t / per];
         const int local = t % per;
@@ -109,14 +136,97 @@ __device__ __forceinline__ Tile get_tile(const Ctrl& c, const TcParams& p, int t
         ti.nt = local % NT;
         ti.row0 = c.off[ti.e];
         ti.rows = c.off[ti.e + 1] - ti.row0;
-        ti.num_kb = (ti.rows + BK - 1) / BK;
+        ti.kfull = ti.rows & ~15;
+        ti.num_kb = (ti.kfull + BK - 1) / BK;
     }
     return ti;
 }
 
-__device__ __forceinline__ void raise_abort(Ctrl& c, const TcParams& p) {
+template <typename C>
+__device__ __forceinline__ void raise_abort(C& c, const TcParams& p) {
     *(volatile int*)&c.abort_flag = 1;
     report(p.status, MOE_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Shared::cluster address of the variable at shared address `a` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Arrivals on a barrier addressed through the cluster window (possibly in the
+// peer CTA).  Default (CTA-scope) semantics: what they publish is ordered by
+// other means (TMA completion bytes, tcgen05 fences), and a cluster-scope
+// release here would wait on the thread's outstanding copies every stage.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cl_addr, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cl_addr),
+                 "r"(bytes)
+                 : "memory");
+}
+// TMA loads whose completion is signalled on the pair's even CTA (cl_bar is a
+// shared::cluster address).
+__device__ __forceinline__ void tma2_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t cl_bar,
+                                             int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(map), "r"(cl_bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void tma2_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t cl_bar,
+                                             int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(map), "r"(cl_bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_mma2_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the barrier at this shared offset in both CTAs of the pair once
+// every tcgen05 op issued so far by this thread has completed.
+__device__ __forceinline__ void tc_commit2_both(uint32_t bar) {
+    const uint16_t mask = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit2_local(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
 }
 
 // ---- epilogue helpers: 32 rows x 64 bytes staging, 16-byte chunks XOR-swizzled
@@ -154,37 +264,49 @@ __device__ __forceinline__ void store_tile_bf16(const uint8_t* stg, int lane, __
     }
 }
 
-template <bool VAR_K, bool A_MN, bool B_MN, int EPI>
+template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB, const TcParams p) {
+    using S = Shape<PAIR>;
+    constexpr int STAGES = S::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t* staging_base = base + (size_t)STAGES * STAGE_BYTES;
-    Ctrl& c = *reinterpret_cast<Ctrl*>(staging_base + (size_t)EPI_WARPS * STAGING_BYTES);
+    uint8_t* staging_base = base + (size_t)STAGES * S::STAGE_BYTES;
+    using CtrlT = Ctrl<STAGES>;
+    CtrlT& c = *reinterpret_cast<CtrlT*>(staging_base + (size_t)EPI_WARPS * STAGING_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
     const int NT = (p.N + BN - 1) / BN;
+    const int rank = PAIR ? (int)cluster_rank() : 0;
+    const bool leader = rank == 0;
+    const int unit0 = blockIdx.x / S::CTAS;          // this (pair of) CTA's first work unit
+    const int nunits = gridDim.x / S::CTAS;
 
     // ---- set-up: barriers, TMEM, tile list ------------------------------------
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&c.full[s]), 1);
+            mbar_init(smem_u32(&c.full[s]), S::CTAS);
             mbar_init(smem_u32(&c.empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&c.tfull[b]), 1);
-            mbar_init(smem_u32(&c.tempty[b]), EPI_WARPS);
+            mbar_init(smem_u32(&c.tempty[b]), EPI_WARPS * S::CTAS);
         }
         mbar_init(smem_u32(&c.drain), 1);
         c.abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&c.tmem_base), TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc2(smem_u32(&c.tmem_base), TMEM_COLS);
+            tmem_relinquish2();
+        } else {
+            tmem_alloc(smem_u32(&c.tmem_base), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     for (int i = threadIdx.x; i <= E; i += THREADS) c.off[i] = p.offsets[i];
     __syncthreads();
@@ -193,10 +315,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             int acc = 0;
             for (int e = 0; e < E; ++e) {
                 c.tile_start[e] = acc;
-                acc += ((c.off[e + 1] - c.off[e] + BM - 1) / BM) * NT;
+                acc += ((c.off[e + 1] - c.off[e] + S::TILE_M - 1) / S::TILE_M) * NT;
             }
             c.tile_start[E] = acc;
-            c.nactive = acc;   // number of tiles
+            c.nactive = acc;   // number of work units
         }
     } else {
         for (int e = threadIdx.x; e < E; e += THREADS) {
@@ -211,15 +333,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (threadIdx.x == 0) {
             int act = 0;
             for (int e = 0; e < E; ++e) act += (c.off[e + 1] - c.off[e]) > 0;
-            const int MT = (p.M + BM - 1) / BM;
-            c.nactive = (p.accumulate ? act : E) * MT * NT;  // number of tiles
+            const int MT = (p.M + S::TILE_M - 1) / S::TILE_M;
+            c.nactive = (p.accumulate ? act : E) * MT * NT;  // number of work units
         }
     }
     tc_fence_before();
-    __syncthreads();
+    if (PAIR) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = c.tmem_base;
-    const int num_tiles = c.nactive;
+    const int num_units = c.nactive;
 
     if (warp == 0) {
         // ---- TMA producer ---------------------------------------------------------
@@ -231,8 +353,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             int issued_parity[STAGES];
             for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const Tile ti = get_tile<VAR_K>(c, p, t, ecur);
+            for (int t = unit0; t < num_units && ok; t += nunits) {
+                const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
                 for (int kb = 0; kb < ti.num_kb; ++kb) {
                     if (!mbar_wait_bounded(smem_u32(&c.empty[stage]), phase ^ 1, p.limit_ns,
                                            &c.abort_flag)) {
@@ -240,49 +362,61 @@ __global__ void __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t sA = smem_u32(base + (size_t)stage * STAGE_BYTES);
-                    const uint32_t sB = sA + A_BYTES;
+                    const uint32_t sA = smem_u32(base + (size_t)stage * S::STAGE_BYTES);
+                    const uint32_t sB = sA + S::A_BYTES;
                     const uint32_t fb = smem_u32(&c.full[stage]);
+                    const uint32_t fbc = PAIR ? mapa_rank(fb, 0) : fb;   // even CTA's barrier
+                    const int nB = ti.nt * BN + rank * S::BN_CTA;      // first B column held here
                     // bytes: full boxes, except MN slabs lying wholly past the edge
                     uint32_t bytes = 0;
                     if (!VAR_K) {
-                        bytes += A_BYTES;
-                        if (!B_MN) bytes += B_BYTES;
+                        bytes += S::A_BYTES;
+                        if (!B_MN) bytes += S::B_BYTES;
                         else
-                            for (int i = 0; i < BN / 64; ++i)
-                                if (ti.nt * BN + 64 * i < p.N) bytes += SLAB_BYTES;
+                            for (int i = 0; i < S::BN_CTA / 64; ++i)
+                                if (nB + 64 * i < p.N) bytes += SLAB_BYTES;
                     } else {
+                        const int mA = ti.mt * S::TILE_M + rank * BM;
                         for (int i = 0; i < BM / 64; ++i)
-                            if (ti.mt * BM + 64 * i < p.M) bytes += SLAB_BYTES;
-                        for (int i = 0; i < BN / 64; ++i)
-                            if (ti.nt * BN + 64 * i < p.N) bytes += SLAB_BYTES;
+                            if (mA + 64 * i < p.M) bytes += SLAB_BYTES;
+                        for (int i = 0; i < S::BN_CTA / 64; ++i)
+                            if (nB + 64 * i < p.N) bytes += SLAB_BYTES;
                     }
-                    mbar_arrive_expect_tx(fb, bytes);
+                    if (PAIR && !leader) mbar_arrive_expect_tx_cluster(fbc, bytes);
+                    else mbar_arrive_expect_tx(fb, bytes);
+                    auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+                        if (PAIR) tma2_load_2d(dst, m, fbc, c0, c1);
+                        else tma_load_2d(dst, m, fb, c0, c1);
+                    };
+                    auto load3 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2) {
+                        if (PAIR) tma2_load_3d(dst, m, fbc, c0, c1, c2);
+                        else tma_load_3d(dst, m, fb, c0, c1, c2);
+                    };
                     if (!VAR_K) {
-                        tma_load_2d(sA, &mapA, fb, kb * BK, ti.row0);
+                        load2(sA, &mapA, kb * BK, ti.row0);
                         if (!B_MN) {
-                            tma_load_3d(sB, &mapB, fb, kb * BK, ti.nt * BN, ti.e);
+                            load3(sB, &mapB, kb * BK, nB, ti.e);
                         } else {
-                            for (int i = 0; i < BN / 64; ++i)
-                                if (ti.nt * BN + 64 * i < p.N)
-                                    tma_load_3d(sB + i * SLAB_BYTES, &mapB, fb,
-                                                ti.nt * BN + 64 * i, kb * BK, ti.e);
+                            for (int i = 0; i < S::BN_CTA / 64; ++i)
+                                if (nB + 64 * i < p.N)
+                                    load3(sB + i * SLAB_BYTES, &mapB, nB + 64 * i, kb * BK, ti.e);
                         }
                     } else {
                         const int r = ti.row0 + kb * BK;
+                        const int mA = ti.mt * S::TILE_M + rank * BM;
                         for (int i = 0; i < BM / 64; ++i)
-                            if (ti.mt * BM + 64 * i < p.M)
-                                tma_load_2d(sA + i * SLAB_BYTES, &mapA, fb, ti.mt * BM + 64 * i, r);
-                        for (int i = 0; i < BN / 64; ++i)
-                            if (ti.nt * BN + 64 * i < p.N)
-                                tma_load_2d(sB + i * SLAB_BYTES, &mapB, fb, ti.nt * BN + 64 * i, r);
+                            if (mA + 64 * i < p.M)
+                                load2(sA + i * SLAB_BYTES, &mapA, mA + 64 * i, r);
+                        for (int i = 0; i < S::BN_CTA / 64; ++i)
+                            if (nB + 64 * i < p.N)
+                                load2(sB + i * SLAB_BYTES, &mapB, nB + 64 * i, r);
                     }
                     issued_parity[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok) {
-                // wait (bounded) for every copy this thread started
+            if (!ok && (!PAIR || leader)) {
+                // wait (bounded) for every copy this CTA's barriers are counting
                 for (int s = 0; s < STAGES; ++s)
                     if (issued_parity[s] >= 0)
                         mbar_wait_bounded(smem_u32(&c.full[s]), (uint32_t)issued_parity[s],
@@ -290,96 +424,80 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        // ---- MMA issuer -------------------------------------------------------------
-        constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
-        int stage = 0, acc = 0, ecur = 0;
-        uint32_t phase = 0, acc_phase = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const Tile ti = get_tile<VAR_K>(c, p, t, ecur);
-            if (ti.num_kb == 0) continue;
-            if (!mbar_wait_warp(smem_u32(&c.tempty[acc]), acc_phase ^ 1, p.limit_ns,
-                                &c.abort_flag)) {
-                raise_abort(c, p);
-                break;
-            }
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            for (int kb = 0; kb < ti.num_kb; ++kb) {
-                if (!mbar_wait_warp(smem_u32(&c.full[stage]), phase, p.limit_ns,
+        // ---- MMA issuer (the even CTA of a pair issues for both) ---------------------
+        if (leader) {
+            constexpr uint32_t IDESC = idesc_bf16_f32(S::TILE_M, BN, A_MN, B_MN);
+            int stage = 0, acc = 0, ecur = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = unit0; t < num_units && ok; t += nunits) {
+                const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
+                if (ti.num_kb == 0) continue;
+                if (!mbar_wait_warp(smem_u32(&c.tempty[acc]), acc_phase ^ 1, p.limit_ns,
                                     &c.abort_flag)) {
                     raise_abort(c, p);
-                    ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint8_t* gA = base + (size_t)stage * STAGE_BYTES;
-                uint8_t* gB = gA + A_BYTES;
-                if (VAR_K) {
-                    const int valid = ti.rows - kb * BK;
-                    if (valid < BK) {
-                        // zero K rows past the segment in all 6 MN slabs
-                        const int nz = (BK - valid) * 8;  // 16-byte chunks per slab
-                        for (int sl = 0; sl < (BM + BN) / 64; ++sl) {
-                            uint8_t* slab = (sl < BM / 64) ? gA + sl * SLAB_BYTES
-                                                           : gB + (sl - BM / 64) * SLAB_BYTES;
-                            for (int i = lane; i < nz; i += 32)
-                                *reinterpret_cast<uint4*>(slab + (valid + (i >> 3)) * 128 +
-                                                          ((i & 7) << 4)) = make_uint4(0, 0, 0, 0);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < ti.num_kb; ++kb) {
+                    if (!mbar_wait_warp(smem_u32(&c.full[stage]), phase, p.limit_ns,
+                                        &c.abort_flag)) {
+                        raise_abort(c, p);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sA = smem_u32(base + (size_t)stage * S::STAGE_BYTES);
+                        const uint32_t sB = sA + S::A_BYTES;
+                        // VarK: only whole 16-row groups of the segment
+                        const int nk = VAR_K ? min(BK / 16, (ti.kfull - kb * BK) / 16) : BK / 16;
+                        for (int kk = 0; kk < nk; ++kk) {
+                            const uint64_t ad =
+                                A_MN ? smem_desc_sw128(sA + kk * 2048, SLAB_BYTES, 1024)
+                                     : smem_desc_sw128(sA + kk * 32, 16, 1024);
+                            const uint64_t bd =
+                                B_MN ? smem_desc_sw128(sB + kk * 2048, SLAB_BYTES, 1024)
+                                     : smem_desc_sw128(sB + kk * 32, 16, 1024);
+                            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+                            if (PAIR) tc_mma2_bf16(d_tmem, ad, bd, IDESC, accum);
+                            else tc_mma_bf16(d_tmem, ad, bd, IDESC, accum);
                         }
-                        fence_proxy_async_smem();
+                        if (PAIR) tc_commit2_both(smem_u32(&c.empty[stage]));
+                        else tc_commit(smem_u32(&c.empty[stage]));
                     }
                     __syncwarp();
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
+                if (!ok) break;
                 if (lane == 0) {
-                    const uint32_t sA = smem_u32(gA), sB = smem_u32(gB);
-                    #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad =
-                            A_MN ? smem_desc_sw128(sA + kk * 2048, SLAB_BYTES, 1024)
-                                 : smem_desc_sw128(sA + kk * 32, 16, 1024);
-                        const uint64_t bd =
-                            B_MN ? smem_desc_sw128(sB + kk * 2048, SLAB_BYTES, 1024)
-                                 : smem_desc_sw128(sB + kk * 32, 16, 1024);
-                        tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                    }
-                    tc_commit(smem_u32(&c.empty[stage]));
+                    if (PAIR) tc_commit2_both(smem_u32(&c.tfull[acc]));
+                    else tc_commit(smem_u32(&c.tfull[acc]));
                 }
                 __syncwarp();
-                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(smem_u32(&c.tfull[acc]));
+            // drain: every MMA this warp issued has completed before TMEM is freed
+            if (lane == 0) {
+                if (PAIR) tc_commit2_local(smem_u32(&c.drain));
+                else tc_commit(smem_u32(&c.drain));
+            }
             __syncwarp();
-            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            mbar_wait_bounded(smem_u32(&c.drain), 0, p.limit_ns, nullptr);
         }
-        // drain: every MMA this warp issued has completed before TMEM is freed
-        if (lane == 0) tc_commit(smem_u32(&c.drain));
-        __syncwarp();
-        mbar_wait_bounded(smem_u32(&c.drain), 0, p.limit_ns, nullptr);
     } else {
         // ---- epilogue warps ----------------------------------------------------------
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const int half = (warp - 2) >> 2;       // which 128 columns of the 256
         uint8_t* stg = staging_base + (warp - 2) * STAGING_BYTES;
+        const uint32_t tempty_local0 = smem_u32(&c.tempty[0]);
+        const uint32_t tempty_local1 = smem_u32(&c.tempty[1]);
         int acc = 0, ecur = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            const Tile ti = get_tile<VAR_K>(c, p, t, ecur);
-            if (ti.num_kb == 0) {
-                // VarK expert without rows and accumulate == 0: gradient is zero
-                if (VAR_K && !p.accumulate) {
-                    const int col0 = ti.nt * BN + half * 128;
-                    for (int rr = 0; rr < 32; ++rr) {
-                        const int m = ti.mt * BM + q * 32 + rr;
-                        const int col = col0 + lane * 4;
-                        if (m < p.M && col < p.N)
-                            *reinterpret_cast<float4*>(p.outf + ((int64_t)ti.e * p.M + m) * p.N + col) =
-                                make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                }
-                continue;
-            }
+        for (int t = unit0; t < num_units; t += nunits) {
+            const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
+            const bool mma_tile = ti.num_kb > 0;
             // GELU' epilogue: the saved pre-activation H of this thread's row is
             // fetched ahead (chunk 0 before the accumulator is ready, chunk c+1
             // while chunk c is processed), so its latency overlaps other work.
@@ -394,12 +512,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                                             (const __nv_bfloat16*)p.aux + grow_lane * p.N + col0 + u * 8))
                                       : make_uint4(0, 0, 0, 0);
             }
-            if (!mbar_wait_warp(smem_u32(&c.tfull[acc]), acc_phase, p.limit_ns,
-                                &c.abort_flag)) {
-                raise_abort(c, p);
-                break;
+            if (mma_tile) {
+                if (!mbar_wait_warp(smem_u32(&c.tfull[acc]), acc_phase, p.limit_ns,
+                                    &c.abort_flag)) {
+                    raise_abort(c, p);
+                    break;
+                }
+                tc_fence_after();
             }
-            tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
@@ -407,7 +527,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int col0 = ti.nt * BN + cl;             // global column
                 if (col0 >= p.N) break;                       // N % 64 == 0: whole chunks
                 float v[32];
-                tmem_ld32(trow + (uint32_t)cl, v);
+                if (mma_tile) {
+                    tmem_ld32(trow + (uint32_t)cl, v);
+                } else {
+                    #pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                }
                 if (!VAR_K) {
                     const int64_t grow0 = (int64_t)ti.row0 + q * 32;   // global row of lane 0
                     const int valid = ti.rows - q * 32;
@@ -473,9 +598,29 @@ __global__ void __launch_bounds__(THREADS, 1)
                         __syncwarp();
                     }
                 } else {
-                    // fp32 weight gradient, 16 columns (64 B per row) at a time
-                    const int m0 = ti.mt * BM + q * 32;
+                    // fp32 weight gradient.  The last rows of the segment that do
+                    // not fill a 16-row group are added here on the CUDA cores
+                    // (after the tensor-core sum, in row order).
+                    const int m0 = ti.mt * S::TILE_M + rank * BM + q * 32;
                     const int valid = p.M - m0;
+                    const int m = m0 + lane;
+                    for (int pr = ti.row0 + ti.kfull; pr < ti.row0 + ti.rows; ++pr) {
+                        const float a =
+                            (m < p.M) ? __bfloat162float(((const __nv_bfloat16*)p.act_a)[(int64_t)pr * p.M + m])
+                                      : 0.f;
+                        const __nv_bfloat16* brow = (const __nv_bfloat16*)p.act_b + (int64_t)pr * p.N + col0;
+                        #pragma unroll
+                        for (int u = 0; u < 32; u += 8) {
+                            const uint4 bv = __ldg(reinterpret_cast<const uint4*>(brow + u));
+                            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&bv);
+                            #pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 f = __bfloat1622float2(h[i]);
+                                v[u + 2 * i] = fmaf(a, f.x, v[u + 2 * i]);
+                                v[u + 2 * i + 1] = fmaf(a, f.y, v[u + 2 * i + 1]);
+                            }
+                        }
+                    }
                     #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         #pragma unroll
@@ -503,19 +648,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
+            if (!mma_tile) continue;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&c.tempty[acc]));
+            if (lane == 0) {
+                const uint32_t tb = acc ? tempty_local1 : tempty_local0;
+                if (PAIR && !leader) mbar_arrive_cluster(mapa_rank(tb, 0));  // even CTA's barrier
+                else mbar_arrive(tb);
+            }
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
     }
 
     // ---- teardown ------------------------------------------------------------------
     tc_fence_before();
-    __syncthreads();
+    if (PAIR) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if (PAIR) tmem_dealloc2(tmem_base, TMEM_COLS);
+        else tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -551,27 +702,80 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
     return r == CUDA_SUCCESS;
 }
 
-template <bool VAR_K, bool A_MN, bool B_MN, int EPI>
+// Which CTA shape to use: CTA pairs unless MOE_GEMM_PAIR=0 selects single CTAs.
+bool use_pairs() {
+    static const bool v = [] {
+        const char* s = getenv("MOE_GEMM_PAIR");
+        return !(s && s[0] == '0');
+    }();
+    return v;
+}
+
+template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool PAIR>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p,
-                      int64_t tiles_upper, cudaStream_t st) {
-    auto kern = gemm_tc_kernel<VAR_K, A_MN, B_MN, EPI>;
+                      int64_t units_upper, cudaStream_t st) {
+    auto kern = gemm_tc_kernel<VAR_K, A_MN, B_MN, EPI, PAIR>;
+    constexpr size_t SMEM = smem_bytes<PAIR>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
+    static int max_units = 0;   // co-resident CTAs (or pairs)
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)SMEM_BYTES);
+                                        (int)SMEM);
+        if (attr_err != cudaSuccess) return;
+        if (PAIR) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(2 * device_sm_count());
+            cfg.blockDim = dim3(THREADS);
+            cfg.dynamicSmemBytes = SMEM;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int n = 0;
+            attr_err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            max_units = n > 0 ? n : device_sm_count() / 2;
+        } else {
+            max_units = device_sm_count();
+        }
     });
     if (attr_err != cudaSuccess) return attr_err;
-    const int64_t sms = device_sm_count();
-    const unsigned grid = (unsigned)(tiles_upper < sms ? (tiles_upper > 0 ? tiles_upper : 1) : sms);
-    kern<<<grid, THREADS, SMEM_BYTES, st>>>(a, b, p);
-    return cudaGetLastError();
+    const int64_t units = units_upper < max_units ? (units_upper > 0 ? units_upper : 1) : max_units;
+    if (!PAIR) {
+        kern<<<(unsigned)units, THREADS, SMEM, st>>>(a, b, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * units));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, b, p);
+}
+
+template <bool VAR_K, bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_either(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p,
+                          int64_t units1, int64_t units2, cudaStream_t st) {
+    if (use_pairs()) return launch_tc<VAR_K, A_MN, B_MN, EPI, true>(a, b, p, units2, st);
+    return launch_tc<VAR_K, A_MN, B_MN, EPI, false>(a, b, p, units1, st);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t st) {
     if (g.E > MAX_E || g.N % 64 || g.K % 64) return cudaErrorInvalidValue;
+    const bool pair = use_pairs();
+    const uint32_t bn_cta = pair ? BN / 2 : BN;
     CUtensorMap ma, mb;
     {
         const uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.P};
@@ -582,7 +786,7 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     if (g.weight_kmajor) {
         const uint64_t dims[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.E};
         const uint64_t strides[2] = {(uint64_t)g.K * 2, (uint64_t)g.N * g.K * 2};
-        const uint32_t box[3] = {BK, BN, 1};
+        const uint32_t box[3] = {BK, bn_cta, 1};
         if (!make_map(&mb, g.weight, 3, dims, strides, box)) return cudaErrorInvalidValue;
     } else {
         const uint64_t dims[3] = {(uint64_t)g.N, (uint64_t)g.K, (uint64_t)g.E};
@@ -595,20 +799,21 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     p.offsets = g.offsets; p.bias = g.bias; p.aux = g.aux; p.out0 = g.out0; p.out1 = g.out1;
     p.outf = nullptr; p.accumulate = 0; p.status = status; p.limit_ns = wait_limit_ns();
     const int64_t NT = (g.N + BN - 1) / BN;
-    const int64_t upper = ((g.P + BM - 1) / BM + g.E) * NT;
+    const int64_t u1 = ((g.P + BM - 1) / BM + g.E) * NT;
+    const int64_t u2 = ((g.P + 2 * BM - 1) / (2 * BM) + g.E) * NT;
     switch (g.epi) {
         case Epi::BiasGelu:
             if (!g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_tc<false, false, false, (int)Epi::BiasGelu>(ma, mb, p, upper, st);
+            return launch_either<false, false, false, (int)Epi::BiasGelu>(ma, mb, p, u1, u2, st);
         case Epi::Bias:
             if (!g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_tc<false, false, false, (int)Epi::Bias>(ma, mb, p, upper, st);
+            return launch_either<false, false, false, (int)Epi::Bias>(ma, mb, p, u1, u2, st);
         case Epi::GeluGrad:
             if (g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_tc<false, false, true, (int)Epi::GeluGrad>(ma, mb, p, upper, st);
+            return launch_either<false, false, true, (int)Epi::GeluGrad>(ma, mb, p, u1, u2, st);
         case Epi::Plain:
             if (g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_tc<false, false, true, (int)Epi::Plain>(ma, mb, p, upper, st);
+            return launch_either<false, false, true, (int)Epi::Plain>(ma, mb, p, u1, u2, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -631,9 +836,12 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
     TcParams p{};
     p.E = g.E; p.M = g.M; p.N = g.N; p.K = 0; p.P = g.P;
     p.offsets = g.offsets; p.outf = g.out; p.accumulate = g.accumulate;
+    p.act_a = g.act_a; p.act_b = g.act_b;
     p.status = status; p.limit_ns = wait_limit_ns();
-    const int64_t upper = (int64_t)g.E * ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
-    return launch_tc<true, true, true, (int)Epi::Plain>(ma, mb, p, upper, st);
+    const int64_t NT = (g.N + BN - 1) / BN;
+    const int64_t u1 = (int64_t)g.E * ((g.M + BM - 1) / BM) * NT;
+    const int64_t u2 = (int64_t)g.E * ((g.M + 2 * BM - 1) / (2 * BM)) * NT;
+    return launch_either<true, true, true, (int)Epi::Plain>(ma, mb, p, u1, u2, st);
 }
 
 }  // namespace moe

@@ -39,8 +39,8 @@ cudaError_t launch_dispatch_rank(const moe_shape& s, const int32_t* idx,
 cudaError_t launch_route_bwd(const moe_shape& s, const float* dw, const float* logits,
                              const int32_t* idx, const float* w, const int32_t* perm,
                              const int32_t* offsets, const void* x, const void* Wg,
-                             void* dx, float* dWg, int accumulate, float* dL,
-                             float* partial, cudaStream_t st);
+                             const void* dx_perm, const int32_t* pos, void* dx, float* dWg,
+                             int accumulate, float* dL, float* partial, cudaStream_t st);
 size_t route_bwd_workspace(const moe_shape& s);  // dL + partials, bytes
 
 // A4, A6/A9, A7

@@ -240,9 +240,9 @@ moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const voi
 
 moe_status moe_route_bwd(const moe_shape* s, const float* dw, const float* logits,
                          const int32_t* idx, const float* w, const int32_t* perm,
-                         const int32_t* offsets, const void* x, const void* Wg, void* dx,
-                         float* dWg, int accumulate, void* ws, int32_t* dev_status,
-                         moe_stream_t stream) {
+                         const int32_t* offsets, const void* x, const void* Wg,
+                         const void* dx_perm, const int32_t* pos, void* dx, float* dWg,
+                         int accumulate, void* ws, int32_t* dev_status, moe_stream_t stream) {
     (void)dev_status;
     moe_status r = check_shape(s);
     if (r != MOE_OK) return r;
@@ -255,11 +255,12 @@ moe_status moe_route_bwd(const moe_shape* s, const float* dw, const float* logit
     if (!ok_ptr(dw) || !ok_ptr(logits) || !ok_ptr(idx) || !ok_ptr(w) || !ok_ptr(perm) ||
         !ok_ptr(offsets) || !ok_ptr(x) || !ok_ptr(Wg) || !ok_ptr(dx) || !ok_ptr(ws))
         return MOE_ERR_INVALID;
+    if (dx_perm != nullptr && !(aligned16(dx_perm) && ok_ptr(pos))) return MOE_ERR_INVALID;
     float* dL = (float*)ws;
     const size_t dl_bytes = (size_t)s->T * (size_t)(s->renorm ? s->k : s->E) * sizeof(float);
     float* partial = (float*)((uint8_t*)ws + align_up(dl_bytes));
-    return cuda_status(launch_route_bwd(*s, dw, logits, idx, w, perm, offsets, x, Wg, dx, dWg,
-                                        accumulate, dL, partial, st));
+    return cuda_status(launch_route_bwd(*s, dw, logits, idx, w, perm, offsets, x, Wg, dx_perm,
+                                        pos, dx, dWg, accumulate, dL, partial, st));
 }
 
 }  // extern "C"

@@ -351,41 +351,57 @@ __global__ void __launch_bounds__(256) router_gate_small_kernel(
     int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ block_counts,
     int32_t* status) {
     using V = Vec<TIn>;
+    // tokens whose dot products a warp accumulates together (sharing Wg loads)
+    constexpr int TPW = EP <= 8 ? 4 : (EP <= 16 ? 2 : 1);
     __shared__ uint32_t bits[256][kRouteWords];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     zero_bits(bits, E);
     __syncthreads();
     const int nv = d / V::N;
-    for (int tt = 0; tt < 8; ++tt) {
-        const int tok = warp * 8 + tt;
-        const int64_t t = (int64_t)blockIdx.x * kRouteBlockTokens + tok;
-        if (t >= T) break;
-        float acc[EP];
+    for (int tt0 = 0; tt0 < 8; tt0 += TPW) {
+        const int64_t t0 = (int64_t)blockIdx.x * kRouteBlockTokens + warp * 8 + tt0;
+        if (t0 >= T) break;
+        float acc[TPW][EP];
         #pragma unroll
-        for (int e = 0; e < EP; ++e) acc[e] = 0.f;
-        #pragma unroll 4
+        for (int i = 0; i < TPW; ++i)
+            #pragma unroll
+            for (int e = 0; e < EP; ++e) acc[i][e] = 0.f;
+        #pragma unroll 2
         for (int c = lane; c < nv; c += 32) {
-            float xv[V::N], wv[V::N];
-            V::load(x + t * d + (int64_t)c * V::N, xv);
+            float xv[TPW][V::N], wv[V::N];
+            #pragma unroll
+            for (int i = 0; i < TPW; ++i) {
+                if (t0 + i < T) V::load(x + (t0 + i) * d + (int64_t)c * V::N, xv[i]);
+                else
+                    #pragma unroll
+                    for (int u = 0; u < V::N; ++u) xv[i][u] = 0.f;
+            }
             #pragma unroll
             for (int e = 0; e < EP; ++e) {
                 if (e < E) {
                     V::load(Wg + (int64_t)e * d + (int64_t)c * V::N, wv);
                     #pragma unroll
-                    for (int u = 0; u < V::N; ++u) acc[e] = fmaf(xv[u], wv[u], acc[e]);
+                    for (int i = 0; i < TPW; ++i)
+                        #pragma unroll
+                        for (int u = 0; u < V::N; ++u) acc[i][e] = fmaf(xv[i][u], wv[u], acc[i][e]);
                 }
             }
         }
-        const float r = reduce_scatter<EP>(acc, lane);
-        // lane e (< E) takes expert e's sum
-        const float le = __shfl_sync(kFull, r, (lane % EP) * (32 / EP));
-        float L[1];
-        L[0] = -INFINITY;
-        if (lane < E) {
-            L[0] = le + (beta ? beta[lane] : 0.f);
-            logits[t * E + lane] = L[0];
+        #pragma unroll
+        for (int i = 0; i < TPW; ++i) {
+            const int64_t t = t0 + i;
+            const float r = reduce_scatter<EP>(acc[i], lane);
+            if (t >= T) continue;   // warp-uniform
+            // lane e (< E) takes expert e's sum
+            const float le = __shfl_sync(kFull, r, (lane % EP) * (32 / EP));
+            float L[1];
+            L[0] = -INFINITY;
+            if (lane < E) {
+                L[0] = le + (beta ? beta[lane] : 0.f);
+                logits[t * E + lane] = L[0];
+            }
+            gate_token<1>(t, E, k, renorm, L, lane, warp * 8 + tt0 + i, bits, idx, w, status);
         }
-        gate_token<1>(t, E, k, renorm, L, lane, tok, bits, idx, w, status);
     }
     __syncthreads();
     write_block_counts(bits, E, nblk, block_counts);
@@ -499,7 +515,8 @@ template <typename TIn, int EPL>
 __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     int64_t T, int d, int E, int k, int renorm, const float* __restrict__ dw,
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
-    const float* __restrict__ w, const TIn* __restrict__ Wg, TIn* __restrict__ dx,
+    const float* __restrict__ w, const TIn* __restrict__ Wg,
+    const TIn* __restrict__ dx_perm, const int32_t* __restrict__ pos, TIn* __restrict__ dx,
     float* __restrict__ dL) {
     __shared__ float g_s[8][256];
     __shared__ int e_s[8][256];
@@ -576,9 +593,26 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     }
     __syncwarp();
     constexpr int VN = V::N;
+    int32_t p[16];
+    if (dx_perm)
+        #pragma unroll
+        for (int j = 0; j < 16; ++j) p[j] = (j < k) ? pos[t * k + j] : 0;
     for (int c = lane * VN; c < d; c += 32 * VN) {
         float acc[VN], wv[VN];
-        V::load(dx + t * d + c, acc);
+        if (dx_perm) {
+            // permute backward fused in: dx = sum_j dx_perm[pos[t,j]] + router term
+            #pragma unroll
+            for (int u = 0; u < VN; ++u) acc[u] = 0.f;
+            #pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (j >= k) break;
+                V::load(dx_perm + (int64_t)p[j] * d + c, wv);
+                #pragma unroll
+                for (int u = 0; u < VN; ++u) acc[u] += wv[u];
+            }
+        } else {
+            V::load(dx + t * d + c, acc);
+        }
         for (int i = 0; i < ng; ++i) {
             const float g = g_s[warp][i];
             V::load(Wg + (int64_t)e_s[warp][i] * d + c, wv);
@@ -722,20 +756,20 @@ __global__ void __launch_bounds__(256) dwg_reduce_dense_kernel(int d, int E, int
 template <typename TIn>
 cudaError_t route_bwd_typed(const moe_shape& s, const float* dw, const float* logits,
                             const int32_t* idx, const float* w, const int32_t* perm,
-                            const int32_t* offsets, const TIn* x, const TIn* Wg, TIn* dx,
-                            float* dWg, int accumulate, float* dL, float* partial,
-                            cudaStream_t st) {
+                            const int32_t* offsets, const TIn* x, const TIn* Wg,
+                            const TIn* dx_perm, const int32_t* pos, TIn* dx, float* dWg,
+                            int accumulate, float* dL, float* partial, cudaStream_t st) {
     const int64_t T = s.T;
     const int d = s.d, E = s.E, k = s.k;
     const unsigned gx = (unsigned)((T + 7) / 8);
     if (E <= 32)
-        route_bwd_dx_kernel<TIn, 1><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx, dL);
+        route_bwd_dx_kernel<TIn, 1><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx_perm, pos, dx, dL);
     else if (E <= 64)
-        route_bwd_dx_kernel<TIn, 2><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx, dL);
+        route_bwd_dx_kernel<TIn, 2><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx_perm, pos, dx, dL);
     else if (E <= 128)
-        route_bwd_dx_kernel<TIn, 4><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx, dL);
+        route_bwd_dx_kernel<TIn, 4><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx_perm, pos, dx, dL);
     else
-        route_bwd_dx_kernel<TIn, 8><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx, dL);
+        route_bwd_dx_kernel<TIn, 8><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx_perm, pos, dx, dL);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     constexpr int VN = Vec<TIn>::N;
@@ -853,15 +887,16 @@ size_t route_bwd_workspace(const moe_shape& s) {
 
 cudaError_t launch_route_bwd(const moe_shape& s, const float* dw, const float* logits,
                              const int32_t* idx, const float* w, const int32_t* perm,
-                             const int32_t* offsets, const void* x, const void* Wg, void* dx,
-                             float* dWg, int accumulate, float* dL, float* partial,
-                             cudaStream_t st) {
+                             const int32_t* offsets, const void* x, const void* Wg,
+                             const void* dx_perm, const int32_t* pos, void* dx, float* dWg,
+                             int accumulate, float* dL, float* partial, cudaStream_t st) {
     if (s.dtype == MOE_BF16)
         return route_bwd_typed(s, dw, logits, idx, w, perm, offsets, (const __nv_bfloat16*)x,
-                               (const __nv_bfloat16*)Wg, (__nv_bfloat16*)dx, dWg, accumulate,
-                               dL, partial, st);
+                               (const __nv_bfloat16*)Wg, (const __nv_bfloat16*)dx_perm, pos,
+                               (__nv_bfloat16*)dx, dWg, accumulate, dL, partial, st);
     return route_bwd_typed(s, dw, logits, idx, w, perm, offsets, (const float*)x,
-                           (const float*)Wg, (float*)dx, dWg, accumulate, dL, partial, st);
+                           (const float*)Wg, (const float*)dx_perm, pos, (float*)dx, dWg,
+                           accumulate, dL, partial, st);
 }
 
 cudaError_t launch_bounded_wait(uint64_t limit_ns, int32_t* status, cudaStream_t st) {

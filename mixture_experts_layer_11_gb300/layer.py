@@ -129,12 +129,11 @@ class LayerPass:
                                    self._rows(self.H, c0, c1, k), self._rows(self.A, c0, c1, k),
                                    offs, W1, W2, dXp, self.dW1, self.db1, self.dW2, self.db2, acc,
                                    self.ws, self.status)
-            dxc = self._rows(self.dx, c0, c1)
-            ops.moe_combine_fwd(s, dXp, pos, None, dxc)
+            # permute backward (A9) fused into the router backward (A10)
             ops.moe_route_bwd(s, self._rows(self.dw, c0, c1), self._rows(self.logits, c0, c1),
                               self._rows(self.idx, c0, c1), w, self._rows(self.perm, c0, c1, k),
-                              offs, self._rows(x, c0, c1), Wg, dxc, self.dWg, acc, self.ws,
-                              self.status)
+                              offs, self._rows(x, c0, c1), Wg, dXp, pos,
+                              self._rows(self.dx, c0, c1), self.dWg, acc, self.ws, self.status)
         return self.dx
 
     def offsets_of(self, ci: int) -> torch.Tensor:

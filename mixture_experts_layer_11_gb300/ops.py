@@ -78,7 +78,7 @@ def lib() -> ctypes.CDLL:
             L.moe_combine_bwd.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P]
             L.moe_expert_ffn_bwd.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                              _P, ctypes.c_int, _P, _P, _P]
-            L.moe_route_bwd.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+            L.moe_route_bwd.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                         ctypes.c_int, _P, _P, _P]
             L.moe_debug_bounded_wait.argtypes = [ctypes.c_uint64, _P, _P]
             L.moe_debug_gelu.argtypes = [ctypes.c_int64, _P, _P, _P, ctypes.c_int, _P]
@@ -179,13 +179,13 @@ def moe_expert_ffn_bwd(s, dy_perm, x_perm, H, A, offsets, W1, W2, dx_perm, dW1, 
         _ptr(db2, _F32), int(accumulate), _ptr(ws), _ptr(dev_status, _I32), _stream(stream)))
 
 
-def moe_route_bwd(s, dw, logits, idx, w, perm, offsets, x, Wg, dx, dWg, accumulate, ws,
-                  dev_status, stream=None):
+def moe_route_bwd(s, dw, logits, idx, w, perm, offsets, x, Wg, dx_perm, pos, dx, dWg,
+                  accumulate, ws, dev_status, stream=None):
     _check("moe_route_bwd", lib().moe_route_bwd(
         ctypes.byref(s), _ptr(dw, _F32), _ptr(logits, _F32), _ptr(idx, _I32), _ptr(w, _F32),
         _ptr(perm, _I32), _ptr(offsets, _I32), _ptr(x, _act(s)), _ptr(Wg, _act(s)),
-        _ptr(dx, _act(s)), _ptr(dWg, _F32), int(accumulate), _ptr(ws), _ptr(dev_status, _I32),
-        _stream(stream)))
+        _ptr(dx_perm, _act(s)), _ptr(pos, _I32), _ptr(dx, _act(s)), _ptr(dWg, _F32),
+        int(accumulate), _ptr(ws), _ptr(dev_status, _I32), _stream(stream)))
 
 
 def moe_debug_bounded_wait(limit_ns: int, dev_status, stream=None):

@@ -136,6 +136,8 @@ def router_logits(x, Wg, beta=None) -> np.ndarray:
 def gate(logits, k: int, renorm: int):
     L = _f64(logits)
     T, E = L.shape
+    if not 1 <= k <= E:
+        raise ValueError(f"top-k needs 1 <= k <= E (k={k}, E={E})")
     idx = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float64)
     lib().oracle_gate(T, E, k, int(renorm), _pd(L), _pi(idx), _pd(w))
@@ -145,6 +147,8 @@ def gate(logits, k: int, renorm: int):
 def dispatch(idx, E: int):
     idx = _i32(idx)
     T, k = idx.shape
+    if idx.size and (idx.min() < 0 or idx.max() >= E):
+        raise ValueError("expert index out of range")
     counts = np.empty(E, np.int32)
     offsets = np.empty(E + 1, np.int32)
     pos = np.empty((T, k), np.int32)

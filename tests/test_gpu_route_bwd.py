@@ -1,0 +1,56 @@
+"""GPU parity of the router backward (A10) against the oracle, with the
+permute backward (A9) fused in (dx = sum_j dX_perm[pos] + router term) and
+without it (dx += router term).  Routing, positions and the fp32 logits come
+from the oracle on both sides."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_11_gb300 import ops, synth
+from parity_util import assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+CASES = [("f32", 256, 64, 4, 1, 0), ("bf16", 1000, 768, 8, 2, 1), ("bf16", 777, 256, 64, 1, 0),
+         ("bf16", 513, 512, 128, 8, 1), ("f32", 300, 96, 16, 4, 0)]
+
+
+@pytest.mark.parametrize("dtype,T,d,E,k,renorm", CASES)
+@pytest.mark.parametrize("fused", [True, False])
+def test_route_bwd(dtype, T, d, E, k, renorm, fused):
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    rb = dtype == "bf16"
+    cfg = synth.MoEConfig("t", T=T, d=d, f=64, E=E, k=k, renorm=renorm, dtype=dtype)
+    inp = synth.make_inputs(cfg, seed=T + E)
+    L = torch.from_numpy(oracle.router_logits(inp["x"], inp["Wg"])).float()
+    idx, w = oracle.gate(L.double().numpy(), k, renorm)
+    counts, offsets, pos, perm = oracle.dispatch(idx, E)
+    g = torch.Generator().manual_seed(T)
+    dw = torch.randn(T, k, generator=g, dtype=torch.float32)
+    dXp = torch.randn(T * k, d, generator=g, dtype=torch.float32).to(tdt)
+    dx0 = torch.randn(T, d, generator=g, dtype=torch.float32).to(tdt)
+    w32 = w.astype(np.float32)
+    _, dxr, rdWg = oracle.router_bwd(dw, L.double().numpy(), idx, w32, inp["x"], inp["Wg"], renorm)
+    if fused:
+        ref_dx = oracle.combine(dXp, pos, None, False) + dxr
+    else:
+        ref_dx = dx0.double().numpy() + dxr
+    if rb:
+        ref_dx = oracle.round_bf16_array(ref_dx)
+    s = ops.make_shape(T, d, 64, E, k, dtype, renorm)
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dt).to(DEV)  # noqa: E731
+    dx = dx0.clone().to(DEV)
+    dWg = torch.full((E, d), float("nan"), dtype=torch.float32, device=DEV)
+    ws = torch.empty(ops.moe_workspace_size(s), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ops.moe_route_bwd(s, dw.to(DEV), L.to(DEV), t(idx, torch.int32), t(w32, torch.float32),
+                      t(perm, torch.int32), t(offsets, torch.int32), inp["x"].to(DEV),
+                      inp["Wg"].to(DEV), dXp.to(DEV) if fused else None,
+                      t(pos, torch.int32) if fused else None, dx, dWg, 0, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert_close("dx", dx, ref_dx, dtype)
+    # dWg is an fp32 output: sums of exact products of stored values
+    assert_close("dWg", dWg, rdWg, "f32", rel=1e-5 if dtype == "f32" else 1e-4)

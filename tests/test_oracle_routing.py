@@ -122,3 +122,10 @@ def test_dispatch_worked_example():
     np.testing.assert_array_equal(offsets, np.array(g["offsets"], np.int32))
     np.testing.assert_array_equal(pos.reshape(-1), np.array(g["pos"], np.int32))
     np.testing.assert_array_equal(perm, np.array(g["perm"], np.int32))
+
+
+def test_oracle_rejects_invalid_routing_shapes():
+    with pytest.raises(ValueError):
+        oracle.gate(np.zeros((3, 1)), 2, 1)
+    with pytest.raises(ValueError):
+        oracle.dispatch(np.array([[0], [3]], np.int32), 2)
