@@ -197,74 +197,92 @@ def run_ours(args, cfg):
     lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
                    chunk=cfg.chunk, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    st = torch.cuda.current_stream()
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = lambda **kw: torch.cuda.Event(enable_timing=True, **kw)  # noqa: E731
+    x_buf, dy_buf = inp["x"], inp["dy"]   # fixed input buffers (the graph reads these)
 
-    def fwd(x):
-        return lp.forward(x, inp["Wg"], inp["W1"], inp["b1"], inp["W2"], inp["b2"], inp["beta"])
-
-    def bwd(x, dy):
-        return lp.backward(dy, x, inp["Wg"], inp["W1"], inp["W2"])
-
-    # ffn timing hooks: events around the expert GEMM calls on the launching stream
+    # events around the expert-FFN calls (the grouped GEMM launches), recorded
+    # on the launching stream; inside a captured graph they are graph nodes
     ffn_events = []
     orig_fwd, orig_bwd = ops.moe_expert_ffn_fwd, ops.moe_expert_ffn_bwd
+    state = {"record": False, "external": False}
 
     def timed(fn, kind):
         def wrapper(*a, **kw):
-            if not recording[0]:
+            if not state["record"]:
                 return fn(*a, **kw)
-            e0, e1 = ev(), ev()
-            e0.record(st)
+            e0, e1 = ev(external=state["external"]), ev(external=state["external"])
+            e0.record()
             r = fn(*a, **kw)
-            e1.record(st)
+            e1.record()
             ffn_events.append((kind, e0, e1))
             return r
         return wrapper
 
-    recording = [False]
     import mixture_experts_layer_11_gb300.layer as layer_mod
     layer_mod.ops.moe_expert_ffn_fwd = timed(orig_fwd, "fwd")
     layer_mod.ops.moe_expert_ffn_bwd = timed(orig_bwd, "bwd")
 
+    def step():
+        lp.forward(x_buf, inp["Wg"], inp["W1"], inp["b1"], inp["W2"], inp["b2"], inp["beta"])
+        lp.backward(dy_buf, x_buf, inp["Wg"], inp["W1"], inp["W2"])
+
     for _ in range(args.warmup):
         flush.fill_(1)
-        fwd(inp["x"])
-        bwd(inp["x"], inp["dy"])
+        step()
     torch.cuda.synchronize()
     lp.check_status()
 
+    graph = None
+    if not args.no_graph:
+        # one whole step (every chunk, forward and backward) as one CUDA graph
+        graph = torch.cuda.CUDAGraph()
+        state.update(record=True, external=True)
+        with torch.cuda.graph(graph):
+            step()
+        state.update(record=False, external=False)
+        graph_ffn = list(ffn_events)
+        ffn_events.clear()
+        graph.replay()
+        torch.cuda.synchronize()
+        lp.check_status()
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    st = torch.cuda.current_stream()
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    recording[0] = True
-    steps = []
+    step_ms = []
+    ffn_ms = {"fwd": 0.0, "bwd": 0.0}
     wall0 = time.perf_counter()
     for _ in range(args.steps):
         flush.fill_(1)
         e0, e1 = ev(), ev()
+        if graph is None:
+            state["record"] = True
         e0.record(st)
-        fwd(inp["x"])
-        bwd(inp["x"], inp["dy"])
+        run_step()
         e1.record(st)
-        steps.append((e0, e1))
-    torch.cuda.synchronize()
+        state["record"] = False
+        torch.cuda.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+        marks = graph_ffn if graph is not None else ffn_events
+        for kind, a, b in marks:
+            ffn_ms[kind] += a.elapsed_time(b)
+        ffn_events.clear()
     wall = time.perf_counter() - wall0
-    recording[0] = False
     if dist:
         dist.barrier()
     clocks = sampler.stop()
     lp.check_status()
-    step_ms = [a.elapsed_time(b) for a, b in steps]
     total_ms = sum(step_ms)
-    ffn_ms = {"fwd": 0.0, "bwd": 0.0}
-    n_ffn = {"fwd": 0, "bwd": 0}
-    for kind, a, b in ffn_events:
-        ffn_ms[kind] += a.elapsed_time(b)
-        n_ffn[kind] += 1
     layer_mod.ops.moe_expert_ffn_fwd, layer_mod.ops.moe_expert_ffn_bwd = orig_fwd, orig_bwd
 
     # ---- end to end through the public API with host buffers ----
@@ -272,19 +290,16 @@ def run_ours(args, cfg):
     dy_h = inp["dy"].cpu().pin_memory()
     y_h = torch.empty_like(x_h).pin_memory()
     dx_h = torch.empty_like(x_h).pin_memory()
-    x_d = torch.empty_like(inp["x"])
-    dy_d = torch.empty_like(inp["dy"])
     e2e_steps = []
     for i in range(args.warmup + args.steps):
         flush.fill_(1)
         e0, e1 = ev(), ev()
         e0.record(st)
-        x_d.copy_(x_h, non_blocking=True)
-        dy_d.copy_(dy_h, non_blocking=True)
-        y = fwd(x_d)
-        dx = bwd(x_d, dy_d)
-        y_h.copy_(y, non_blocking=True)
-        dx_h.copy_(dx, non_blocking=True)
+        x_buf.copy_(x_h, non_blocking=True)
+        dy_buf.copy_(dy_h, non_blocking=True)
+        run_step()
+        y_h.copy_(lp.y, non_blocking=True)
+        dx_h.copy_(lp.dx, non_blocking=True)
         e1.record(st)
         if i >= args.warmup:
             e2e_steps.append((e0, e1))
@@ -322,6 +337,7 @@ def run_ours(args, cfg):
         "config": {"workload": workload_desc(cfg), "T": cfg.T, "d_model": cfg.d,
                    "d_ffn": cfg.f, "E": cfg.E, "k": cfg.k,
                    "l2": "flushed between steps (256 MiB write, outside the step timing)",
+                   "launch": "one CUDA graph per step" if graph is not None else "eager",
                    "parallelism": f"replicas x{world}"},
         "roofline": {
             "bound": "tensor", "kernel": "grouped expert GEMM (tcgen05), all expert FFN calls",
@@ -356,6 +372,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the step's kernels one by one instead of as one CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
