@@ -10,7 +10,7 @@
  *   A3  counts, offsets, pos, perm                 stable dispatch by expert
  *   A4  X_perm[pos[t,j]] = x[t]                    permute            [T*k,d]
  *   A5  per expert e over its segment of X_perm:
- *         H = X W1[e]^T + b1[e],  A = GELU(H),  Y_perm = A W2[e]^T + b2[e]
+ *         h = X W1[e]^T + b1[e],  A = GELU(h),  Y_perm = A W2[e]^T + b2[e]
  *   A6  y[t] = sum_j w[t,j] Y_perm[pos[t,j]]       combine            [T,d]
  *   and the backward of each step (A7 combine, A8 expert FFN, A9 permute,
  *   A10 router).
@@ -142,13 +142,14 @@ MOE_API moe_status moe_permute(const moe_shape* s, const void* x, const int32_t*
 /* A5: expert FFN forward over the contiguous expert segments
  * [offsets[e], offsets[e+1]) of X_perm (offsets as produced by moe_route).
  *   W1 [E,f,d], b1 [E,f] (or NULL = 0), W2 [E,d,f], b2 [E,d] (or NULL), dtype
- *   H  [T*k,f] out  pre-activation (kept for the backward)
- *   A  [T*k,f] out  GELU(H), computed from the unrounded pre-activation
+ *   with h = X W1[e]^T + b1[e], the pre-activation (not stored):
+ *   G  [T*k,f] out  GELU'(h), kept for the backward (the only use of h there)
+ *   A  [T*k,f] out  GELU(h)
  *   y_perm [T*k,d] out
  * Experts with no tokens read no weights. */
 MOE_API moe_status moe_expert_ffn_fwd(const moe_shape* s, const void* x_perm,
                               const int32_t* offsets, const void* W1, const void* b1,
-                              const void* W2, const void* b2, void* H, void* A,
+                              const void* W2, const void* b2, void* G, void* A,
                               void* y_perm, void* ws, int32_t* dev_status,
                               moe_stream_t stream);
 
@@ -166,16 +167,17 @@ MOE_API moe_status moe_combine_bwd(const moe_shape* s, const void* dy, const voi
                            moe_stream_t stream);
 
 /* A8: expert FFN backward over the same segments.
- *   dA = dY W2[e];  dH = dA * GELU'(H);  dx_perm = dH W1[e]
+ *   dA = dY W2[e];  dH = dA * G (G = GELU'(h) from moe_expert_ffn_fwd);
+ *   dx_perm = dH W1[e]
  *   dW2[e] (+)= dY^T A,  db2[e] (+)= sum_rows dY
  *   dW1[e] (+)= dH^T X,  db1[e] (+)= sum_rows dH
- * dy_perm, x_perm [T*k,d], H, A [T*k,f] dtype; dx_perm [T*k,d] dtype out;
+ * dy_perm, x_perm [T*k,d], G, A [T*k,f] dtype; dx_perm [T*k,d] dtype out;
  * dW1 [E,f,d], db1 [E,f], dW2 [E,d,f], db2 [E,d] fp32.  accumulate == 0
  * overwrites the weight/bias gradients (experts with no tokens get zeros);
  * accumulate != 0 adds to them (used across dispatch chunks).  The row sums
  * are taken in a fixed order: results are deterministic. */
 MOE_API moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const void* x_perm,
-                              const void* H, const void* A, const int32_t* offsets,
+                              const void* G, const void* A, const int32_t* offsets,
                               const void* W1, const void* W2, void* dx_perm, float* dW1,
                               float* db1, float* dW2, float* db2, int accumulate, void* ws,
                               int32_t* dev_status, moe_stream_t stream);

@@ -86,15 +86,15 @@ __global__ void __launch_bounds__(256) gemm_varm_f32_kernel(GemmVarM g) {
             switch (g.epi) {
                 case Epi::BiasGelu:
                     v += bias ? bias[(int64_t)e * g.N + n] : 0.f;
-                    ((float*)g.out0)[o] = v;
+                    ((float*)g.out0)[o] = gelu_grad_f(v);
                     ((float*)g.out1)[o] = gelu_f(v);
                     break;
                 case Epi::Bias:
                     v += bias ? bias[(int64_t)e * g.N + n] : 0.f;
                     ((float*)g.out0)[o] = v;
                     break;
-                case Epi::GeluGrad:
-                    ((float*)g.out0)[o] = v * gelu_grad_f(((const float*)g.aux)[o]);
+                case Epi::ScaleAux:
+                    ((float*)g.out0)[o] = v * ((const float*)g.aux)[o];
                     break;
                 case Epi::Plain:
                     ((float*)g.out0)[o] = v;

@@ -498,13 +498,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int t = unit0; t < num_units; t += nunits) {
             const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
             const bool mma_tile = ti.num_kb > 0;
-            // GELU' epilogue: the saved pre-activation H of this thread's row is
-            // fetched ahead (chunk 0 before the accumulator is ready, chunk c+1
-            // while chunk c is processed), so its latency overlaps other work.
+            // ScaleAux epilogue (backward of the GELU): the saved GELU'(h) of this
+            // thread's row is fetched ahead (chunk 0 before the accumulator is
+            // ready, chunk c+1 while chunk c is processed).
             uint4 hnext[4];
             const int64_t grow_lane = (int64_t)ti.row0 + q * 32 + lane;
             const bool row_ok = (q * 32 + lane) < ti.rows;
-            if (EPI == (int)Epi::GeluGrad && !VAR_K) {
+            if (EPI == (int)Epi::ScaleAux && !VAR_K) {
                 const int col0 = ti.nt * BN + half * 128;
                 #pragma unroll
                 for (int u = 0; u < 4; ++u)
@@ -553,19 +553,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 }
                             }
                         }
-                        stage_row_bf16(stg, lane, v);
-                        __syncwarp();
-                        store_tile_bf16(stg, lane, (__nv_bfloat16*)p.out0, grow0, valid, N, col0);
-                        __syncwarp();
                         if (EPI == (int)Epi::BiasGelu) {
+                            // one Phi / exp evaluation gives both GELU(h) (kept in v)
+                            // and GELU'(h) (staged and stored for the backward)
+                            float gd[32];
                             #pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = gelu_fast(v[i]);
+                            for (int i = 0; i < 32; ++i) {
+                                const PhiFast r = phi_fast(v[i]);
+                                gd[i] = fmaf(v[i] * 0.39894228040143268f, r.g, r.Phi);
+                                v[i] *= r.Phi;
+                            }
+                            stage_row_bf16(stg, lane, gd);
+                            __syncwarp();
+                            store_tile_bf16(stg, lane, (__nv_bfloat16*)p.out0, grow0, valid, N, col0);
+                            __syncwarp();
                             stage_row_bf16(stg, lane, v);
                             __syncwarp();
                             store_tile_bf16(stg, lane, (__nv_bfloat16*)p.out1, grow0, valid, N, col0);
                             __syncwarp();
+                        } else {
+                            stage_row_bf16(stg, lane, v);
+                            __syncwarp();
+                            store_tile_bf16(stg, lane, (__nv_bfloat16*)p.out0, grow0, valid, N, col0);
+                            __syncwarp();
                         }
-                    } else if (EPI == (int)Epi::GeluGrad) {
+                    } else if (EPI == (int)Epi::ScaleAux) {
                         uint4 hcur[4];
                         #pragma unroll
                         for (int u = 0; u < 4; ++u) hcur[u] = hnext[u];
@@ -583,8 +595,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const float2 f = __bfloat1622float2(h[i]);
-                                v[cc * 8 + 2 * i] *= gelu_grad_fast(f.x);
-                                v[cc * 8 + 2 * i + 1] *= gelu_grad_fast(f.y);
+                                v[cc * 8 + 2 * i] *= f.x;
+                                v[cc * 8 + 2 * i + 1] *= f.y;
                             }
                         }
                         stage_row_bf16(stg, lane, v);
@@ -808,9 +820,9 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
         case Epi::Bias:
             if (!g.weight_kmajor) return cudaErrorInvalidValue;
             return launch_either<false, false, false, (int)Epi::Bias>(ma, mb, p, u1, u2, st);
-        case Epi::GeluGrad:
+        case Epi::ScaleAux:
             if (g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_either<false, false, true, (int)Epi::GeluGrad>(ma, mb, p, u1, u2, st);
+            return launch_either<false, false, true, (int)Epi::ScaleAux>(ma, mb, p, u1, u2, st);
         case Epi::Plain:
             if (g.weight_kmajor) return cudaErrorInvalidValue;
             return launch_either<false, false, true, (int)Epi::Plain>(ma, mb, p, u1, u2, st);

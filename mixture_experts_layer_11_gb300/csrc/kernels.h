@@ -62,7 +62,9 @@ size_t segment_colsum_workspace(const moe_shape& s, int n);
 //   [P, K] times the expert's weight, giving out rows [P, N].  The weight is
 //   [E, N, K] (b_kmajor) or [E, K, N].
 //   VarK ("wgrad"): C_e [M, N] (+)= act_a[seg_e, M]^T act_b[seg_e, N], fp32.
-enum class Epi : int { BiasGelu = 0, Bias = 1, GeluGrad = 2, Plain = 3 };
+// BiasGelu: h = acc + bias; out0 = GELU'(h), out1 = GELU(h).
+// Bias: out0 = acc + bias.  ScaleAux: out0 = acc * aux.  Plain: out0 = acc.
+enum class Epi : int { BiasGelu = 0, Bias = 1, ScaleAux = 2, Plain = 3 };
 
 struct GemmVarM {
     int E, N, K;
@@ -73,9 +75,9 @@ struct GemmVarM {
     bool weight_kmajor;     // true: [E,N,K]
     Epi epi;
     const void* bias;       // [E,N] or null
-    const void* aux;        // GeluGrad: H [P,N]
+    const void* aux;        // ScaleAux: G = GELU'(h) [P,N]
     void* out0;             // [P,N]
-    void* out1;             // BiasGelu: A = GELU(out0 pre-rounding) [P,N]
+    void* out1;             // BiasGelu: A = GELU(h) [P,N]
 };
 struct GemmVarK {
     int E, M, N;

@@ -147,18 +147,18 @@ moe_status moe_permute(const moe_shape* s, const void* x, const int32_t* pos, vo
 
 moe_status moe_expert_ffn_fwd(const moe_shape* s, const void* x_perm, const int32_t* offsets,
                               const void* W1, const void* b1, const void* W2, const void* b2,
-                              void* H, void* A, void* y_perm, void* ws, int32_t* dev_status,
+                              void* G, void* A, void* y_perm, void* ws, int32_t* dev_status,
                               moe_stream_t stream) {
     (void)ws;
     moe_status r = check_gemm_shape(s);
     if (r != MOE_OK) return r;
     if (s->T == 0) return MOE_OK;
     if (!ok_ptr(x_perm) || !ok_ptr(offsets) || !ok_ptr(W1) || !ok_ptr(W2) || !ok_opt(b1) ||
-        !ok_opt(b2) || !ok_ptr(H) || !ok_ptr(A) || !ok_ptr(y_perm) || !ok_status(dev_status))
+        !ok_opt(b2) || !ok_ptr(G) || !ok_ptr(A) || !ok_ptr(y_perm) || !ok_status(dev_status))
         return MOE_ERR_INVALID;
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t P = s->T * s->k;
-    GemmVarM g1{s->E, s->f, s->d, P, offsets, x_perm, W1, true, Epi::BiasGelu, b1, nullptr, H, A};
+    GemmVarM g1{s->E, s->f, s->d, P, offsets, x_perm, W1, true, Epi::BiasGelu, b1, nullptr, G, A};
     GemmVarM g2{s->E, s->d, s->f, P, offsets, A, W2, true, Epi::Bias, b2, nullptr, y_perm, nullptr};
     cudaError_t e;
     if (s->dtype == MOE_BF16) {
@@ -194,7 +194,7 @@ moe_status moe_combine_bwd(const moe_shape* s, const void* dy, const void* y_per
 }
 
 moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const void* x_perm,
-                              const void* H, const void* A, const int32_t* offsets,
+                              const void* G, const void* A, const int32_t* offsets,
                               const void* W1, const void* W2, void* dx_perm, float* dW1,
                               float* db1, float* dW2, float* db2, int accumulate, void* ws,
                               int32_t* dev_status, moe_stream_t stream) {
@@ -211,15 +211,15 @@ moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const voi
         if (e == cudaSuccess) e = cudaMemsetAsync(db2, 0, sizeof(float) * (size_t)E * d, st);
         return cuda_status(e);
     }
-    if (!ok_ptr(dy_perm) || !ok_ptr(x_perm) || !ok_ptr(H) || !ok_ptr(A) || !ok_ptr(offsets) ||
+    if (!ok_ptr(dy_perm) || !ok_ptr(x_perm) || !ok_ptr(G) || !ok_ptr(A) || !ok_ptr(offsets) ||
         !ok_ptr(W1) || !ok_ptr(W2) || !ok_ptr(dx_perm) || !ok_ptr(ws) || !ok_status(dev_status))
         return MOE_ERR_INVALID;
     const int64_t P = s->T * s->k;
     uint8_t* wsb = (uint8_t*)ws;
     void* dH = wsb;
     float* partial = (float*)(wsb + align_up((size_t)P * f * esize(*s)));
-    // dA = dY W2[e] (W2 stored [E,d,f] = [E,K,N]); dH = dA * GELU'(H)
-    GemmVarM g_dh{E, f, d, P, offsets, dy_perm, W2, false, Epi::GeluGrad, nullptr, H, dH, nullptr};
+    // dA = dY W2[e] (W2 stored [E,d,f] = [E,K,N]); dH = dA * G, G = GELU'(h)
+    GemmVarM g_dh{E, f, d, P, offsets, dy_perm, W2, false, Epi::ScaleAux, nullptr, G, dH, nullptr};
     // dX = dH W1[e] (W1 stored [E,f,d] = [E,K,N])
     GemmVarM g_dx{E, d, f, P, offsets, dH, W1, false, Epi::Plain, nullptr, nullptr, dx_perm, nullptr};
     // dW2[e] = dY^T A  ([d, f]);  dW1[e] = dH^T X  ([f, d])

@@ -7,7 +7,7 @@ tokens, the bounded dispatch chunk of PipelinedLLEP ("Flattening Every Memory
 Peak in Long-Context Mixture-of-Experts Training", abstract): routing is per
 token, the histogram / offsets / positions are per chunk, and the weight
 gradients accumulate over chunks in fp32 in chunk order.  The activations a
-chunk's backward needs (X_perm, H, A, Y_perm) stay resident in HBM between
+chunk's backward needs (X_perm, G = GELU'(h), A, Y_perm) stay resident in HBM between
 the forward and the backward; the backward's transient buffers (dY_perm,
 dX_perm and the library workspace) are shared by all chunks.
 
@@ -60,7 +60,7 @@ class LayerPass:
         self.offsets = z(nch, _pad4(E + 1), dt=i32)
         # saved activations of every chunk
         self.X_perm = z(T * k, d)
-        self.H = z(T * k, f)
+        self.G = z(T * k, f)
         self.A = z(T * k, f)
         self.Y_perm = z(T * k, d)
         self.y = z(T, d)
@@ -104,7 +104,7 @@ class LayerPass:
             Xp = self._rows(self.X_perm, c0, c1, k)
             ops.moe_permute(s, xc, pos, Xp)
             Yp = self._rows(self.Y_perm, c0, c1, k)
-            ops.moe_expert_ffn_fwd(s, Xp, offs, W1, b1, W2, b2, self._rows(self.H, c0, c1, k),
+            ops.moe_expert_ffn_fwd(s, Xp, offs, W1, b1, W2, b2, self._rows(self.G, c0, c1, k),
                                    self._rows(self.A, c0, c1, k), Yp, self.ws, self.status)
             ops.moe_combine_fwd(s, Yp, pos, self._rows(self.w, c0, c1), self._rows(self.y, c0, c1))
         return self.y
@@ -126,7 +126,7 @@ class LayerPass:
             ops.moe_combine_bwd(s, self._rows(dy, c0, c1), self._rows(self.Y_perm, c0, c1, k), pos,
                                 w, dYp, self._rows(self.dw, c0, c1))
             ops.moe_expert_ffn_bwd(s, dYp, self._rows(self.X_perm, c0, c1, k),
-                                   self._rows(self.H, c0, c1, k), self._rows(self.A, c0, c1, k),
+                                   self._rows(self.G, c0, c1, k), self._rows(self.A, c0, c1, k),
                                    offs, W1, W2, dXp, self.dW1, self.db1, self.dW2, self.db2, acc,
                                    self.ws, self.status)
             # permute backward (A9) fused into the router backward (A10)

@@ -149,11 +149,11 @@ def moe_permute(s, x, pos, x_perm, stream=None):
                                             _ptr(x_perm, _act(s)), _stream(stream)))
 
 
-def moe_expert_ffn_fwd(s, x_perm, offsets, W1, b1, W2, b2, H, A, y_perm, ws, dev_status,
+def moe_expert_ffn_fwd(s, x_perm, offsets, W1, b1, W2, b2, G, A, y_perm, ws, dev_status,
                        stream=None):
     _check("moe_expert_ffn_fwd", lib().moe_expert_ffn_fwd(
         ctypes.byref(s), _ptr(x_perm, _act(s)), _ptr(offsets, _I32), _ptr(W1, _act(s)),
-        _ptr(b1, _act(s)), _ptr(W2, _act(s)), _ptr(b2, _act(s)), _ptr(H, _act(s)),
+        _ptr(b1, _act(s)), _ptr(W2, _act(s)), _ptr(b2, _act(s)), _ptr(G, _act(s)),
         _ptr(A, _act(s)), _ptr(y_perm, _act(s)), _ptr(ws), _ptr(dev_status, _I32),
         _stream(stream)))
 
@@ -170,10 +170,10 @@ def moe_combine_bwd(s, dy, y_perm, pos, w, dy_perm, dw, stream=None):
         _ptr(dy_perm, _act(s)), _ptr(dw, _F32), _stream(stream)))
 
 
-def moe_expert_ffn_bwd(s, dy_perm, x_perm, H, A, offsets, W1, W2, dx_perm, dW1, db1, dW2, db2,
+def moe_expert_ffn_bwd(s, dy_perm, x_perm, G, A, offsets, W1, W2, dx_perm, dW1, db1, dW2, db2,
                        accumulate, ws, dev_status, stream=None):
     _check("moe_expert_ffn_bwd", lib().moe_expert_ffn_bwd(
-        ctypes.byref(s), _ptr(dy_perm, _act(s)), _ptr(x_perm, _act(s)), _ptr(H, _act(s)),
+        ctypes.byref(s), _ptr(dy_perm, _act(s)), _ptr(x_perm, _act(s)), _ptr(G, _act(s)),
         _ptr(A, _act(s)), _ptr(offsets, _I32), _ptr(W1, _act(s)), _ptr(W2, _act(s)),
         _ptr(dx_perm, _act(s)), _ptr(dW1, _F32), _ptr(db1, _F32), _ptr(dW2, _F32),
         _ptr(db2, _F32), int(accumulate), _ptr(ws), _ptr(dev_status, _I32), _stream(stream)))

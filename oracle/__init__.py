@@ -171,12 +171,12 @@ def expert_ffn_fwd(X, offsets, W1, b1, W2, b2, round_bf16: bool):
     W1, b1, W2, b2 = _f64(W1), _f64(b1), _f64(W2), _f64(b2)
     P, d = X.shape
     E, f, _ = W1.shape
-    H = np.zeros((P, f), np.float64)
+    G = np.zeros((P, f), np.float64)
     A = np.zeros((P, f), np.float64)
     Y = np.zeros((P, d), np.float64)
     lib().oracle_expert_ffn_fwd(d, f, E, _pi(offsets), _pd(X), _pd(W1), _pd(b1),
-                                _pd(W2), _pd(b2), _pd(H), _pd(A), _pd(Y), int(round_bf16))
-    return H, A, Y
+                                _pd(W2), _pd(b2), _pd(G), _pd(A), _pd(Y), int(round_bf16))
+    return G, A, Y
 
 
 def combine(Y, pos, w, round_bf16: bool) -> np.ndarray:
@@ -200,10 +200,11 @@ def combine_bwd(dy, Y, pos, w, round_bf16: bool):
     return dY, dw
 
 
-def expert_ffn_bwd(dY, X, H, A, offsets, W1, W2, round_bf16: bool, grads=None):
-    """Returns dH, dX, dW1, db1, dW2, db2.  ``grads`` (a dict with dW1, db1,
-    dW2, db2 float64 arrays) makes the weight gradients accumulate into it."""
-    dY, X, H, A = _f64(dY), _f64(X), _f64(H), _f64(A)
+def expert_ffn_bwd(dY, X, G, A, offsets, W1, W2, round_bf16: bool, grads=None):
+    """Returns dH, dX, dW1, db1, dW2, db2 (G = GELU'(h) from the forward).
+    ``grads`` (a dict with dW1, db1, dW2, db2 float64 arrays) makes the weight
+    gradients accumulate into it."""
+    dY, X, G, A = _f64(dY), _f64(X), _f64(G), _f64(A)
     offsets, W1, W2 = _i32(offsets), _f64(W1), _f64(W2)
     P, d = X.shape
     E, f, _ = W1.shape
@@ -213,7 +214,7 @@ def expert_ffn_bwd(dY, X, H, A, offsets, W1, W2, round_bf16: bool, grads=None):
     if grads is None:
         grads = dict(dW1=np.empty((E, f, d)), db1=np.empty((E, f)),
                      dW2=np.empty((E, d, f)), db2=np.empty((E, d)))
-    lib().oracle_expert_ffn_bwd(d, f, E, _pi(offsets), _pd(dY), _pd(X), _pd(H), _pd(A),
+    lib().oracle_expert_ffn_bwd(d, f, E, _pi(offsets), _pd(dY), _pd(X), _pd(G), _pd(A),
                                 _pd(W1), _pd(W2), _pd(dH), _pd(dX), _pd(grads["dW1"]),
                                 _pd(grads["db1"]), _pd(grads["dW2"]), _pd(grads["db2"]),
                                 int(acc), int(round_bf16))
@@ -268,7 +269,7 @@ def layer(inp: dict, k: int, renorm: int, round_bf16: bool, chunk: int | None = 
         idx, w = gate(Lc, k, renorm)
         counts, offsets, pos, perm = dispatch(idx, E)
         X = permute(xc, pos)
-        H, A, Y = expert_ffn_fwd(X, offsets, W1, b1, W2, b2, round_bf16)
+        G, A, Y = expert_ffn_fwd(X, offsets, W1, b1, W2, b2, round_bf16)
         y = combine(Y, pos, w, round_bf16)
         for name, v in (("logits", Lc), ("idx", idx), ("w", w), ("counts", counts),
                         ("offsets", offsets), ("pos", pos), ("perm", perm), ("y", y)):
@@ -277,10 +278,10 @@ def layer(inp: dict, k: int, renorm: int, round_bf16: bool, chunk: int | None = 
             continue
         dY, dw = combine_bwd(dy[c0:c1], Y, pos, w, round_bf16)
         if grads is None:
-            res = expert_ffn_bwd(dY, X, H, A, offsets, W1, W2, round_bf16)
+            res = expert_ffn_bwd(dY, X, G, A, offsets, W1, W2, round_bf16)
             grads = dict(zip(("dW1", "db1", "dW2", "db2"), res[2:]))
         else:
-            res = expert_ffn_bwd(dY, X, H, A, offsets, W1, W2, round_bf16, grads)
+            res = expert_ffn_bwd(dY, X, G, A, offsets, W1, W2, round_bf16, grads)
         dX = res[1]
         dx_perm = combine(dX, pos, None, False)
         dL, dxr, dWg = router_bwd(dw, Lc, idx, w, xc, Wg, renorm, dWg)
@@ -291,7 +292,7 @@ def layer(inp: dict, k: int, renorm: int, round_bf16: bool, chunk: int | None = 
         out["dx"].append(dx)
         out["dL"].append(dL)
         if chunk is None:
-            out.update(X=X, H=H, A=A, Y=Y, dY=dY, dH=res[0], dX=dX)
+            out.update(X=X, G=G, A=A, Y=Y, dY=dY, dH=res[0], dX=dX)
     res = {}
     for name, v in out.items():
         if isinstance(v, list):

@@ -36,7 +36,7 @@
  *   A10 router backward.
  *
  * Floating point: all arithmetic in double.  When `round_bf16` is non-zero
- * the activations that the bf16 configurations store in bf16 (H, A, Y_perm,
+ * the activations that the bf16 configurations store in bf16 (G, A, Y_perm,
  * dY_perm, dH, dX_perm and the layer outputs y, dx) are rounded to bf16
  * (round to nearest, ties to even) at the point where they are stored; the
  * values they are computed from are never rounded.  Weight and bias
@@ -195,12 +195,13 @@ ORACLE_API void oracle_permute(int64_t T, int d, int k, const double* x,
 
 /* For each expert e, one after another, over rows p in [offsets[e], offsets[e+1]):
  *   h      = W1[e] x_p + b1[e]          (W1: [E][f][d], b1: [E][f])
- *   H[p]   = h,  A[p] = GELU(h)
+ *   A[p]   = GELU(h)
+ *   G[p]   = GELU'(h)   (kept for the backward, which needs only this of h)
  *   Y[p]   = W2[e] A[p] + b2[e]         (W2: [E][d][f], b2: [E][d]) */
 ORACLE_API void oracle_expert_ffn_fwd(int d, int f, int E, const int32_t* offsets,
                                       const double* X, const double* W1,
                                       const double* b1, const double* W2,
-                                      const double* b2, double* H, double* A,
+                                      const double* b2, double* G, double* A,
                                       double* Y, int round_bf16) {
     for (int e = 0; e < E; ++e) {
         const double* W1e = W1 + (int64_t)e * f * d;
@@ -210,7 +211,7 @@ ORACLE_API void oracle_expert_ffn_fwd(int d, int f, int E, const int32_t* offset
             for (int n = 0; n < f; ++n) {
                 double h = b1[(int64_t)e * f + n];
                 for (int c = 0; c < d; ++c) h += W1e[(int64_t)n * d + c] * X[p * d + c];
-                H[p * f + n] = rnd(h, round_bf16);
+                G[p * f + n] = rnd(oracle_gelu_grad(h), round_bf16);
                 A[p * f + n] = rnd(oracle_gelu(h), round_bf16);
             }
             for (int m = 0; m < d; ++m) {
@@ -263,14 +264,14 @@ ORACLE_API void oracle_combine_bwd(int64_t T, int d, int k, const double* dy,
 
 /* For each expert e over its segment (chain rule through A5):
  *   dA      = W2[e]^T dY[p]
- *   dH[p]   = dA * GELU'(H[p])
+ *   dH[p]   = dA * G[p]          (G[p] = GELU'(h) from the forward)
  *   dX[p]   = W1[e]^T dH[p]
  *   dW2[e] += dY[p] A[p]^T,  db2[e] += dY[p]
  *   dW1[e] += dH[p] X[p]^T,  db1[e] += dH[p]
  * When accumulate == 0 the weight and bias gradients are overwritten. */
 ORACLE_API void oracle_expert_ffn_bwd(int d, int f, int E, const int32_t* offsets,
                                       const double* dY, const double* X,
-                                      const double* H, const double* A,
+                                      const double* G, const double* A,
                                       const double* W1, const double* W2,
                                       double* dH, double* dX, double* dW1,
                                       double* db1, double* dW2, double* db2,
@@ -291,7 +292,7 @@ ORACLE_API void oracle_expert_ffn_bwd(int d, int f, int E, const int32_t* offset
             for (int n = 0; n < f; ++n) {
                 double a = 0.0;
                 for (int m = 0; m < d; ++m) a += W2e[(int64_t)m * f + n] * dY[p * d + m];
-                dH[p * f + n] = rnd(a * oracle_gelu_grad(H[p * f + n]), round_bf16);
+                dH[p * f + n] = rnd(a * G[p * f + n], round_bf16);
             }
             for (int c = 0; c < d; ++c) {
                 double s = 0.0;

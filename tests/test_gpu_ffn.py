@@ -48,26 +48,26 @@ def test_expert_ffn_fwd_bwd(dtype, T, d, f, E, k, zipf):
     dev = {n: inp[n].to(DEV) for n in ("W1", "b1", "W2", "b2")}
     offs = torch.from_numpy(offsets).to(DEV)
     Xd, dYd = X.to(DEV), dY.to(DEV)
-    H = torch.empty(P, f, dtype=tdt, device=DEV)
+    G = torch.empty(P, f, dtype=tdt, device=DEV)
     A = torch.empty(P, f, dtype=tdt, device=DEV)
     Y = torch.empty(P, d, dtype=tdt, device=DEV)
     ws = torch.empty(ops.moe_workspace_size(s), dtype=torch.uint8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    ops.moe_expert_ffn_fwd(s, Xd, offs, dev["W1"], dev["b1"], dev["W2"], dev["b2"], H, A, Y, ws, st)
-    rH, rA, rY = oracle.expert_ffn_fwd(X, offsets, inp["W1"], inp["b1"], inp["W2"], inp["b2"], rb)
+    ops.moe_expert_ffn_fwd(s, Xd, offs, dev["W1"], dev["b1"], dev["W2"], dev["b2"], G, A, Y, ws, st)
+    rG, rA, rY = oracle.expert_ffn_fwd(X, offsets, inp["W1"], inp["b1"], inp["W2"], inp["b2"], rb)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    assert_close("H", H, rH, dtype)
+    assert_close("G", G, rG, dtype)
     assert_close("A", A, rA, dtype)
     assert_close("Y", Y, rY, dtype)
 
     dX = torch.empty(P, d, dtype=tdt, device=DEV)
     grads = {n: torch.full(sh, float("nan"), dtype=torch.float32, device=DEV) for n, sh in
              (("dW1", (E, f, d)), ("db1", (E, f)), ("dW2", (E, d, f)), ("db2", (E, d)))}
-    ops.moe_expert_ffn_bwd(s, dYd, Xd, H, A, offs, dev["W1"], dev["W2"], dX, grads["dW1"],
+    ops.moe_expert_ffn_bwd(s, dYd, Xd, G, A, offs, dev["W1"], dev["W2"], dX, grads["dW1"],
                            grads["db1"], grads["dW2"], grads["db2"], 0, ws, st)
     # oracle backward from the oracle's own forward activations
-    _, rdX, rdW1, rdb1, rdW2, rdb2 = oracle.expert_ffn_bwd(dY, X, rH, rA, offsets, inp["W1"],
+    _, rdX, rdW1, rdb1, rdW2, rdb2 = oracle.expert_ffn_bwd(dY, X, rG, rA, offsets, inp["W1"],
                                                            inp["W2"], rb)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
@@ -80,7 +80,7 @@ def test_expert_ffn_fwd_bwd(dtype, T, d, f, E, k, zipf):
         assert float(grads["db2"][e].abs().max()) == 0.0
     # accumulate: a second identical pass doubles every gradient exactly
     first = {n: t.clone() for n, t in grads.items()}
-    ops.moe_expert_ffn_bwd(s, dYd, Xd, H, A, offs, dev["W1"], dev["W2"], dX, grads["dW1"],
+    ops.moe_expert_ffn_bwd(s, dYd, Xd, G, A, offs, dev["W1"], dev["W2"], dX, grads["dW1"],
                            grads["db1"], grads["dW2"], grads["db2"], 1, ws, st)
     torch.cuda.synchronize()
     for n in grads:

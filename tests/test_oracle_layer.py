@@ -226,7 +226,7 @@ def test_bf16_storage_rounds_only_stored_activations():
     cfg = synth.MoEConfig("t", T=32, d=16, f=32, E=4, k=2, renorm=1, dtype="bf16")
     inp = _inputs(cfg, seed=8)
     r = oracle.layer(inp, 2, 1, round_bf16=True)
-    for n in ("H", "A", "Y", "dY", "dH", "dX", "y", "dx"):
+    for n in ("G", "A", "Y", "dY", "dH", "dX", "y", "dx"):
         np.testing.assert_array_equal(oracle.round_bf16_array(r[n]), r[n])
     full = oracle.layer(inp, 2, 1, round_bf16=False)
     # rounding moves results by about bf16 precision, not more
