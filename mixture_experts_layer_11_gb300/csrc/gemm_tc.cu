@@ -16,9 +16,10 @@
 //     length varies per expert.  Rows past the segment are computed from
 //     whatever TMA loads there and never stored.
 //   VarK (weight gradient): C_e[M, N] (+)= act_a[seg_e, M]^T act_b[seg_e, N];
-//     the reduction runs over the segment's rows.  The tensor cores take the
-//     whole 16-row groups; the last n_e mod 16 rows are added by the epilogue
-//     on the CUDA cores, so no row past the segment is ever summed.
+//     the reduction runs over the segment's rows, so rows past the segment in
+//     the last K block are zeroed in shared memory before the MMA reads them.
+//     Single CTAs only: the pair variant would have to zero rows in the peer
+//     CTA's shared memory before the even CTA's MMA.
 //
 // Two CTA shapes (template PAIR):
 //   1 CTA: tile 128 x 256, tcgen05.mma.cta_group::1 (M 128, N 256, K 16);
@@ -76,8 +77,6 @@ struct TcParams {
     void* out0;
     void* out1;
     float* outf;
-    const void* act_a;       // VarK: CUDA-core tail rows
-    const void* act_b;
     int accumulate;
     int32_t* status;
     uint64_t limit_ns;
@@ -108,7 +107,6 @@ struct Tile {
     int e, mt, nt, num_kb;
     int row0;     // VarM: first row of this CTA's part; VarK: first row of the segment
     int rows;     // VarM: valid rows of this CTA's part (may be <= 0); VarK: segment rows
-    int kfull;    // VarK: rows taken by the tensor cores (whole 16-row groups)
 };
 
 template <bool VAR_K, bool PAIR, typename C>
@@ -126,7 +124,6 @@ __device__ __forceinline__ Tile get_tile(const C& c, const TcParams& p, int t, i
         ti.row0 = c.off[ecur] + ti.mt * S::TILE_M + rank * BM;
         ti.rows = min(BM, c.off[ecur + 1] - ti.row0);
         ti.num_kb = p.K / BK;
-        ti.kfull = p.K;
     } else {
         const int MT = (p.M + S::TILE_M - 1) / S::TILE_M;
         const int per = MT * NT;
@@ -136,8 +133,7 @@ __device__ __forceinline__ Tile get_tile(const C& c, const TcParams& p, int t, i
         ti.nt = local % NT;
         ti.row0 = c.off[ti.e];
         ti.rows = c.off[ti.e + 1] - ti.row0;
-        ti.kfull = ti.rows & ~15;
-        ti.num_kb = (ti.kfull + BK - 1) / BK;
+        ti.num_kb = (ti.rows + BK - 1) / BK;
     }
     return ti;
 }
@@ -268,6 +264,7 @@ template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB, const TcParams p) {
+    static_assert(!(VAR_K && PAIR), "weight-gradient GEMMs run on single CTAs");
     using S = Shape<PAIR>;
     constexpr int STAGES = S::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -448,12 +445,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (VAR_K) {
+                        const int valid = ti.rows - kb * BK;
+                        if (valid < BK) {
+                            // zero K rows past the segment in every MN slab of the stage
+                            uint8_t* gA = base + (size_t)stage * S::STAGE_BYTES;
+                            const int nz = (BK - valid) * 8;  // 16-byte chunks per slab
+                            for (int sl = 0; sl < S::STAGE_BYTES / SLAB_BYTES; ++sl) {
+                                uint8_t* slab = gA + sl * SLAB_BYTES;
+                                for (int i = lane; i < nz; i += 32)
+                                    *reinterpret_cast<uint4*>(slab + (valid + (i >> 3)) * 128 +
+                                                              ((i & 7) << 4)) = make_uint4(0, 0, 0, 0);
+                            }
+                            fence_proxy_async_smem();
+                        }
+                        __syncwarp();
+                    }
                     if (lane == 0) {
                         const uint32_t sA = smem_u32(base + (size_t)stage * S::STAGE_BYTES);
                         const uint32_t sB = sA + S::A_BYTES;
-                        // VarK: only whole 16-row groups of the segment
-                        const int nk = VAR_K ? min(BK / 16, (ti.kfull - kb * BK) / 16) : BK / 16;
-                        for (int kk = 0; kk < nk; ++kk) {
+                        for (int kk = 0; kk < BK / 16; ++kk) {
                             const uint64_t ad =
                                 A_MN ? smem_desc_sw128(sA + kk * 2048, SLAB_BYTES, 1024)
                                      : smem_desc_sw128(sA + kk * 32, 16, 1024);
@@ -610,29 +621,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         __syncwarp();
                     }
                 } else {
-                    // fp32 weight gradient.  The last rows of the segment that do
-                    // not fill a 16-row group are added here on the CUDA cores
-                    // (after the tensor-core sum, in row order).
+                    // fp32 weight gradient
                     const int m0 = ti.mt * S::TILE_M + rank * BM + q * 32;
                     const int valid = p.M - m0;
-                    const int m = m0 + lane;
-                    for (int pr = ti.row0 + ti.kfull; pr < ti.row0 + ti.rows; ++pr) {
-                        const float a =
-                            (m < p.M) ? __bfloat162float(((const __nv_bfloat16*)p.act_a)[(int64_t)pr * p.M + m])
-                                      : 0.f;
-                        const __nv_bfloat16* brow = (const __nv_bfloat16*)p.act_b + (int64_t)pr * p.N + col0;
-                        #pragma unroll
-                        for (int u = 0; u < 32; u += 8) {
-                            const uint4 bv = __ldg(reinterpret_cast<const uint4*>(brow + u));
-                            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&bv);
-                            #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float2 f = __bfloat1622float2(h[i]);
-                                v[u + 2 * i] = fmaf(a, f.x, v[u + 2 * i]);
-                                v[u + 2 * i + 1] = fmaf(a, f.y, v[u + 2 * i + 1]);
-                            }
-                        }
-                    }
                     #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         #pragma unroll
@@ -848,12 +839,10 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
     TcParams p{};
     p.E = g.E; p.M = g.M; p.N = g.N; p.K = 0; p.P = g.P;
     p.offsets = g.offsets; p.outf = g.out; p.accumulate = g.accumulate;
-    p.act_a = g.act_a; p.act_b = g.act_b;
     p.status = status; p.limit_ns = wait_limit_ns();
     const int64_t NT = (g.N + BN - 1) / BN;
     const int64_t u1 = (int64_t)g.E * ((g.M + BM - 1) / BM) * NT;
-    const int64_t u2 = (int64_t)g.E * ((g.M + 2 * BM - 1) / (2 * BM)) * NT;
-    return launch_either<true, true, true, (int)Epi::Plain>(ma, mb, p, u1, u2, st);
+    return launch_tc<true, true, true, (int)Epi::Plain, false>(ma, mb, p, u1, st);
 }
 
 }  // namespace moe

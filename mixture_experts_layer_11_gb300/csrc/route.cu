@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(kRouteBlockTokens) dispatch_rank_kernel(
 // [T][E]).  dx[t] += sum_e dL[t][e] Wg[e] (read-modify-write in the storage
 // dtype, fp32 arithmetic).
 
-template <typename TIn, int EPL>
+template <typename TIn, int EPL, int KMAX>
 __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     int64_t T, int d, int E, int k, int renorm, const float* __restrict__ dw,
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
@@ -593,33 +593,52 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     }
     __syncwarp();
     constexpr int VN = V::N;
-    int32_t p[16];
-    if (dx_perm)
-        #pragma unroll
-        for (int j = 0; j < 16; ++j) p[j] = (j < k) ? pos[t * k + j] : 0;
-    for (int c = lane * VN; c < d; c += 32 * VN) {
-        float acc[VN], wv[VN];
+    // vectors per lane in flight: U * KMAX row loads before any use
+    constexpr int U = KMAX >= 8 ? 1 : 8 / KMAX;
+    int32_t p[KMAX];
+    #pragma unroll
+    for (int j = 0; j < KMAX; ++j) p[j] = (dx_perm && j < k) ? pos[t * k + j] : 0;
+    for (int c0 = lane * VN; c0 < d; c0 += 32 * VN * U) {
+        float acc[U][VN], wv[VN];
         if (dx_perm) {
             // permute backward fused in: dx = sum_j dx_perm[pos[t,j]] + router term
+            float xr[U][KMAX][VN];
             #pragma unroll
-            for (int u = 0; u < VN; ++u) acc[u] = 0.f;
-            #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                if (j >= k) break;
-                V::load(dx_perm + (int64_t)p[j] * d + c, wv);
+            for (int u = 0; u < U; ++u)
                 #pragma unroll
-                for (int u = 0; u < VN; ++u) acc[u] += wv[u];
+                for (int j = 0; j < KMAX; ++j)
+                    if (j < k && c0 + 32 * VN * u < d)
+                        V::load(dx_perm + (int64_t)p[j] * d + c0 + 32 * VN * u, xr[u][j]);
+            #pragma unroll
+            for (int u = 0; u < U; ++u) {
+                #pragma unroll
+                for (int e = 0; e < VN; ++e) acc[u][e] = 0.f;
+                #pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j >= k) break;
+                    #pragma unroll
+                    for (int e = 0; e < VN; ++e) acc[u][e] += xr[u][j][e];
+                }
             }
         } else {
-            V::load(dx + t * d + c, acc);
+            #pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (c0 + 32 * VN * u < d) V::load(dx + t * d + c0 + 32 * VN * u, acc[u]);
         }
         for (int i = 0; i < ng; ++i) {
             const float g = g_s[warp][i];
-            V::load(Wg + (int64_t)e_s[warp][i] * d + c, wv);
+            const TIn* wrow = Wg + (int64_t)e_s[warp][i] * d;
             #pragma unroll
-            for (int u = 0; u < VN; ++u) acc[u] = fmaf(g, wv[u], acc[u]);
+            for (int u = 0; u < U; ++u) {
+                if (c0 + 32 * VN * u >= d) break;
+                V::load(wrow + c0 + 32 * VN * u, wv);
+                #pragma unroll
+                for (int e = 0; e < VN; ++e) acc[u][e] = fmaf(g, wv[e], acc[u][e]);
+            }
         }
-        V::store(dx + t * d + c, acc);
+        #pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (c0 + 32 * VN * u < d) V::store(dx + t * d + c0 + 32 * VN * u, acc[u]);
     }
 }
 
@@ -762,14 +781,25 @@ cudaError_t route_bwd_typed(const moe_shape& s, const float* dw, const float* lo
     const int64_t T = s.T;
     const int d = s.d, E = s.E, k = s.k;
     const unsigned gx = (unsigned)((T + 7) / 8);
-    if (E <= 32)
-        route_bwd_dx_kernel<TIn, 1><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx_perm, pos, dx, dL);
-    else if (E <= 64)
-        route_bwd_dx_kernel<TIn, 2><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx_perm, pos, dx, dL);
-    else if (E <= 128)
-        route_bwd_dx_kernel<TIn, 4><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx_perm, pos, dx, dL);
-    else
-        route_bwd_dx_kernel<TIn, 8><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, idx, w, Wg, dx_perm, pos, dx, dL);
+    // KMAX: compile-time bound on k for the fused permute backward (1 when not fused)
+    const int kb = dx_perm == nullptr ? 1 : (k <= 1 ? 1 : k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 16);
+#define MOE_RBWD(EPLV, KMV)                                                                    \
+    route_bwd_dx_kernel<TIn, EPLV, KMV><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, \
+                                                           idx, w, Wg, dx_perm, pos, dx, dL)
+#define MOE_RBWD_K(EPLV)                                                                       \
+    switch (kb) {                                                                              \
+        case 1: MOE_RBWD(EPLV, 1); break;                                                      \
+        case 2: MOE_RBWD(EPLV, 2); break;                                                      \
+        case 4: MOE_RBWD(EPLV, 4); break;                                                      \
+        case 8: MOE_RBWD(EPLV, 8); break;                                                      \
+        default: MOE_RBWD(EPLV, 16); break;                                                    \
+    }
+    if (E <= 32) { MOE_RBWD_K(1) }
+    else if (E <= 64) { MOE_RBWD_K(2) }
+    else if (E <= 128) { MOE_RBWD_K(4) }
+    else { MOE_RBWD_K(8) }
+#undef MOE_RBWD_K
+#undef MOE_RBWD
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     constexpr int VN = Vec<TIn>::N;
