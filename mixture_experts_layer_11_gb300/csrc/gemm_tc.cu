@@ -23,22 +23,24 @@
 //
 // Two CTA shapes (template PAIR):
 //   1 CTA: tile 128 x 256, tcgen05.mma.cta_group::1 (M 128, N 256, K 16);
-//     4 stages of 48 KB (A 128x64, B 256x64).
+//     stages of 48 KB (A 128x64, B 256x64).
 //   CTA pair (cluster of 2): tile 256 x 256, tcgen05.mma.cta_group::2 (M 256,
 //     N 256, K 16) issued by the even CTA; each CTA holds its 128 rows of A
-//     and 128 columns of B, so a stage is 32 KB and 6 stages fit.  Both CTAs'
-//     TMA loads complete on the even CTA's stage barrier; MMA completion is
-//     multicast to both CTAs' barriers; each CTA drains its own TMEM rows.
+//     and 128 columns of B, so a stage is 32 KB.  Both CTAs' TMA loads
+//     complete on the even CTA's stage barrier; MMA completion is multicast to
+//     both CTAs' barriers; each CTA drains its own TMEM rows.
 //
-// CTA = 10 warps: warp 0 issues TMA loads, warp 1 issues the MMAs into one of
-// two TMEM accumulators (2 x 256 fp32 columns), warps 2-9 drain the other
-// accumulator (tcgen05.ld), apply the fused epilogue (bias, GELU, GELU', fp32
-// accumulate) and write through a swizzled shared staging buffer with
+// CTA = 2 + 8 or 16 warps: warp 0 issues TMA loads, warp 1 issues the MMAs
+// into one of two TMEM accumulators (2 x 256 fp32 columns), the other warps
+// drain the other accumulator (tcgen05.ld) and apply the fused epilogue (bias,
+// GELU, GELU', fp32 accumulate).  bf16 results go through a swizzled shared
+// staging buffer and out by TMA tensor stores; fp32 weight gradients by
 // coalesced stores.  Every wait is bounded; on expiry the CTA records
 // MOE_ERR_TIMEOUT, waits for its own copies and MMAs in flight, frees TMEM
 // and exits.
 #include <cudaTypedefs.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -51,10 +53,7 @@ namespace {
 constexpr int BM = 128;            // rows per CTA (TMEM lanes)
 constexpr int BN = 256;            // tile columns (MMA N)
 constexpr int BK = 64;             // K per stage: one 128-byte swizzle row of bf16
-constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 32 * (2 + EPI_WARPS);
 constexpr int SLAB_BYTES = 64 * BK * 2;    // one 64-wide MN slab of BK rows
-constexpr int STAGING_BYTES = 32 * 64;     // per epilogue warp: 32 rows x 64 B
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_E = 256;
 
@@ -65,8 +64,35 @@ template <bool PAIR> struct Shape {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN_CTA * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = PAIR ? 6 : 4;
 };
+
+// Operand pipeline depth and epilogue staging.  The bf16 epilogues stage two
+// 32-row chunks per warp (32 KB in all), so that the TMA store of one chunk
+// runs while the next is computed; that leaves room for 5 (pair) or 3
+// (single CTA) operand stages under the 227 KB per-CTA limit.  The fp32
+// weight-gradient epilogue stages one chunk per warp (16 KB).
+template <bool PAIR, bool VAR_K> struct Pipe {
+    static constexpr int STAGING = VAR_K ? 16 * 1024 : 32 * 1024;
+    static constexpr int STAGES = PAIR ? (VAR_K ? 6 : 5) : (VAR_K ? 4 : 3);
+};
+
+// Epilogue shape.  The epilogue warps drain a 128 x 256 accumulator, each
+// warp the TMEM lane quarter it may access (warp % 4) and a range of columns.
+// The GELU epilogues (instruction-heavy: a short-K tile's drain takes longer
+// than its MMAs) get 16 warps, 64 columns each, in 16-column chunks (register
+// budget of 576 threads); the others 8 warps, 128 columns each, in 32-column
+// chunks.
+template <int EPI, bool VAR_K> struct EpiShape {
+    static constexpr bool WIDE = !VAR_K && (EPI == (int)Epi::BiasGelu || EPI == (int)Epi::ScaleAux);
+    static constexpr int WARPS = WIDE ? 16 : 8;
+    static constexpr int CW = WIDE ? 16 : 32;              // columns per chunk
+    static constexpr int COLS = BN / (WARPS / 4);          // columns per warp
+    static constexpr int NCH = COLS / CW;                  // chunks per warp
+    static constexpr int CHUNK_BYTES = 32 * CW * 2;        // one staged bf16 chunk
+    static constexpr int THREADS = 32 * (2 + WARPS);
+};
+
+template <int N> struct U4s { uint4 u[N]; };
 
 struct TcParams {
     int E, M, N, K;          // VarM: N, K (M unused); VarK: M, N (K = segment)
@@ -96,11 +122,12 @@ template <int STAGES> struct Ctrl {
     int order[MAX_E];            // VarK: experts by descending row count
 };
 
-template <bool PAIR>
+template <bool PAIR, bool VAR_K>
 constexpr size_t smem_bytes() {
     using S = Shape<PAIR>;
-    return 1024 + (size_t)S::STAGES * S::STAGE_BYTES + (size_t)EPI_WARPS * STAGING_BYTES +
-           sizeof(Ctrl<S::STAGES>);
+    using PP = Pipe<PAIR, VAR_K>;
+    return 1024 + (size_t)PP::STAGES * S::STAGE_BYTES + (size_t)PP::STAGING +
+           sizeof(Ctrl<PP::STAGES>);
 }
 
 struct Tile {
@@ -225,10 +252,15 @@ __device__ __forceinline__ void tc_commit2_local(uint32_t bar) {
                  : "memory");
 }
 
-// ---- epilogue helpers: 32 rows x 64 bytes staging, 16-byte chunks XOR-swizzled
-// so that both the per-row writes and the coalesced reads are conflict-free.
+// ---- epilogue helpers: staging of 32 rows x CW bf16 (CW*2 bytes per row),
+// 16-byte chunks XOR-swizzled so that the per-row writes (one row per
+// thread) and the coalesced reads are both free of bank conflicts.  The
+// pattern is the TMA's: chunk index XOR address bit 7 for 32-byte rows
+// (SWIZZLE_32B), XOR address bits 8:7 for 64-byte rows (SWIZZLE_64B).
+template <int CW>
 __device__ __forceinline__ uint32_t stg_off(int row, int ch) {
-    return (uint32_t)(row * 64 + ((ch ^ ((row >> 1) & 3)) << 4));
+    if (CW == 32) return (uint32_t)(row * 64 + ((ch ^ ((row >> 1) & 3)) << 4));
+    return (uint32_t)(row * 32 + ((ch ^ ((row >> 2) & 1)) << 4));
 }
 
 __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
@@ -239,40 +271,75 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
     return u;
 }
 
-// this thread's row (lane) of 32 bf16 values -> staging
-__device__ __forceinline__ void stage_row_bf16(uint8_t* stg, int lane, const float* v) {
+// this thread's row (lane) of CW bf16 values, packed -> staging
+template <int CW>
+__device__ __forceinline__ void stage_row_packed(uint8_t* stg, int lane, const uint4* pk) {
     #pragma unroll
-    for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4*>(stg + stg_off(lane, ch)) = pack8_bf16(v + 8 * ch);
+    for (int ch = 0; ch < CW / 8; ++ch)
+        *reinterpret_cast<uint4*>(stg + stg_off<CW>(lane, ch)) = pk[ch];
 }
 
-// staging (32 rows x 32 bf16) -> global rows row0.., columns col0.., ld = N
+// staging (32 rows x CW bf16) -> global rows row0.., columns col0.., ld = N
+template <int CW>
 __device__ __forceinline__ void store_tile_bf16(const uint8_t* stg, int lane, __nv_bfloat16* out,
                                                 int64_t row0, int valid_rows, int64_t ld,
                                                 int col0) {
+    constexpr int CPR = CW / 8;                 // 16-byte chunks per row
     #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int rr = it * 8 + (lane >> 2), ch = lane & 3;
+    for (int it = 0; it < CPR; ++it) {
+        const int rr = it * (32 / CPR) + lane / CPR, ch = lane % CPR;
         if (rr < valid_rows) {
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + stg_off(rr, ch));
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + stg_off<CW>(rr, ch));
             *reinterpret_cast<uint4*>(out + (row0 + rr) * ld + col0 + ch * 8) = v;
         }
     }
 }
 
+// TMA tensor store of a staged box (shared -> global), tracked by this
+// thread's bulk async-groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0,
+                                             int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(map), "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// until at most N committed groups still read their shared-memory source
+template <int N> __device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// until every committed group has completed its writes
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+template <int CW>
+__device__ __forceinline__ void tmem_ld_cw(uint32_t taddr, float (&v)[CW]) {
+    if constexpr (CW == 32) tmem_ld32(taddr, v);
+    else tmem_ld16(taddr, v);
+}
+
 template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool PAIR>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
-                   const __grid_constant__ CUtensorMap mapB, const TcParams p) {
+                   const __grid_constant__ CUtensorMap mapB,
+                   const __grid_constant__ CUtensorMap mapO0,
+                   const __grid_constant__ CUtensorMap mapO1, const TcParams p) {
     static_assert(!(VAR_K && PAIR), "weight-gradient GEMMs run on single CTAs");
     using S = Shape<PAIR>;
-    constexpr int STAGES = S::STAGES;
+    using ES = EpiShape<EPI, VAR_K>;
+    using PP = Pipe<PAIR, VAR_K>;
+    constexpr int THREADS = ES::THREADS;
+    constexpr int CW = ES::CW;
+    constexpr int STAGES = PP::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* staging_base = base + (size_t)STAGES * S::STAGE_BYTES;
     using CtrlT = Ctrl<STAGES>;
-    CtrlT& c = *reinterpret_cast<CtrlT*>(staging_base + (size_t)EPI_WARPS * STAGING_BYTES);
+    CtrlT& c = *reinterpret_cast<CtrlT*>(staging_base + (size_t)PP::STAGING);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
@@ -290,7 +357,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&c.tfull[b]), 1);
-            mbar_init(smem_u32(&c.tempty[b]), EPI_WARPS * S::CTAS);
+            mbar_init(smem_u32(&c.tempty[b]), ES::WARPS * S::CTAS);
         }
         mbar_init(smem_u32(&c.drain), 1);
         c.abort_flag = 0;
@@ -424,6 +491,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---- MMA issuer (the even CTA of a pair issues for both) ---------------------
         if (leader) {
             constexpr uint32_t IDESC = idesc_bf16_f32(S::TILE_M, BN, A_MN, B_MN);
+            // Descriptors of stage 0's A and B; a stage or K step only moves the
+            // start address (bits 0-13, in 16-byte units; shared addresses stay
+            // below 256 KB, so the field never carries into the next one).
+            const uint32_t smem0 = smem_u32(base);
+            const uint64_t a_desc0 = smem_desc_sw128(smem0, A_MN ? SLAB_BYTES : 16, 1024);
+            const uint64_t b_desc0 =
+                smem_desc_sw128(smem0 + S::A_BYTES, B_MN ? SLAB_BYTES : 16, 1024);
+            const uint32_t a_lo0 = (uint32_t)a_desc0, a_hi = (uint32_t)(a_desc0 >> 32);
+            const uint32_t b_lo0 = (uint32_t)b_desc0, b_hi = (uint32_t)(b_desc0 >> 32);
+            constexpr uint32_t A_KSTEP = (A_MN ? 2048u : 32u) >> 4;   // one K step of 16
+            constexpr uint32_t B_KSTEP = (B_MN ? 2048u : 32u) >> 4;
             int stage = 0, acc = 0, ecur = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
@@ -462,16 +540,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         __syncwarp();
                     }
                     if (lane == 0) {
-                        const uint32_t sA = smem_u32(base + (size_t)stage * S::STAGE_BYTES);
-                        const uint32_t sB = sA + S::A_BYTES;
+                        const uint32_t so = (uint32_t)stage * (uint32_t)(S::STAGE_BYTES >> 4);
+                        #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             const uint64_t ad =
-                                A_MN ? smem_desc_sw128(sA + kk * 2048, SLAB_BYTES, 1024)
-                                     : smem_desc_sw128(sA + kk * 32, 16, 1024);
+                                ((uint64_t)a_hi << 32) | (uint64_t)(a_lo0 + so + kk * A_KSTEP);
                             const uint64_t bd =
-                                B_MN ? smem_desc_sw128(sB + kk * 2048, SLAB_BYTES, 1024)
-                                     : smem_desc_sw128(sB + kk * 32, 16, 1024);
-                            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+                                ((uint64_t)b_hi << 32) | (uint64_t)(b_lo0 + so + kk * B_KSTEP);
+                            const uint32_t accum = (kk != 0 || kb != 0) ? 1u : 0u;
                             if (PAIR) tc_mma2_bf16(d_tmem, ad, bd, IDESC, accum);
                             else tc_mma_bf16(d_tmem, ad, bd, IDESC, accum);
                         }
@@ -499,30 +575,59 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ---- epilogue warps ----------------------------------------------------------
+        const int ew = warp - 2;
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int half = (warp - 2) >> 2;       // which 128 columns of the 256
-        uint8_t* stg = staging_base + (warp - 2) * STAGING_BYTES;
+        const int cq = ew >> 2;                 // which ES::COLS columns of the 256
+        uint8_t* stg = staging_base + ew * (PP::STAGING / ES::WARPS);
         const uint32_t tempty_local0 = smem_u32(&c.tempty[0]);
         const uint32_t tempty_local1 = smem_u32(&c.tempty[1]);
-        int acc = 0, ecur = 0;
+        if (!VAR_K && lane == 0) {
+            tma_prefetch_map(&mapO0);
+            if (EPI == (int)Epi::BiasGelu) tma_prefetch_map(&mapO1);
+        }
+        int acc = 0, ecur = 0, sbuf = 0;
         uint32_t acc_phase = 0;
         for (int t = unit0; t < num_units; t += nunits) {
             const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
             const bool mma_tile = ti.num_kb > 0;
-            // ScaleAux epilogue (backward of the GELU): the saved GELU'(h) of this
-            // thread's row is fetched ahead (chunk 0 before the accumulator is
-            // ready, chunk c+1 while chunk c is processed).
-            uint4 hnext[4];
             const int64_t grow_lane = (int64_t)ti.row0 + q * 32 + lane;
             const bool row_ok = (q * 32 + lane) < ti.rows;
-            if (EPI == (int)Epi::ScaleAux && !VAR_K) {
-                const int col0 = ti.nt * BN + half * 128;
+            const int colw = ti.nt * BN + cq * ES::COLS;   // first global column of this warp
+            // Operands of the epilogue read from global memory are fetched ahead:
+            // the saved GELU'(h) of this thread's row (ScaleAux) two chunks
+            // ahead, the bias columns (the same for every lane) one chunk ahead;
+            // the first ones before the accumulator is ready.
+            auto load_aux = [&](int ch) {
+                U4s<CW / 8> r;
+                const int col = colw + ch * CW;
                 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    hnext[u] = row_ok ? __ldg(reinterpret_cast<const uint4*>(
-                                            (const __nv_bfloat16*)p.aux + grow_lane * p.N + col0 + u * 8))
-                                      : make_uint4(0, 0, 0, 0);
+                for (int u = 0; u < CW / 8; ++u)
+                    r.u[u] = (row_ok && col < p.N)
+                                 ? __ldg(reinterpret_cast<const uint4*>(
+                                       (const __nv_bfloat16*)p.aux + grow_lane * p.N + col + u * 8))
+                                 : make_uint4(0, 0, 0, 0);
+                return r;
+            };
+            auto load_bias = [&](int ch) {
+                U4s<CW / 8> r;
+                const int col = colw + ch * CW;
+                #pragma unroll
+                for (int u = 0; u < CW / 8; ++u)
+                    r.u[u] = (p.bias && col < p.N)
+                                 ? __ldg(reinterpret_cast<const uint4*>(
+                                       (const __nv_bfloat16*)p.bias + (int64_t)ti.e * p.N + col +
+                                       u * 8))
+                                 : make_uint4(0, 0, 0, 0);
+                return r;
+            };
+            constexpr bool kAux = EPI == (int)Epi::ScaleAux && !VAR_K;
+            constexpr bool kBias = (EPI == (int)Epi::BiasGelu || EPI == (int)Epi::Bias) && !VAR_K;
+            U4s<CW / 8> h0, h1, bnext;
+            if (kAux) {
+                h0 = load_aux(0);
+                if (ES::NCH > 1) h1 = load_aux(1);
             }
+            if (kBias) bnext = load_bias(0);
             if (mma_tile) {
                 if (!mbar_wait_warp(smem_u32(&c.tfull[acc]), acc_phase, p.limit_ns,
                                     &c.abort_flag)) {
@@ -532,30 +637,43 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
             }
             const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            const int64_t grow0 = (int64_t)ti.row0 + q * 32;   // global row of lane 0
+            const int valid = ti.rows - q * 32;                 // rows of this warp's box
+            // One bf16 output chunk: the staged box goes out by TMA when all its
+            // 32 rows belong to the segment, else row by row (segment end).
+            auto emit = [&](uint8_t* buf, const uint4* pk, const CUtensorMap* map, void* out,
+                            int col0) {
+                stage_row_packed<CW>(buf, lane, pk);
+                if (valid >= 32) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tma_store_2d(map, smem_u32(buf), col0, (int32_t)grow0);
+                } else {
+                    __syncwarp();
+                    store_tile_bf16<CW>(buf, lane, (__nv_bfloat16*)out, grow0, valid, p.N, col0);
+                }
+            };
             #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                const int cl = half * 128 + ch * 32;          // column inside the tile
+            for (int ch = 0; ch < ES::NCH; ++ch) {
+                const int cl = cq * ES::COLS + ch * CW;       // column inside the tile
                 const int col0 = ti.nt * BN + cl;             // global column
                 if (col0 >= p.N) break;                       // N % 64 == 0: whole chunks
-                float v[32];
+                float v[CW];
                 if (mma_tile) {
-                    tmem_ld32(trow + (uint32_t)cl, v);
+                    tmem_ld_cw<CW>(trow + (uint32_t)cl, v);
                 } else {
                     #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    for (int i = 0; i < CW; ++i) v[i] = 0.f;
                 }
                 if (!VAR_K) {
-                    const int64_t grow0 = (int64_t)ti.row0 + q * 32;   // global row of lane 0
-                    const int valid = ti.rows - q * 32;
-                    const int64_t N = p.N;
-                    if (EPI == (int)Epi::BiasGelu || EPI == (int)Epi::Bias) {
+                    if (kBias) {
+                        const U4s<CW / 8> bcur = bnext;
+                        if (ch + 1 < ES::NCH) bnext = load_bias(ch + 1);
                         if (p.bias) {
-                            const __nv_bfloat16* bp =
-                                (const __nv_bfloat16*)p.bias + (int64_t)ti.e * N + col0;
                             #pragma unroll
-                            for (int u = 0; u < 32; u += 8) {
-                                const uint4 bv = *reinterpret_cast<const uint4*>(bp + u);
-                                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&bv);
+                            for (int u = 0; u < CW; u += 8) {
+                                const __nv_bfloat162* h =
+                                    reinterpret_cast<const __nv_bfloat162*>(&bcur.u[u / 8]);
                                 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
                                     const float2 f = __bfloat1622float2(h[i]);
@@ -564,45 +682,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 }
                             }
                         }
-                        if (EPI == (int)Epi::BiasGelu) {
-                            // one Phi / exp evaluation gives both GELU(h) (kept in v)
-                            // and GELU'(h) (staged and stored for the backward)
-                            float gd[32];
-                            #pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const PhiFast r = phi_fast(v[i]);
-                                gd[i] = fmaf(v[i] * 0.39894228040143268f, r.g, r.Phi);
-                                v[i] *= r.Phi;
-                            }
-                            stage_row_bf16(stg, lane, gd);
-                            __syncwarp();
-                            store_tile_bf16(stg, lane, (__nv_bfloat16*)p.out0, grow0, valid, N, col0);
-                            __syncwarp();
-                            stage_row_bf16(stg, lane, v);
-                            __syncwarp();
-                            store_tile_bf16(stg, lane, (__nv_bfloat16*)p.out1, grow0, valid, N, col0);
-                            __syncwarp();
-                        } else {
-                            stage_row_bf16(stg, lane, v);
-                            __syncwarp();
-                            store_tile_bf16(stg, lane, (__nv_bfloat16*)p.out0, grow0, valid, N, col0);
-                            __syncwarp();
-                        }
-                    } else if (EPI == (int)Epi::ScaleAux) {
-                        uint4 hcur[4];
+                    }
+                    if (kAux) {
+                        const U4s<CW / 8> hcur = h0;
+                        h0 = h1;
+                        if (ch + 2 < ES::NCH) h1 = load_aux(ch + 2);
                         #pragma unroll
-                        for (int u = 0; u < 4; ++u) hcur[u] = hnext[u];
-                        if (ch < 3 && col0 + 32 < p.N) {
-                            #pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                hnext[u] = row_ok ? __ldg(reinterpret_cast<const uint4*>(
-                                                        (const __nv_bfloat16*)p.aux + grow_lane * N +
-                                                        col0 + 32 + u * 8))
-                                                  : make_uint4(0, 0, 0, 0);
-                        }
-                        #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&hcur[cc]);
+                        for (int cc = 0; cc < CW / 8; ++cc) {
+                            const __nv_bfloat162* h =
+                                reinterpret_cast<const __nv_bfloat162*>(&hcur.u[cc]);
                             #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const float2 f = __bfloat1622float2(h[i]);
@@ -610,33 +698,62 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 v[cc * 8 + 2 * i + 1] *= f.y;
                             }
                         }
-                        stage_row_bf16(stg, lane, v);
-                        __syncwarp();
-                        store_tile_bf16(stg, lane, (__nv_bfloat16*)p.out0, grow0, valid, N, col0);
-                        __syncwarp();
-                    } else {  // Plain
-                        stage_row_bf16(stg, lane, v);
-                        __syncwarp();
-                        store_tile_bf16(stg, lane, (__nv_bfloat16*)p.out0, grow0, valid, N, col0);
-                        __syncwarp();
                     }
+                    // The staging buffers written below were last read by the TMA
+                    // stores committed two chunks ago (one-output epilogues,
+                    // alternating buffers) or one chunk ago (BiasGelu, which
+                    // stages two outputs per chunk).
+                    if (lane == 0) {
+                        if (EPI == (int)Epi::BiasGelu) bulk_wait_read<0>();
+                        else bulk_wait_read<1>();
+                    }
+                    __syncwarp();
+                    if (EPI == (int)Epi::BiasGelu) {
+                        // one Phi / exp evaluation gives both GELU(h) (kept in v)
+                        // and GELU'(h) (stored for the backward)
+                        float gd[CW];
+                        #pragma unroll
+                        for (int i = 0; i < CW; ++i) {
+                            const PhiFast r = phi_fast(v[i]);
+                            gd[i] = fmaf(v[i] * 0.39894228040143268f, r.g, r.Phi);
+                            v[i] *= r.Phi;
+                        }
+                        uint4 pg[CW / 8], pa[CW / 8];
+                        #pragma unroll
+                        for (int u = 0; u < CW / 8; ++u) {
+                            pg[u] = pack8_bf16(gd + 8 * u);
+                            pa[u] = pack8_bf16(v + 8 * u);
+                        }
+                        emit(stg, pg, &mapO0, p.out0, col0);
+                        emit(stg + ES::CHUNK_BYTES, pa, &mapO1, p.out1, col0);
+                    } else {
+                        uint4 pk[CW / 8];
+                        #pragma unroll
+                        for (int u = 0; u < CW / 8; ++u) pk[u] = pack8_bf16(v + 8 * u);
+                        emit(stg + sbuf * ES::CHUNK_BYTES, pk, &mapO0, p.out0, col0);
+                        sbuf ^= 1;
+                    }
+                    if (lane == 0) bulk_commit();
+                    __syncwarp();
                 } else {
-                    // fp32 weight gradient
+                    // fp32 weight gradient, 16 columns (64 B per row) at a time
+                    static_assert(!VAR_K || CW == 32, "fp32 epilogue drains 32-column chunks");
                     const int m0 = ti.mt * S::TILE_M + rank * BM + q * 32;
-                    const int valid = p.M - m0;
+                    const int valid_m = p.M - m0;
                     #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int hh = 0; hh < CW / 16; ++hh) {
                         #pragma unroll
                         for (int cc = 0; cc < 4; ++cc)
-                            *reinterpret_cast<float4*>(stg + stg_off(lane, cc)) =
+                            *reinterpret_cast<float4*>(stg + stg_off<32>(lane, cc)) =
                                 make_float4(v[hh * 16 + cc * 4], v[hh * 16 + cc * 4 + 1],
                                             v[hh * 16 + cc * 4 + 2], v[hh * 16 + cc * 4 + 3]);
                         __syncwarp();
                         #pragma unroll
                         for (int it = 0; it < 4; ++it) {
                             const int rr = it * 8 + (lane >> 2), cc = lane & 3;
-                            if (rr < valid) {
-                                float4 o = *reinterpret_cast<const float4*>(stg + stg_off(rr, cc));
+                            if (rr < valid_m) {
+                                float4 o =
+                                    *reinterpret_cast<const float4*>(stg + stg_off<32>(rr, cc));
                                 float4* dst = reinterpret_cast<float4*>(
                                     p.outf + ((int64_t)ti.e * p.M + m0 + rr) * p.N + col0 +
                                     hh * 16 + cc * 4);
@@ -661,6 +778,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
+        // every TMA store has written global memory (and read its staging)
+        // before the CTA exits
+        if (!VAR_K && lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     // ---- teardown ------------------------------------------------------------------
@@ -689,10 +810,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// bf16 tensor map, 128-byte swizzle, zero fill outside the tensor.
+// bf16 tensor map (128-byte swizzle unless given), zero fill outside the tensor.
 // dims/box innermost first; strides in bytes for dims 1.. .
 bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
-              const uint64_t* strides, const uint32_t* box) {
+              const uint64_t* strides, const uint32_t* box,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t gd[3], gs[2];
@@ -700,7 +822,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
     for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; }
     for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr),
-                    gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -715,10 +837,13 @@ bool use_pairs() {
 }
 
 template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool PAIR>
-cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p,
-                      int64_t units_upper, cudaStream_t st) {
+cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
+                      const CUtensorMap& o1, const TcParams& p, int64_t units_upper,
+                      cudaStream_t st) {
     auto kern = gemm_tc_kernel<VAR_K, A_MN, B_MN, EPI, PAIR>;
-    constexpr size_t SMEM = smem_bytes<PAIR>();
+    constexpr size_t SMEM = smem_bytes<PAIR, VAR_K>();
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+    constexpr int THREADS = EpiShape<EPI, VAR_K>::THREADS;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_units = 0;   // co-resident CTAs (or pairs)
@@ -748,7 +873,7 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcParams
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t units = units_upper < max_units ? (units_upper > 0 ? units_upper : 1) : max_units;
     if (!PAIR) {
-        kern<<<(unsigned)units, THREADS, SMEM, st>>>(a, b, p);
+        kern<<<(unsigned)units, THREADS, SMEM, st>>>(a, b, o0, o1, p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -763,14 +888,25 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcParams
     cfg.stream = st;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, b, p);
+    return cudaLaunchKernelEx(&cfg, kern, a, b, o0, o1, p);
 }
 
 template <bool VAR_K, bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_either(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p,
-                          int64_t units1, int64_t units2, cudaStream_t st) {
-    if (use_pairs()) return launch_tc<VAR_K, A_MN, B_MN, EPI, true>(a, b, p, units2, st);
-    return launch_tc<VAR_K, A_MN, B_MN, EPI, false>(a, b, p, units1, st);
+cudaError_t launch_either(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
+                          const CUtensorMap& o1, const TcParams& p, int64_t units1,
+                          int64_t units2, cudaStream_t st) {
+    if (use_pairs()) return launch_tc<VAR_K, A_MN, B_MN, EPI, true>(a, b, o0, o1, p, units2, st);
+    return launch_tc<VAR_K, A_MN, B_MN, EPI, false>(a, b, o0, o1, p, units1, st);
+}
+
+// Map of a bf16 [P, N] output for the epilogue's TMA stores: boxes of 32 rows
+// x CW columns, swizzled like the staging buffers.
+bool make_out_map(CUtensorMap* m, void* ptr, int64_t P, int N, int CW) {
+    const uint64_t dims[2] = {(uint64_t)N, (uint64_t)P};
+    const uint64_t strides[1] = {(uint64_t)N * 2};
+    const uint32_t box[2] = {(uint32_t)CW, 32};
+    return make_map(m, ptr, 2, dims, strides, box,
+                    CW == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 }  // namespace
@@ -804,19 +940,34 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     const int64_t NT = (g.N + BN - 1) / BN;
     const int64_t u1 = ((g.P + BM - 1) / BM + g.E) * NT;
     const int64_t u2 = ((g.P + 2 * BM - 1) / (2 * BM) + g.E) * NT;
+    if (g.P >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;   // TMA row coordinate
+    const bool wide = g.epi == Epi::BiasGelu || g.epi == Epi::ScaleAux;
+    const int cw = wide ? EpiShape<(int)Epi::BiasGelu, false>::CW
+                        : EpiShape<(int)Epi::Bias, false>::CW;
+    CUtensorMap mo0, mo1;
+    if (!make_out_map(&mo0, g.out0, g.P, g.N, cw)) return cudaErrorInvalidValue;
+    if (g.epi == Epi::BiasGelu) {
+        if (!make_out_map(&mo1, g.out1, g.P, g.N, cw)) return cudaErrorInvalidValue;
+    } else {
+        mo1 = mo0;
+    }
     switch (g.epi) {
         case Epi::BiasGelu:
             if (!g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_either<false, false, false, (int)Epi::BiasGelu>(ma, mb, p, u1, u2, st);
+            return launch_either<false, false, false, (int)Epi::BiasGelu>(ma, mb, mo0, mo1, p, u1,
+                                                                          u2, st);
         case Epi::Bias:
             if (!g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_either<false, false, false, (int)Epi::Bias>(ma, mb, p, u1, u2, st);
+            return launch_either<false, false, false, (int)Epi::Bias>(ma, mb, mo0, mo1, p, u1, u2,
+                                                                      st);
         case Epi::ScaleAux:
             if (g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_either<false, false, true, (int)Epi::ScaleAux>(ma, mb, p, u1, u2, st);
+            return launch_either<false, false, true, (int)Epi::ScaleAux>(ma, mb, mo0, mo1, p, u1,
+                                                                         u2, st);
         case Epi::Plain:
             if (g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_either<false, false, true, (int)Epi::Plain>(ma, mb, p, u1, u2, st);
+            return launch_either<false, false, true, (int)Epi::Plain>(ma, mb, mo0, mo1, p, u1, u2,
+                                                                      st);
     }
     return cudaErrorInvalidValue;
 }
@@ -842,7 +993,9 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
     p.status = status; p.limit_ns = wait_limit_ns();
     const int64_t NT = (g.N + BN - 1) / BN;
     const int64_t u1 = (int64_t)g.E * ((g.M + BM - 1) / BM) * NT;
-    return launch_tc<true, true, true, (int)Epi::Plain, false>(ma, mb, p, u1, st);
+    CUtensorMap unused;   // no bf16 output: the fp32 epilogue stores directly
+    memset(&unused, 0, sizeof(unused));
+    return launch_tc<true, true, true, (int)Epi::Plain, false>(ma, mb, unused, unused, p, u1, st);
 }
 
 }  // namespace moe
