@@ -17,7 +17,6 @@ namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kMaxK = 16;
 
 template <typename T> struct V16;  // 16 bytes of T as fp32 lanes
 template <> struct V16<__nv_bfloat16> {
@@ -207,15 +206,28 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int64_t Tn, int nv, in
     }
 }
 
-// ---- per-expert column sums (bias gradients) -------------------------------------
-// Phase 1: one partial per (expert, chunk of kDwgChunk rows of its segment);
-// phase 2: partials added in chunk order.  Deterministic.
+// ---- per-expert weighted row sums over segments ------------------------------------
+// out[e][c] (+)= sum over the rows p of expert e's segment of wgt(p) * src[row(p)][c]:
+// wgt = 1, row = p for the column sums of a permuted matrix (bias gradients);
+// with perm given, slot s = perm[p], wgt = wsel[s], row = s / k (the router
+// weight gradient of the selected experts, summed over their tokens).
+// Phase 1: one partial per (expert, chunk of kDwgChunk segment rows) and
+// column tile; the block's 8 warps take every 8th row of the chunk, lanes
+// consecutive 16-byte column vectors, and are added in warp order through
+// shared memory.  Phase 2: per expert and 32 columns, 8 warps take every 8th
+// partial, added in warp order.  Deterministic.
+constexpr int kSegCPL = 4;   // 16-byte vectors per lane in a column tile
+
 template <typename T>
-__global__ void __launch_bounds__(256) colsum_partial_kernel(int n, int E,
-                                                             const int32_t* __restrict__ offsets,
-                                                             const T* __restrict__ g,
-                                                             float* __restrict__ partial) {
+__global__ void __launch_bounds__(256) seg_partial_kernel(int n, int E, int k,
+                                                          const int32_t* __restrict__ offsets,
+                                                          const int32_t* __restrict__ perm,
+                                                          const float* __restrict__ wsel,
+                                                          const T* __restrict__ src,
+                                                          float* __restrict__ partial) {
     using V = V16<T>;
+    constexpr int TILE = 32 * kSegCPL * V::N;      // columns of one tile
+    __shared__ __align__(16) float red[8][TILE];
     int e = 0, acc = 0, sub = -1;
     for (; e < E; ++e) {
         const int cnt = offsets[e + 1] - offsets[e];
@@ -223,44 +235,64 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(int n, int E,
         if ((int)blockIdx.x < acc + nc) { sub = blockIdx.x - acc; break; }
         acc += nc;
     }
-    if (sub < 0) return;
-    const int c = (blockIdx.y * 256 + threadIdx.x) * V::N;
-    if (c >= n) return;
+    if (sub < 0) return;   // block-uniform
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ct0 = blockIdx.y * TILE;
     const int p0 = offsets[e] + sub * kDwgChunk;
     const int p1 = min(offsets[e + 1], p0 + kDwgChunk);
-    float a[V::N], v[V::N];
+    float a[kSegCPL][V::N];
     #pragma unroll
-    for (int u = 0; u < V::N; ++u) a[u] = 0.f;
-    int p = p0;
-    for (; p + 8 <= p1; p += 8) {       // 8 loads in flight, summed in row order
-        uint4 r[8];
+    for (int i = 0; i < kSegCPL; ++i)
         #pragma unroll
-        for (int q = 0; q < 8; ++q) r[q] = ldg16(g + (int64_t)(p + q) * n + c);
+        for (int u = 0; u < V::N; ++u) a[i][u] = 0.f;
+    #pragma unroll 2
+    for (int r = p0 + warp; r < p1; r += 8) {
+        int64_t row = r;
+        float g = 1.f;
+        if (perm) {
+            const int sl = __ldg(perm + r);
+            g = __ldg(wsel + sl);
+            row = sl / k;
+        }
+        uint4 raw[kSegCPL];
         #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            V::unpack(r[q], v);
+        for (int i = 0; i < kSegCPL; ++i) {
+            const int c = ct0 + (lane + 32 * i) * V::N;
+            raw[i] = c < n ? ldg16(src + row * n + c) : make_uint4(0, 0, 0, 0);
+        }
+        #pragma unroll
+        for (int i = 0; i < kSegCPL; ++i) {
+            float v[V::N];
+            V::unpack(raw[i], v);
             #pragma unroll
-            for (int u = 0; u < V::N; ++u) a[u] += v[u];
+            for (int u = 0; u < V::N; ++u) a[i][u] = fmaf(g, v[u], a[i][u]);
         }
     }
-    for (; p < p1; ++p) {
-        V::unpack(ldg16(g + (int64_t)p * n + c), v);
-        #pragma unroll
-        for (int u = 0; u < V::N; ++u) a[u] += v[u];
-    }
-    float* out = partial + (int64_t)blockIdx.x * n + c;
     #pragma unroll
-    for (int u = 0; u < V::N; ++u) out[u] = a[u];
+    for (int i = 0; i < kSegCPL; ++i)
+        #pragma unroll
+        for (int u = 0; u < V::N; u += 4)
+            *reinterpret_cast<float4*>(&red[warp][(lane + 32 * i) * V::N + u]) =
+                make_float4(a[i][u], a[i][u + 1], a[i][u + 2], a[i][u + 3]);
+    __syncthreads();
+    for (int j = threadIdx.x; j < TILE; j += 256) {
+        const int c = ct0 + j;
+        if (c >= n) break;
+        float sum = 0.f;
+        #pragma unroll
+        for (int w = 0; w < 8; ++w) sum += red[w][j];
+        partial[(int64_t)blockIdx.x * n + c] = sum;
+    }
 }
 
-__global__ void __launch_bounds__(256) colsum_reduce_kernel(int n, int E,
-                                                            const int32_t* __restrict__ offsets,
-                                                            const float* __restrict__ partial,
-                                                            float* __restrict__ out,
-                                                            int accumulate) {
+__global__ void __launch_bounds__(256) seg_reduce_kernel(int n, int E,
+                                                         const int32_t* __restrict__ offsets,
+                                                         const float* __restrict__ partial,
+                                                         float* __restrict__ out, int accumulate) {
+    __shared__ float red[8][32];
     const int e = blockIdx.x;
-    const int c = blockIdx.y * 256 + threadIdx.x;
-    if (c >= n) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.y * 32 + lane;
     int start = 0;
     for (int q = 0; q < e; ++q) {
         const int cnt = offsets[q + 1] - offsets[q];
@@ -268,20 +300,28 @@ __global__ void __launch_bounds__(256) colsum_reduce_kernel(int n, int E,
     }
     const int cnt = offsets[e + 1] - offsets[e];
     const int nc = (cnt + kDwgChunk - 1) / kDwgChunk;
-    float s = 0.f;
-    int i = 0;
-    for (; i + 8 <= nc; i += 8) {   // 8 loads in flight, added in chunk order
-        float v[8];
-        #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = partial[(int64_t)(start + i + q) * n + c];
-        #pragma unroll
-        for (int q = 0; q < 8; ++q) s += v[q];
+    float sum = 0.f;
+    if (c < n) {
+        int i = warp;
+        for (; i + 24 < nc; i += 32) {   // 4 loads in flight, added in partial order
+            float v[4];
+            #pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = partial[(int64_t)(start + i + 8 * u) * n + c];
+            #pragma unroll
+            for (int u = 0; u < 4; ++u) sum += v[u];
+        }
+        for (; i < nc; i += 8) sum += partial[(int64_t)(start + i) * n + c];
     }
-    for (; i < nc; ++i) s += partial[(int64_t)(start + i) * n + c];
-    float* o = out + (int64_t)e * n + c;
-    *o = accumulate ? *o + s : s;
+    red[warp][lane] = sum;
+    __syncthreads();
+    if (warp == 0 && c < n) {
+        float s = 0.f;
+        #pragma unroll
+        for (int w = 0; w < 8; ++w) s += red[w][lane];
+        float* o = out + (int64_t)e * n + c;
+        *o = accumulate ? *o + s : s;
+    }
 }
-
 
 template <template <int> class F, typename... Args>
 cudaError_t by_k(int k, Args... args) {
@@ -350,21 +390,29 @@ size_t segment_colsum_workspace(const moe_shape& s, int n) {
     return (size_t)((s.T * s.k + kDwgChunk - 1) / kDwgChunk + s.E) * (size_t)n * sizeof(float);
 }
 
+cudaError_t launch_segment_rowsum(const moe_shape& s, const void* src, int n,
+                                  const int32_t* offsets, const int32_t* perm,
+                                  const float* wsel, float* out, int accumulate, float* partial,
+                                  cudaStream_t st) {
+    const int64_t nchunks = (s.T * s.k + kDwgChunk - 1) / kDwgChunk + s.E;
+    const int tile = 32 * kSegCPL * (s.dtype == MOE_BF16 ? 8 : 4);
+    const dim3 grid((unsigned)nchunks, (unsigned)((n + tile - 1) / tile));
+    if (s.dtype == MOE_BF16)
+        seg_partial_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+            n, s.E, s.k, offsets, perm, wsel, (const __nv_bfloat16*)src, partial);
+    else
+        seg_partial_kernel<float><<<grid, 256, 0, st>>>(n, s.E, s.k, offsets, perm, wsel,
+                                                        (const float*)src, partial);
+    seg_reduce_kernel<<<dim3(s.E, (unsigned)((n + 31) / 32)), 256, 0, st>>>(
+        n, s.E, offsets, partial, out, accumulate);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_segment_colsum(const moe_shape& s, const void* g, int n,
                                   const int32_t* offsets, float* out, int accumulate,
                                   float* partial, cudaStream_t st) {
-    const int64_t nchunks = (s.T * s.k + kDwgChunk - 1) / kDwgChunk + s.E;
-    const int vn = s.dtype == MOE_BF16 ? 8 : 4;
-    const unsigned gy = (unsigned)((n + 256 * vn - 1) / (256 * vn));
-    if (s.dtype == MOE_BF16)
-        colsum_partial_kernel<__nv_bfloat16><<<dim3((unsigned)nchunks, gy), 256, 0, st>>>(
-            n, s.E, offsets, (const __nv_bfloat16*)g, partial);
-    else
-        colsum_partial_kernel<float><<<dim3((unsigned)nchunks, gy), 256, 0, st>>>(
-            n, s.E, offsets, (const float*)g, partial);
-    colsum_reduce_kernel<<<dim3(s.E, (unsigned)((n + 255) / 256)), 256, 0, st>>>(
-        n, s.E, offsets, partial, out, accumulate);
-    return cudaGetLastError();
+    return launch_segment_rowsum(s, g, n, offsets, nullptr, nullptr, out, accumulate, partial,
+                                 st);
 }
 
 }  // namespace moe

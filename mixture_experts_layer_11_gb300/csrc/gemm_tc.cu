@@ -103,6 +103,7 @@ struct TcParams {
     void* out0;
     void* out1;
     float* outf;
+    float* cpart;            // ScaleAux: column-sum partial rows [rows][N], or null
     int accumulate;
     int32_t* status;
     uint64_t limit_ns;
@@ -313,6 +314,24 @@ template <int N> __device__ __forceinline__ void bulk_wait_read() {
 // until every committed group has completed its writes
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Column sums over a warp's 32 rows (one row per lane) of 16 values: five
+// butterfly steps, each lane keeping half of the columns still open;
+// afterwards lanes 2c and 2c+1 both hold the sum of column c.
+__device__ __forceinline__ float warp_colsum16(float (&a)[16], int lane) {
+    #pragma unroll
+    for (int h = 8; h >= 1; h >>= 1) {
+        const int m = 2 * h;                 // lane bit deciding which half stays
+        const bool up = (lane & m) != 0;
+        #pragma unroll
+        for (int j = 0; j < h; ++j) {
+            const float send = up ? a[j] : a[j + h];
+            const float keep = up ? a[j + h] : a[j];
+            a[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+    }
+    return a[0] + __shfl_xor_sync(0xffffffffu, a[0], 1);
 }
 
 template <int CW>
@@ -732,6 +751,26 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         for (int u = 0; u < CW / 8; ++u) pk[u] = pack8_bf16(v + 8 * u);
                         emit(stg + sbuf * ES::CHUNK_BYTES, pk, &mapO0, p.out0, col0);
                         sbuf ^= 1;
+                        if (EPI == (int)Epi::ScaleAux && CW == 16 && p.cpart) {
+                            // column sums of the stored (bf16) values of this warp's
+                            // rows inside the segment -> one partial row per
+                            // (m-tile, CTA, lane quarter)
+                            float a[16];
+                            #pragma unroll
+                            for (int u = 0; u < CW / 8; ++u) {
+                                const uint32_t* wd = reinterpret_cast<const uint32_t*>(&pk[u]);
+                                #pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    a[8 * u + 2 * i] =
+                                        row_ok ? __uint_as_float(wd[i] << 16) : 0.f;
+                                    a[8 * u + 2 * i + 1] =
+                                        row_ok ? __uint_as_float(wd[i] & 0xffff0000u) : 0.f;
+                                }
+                            }
+                            const float cs = warp_colsum16(a, lane);
+                            const int64_t prow = ((int64_t)(t / NT) * S::CTAS + rank) * 4 + q;
+                            if ((lane & 1) == 0) p.cpart[prow * p.N + col0 + (lane >> 1)] = cs;
+                        }
                     }
                     if (lane == 0) bulk_commit();
                     __syncwarp();
@@ -899,6 +938,33 @@ cudaError_t launch_either(const CUtensorMap& a, const CUtensorMap& b, const CUte
     return launch_tc<VAR_K, A_MN, B_MN, EPI, false>(a, b, o0, o1, p, units1, st);
 }
 
+// Column sums from the ScaleAux epilogue's partial rows: expert e owns the
+// rows of its ceil(n_e / tile_m) m-tiles (rows_per_mtile each, experts in
+// order); they are summed in row order.
+__global__ void __launch_bounds__(256) colsum_mtile_reduce_kernel(
+    int N, int E, const int32_t* __restrict__ offsets, int tile_m, int rows_per_mtile,
+    const float* __restrict__ part, float* __restrict__ out, int accumulate) {
+    const int e = blockIdx.x;
+    const int c = blockIdx.y * 256 + threadIdx.x;
+    if (c >= N) return;
+    int64_t m0 = 0;
+    for (int q = 0; q < e; ++q) m0 += (offsets[q + 1] - offsets[q] + tile_m - 1) / tile_m;
+    const int R = ((offsets[e + 1] - offsets[e] + tile_m - 1) / tile_m) * rows_per_mtile;
+    const float* src = part + m0 * rows_per_mtile * N + c;
+    float s = 0.f;
+    int i = 0;
+    for (; i + 8 <= R; i += 8) {   // 8 loads in flight, added in row order
+        float v[8];
+        #pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = src[(int64_t)(i + u) * N];
+        #pragma unroll
+        for (int u = 0; u < 8; ++u) s += v[u];
+    }
+    for (; i < R; ++i) s += src[(int64_t)i * N];
+    float* o = out + (int64_t)e * N + c;
+    *o = accumulate ? *o + s : s;
+}
+
 // Map of a bf16 [P, N] output for the epilogue's TMA stores: boxes of 32 rows
 // x CW columns, swizzled like the staging buffers.
 bool make_out_map(CUtensorMap* m, void* ptr, int64_t P, int N, int CW) {
@@ -937,6 +1003,9 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     p.E = g.E; p.N = g.N; p.K = g.K; p.M = 0; p.P = g.P;
     p.offsets = g.offsets; p.bias = g.bias; p.aux = g.aux; p.out0 = g.out0; p.out1 = g.out1;
     p.outf = nullptr; p.accumulate = 0; p.status = status; p.limit_ns = wait_limit_ns();
+    const bool colsum = g.epi == Epi::ScaleAux && g.colsum != nullptr;
+    if (colsum && !g.colsum_partial) return cudaErrorInvalidValue;
+    p.cpart = colsum ? g.colsum_partial : nullptr;
     const int64_t NT = (g.N + BN - 1) / BN;
     const int64_t u1 = ((g.P + BM - 1) / BM + g.E) * NT;
     const int64_t u2 = ((g.P + 2 * BM - 1) / (2 * BM) + g.E) * NT;
@@ -960,16 +1029,29 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
             if (!g.weight_kmajor) return cudaErrorInvalidValue;
             return launch_either<false, false, false, (int)Epi::Bias>(ma, mb, mo0, mo1, p, u1, u2,
                                                                       st);
-        case Epi::ScaleAux:
+        case Epi::ScaleAux: {
             if (g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_either<false, false, true, (int)Epi::ScaleAux>(ma, mb, mo0, mo1, p, u1,
-                                                                         u2, st);
+            cudaError_t e = launch_either<false, false, true, (int)Epi::ScaleAux>(
+                ma, mb, mo0, mo1, p, u1, u2, st);
+            if (e != cudaSuccess || !colsum) return e;
+            colsum_mtile_reduce_kernel<<<dim3((unsigned)g.E, (unsigned)((g.N + 255) / 256)), 256,
+                                         0, st>>>(g.N, g.E, g.offsets, pair ? 2 * BM : BM,
+                                                  (pair ? 2 : 1) * 4, g.colsum_partial, g.colsum,
+                                                  g.colsum_accumulate);
+            return cudaGetLastError();
+        }
         case Epi::Plain:
             if (g.weight_kmajor) return cudaErrorInvalidValue;
             return launch_either<false, false, true, (int)Epi::Plain>(ma, mb, mo0, mo1, p, u1, u2,
                                                                       st);
     }
     return cudaErrorInvalidValue;
+}
+
+size_t gemm_colsum_workspace(int64_t P, int E, int N) {
+    // 4 partial rows per 128-row CTA tile.  Single CTAs: at most ceil(P/128) + E
+    // tiles; pairs: 2 (ceil(P/256) + E) <= ceil(P/128) + 1 + 2E.
+    return (size_t)((P + BM - 1) / BM + 2 * (int64_t)E + 1) * 4 * (size_t)N * sizeof(float);
 }
 
 cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t st) {

@@ -55,6 +55,12 @@ cudaError_t launch_combine_bwd(const moe_shape& s, const void* dy, const void* y
 cudaError_t launch_segment_colsum(const moe_shape& s, const void* g, int n,
                                   const int32_t* offsets, float* out, int accumulate,
                                   float* partial, cudaStream_t st);
+// per-expert weighted, gathered row sums: for the rows p of expert e's segment,
+// slot = perm[p], out[e][c] (+)= sum wsel[slot] src[slot / k][c]
+cudaError_t launch_segment_rowsum(const moe_shape& s, const void* src, int n,
+                                  const int32_t* offsets, const int32_t* perm,
+                                  const float* wsel, float* out, int accumulate, float* partial,
+                                  cudaStream_t st);
 size_t segment_colsum_workspace(const moe_shape& s, int n);
 
 // Grouped expert GEMMs.  Operand layouts (row-major):
@@ -78,7 +84,15 @@ struct GemmVarM {
     const void* aux;        // ScaleAux: G = GELU'(h) [P,N]
     void* out0;             // [P,N]
     void* out1;             // BiasGelu: A = GELU(h) [P,N]
+    // ScaleAux, tensor-core path: when non-null, also the per-expert column
+    // sums of the stored out0 into colsum [E,N] (added to it when
+    // colsum_accumulate), through colsum_partial (gemm_colsum_workspace bytes).
+    float* colsum = nullptr;
+    float* colsum_partial = nullptr;
+    int colsum_accumulate = 0;
 };
+// Bytes of GemmVarM::colsum_partial for P rows, E experts, N columns.
+size_t gemm_colsum_workspace(int64_t P, int E, int N);
 struct GemmVarK {
     int E, M, N;
     int64_t P;

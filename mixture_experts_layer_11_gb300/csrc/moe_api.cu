@@ -82,7 +82,10 @@ size_t route_ws(const moe_shape& s) {
 size_t ffn_bwd_ws(const moe_shape& s) {
     const size_t dh = align_up((size_t)s.T * s.k * s.f * esize(s));
     const int n = s.d > s.f ? s.d : s.f;
-    return dh + align_up(segment_colsum_workspace(s, n));
+    size_t part = segment_colsum_workspace(s, n);
+    const size_t fused = gemm_colsum_workspace(s.T * s.k, s.E, s.f);   // db1 in the dH GEMM
+    if (fused > part) part = fused;
+    return dh + align_up(part);
 }
 
 }  // namespace
@@ -220,12 +223,17 @@ moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const voi
     float* partial = (float*)(wsb + align_up((size_t)P * f * esize(*s)));
     // dA = dY W2[e] (W2 stored [E,d,f] = [E,K,N]); dH = dA * G, G = GELU'(h)
     GemmVarM g_dh{E, f, d, P, offsets, dy_perm, W2, false, Epi::ScaleAux, nullptr, G, dH, nullptr};
+    const bool tc = s->dtype == MOE_BF16;
+    if (tc) {   // db1 = column sums of dH, taken in the dH GEMM's epilogue
+        g_dh.colsum = db1;
+        g_dh.colsum_partial = partial;
+        g_dh.colsum_accumulate = accumulate;
+    }
     // dX = dH W1[e] (W1 stored [E,f,d] = [E,K,N])
     GemmVarM g_dx{E, d, f, P, offsets, dH, W1, false, Epi::Plain, nullptr, nullptr, dx_perm, nullptr};
     // dW2[e] = dY^T A  ([d, f]);  dW1[e] = dH^T X  ([f, d])
     GemmVarK g_w2{E, d, f, P, offsets, dy_perm, A, dW2, accumulate};
     GemmVarK g_w1{E, f, d, P, offsets, dH, x_perm, dW1, accumulate};
-    const bool tc = s->dtype == MOE_BF16;
     cudaError_t e = tc ? launch_gemm_varm_tc(g_dh, dev_status, st) : launch_gemm_varm_simt(g_dh, st);
     if (e == cudaSuccess)
         e = tc ? launch_gemm_varm_tc(g_dx, dev_status, st) : launch_gemm_varm_simt(g_dx, st);
@@ -234,7 +242,8 @@ moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const voi
     if (e == cudaSuccess)
         e = tc ? launch_gemm_vark_tc(g_w1, dev_status, st) : launch_gemm_vark_simt(g_w1, st);
     if (e == cudaSuccess) e = launch_segment_colsum(*s, dy_perm, d, offsets, db2, accumulate, partial, st);
-    if (e == cudaSuccess) e = launch_segment_colsum(*s, dH, f, offsets, db1, accumulate, partial, st);
+    if (e == cudaSuccess && !tc)
+        e = launch_segment_colsum(*s, dH, f, offsets, db1, accumulate, partial, st);
     return cuda_status(e);
 }
 

@@ -51,6 +51,15 @@ template <> struct Vec<__nv_bfloat16> {
             v[2 * i + 1] = f.y;
         }
     }
+    static __device__ __forceinline__ void unpack(const uint4& u, float* v) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+        #pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(h[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
     static __device__ __forceinline__ void store(__nv_bfloat16* p, const float* v) {
         uint4 u;
         __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
@@ -64,6 +73,10 @@ template <> struct Vec<float> {
     static __device__ __forceinline__ void load(const float* p, float* v) {
         float4 u = *reinterpret_cast<const float4*>(p);
         v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+    }
+    static __device__ __forceinline__ void unpack(const uint4& u, float* v) {
+        v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+        v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
     }
     static __device__ __forceinline__ void store(float* p, const float* v) {
         *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
@@ -344,22 +357,25 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[EP], int lane) {
     return r;
 }
 
-template <typename TIn, int EP>
-__global__ void __launch_bounds__(256) router_gate_small_kernel(
+// Router logits + gate for E <= 32, one launch.  A block owns one 64-token
+// dispatch block; its WARPS warps own 64 / WARPS tokens each and take TPW of
+// them at a time (their Wg loads shared).  Many warps per block keep enough
+// loads in flight: the work per token is small and latency-bound.
+template <typename TIn, int EP, int WARPS, int TPW>
+__global__ void __launch_bounds__(WARPS * 32) router_gate_small_kernel(
     int64_t T, int d, int E, int k, int renorm, int nblk, const TIn* __restrict__ x,
     const TIn* __restrict__ Wg, const float* __restrict__ beta, float* __restrict__ logits,
     int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ block_counts,
     int32_t* status) {
     using V = Vec<TIn>;
-    // tokens whose dot products a warp accumulates together (sharing Wg loads)
-    constexpr int TPW = EP <= 8 ? 4 : (EP <= 16 ? 2 : 1);
+    constexpr int TOK = kRouteBlockTokens / WARPS;   // tokens per warp
     __shared__ uint32_t bits[256][kRouteWords];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     zero_bits(bits, E);
     __syncthreads();
     const int nv = d / V::N;
-    for (int tt0 = 0; tt0 < 8; tt0 += TPW) {
-        const int64_t t0 = (int64_t)blockIdx.x * kRouteBlockTokens + warp * 8 + tt0;
+    for (int tt0 = 0; tt0 < TOK; tt0 += TPW) {
+        const int64_t t0 = (int64_t)blockIdx.x * kRouteBlockTokens + warp * TOK + tt0;
         if (t0 >= T) break;
         float acc[TPW][EP];
         #pragma unroll
@@ -400,7 +416,7 @@ __global__ void __launch_bounds__(256) router_gate_small_kernel(
                 L[0] = le + (beta ? beta[lane] : 0.f);
                 logits[t * E + lane] = L[0];
             }
-            gate_token<1>(t, E, k, renorm, L, lane, warp * 8 + tt0 + i, bits, idx, w, status);
+            gate_token<1>(t, E, k, renorm, L, lane, warp * TOK + tt0 + i, bits, idx, w, status);
         }
     }
     __syncthreads();
@@ -412,16 +428,15 @@ cudaError_t router_gate_small(const moe_shape& s, const TIn* x, const TIn* Wg, c
                               float* logits, int32_t* idx, float* w, int32_t* block_counts,
                               int32_t* status, cudaStream_t st) {
     const int nblk = (int)route_blocks(s.T);
-#define MOE_SMALL(EPV)                                                                        \
-    router_gate_small_kernel<TIn, EPV><<<nblk, 256, 0, st>>>(s.T, s.d, s.E, s.k, s.renorm,  \
-                                                              nblk, x, Wg, beta, logits, idx, \
-                                                              w, block_counts, status)
-    if (s.E <= 1) MOE_SMALL(1);
-    else if (s.E <= 2) MOE_SMALL(2);
-    else if (s.E <= 4) MOE_SMALL(4);
-    else if (s.E <= 8) MOE_SMALL(8);
-    else if (s.E <= 16) MOE_SMALL(16);
-    else MOE_SMALL(32);
+#define MOE_SMALL(EPV, WV, TV)                                                             \
+    router_gate_small_kernel<TIn, EPV, WV, TV><<<nblk, (WV) * 32, 0, st>>>(                \
+        s.T, s.d, s.E, s.k, s.renorm, nblk, x, Wg, beta, logits, idx, w, block_counts, status)
+    if (s.E <= 1) MOE_SMALL(1, 32, 2);
+    else if (s.E <= 2) MOE_SMALL(2, 32, 2);
+    else if (s.E <= 4) MOE_SMALL(4, 32, 2);
+    else if (s.E <= 8) MOE_SMALL(8, 32, 2);
+    else if (s.E <= 16) MOE_SMALL(16, 16, 2);
+    else MOE_SMALL(32, 16, 1);
 #undef MOE_SMALL
     return cudaGetLastError();
 }
@@ -524,6 +539,25 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * 8 + warp;
     if (t >= T) return;
+    constexpr int VN = V::N;
+    // vectors per lane in flight: U * KMAX row loads before any use
+    constexpr int U = KMAX >= 8 ? 1 : (KMAX >= 2 ? 8 / KMAX : 4);
+    // The gather of the permute backward (rows pos[t, j] of dx_perm) does not
+    // depend on dL: its first loads are issued before dL is computed.
+    int32_t p[KMAX];
+    #pragma unroll
+    for (int j = 0; j < KMAX; ++j) p[j] = (dx_perm && j < k) ? pos[t * k + j] : 0;
+    uint4 raw[U][KMAX];
+    auto gather = [&](int c0) {
+        #pragma unroll
+        for (int u = 0; u < U; ++u)
+            #pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (j < k && c0 + 32 * VN * u < d)
+                    raw[u][j] = __ldg(reinterpret_cast<const uint4*>(
+                        dx_perm + (int64_t)p[j] * d + c0 + 32 * VN * u));
+    };
+    if (dx_perm) gather(lane * VN);
     int ng;  // number of (expert, dL) terms for this token
     if (renorm) {
         float wj = 0.f, dwj = 0.f;
@@ -592,32 +626,22 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
         ng = E;
     }
     __syncwarp();
-    constexpr int VN = V::N;
-    // vectors per lane in flight: U * KMAX row loads before any use
-    constexpr int U = KMAX >= 8 ? 1 : 8 / KMAX;
-    int32_t p[KMAX];
-    #pragma unroll
-    for (int j = 0; j < KMAX; ++j) p[j] = (dx_perm && j < k) ? pos[t * k + j] : 0;
     for (int c0 = lane * VN; c0 < d; c0 += 32 * VN * U) {
         float acc[U][VN], wv[VN];
         if (dx_perm) {
             // permute backward fused in: dx = sum_j dx_perm[pos[t,j]] + router term
-            float xr[U][KMAX][VN];
-            #pragma unroll
-            for (int u = 0; u < U; ++u)
-                #pragma unroll
-                for (int j = 0; j < KMAX; ++j)
-                    if (j < k && c0 + 32 * VN * u < d)
-                        V::load(dx_perm + (int64_t)p[j] * d + c0 + 32 * VN * u, xr[u][j]);
+            if (c0 != lane * VN) gather(c0);
             #pragma unroll
             for (int u = 0; u < U; ++u) {
                 #pragma unroll
                 for (int e = 0; e < VN; ++e) acc[u][e] = 0.f;
                 #pragma unroll
                 for (int j = 0; j < KMAX; ++j) {
-                    if (j >= k) break;
+                    if (j >= k || c0 + 32 * VN * u >= d) break;
+                    float xr[VN];
+                    V::unpack(raw[u][j], xr);
                     #pragma unroll
-                    for (int e = 0; e < VN; ++e) acc[u][e] += xr[u][j][e];
+                    for (int e = 0; e < VN; ++e) acc[u][e] += xr[e];
                 }
             }
         } else {
@@ -640,86 +664,6 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
         for (int u = 0; u < U; ++u)
             if (c0 + 32 * VN * u < d) V::store(dx + t * d + c0 + 32 * VN * u, acc[u]);
     }
-}
-
-// Sparse (renorm) partial sums of dWg: one partial per (expert, chunk of
-// kDwgChunk consecutive rows of the expert's segment), rows in segment order.
-template <typename TIn>
-__global__ void __launch_bounds__(256) dwg_partial_sparse_kernel(
-    int d, int E, int k, const int32_t* __restrict__ offsets,
-    const int32_t* __restrict__ perm, const float* __restrict__ dLsel,
-    const TIn* __restrict__ x, float* __restrict__ partial) {
-    using V = Vec<TIn>;
-    constexpr int VN = V::N;
-    // locate (expert, chunk) of this block
-    int e = 0, acc = 0, sub = -1;
-    for (; e < E; ++e) {
-        const int n = offsets[e + 1] - offsets[e];
-        const int nc = (n + kDwgChunk - 1) / kDwgChunk;
-        if ((int)blockIdx.x < acc + nc) { sub = blockIdx.x - acc; break; }
-        acc += nc;
-    }
-    if (sub < 0) return;
-    const int c = (blockIdx.y * 256 + threadIdx.x) * VN;
-    if (c >= d) return;
-    const int p0 = offsets[e] + sub * kDwgChunk;
-    const int p1 = min(offsets[e + 1], p0 + kDwgChunk);
-    float a[VN], xv[VN];
-    #pragma unroll
-    for (int u = 0; u < VN; ++u) a[u] = 0.f;
-    int p = p0;
-    for (; p + 4 <= p1; p += 4) {       // 4 rows in flight, summed in segment order
-        int sl[4];
-        float g[4], xr[4][VN];
-        #pragma unroll
-        for (int q = 0; q < 4; ++q) sl[q] = perm[p + q];
-        #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            g[q] = dLsel[sl[q]];
-            V::load(x + (int64_t)(sl[q] / k) * d + c, xr[q]);
-        }
-        #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            #pragma unroll
-            for (int u = 0; u < VN; ++u) a[u] = fmaf(g[q], xr[q][u], a[u]);
-    }
-    for (; p < p1; ++p) {
-        const int s = perm[p];
-        const float g = dLsel[s];
-        V::load(x + (int64_t)(s / k) * d + c, xv);
-        #pragma unroll
-        for (int u = 0; u < VN; ++u) a[u] = fmaf(g, xv[u], a[u]);
-    }
-    float* out = partial + (int64_t)blockIdx.x * d + c;
-    #pragma unroll
-    for (int u = 0; u < VN; ++u) out[u] = a[u];
-}
-
-__global__ void __launch_bounds__(256) dwg_reduce_sparse_kernel(
-    int d, int E, const int32_t* __restrict__ offsets, const float* __restrict__ partial,
-    float* __restrict__ dWg, int accumulate) {
-    const int e = blockIdx.x;
-    const int c = blockIdx.y * 256 + threadIdx.x;
-    if (c >= d) return;
-    int start = 0;
-    for (int q = 0; q < e; ++q) {
-        const int n = offsets[q + 1] - offsets[q];
-        start += (n + kDwgChunk - 1) / kDwgChunk;
-    }
-    const int n = offsets[e + 1] - offsets[e];
-    const int nc = (n + kDwgChunk - 1) / kDwgChunk;
-    float s = 0.f;
-    int i = 0;
-    for (; i + 8 <= nc; i += 8) {   // 8 loads in flight, added in chunk order
-        float v[8];
-        #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = partial[(int64_t)(start + i + q) * d + c];
-        #pragma unroll
-        for (int q = 0; q < 8; ++q) s += v[q];
-    }
-    for (; i < nc; ++i) s += partial[(int64_t)(start + i) * d + c];
-    float* o = dWg + (int64_t)e * d + c;
-    *o = accumulate ? *o + s : s;
 }
 
 // Dense (softmax Jacobian) partial sums: partial[tc][e][c] over kDwgChunk
@@ -806,11 +750,8 @@ cudaError_t route_bwd_typed(const moe_shape& s, const float* dw, const float* lo
     const unsigned gy = (unsigned)((d + 256 * VN - 1) / (256 * VN));
     const unsigned gy_red = (unsigned)((d + 255) / 256);
     if (s.renorm) {
-        const int64_t nchunks = (T * k + kDwgChunk - 1) / kDwgChunk + E;
-        dwg_partial_sparse_kernel<TIn><<<dim3((unsigned)nchunks, gy), 256, 0, st>>>(
-            d, E, k, offsets, perm, dL, x, partial);
-        dwg_reduce_sparse_kernel<<<dim3(E, gy_red), 256, 0, st>>>(d, E, offsets, partial, dWg,
-                                                                 accumulate);
+        // dWg[e] = sum over e's selected slots of dL(slot) x[token(slot)]
+        return launch_segment_rowsum(s, x, d, offsets, perm, dL, dWg, accumulate, partial, st);
     } else {
         const int ntc = (int)((T + kDwgChunk - 1) / kDwgChunk);
         dwg_partial_dense_kernel<TIn><<<dim3(ntc, gy, (E + 7) / 8), 256, 0, st>>>(T, d, E, dL, x,
