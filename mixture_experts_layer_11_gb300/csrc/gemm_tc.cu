@@ -391,7 +391,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             tmem_relinquish();
         }
     }
-    for (int i = threadIdx.x; i <= E; i += THREADS) c.off[i] = p.offsets[i];
+    for (int i = threadIdx.x; i <= E; i += THREADS)
+        c.off[i] = p.offsets ? p.offsets[i] : (i == 0 ? 0 : (int)p.P);   // null: rows [0, P)
     __syncthreads();
     if (!VAR_K) {
         if (threadIdx.x == 0) {
@@ -600,7 +601,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
         uint8_t* stg = staging_base + ew * (PP::STAGING / ES::WARPS);
         const uint32_t tempty_local0 = smem_u32(&c.tempty[0]);
         const uint32_t tempty_local1 = smem_u32(&c.tempty[1]);
-        if (!VAR_K && lane == 0) {
+        if (!VAR_K && EPI != (int)Epi::Logits && lane == 0) {
             tma_prefetch_map(&mapO0);
             if (EPI == (int)Epi::BiasGelu) tma_prefetch_map(&mapO1);
         }
@@ -684,7 +685,28 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     #pragma unroll
                     for (int i = 0; i < CW; ++i) v[i] = 0.f;
                 }
-                if (!VAR_K) {
+                if (EPI == (int)Epi::Logits) {
+                    // fp32 logits [P, N], N any: + bias, staged as 32 x 32 fp32
+                    // (word j of row r at r*32 + (j ^ r): conflict-free both
+                    // ways), then stored row by row, columns < N only.
+                    const float* beta = (const float*)p.bias;
+                    float* sf = reinterpret_cast<float*>(stg);
+                    #pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float b = (beta && col0 + j < p.N) ? __ldg(beta + col0 + j) : 0.f;
+                        sf[lane * 32 + (j ^ lane)] = v[j] + b;
+                    }
+                    __syncwarp();
+                    float* out = (float*)p.out0;
+                    const bool col_ok = col0 + lane < p.N;
+                    const int64_t grow0 = (int64_t)ti.row0 + q * 32;
+                    const int valid = ti.rows - q * 32;
+                    #pragma unroll 4
+                    for (int r = 0; r < 32; ++r)
+                        if (r < valid && col_ok)
+                            out[(grow0 + r) * p.N + col0 + lane] = sf[r * 32 + (lane ^ r)];
+                    __syncwarp();
+                } else if (!VAR_K) {
                     if (kBias) {
                         const U4s<CW / 8> bcur = bnext;
                         if (ch + 1 < ES::NCH) bnext = load_bias(ch + 1);
@@ -940,29 +962,40 @@ cudaError_t launch_either(const CUtensorMap& a, const CUtensorMap& b, const CUte
 
 // Column sums from the ScaleAux epilogue's partial rows: expert e owns the
 // rows of its ceil(n_e / tile_m) m-tiles (rows_per_mtile each, experts in
-// order); they are summed in row order.
+// order).  A block takes one expert and 32 columns; its 8 warps take every
+// 8th row and are added in warp order.  Deterministic.
 __global__ void __launch_bounds__(256) colsum_mtile_reduce_kernel(
     int N, int E, const int32_t* __restrict__ offsets, int tile_m, int rows_per_mtile,
     const float* __restrict__ part, float* __restrict__ out, int accumulate) {
+    __shared__ float red[8][32];
     const int e = blockIdx.x;
-    const int c = blockIdx.y * 256 + threadIdx.x;
-    if (c >= N) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.y * 32 + lane;
     int64_t m0 = 0;
     for (int q = 0; q < e; ++q) m0 += (offsets[q + 1] - offsets[q] + tile_m - 1) / tile_m;
     const int R = ((offsets[e + 1] - offsets[e] + tile_m - 1) / tile_m) * rows_per_mtile;
     const float* src = part + m0 * rows_per_mtile * N + c;
     float s = 0.f;
-    int i = 0;
-    for (; i + 8 <= R; i += 8) {   // 8 loads in flight, added in row order
-        float v[8];
-        #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = src[(int64_t)(i + u) * N];
-        #pragma unroll
-        for (int u = 0; u < 8; ++u) s += v[u];
+    if (c < N) {
+        int i = warp;
+        for (; i + 24 < R; i += 32) {   // 4 loads in flight, added in row order
+            float v[4];
+            #pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = src[(int64_t)(i + 8 * u) * N];
+            #pragma unroll
+            for (int u = 0; u < 4; ++u) s += v[u];
+        }
+        for (; i < R; i += 8) s += src[(int64_t)i * N];
     }
-    for (; i < R; ++i) s += src[(int64_t)i * N];
-    float* o = out + (int64_t)e * N + c;
-    *o = accumulate ? *o + s : s;
+    red[warp][lane] = s;
+    __syncthreads();
+    if (warp == 0 && c < N) {
+        float t = 0.f;
+        #pragma unroll
+        for (int w = 0; w < 8; ++w) t += red[w][lane];
+        float* o = out + (int64_t)e * N + c;
+        *o = accumulate ? *o + t : t;
+    }
 }
 
 // Map of a bf16 [P, N] output for the epilogue's TMA stores: boxes of 32 rows
@@ -978,7 +1011,9 @@ bool make_out_map(CUtensorMap* m, void* ptr, int64_t P, int N, int CW) {
 }  // namespace
 
 cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t st) {
-    if (g.E > MAX_E || g.N % 64 || g.K % 64) return cudaErrorInvalidValue;
+    const bool logits = g.epi == Epi::Logits;
+    if (g.E > MAX_E || g.K % 64 || g.N < 1) return cudaErrorInvalidValue;
+    if (logits ? (g.E != 1 || g.N > BN) : (g.N % 64 != 0)) return cudaErrorInvalidValue;
     const bool pair = use_pairs();
     const uint32_t bn_cta = pair ? BN / 2 : BN;
     CUtensorMap ma, mb;
@@ -1014,6 +1049,11 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     const int cw = wide ? EpiShape<(int)Epi::BiasGelu, false>::CW
                         : EpiShape<(int)Epi::Bias, false>::CW;
     CUtensorMap mo0, mo1;
+    if (logits) {   // fp32 output, stored by the epilogue warps
+        memset(&mo0, 0, sizeof(mo0));
+        return launch_either<false, false, false, (int)Epi::Logits>(ma, mb, mo0, mo0, p, u1, u2,
+                                                                    st);
+    }
     if (!make_out_map(&mo0, g.out0, g.P, g.N, cw)) return cudaErrorInvalidValue;
     if (g.epi == Epi::BiasGelu) {
         if (!make_out_map(&mo1, g.out1, g.P, g.N, cw)) return cudaErrorInvalidValue;
@@ -1034,7 +1074,7 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
             cudaError_t e = launch_either<false, false, true, (int)Epi::ScaleAux>(
                 ma, mb, mo0, mo1, p, u1, u2, st);
             if (e != cudaSuccess || !colsum) return e;
-            colsum_mtile_reduce_kernel<<<dim3((unsigned)g.E, (unsigned)((g.N + 255) / 256)), 256,
+            colsum_mtile_reduce_kernel<<<dim3((unsigned)g.E, (unsigned)((g.N + 31) / 32)), 256,
                                          0, st>>>(g.N, g.E, g.offsets, pair ? 2 * BM : BM,
                                                   (pair ? 2 : 1) * 4, g.colsum_partial, g.colsum,
                                                   g.colsum_accumulate);

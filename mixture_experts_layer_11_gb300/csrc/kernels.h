@@ -70,7 +70,9 @@ size_t segment_colsum_workspace(const moe_shape& s, int n);
 //   VarK ("wgrad"): C_e [M, N] (+)= act_a[seg_e, M]^T act_b[seg_e, N], fp32.
 // BiasGelu: h = acc + bias; out0 = GELU'(h), out1 = GELU(h).
 // Bias: out0 = acc + bias.  ScaleAux: out0 = acc * aux.  Plain: out0 = acc.
-enum class Epi : int { BiasGelu = 0, Bias = 1, ScaleAux = 2, Plain = 3 };
+// Logits: fp32 out0 [P,N] = act W^T + bias (fp32 [N], optional), any N >= 1;
+// the router logits, one segment (offsets may be null: rows [0, P)).
+enum class Epi : int { BiasGelu = 0, Bias = 1, ScaleAux = 2, Plain = 3, Logits = 4 };
 
 struct GemmVarM {
     int E, N, K;

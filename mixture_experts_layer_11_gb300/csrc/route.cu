@@ -308,18 +308,21 @@ __device__ __forceinline__ void write_block_counts(uint32_t (*bits)[kRouteWords]
     }
 }
 
-// Gate on logits already in memory (given, or from the tiled GEMM).
-template <int EPL>
-__global__ void __launch_bounds__(256) gate_hist_kernel(
+// Gate on logits already in memory (given, or from a logits GEMM).  WARPS
+// warps per 64-token block, 64 / WARPS tokens each: the per-token work is a
+// chain of dependent shuffles, so many warps are kept in flight.
+template <int EPL, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) gate_hist_kernel(
     int64_t T, int E, int k, int renorm, int nblk, const float* __restrict__ logits,
     int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ block_counts,
     int32_t* status) {
+    constexpr int TOK = kRouteBlockTokens / WARPS;
     __shared__ uint32_t bits[256][kRouteWords];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     zero_bits(bits, E);
     __syncthreads();
-    for (int tt = 0; tt < 8; ++tt) {
-        const int tok = warp * 8 + tt;
+    for (int tt = 0; tt < TOK; ++tt) {
+        const int tok = warp * TOK + tt;
         const int64_t t = (int64_t)blockIdx.x * kRouteBlockTokens + tok;
         if (t >= T) break;
         float L[EPL];
@@ -803,6 +806,14 @@ cudaError_t launch_route_gate(const moe_shape& s, const void* x, const void* Wg,
                              const float* beta, float* logits, int compute_logits, int32_t* idx,
                              float* w, int32_t* block_counts, int32_t* status, cudaStream_t st) {
     const bool bf = s.dtype == MOE_BF16;
+    if (compute_logits && bf && s.d % 64 == 0) {
+        // bf16 logits on the tensor cores (fp32 accumulation), then the gate
+        GemmVarM g{1, s.E, s.d, s.T, nullptr, x, Wg, true, Epi::Logits, beta, nullptr, logits,
+                   nullptr};
+        const cudaError_t e = launch_gemm_varm_tc(g, status, st);
+        if (e != cudaSuccess) return e;
+        compute_logits = 0;
+    }
     if (compute_logits && s.E <= 32) {
         if (bf)
             return router_gate_small(s, (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg, beta,
@@ -819,14 +830,14 @@ cudaError_t launch_route_gate(const moe_shape& s, const void* x, const void* Wg,
     }
     const int nblk = (int)route_blocks(s.T);
     const int E = s.E;
-    if (E <= 32)
-        gate_hist_kernel<1><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
-    else if (E <= 64)
-        gate_hist_kernel<2><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
-    else if (E <= 128)
-        gate_hist_kernel<4><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
-    else
-        gate_hist_kernel<8><<<nblk, 256, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, idx, w, block_counts, status);
+#define MOE_GATE(EPLV, WV)                                                                  \
+    gate_hist_kernel<EPLV, WV><<<nblk, (WV) * 32, 0, st>>>(s.T, E, s.k, s.renorm, nblk, logits, \
+                                                           idx, w, block_counts, status)
+    if (E <= 32) MOE_GATE(1, 32);
+    else if (E <= 64) MOE_GATE(2, 32);
+    else if (E <= 128) MOE_GATE(4, 16);
+    else MOE_GATE(8, 16);
+#undef MOE_GATE
     return cudaGetLastError();
 }
 

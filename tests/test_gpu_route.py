@@ -76,7 +76,8 @@ def test_route_nonfinite_flags_and_stays_in_range():
 
 @pytest.mark.parametrize("dtype,T,d,E,zipf", [("f32", 256, 64, 4, None), ("bf16", 1000, 768, 8, None),
                                               ("bf16", 777, 256, 64, 1.2), ("bf16", 300, 4096, 128, 1.1),
-                                              ("f32", 129, 200, 256, None)])
+                                              ("f32", 129, 200, 256, None),
+                                              ("bf16", 333, 128, 5, None), ("bf16", 200, 192, 256, None)])
 def test_router_logits(dtype, T, d, E, zipf):
     cfg = synth.MoEConfig("t", T=T, d=d, f=64, E=E, k=1, renorm=0, dtype=dtype, zipf_s=zipf)
     inp = synth.make_inputs(cfg, seed=3)
