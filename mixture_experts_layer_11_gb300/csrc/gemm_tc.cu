@@ -18,8 +18,10 @@
 //   VarK (weight gradient): C_e[M, N] (+)= act_a[seg_e, M]^T act_b[seg_e, N];
 //     the reduction runs over the segment's rows, so rows past the segment in
 //     the last K block are zeroed in shared memory before the MMA reads them.
-//     Single CTAs only: the pair variant would have to zero rows in the peer
-//     CTA's shared memory before the even CTA's MMA.
+//     On a CTA pair each CTA zeroes its own operands: for a segment's last K
+//     block the odd CTA's loads complete on its own stage barrier, its
+//     otherwise idle MMA warp zeroes the tail and then arrives on the even
+//     CTA's stage barrier (every other stage goes straight to the even CTA).
 //
 // Two CTA shapes (template PAIR):
 //   1 CTA: tile 128 x 256, tcgen05.mma.cta_group::1 (M 128, N 256, K 16);
@@ -193,6 +195,12 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
 }
+// Arrive with release semantics at cluster scope: this thread's earlier
+// shared-memory writes are visible to the peer CTA once the phase completes.
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cl_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+                 : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cl_addr, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cl_addr),
                  "r"(bytes)
@@ -346,7 +354,6 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                    const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapO0,
                    const __grid_constant__ CUtensorMap mapO1, const TcParams p) {
-    static_assert(!(VAR_K && PAIR), "weight-gradient GEMMs run on single CTAs");
     using S = Shape<PAIR>;
     using ES = EpiShape<EPI, VAR_K>;
     using PP = Pipe<PAIR, VAR_K>;
@@ -371,7 +378,9 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
     // ---- set-up: barriers, TMEM, tile list ------------------------------------
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&c.full[s]), S::CTAS);
+            // even CTA: its own producer + the odd CTA (remote expect_tx, or the
+            // weight-gradient relay); odd CTA of a weight-gradient pair: its producer
+            mbar_init(smem_u32(&c.full[s]), leader ? S::CTAS : 1);
             mbar_init(smem_u32(&c.empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -460,20 +469,20 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                             for (int i = 0; i < S::BN_CTA / 64; ++i)
                                 if (nB + 64 * i < p.N) bytes += SLAB_BYTES;
                     } else {
-                        const int mA = ti.mt * S::TILE_M + rank * BM;
-                        for (int i = 0; i < BM / 64; ++i)
-                            if (mA + 64 * i < p.M) bytes += SLAB_BYTES;
-                        for (int i = 0; i < S::BN_CTA / 64; ++i)
-                            if (nB + 64 * i < p.N) bytes += SLAB_BYTES;
+                        // whole boxes (slabs past the M / N edge are zero-filled)
+                        bytes = S::A_BYTES + S::B_BYTES;
                     }
-                    if (PAIR && !leader) mbar_arrive_expect_tx_cluster(fbc, bytes);
+                    // a weight-gradient pair's odd CTA loads a segment's last K block
+                    // onto its own barrier, for its relay warp to zero the tail first
+                    const bool relay = PAIR && VAR_K && !leader && ti.rows - kb * BK < BK;
+                    if (PAIR && !leader && !relay) mbar_arrive_expect_tx_cluster(fbc, bytes);
                     else mbar_arrive_expect_tx(fb, bytes);
                     auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
-                        if (PAIR) tma2_load_2d(dst, m, fbc, c0, c1);
+                        if (PAIR && !relay) tma2_load_2d(dst, m, fbc, c0, c1);
                         else tma_load_2d(dst, m, fb, c0, c1);
                     };
                     auto load3 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2) {
-                        if (PAIR) tma2_load_3d(dst, m, fbc, c0, c1, c2);
+                        if (PAIR && !relay) tma2_load_3d(dst, m, fbc, c0, c1, c2);
                         else tma_load_3d(dst, m, fb, c0, c1, c2);
                     };
                     if (!VAR_K) {
@@ -486,14 +495,12 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                                     load3(sB + i * SLAB_BYTES, &mapB, nB + 64 * i, kb * BK, ti.e);
                         }
                     } else {
+                        // one box per operand: this CTA's 64-column slabs of BK rows
+                        // (maps: {column in slab, row, slab})
                         const int r = ti.row0 + kb * BK;
                         const int mA = ti.mt * S::TILE_M + rank * BM;
-                        for (int i = 0; i < BM / 64; ++i)
-                            if (mA + 64 * i < p.M)
-                                load2(sA + i * SLAB_BYTES, &mapA, mA + 64 * i, r);
-                        for (int i = 0; i < S::BN_CTA / 64; ++i)
-                            if (nB + 64 * i < p.N)
-                                load2(sB + i * SLAB_BYTES, &mapB, nB + 64 * i, r);
+                        load3(sA, &mapA, 0, r, mA / 64);
+                        load3(sB, &mapB, 0, r, nB / 64);
                     }
                     issued_parity[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -508,6 +515,49 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             }
         }
     } else if (warp == 1) {
+        // zero this CTA's K rows past the segment (valid of BK) in every MN slab
+        // of the stage (whole 128-byte rows: the swizzle only permutes chunks
+        // inside a row); the writes are made visible to the tensor core's reads
+        auto zero_tail = [&](int stage, int valid) {
+            if (valid >= BK) return;
+            uint8_t* gA = base + (size_t)stage * S::STAGE_BYTES;
+            const int nz = (BK - valid) * 8;  // 16-byte chunks per slab
+            for (int sl = 0; sl < S::STAGE_BYTES / SLAB_BYTES; ++sl) {
+                uint8_t* slab = gA + sl * SLAB_BYTES;
+                for (int i = lane; i < nz; i += 32)
+                    *reinterpret_cast<uint4*>(slab + (valid + (i >> 3)) * 128 + ((i & 7) << 4)) =
+                        make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+        };
+        if (PAIR && VAR_K && !leader) {
+            // ---- odd CTA of a weight-gradient pair: tail relay ---------------------
+            // Its own stage barriers only complete for segments' last K blocks, so
+            // their phases are tracked per stage.
+            int stage = 0, ecur = 0;
+            uint32_t local_phase = 0;   // bit s: parity of stage s's next own phase
+            bool ok = true;
+            for (int t = unit0; t < num_units && ok; t += nunits) {
+                const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
+                for (int kb = 0; kb < ti.num_kb; ++kb) {
+                    const int valid = ti.rows - kb * BK;
+                    if (valid < BK) {
+                        if (!mbar_wait_warp(smem_u32(&c.full[stage]), (local_phase >> stage) & 1u,
+                                            p.limit_ns, &c.abort_flag)) {
+                            raise_abort(c, p);
+                            ok = false;
+                            break;
+                        }
+                        local_phase ^= 1u << stage;
+                        zero_tail(stage, valid);
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive_cluster_release(mapa_rank(smem_u32(&c.full[stage]), 0));
+                    }
+                    if (++stage == STAGES) stage = 0;
+                }
+            }
+        }
         // ---- MMA issuer (the even CTA of a pair issues for both) ---------------------
         if (leader) {
             constexpr uint32_t IDESC = idesc_bf16_f32(S::TILE_M, BN, A_MN, B_MN);
@@ -544,19 +594,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     }
                     tc_fence_after();
                     if (VAR_K) {
-                        const int valid = ti.rows - kb * BK;
-                        if (valid < BK) {
-                            // zero K rows past the segment in every MN slab of the stage
-                            uint8_t* gA = base + (size_t)stage * S::STAGE_BYTES;
-                            const int nz = (BK - valid) * 8;  // 16-byte chunks per slab
-                            for (int sl = 0; sl < S::STAGE_BYTES / SLAB_BYTES; ++sl) {
-                                uint8_t* slab = gA + sl * SLAB_BYTES;
-                                for (int i = lane; i < nz; i += 32)
-                                    *reinterpret_cast<uint4*>(slab + (valid + (i >> 3)) * 128 +
-                                                              ((i & 7) << 4)) = make_uint4(0, 0, 0, 0);
-                            }
-                            fence_proxy_async_smem();
-                        }
+                        zero_tail(stage, ti.rows - kb * BK);
                         __syncwarp();
                     }
                     if (lane == 0) {
@@ -1096,18 +1134,22 @@ size_t gemm_colsum_workspace(int64_t P, int E, int N) {
 
 cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t st) {
     if (g.E > MAX_E || g.M % 64 || g.N % 64) return cudaErrorInvalidValue;
+    // Activations [P, M] and [P, N] seen as {column in 64-wide slab, row, slab}
+    // (the slab stride, 128 bytes, is below the row stride): one TMA box fills a
+    // CTA's MN-major slabs of BK rows, slab after slab.
+    const bool pair = use_pairs();
     CUtensorMap ma, mb;
     {
-        const uint64_t dims[2] = {(uint64_t)g.M, (uint64_t)g.P};
-        const uint64_t strides[1] = {(uint64_t)g.M * 2};
-        const uint32_t box[2] = {64, BK};
-        if (!make_map(&ma, g.act_a, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        const uint64_t dims[3] = {64, (uint64_t)g.P, (uint64_t)g.M / 64};
+        const uint64_t strides[2] = {(uint64_t)g.M * 2, 128};
+        const uint32_t box[3] = {64, BK, BM / 64};
+        if (!make_map(&ma, g.act_a, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
-        const uint64_t dims[2] = {(uint64_t)g.N, (uint64_t)g.P};
-        const uint64_t strides[1] = {(uint64_t)g.N * 2};
-        const uint32_t box[2] = {64, BK};
-        if (!make_map(&mb, g.act_b, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        const uint64_t dims[3] = {64, (uint64_t)g.P, (uint64_t)g.N / 64};
+        const uint64_t strides[2] = {(uint64_t)g.N * 2, 128};
+        const uint32_t box[3] = {64, BK, (uint32_t)(pair ? BN / 2 : BN) / 64};
+        if (!make_map(&mb, g.act_b, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     TcParams p{};
     p.E = g.E; p.M = g.M; p.N = g.N; p.K = 0; p.P = g.P;
@@ -1115,9 +1157,10 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
     p.status = status; p.limit_ns = wait_limit_ns();
     const int64_t NT = (g.N + BN - 1) / BN;
     const int64_t u1 = (int64_t)g.E * ((g.M + BM - 1) / BM) * NT;
+    const int64_t u2 = (int64_t)g.E * ((g.M + 2 * BM - 1) / (2 * BM)) * NT;
     CUtensorMap unused;   // no bf16 output: the fp32 epilogue stores directly
     memset(&unused, 0, sizeof(unused));
-    return launch_tc<true, true, true, (int)Epi::Plain, false>(ma, mb, unused, unused, p, u1, st);
+    return launch_either<true, true, true, (int)Epi::Plain>(ma, mb, unused, unused, p, u1, u2, st);
 }
 
 }  // namespace moe
