@@ -224,6 +224,14 @@ __device__ __forceinline__ void tma2_load_3d(uint32_t dst, const CUtensorMap* ma
         "l"(map), "r"(cl_bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+__device__ __forceinline__ void tma2_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t cl_bar,
+                                             int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(map), "r"(cl_bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                  "r"(ncols)
@@ -464,10 +472,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     uint32_t bytes = 0;
                     if (!VAR_K) {
                         bytes += S::A_BYTES;
-                        if (!B_MN) bytes += S::B_BYTES;
-                        else
-                            for (int i = 0; i < S::BN_CTA / 64; ++i)
-                                if (nB + 64 * i < p.N) bytes += SLAB_BYTES;
+                        bytes += S::B_BYTES;   // whole box (columns past N zero-filled)
                     } else {
                         // whole boxes (slabs past the M / N edge are zero-filled)
                         bytes = S::A_BYTES + S::B_BYTES;
@@ -490,9 +495,10 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         if (!B_MN) {
                             load3(sB, &mapB, kb * BK, nB, ti.e);
                         } else {
-                            for (int i = 0; i < S::BN_CTA / 64; ++i)
-                                if (nB + 64 * i < p.N)
-                                    load3(sB + i * SLAB_BYTES, &mapB, nB + 64 * i, kb * BK, ti.e);
+                            // this CTA's 64-column slabs of BK rows in one box
+                            // (map: {column in slab, K row, slab, expert})
+                            if (PAIR && !relay) tma2_load_4d(sB, &mapB, fbc, 0, kb * BK, nB / 64, ti.e);
+                            else tma_load_4d(sB, &mapB, fb, 0, kb * BK, nB / 64, ti.e);
                         }
                     } else {
                         // one box per operand: this CTA's 64-column slabs of BK rows
@@ -916,8 +922,9 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t gd[3], gs[2];
-    cuuint32_t bx[3], es[3] = {1, 1, 1};
+    if (rank < 1 || rank > 5) return false;
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], es[5] = {1, 1, 1, 1, 1};
     for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; }
     for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr),
@@ -1067,10 +1074,12 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
         const uint32_t box[3] = {BK, bn_cta, 1};
         if (!make_map(&mb, g.weight, 3, dims, strides, box)) return cudaErrorInvalidValue;
     } else {
-        const uint64_t dims[3] = {(uint64_t)g.N, (uint64_t)g.K, (uint64_t)g.E};
-        const uint64_t strides[2] = {(uint64_t)g.N * 2, (uint64_t)g.K * g.N * 2};
-        const uint32_t box[3] = {64, BK, 1};
-        if (!make_map(&mb, g.weight, 3, dims, strides, box)) return cudaErrorInvalidValue;
+        // [E, K, N] seen as {column in 64-wide slab, K row, slab, expert}: one box
+        // fills a CTA's MN-major slabs of BK rows, slab after slab
+        const uint64_t dims[4] = {64, (uint64_t)g.K, (uint64_t)g.N / 64, (uint64_t)g.E};
+        const uint64_t strides[3] = {(uint64_t)g.N * 2, 128, (uint64_t)g.K * g.N * 2};
+        const uint32_t box[4] = {64, BK, bn_cta / 64, 1};
+        if (!make_map(&mb, g.weight, 4, dims, strides, box)) return cudaErrorInvalidValue;
     }
     TcParams p{};
     p.E = g.E; p.N = g.N; p.K = g.K; p.M = 0; p.P = g.P;
