@@ -40,13 +40,39 @@ DEFAULT_CONFIG = "moe_s_bf16"
 L2_FLUSH_BYTES = 256 << 20
 
 def launches_per_chunk(cfg) -> int:
-    """Library kernels one dispatch chunk of a step launches: route (logits +
-    gate fused for E <= 32, else separate) + scan + rank; permute; two expert
-    GEMMs; combine; combine backward; four expert GEMMs + two column sums of
-    two kernels each; router backward (dx with the permute backward fused in,
-    dWg partials, dWg reduction)."""
-    route = 3 if cfg.E <= 32 else 4
-    return route + 1 + 2 + 1 + 1 + 8 + 3
+    """Library kernels one dispatch chunk of a step launches.
+    Route: bf16 with d_model % 64 == 0 runs the logits GEMM, the gate, the
+    scan and the rank (4); otherwise logits + gate fused for E <= 32 (3) or
+    separate (4).  Permute (1); two expert GEMMs (2); combine (1); combine
+    backward (1).  Expert backward: bf16 has the dH GEMM + its db1 reduction,
+    the dX GEMM, two weight-gradient GEMMs and the db2 row sum (2 kernels) = 7;
+    fp32 has four GEMMs and two column sums of two kernels each = 8.  Router
+    backward: dx with the permute backward fused in, and dWg (2 kernels) = 3."""
+    bf16_tc = cfg.dtype == "bf16" and cfg.d % 64 == 0
+    route = 4 if (bf16_tc or cfg.E > 32) else 3
+    ffn_bwd = 7 if cfg.dtype == "bf16" else 8
+    return route + 1 + 2 + 1 + 1 + ffn_bwd + 3
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the six expert
+# GEMM launches of one step, from one ncu capture (profiles/gemm_tc_moe_s_bf16.md),
+# valid only for the grouped-GEMM source it was taken on (first 16 hex digits of
+# its SHA-256); any other source or workload reports null.
+GEMM_TRAFFIC = {"moe_s_bf16": (1091.0e6, "228599e7f785be19")}
+
+
+def gemm_traffic(cfg):
+    entry = GEMM_TRAFFIC.get(cfg.name)
+    if entry is None:
+        return None
+    import hashlib
+    src = os.path.join(ROOT, "mixture_experts_layer_11_gb300", "csrc", "gemm_tc.cu")
+    try:
+        with open(src, "rb") as fh:
+            digest = hashlib.sha256(fh.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return entry[0] if digest == entry[1] else None
 
 
 def workload_desc(cfg) -> str:
@@ -343,7 +369,8 @@ def run_ours(args, cfg):
             "bound": "tensor", "kernel": "grouped expert GEMM (tcgen05), all expert FFN calls",
             "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "peak_kind": f"bf16 dense cuBLAS, sustained ({pk_kind})",
-            "traffic": None,
+            "traffic": gemm_traffic(cfg),
+            "traffic_unit": "bytes per step (the six expert GEMM launches)",
             "algorithmic_flops_per_step": cfg.expert_flops(),
             "ffn_ms_per_step": {k: v / args.steps for k, v in ffn_ms.items()},
         },
