@@ -47,11 +47,14 @@ def launches_per_chunk(cfg) -> int:
     backward (1).  Expert backward: bf16 has the dH GEMM + its db1 reduction,
     the dX GEMM, two weight-gradient GEMMs and the db2 row sum (2 kernels) = 7;
     fp32 has four GEMMs and two column sums of two kernels each = 8.  Router
-    backward: dx with the permute backward fused in, and dWg (2 kernels) = 3."""
+    backward: with renorm, dx with the permute backward fused in and dWg (2
+    kernels) = 3; without (dense gate Jacobian), dL, the tiled dx product
+    with the permute backward, and dWg (2 kernels) = 4."""
     bf16_tc = cfg.dtype == "bf16" and cfg.d % 64 == 0
     route = 4 if (bf16_tc or cfg.E > 32) else 3
     ffn_bwd = 7 if cfg.dtype == "bf16" else 8
-    return route + 1 + 2 + 1 + 1 + ffn_bwd + 3
+    route_bwd = 3 if cfg.renorm else 4
+    return route + 1 + 2 + 1 + 1 + ffn_bwd + route_bwd
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the six expert

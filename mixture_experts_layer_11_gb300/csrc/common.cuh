@@ -53,30 +53,39 @@ __device__ __forceinline__ float gelu_grad_f(float x) {
 
 // Fast GELU for bf16 outputs.  erf from the rational approximation of
 // Abramowitz & Stegun, "Handbook of Mathematical Functions" (1964), formula
-// 7.1.26: erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2),
-// t = 1 / (1 + p z), z >= 0, |error| <= 1.5e-7.  With z = |x|/sqrt(2) the
-// factor exp(-z^2) = exp(-x^2/2) is also sqrt(2 pi) phi(x), so one exponential
-// serves Phi(x) and phi(x).  Used only where the result is rounded to bf16
-// (relative spacing 2^-8), far above the approximation error.
-struct PhiFast {
-    float Phi;   // standard normal CDF at x
-    float g;     // exp(-x^2 / 2)
+// 7.1.26: erfc(z) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2),
+// t = 1 / (1 + p z), z >= 0, |error| <= 1.5e-7.  With z = |x|/sqrt(2),
+// exp(-z^2) = sqrt(2 pi) phi(x), so
+//   Phi(-|x|) = erfc(z) / 2 = t (a1' + a2' t + ... + a5' t^4) phi(x),
+//   a_i' = a_i sqrt(2 pi) / 2,
+// and one exponential, phi(x) = 2^(-x^2 log2(e) / 2 - log2(sqrt(2 pi))), gives
+// GELU(x) = x Phi(x) and GELU'(x) = Phi(x) + x phi(x).  Used only where the
+// result is rounded to bf16 (relative spacing 2^-8), far above the
+// approximation error.
+struct GeluParts {
+    float Phi;    // standard normal CDF at x
+    float xphi;   // x times the standard normal density at x
 };
-__device__ __forceinline__ PhiFast phi_fast(float x) {
+__device__ __forceinline__ float ex2_approx(float v) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ GeluParts gelu_parts_fast(float x) {
     const float z = fabsf(x) * 0.70710678118654752f;
     const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
-    const float g = __expf(-0.5f * x * x);
-    const float poly =
-        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f),
-                         -0.284496736f),
-                 0.254829592f);
-    const float q = 0.5f * poly * g;  // 0.5 * (1 - erf(z)) = Phi(-|x|)
-    return {x >= 0.f ? 1.0f - q : q, g};
+    const float phi = ex2_approx(fmaf(x * x, -0.72134752044448170f, -1.32574806473615950f));
+    const float q =
+        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.33027442958912330f, -1.82125597917760770f),
+                                 1.78147793656981300f),
+                         -0.35656378124891563f),
+                 0.31938153025994090f) * phi;   // Phi(-|x|)
+    return {x >= 0.f ? 1.0f - q : q, x * phi};
 }
-__device__ __forceinline__ float gelu_fast(float x) { return x * phi_fast(x).Phi; }
+__device__ __forceinline__ float gelu_fast(float x) { return x * gelu_parts_fast(x).Phi; }
 __device__ __forceinline__ float gelu_grad_fast(float x) {
-    const PhiFast r = phi_fast(x);
-    return fmaf(x * 0.39894228040143268f, r.g, r.Phi);
+    const GeluParts r = gelu_parts_fast(x);
+    return r.Phi + r.xphi;
 }
 
 // ---- shared-memory addresses and mbarriers ---------------------------------------

@@ -41,6 +41,7 @@
 // MOE_ERR_TIMEOUT, waits for its own copies and MMAs in flight, frees TMEM
 // and exits.
 #include <cudaTypedefs.h>
+#include <limits.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -75,6 +76,7 @@ template <bool PAIR> struct Shape {
 // weight-gradient epilogue stages one chunk per warp (16 KB).
 template <bool PAIR, bool VAR_K> struct Pipe {
     static constexpr int STAGING = VAR_K ? 16 * 1024 : 32 * 1024;
+    static constexpr int BIAS = VAR_K ? 0 : 4 * 1024;   // fp32 bias of each warp's columns
     static constexpr int STAGES = PAIR ? (VAR_K ? 6 : 5) : (VAR_K ? 4 : 3);
 };
 
@@ -129,7 +131,7 @@ template <bool PAIR, bool VAR_K>
 constexpr size_t smem_bytes() {
     using S = Shape<PAIR>;
     using PP = Pipe<PAIR, VAR_K>;
-    return 1024 + (size_t)PP::STAGES * S::STAGE_BYTES + (size_t)PP::STAGING +
+    return 1024 + (size_t)PP::STAGES * S::STAGE_BYTES + (size_t)PP::STAGING + (size_t)PP::BIAS +
            sizeof(Ctrl<PP::STAGES>);
 }
 
@@ -373,7 +375,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* staging_base = base + (size_t)STAGES * S::STAGE_BYTES;
     using CtrlT = Ctrl<STAGES>;
-    CtrlT& c = *reinterpret_cast<CtrlT*>(staging_base + (size_t)PP::STAGING);
+    float* bias_base = reinterpret_cast<float*>(staging_base + (size_t)PP::STAGING);
+    CtrlT& c = *reinterpret_cast<CtrlT*>(staging_base + (size_t)PP::STAGING + (size_t)PP::BIAS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
@@ -422,12 +425,18 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             c.nactive = acc;   // number of work units
         }
     } else {
+        // Unit order: without accumulation the experts without tokens come first
+        // (their units only write zero tiles: the MMA warp skips them and the
+        // epilogue writes them while the first real tiles are computed), then
+        // the others by descending row count (longest processing time first).
         for (int e = threadIdx.x; e < E; e += THREADS) {
             const int n = c.off[e + 1] - c.off[e];
+            const int kn = (n == 0 && !p.accumulate) ? INT_MAX : n;
             int r = 0;
             for (int q = 0; q < E; ++q) {
                 const int m = c.off[q + 1] - c.off[q];
-                r += (m > n) || (m == n && q < e);
+                const int km = (m == 0 && !p.accumulate) ? INT_MAX : m;
+                r += (km > kn) || (km == kn && q < e);
             }
             c.order[r] = e;
         }
@@ -657,10 +666,10 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             const int64_t grow_lane = (int64_t)ti.row0 + q * 32 + lane;
             const bool row_ok = (q * 32 + lane) < ti.rows;
             const int colw = ti.nt * BN + cq * ES::COLS;   // first global column of this warp
-            // Operands of the epilogue read from global memory are fetched ahead:
-            // the saved GELU'(h) of this thread's row (ScaleAux) two chunks
-            // ahead, the bias columns (the same for every lane) one chunk ahead;
-            // the first ones before the accumulator is ready.
+            // Operands of the epilogue read from global memory are fetched ahead
+            // of the accumulator: the saved GELU'(h) of this thread's row
+            // (ScaleAux) two chunks ahead; the bias of the warp's columns once
+            // per tile, as fp32 into shared memory.
             auto load_aux = [&](int ch) {
                 U4s<CW / 8> r;
                 const int col = colw + ch * CW;
@@ -672,26 +681,21 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                                  : make_uint4(0, 0, 0, 0);
                 return r;
             };
-            auto load_bias = [&](int ch) {
-                U4s<CW / 8> r;
-                const int col = colw + ch * CW;
-                #pragma unroll
-                for (int u = 0; u < CW / 8; ++u)
-                    r.u[u] = (p.bias && col < p.N)
-                                 ? __ldg(reinterpret_cast<const uint4*>(
-                                       (const __nv_bfloat16*)p.bias + (int64_t)ti.e * p.N + col +
-                                       u * 8))
-                                 : make_uint4(0, 0, 0, 0);
-                return r;
-            };
             constexpr bool kAux = EPI == (int)Epi::ScaleAux && !VAR_K;
             constexpr bool kBias = (EPI == (int)Epi::BiasGelu || EPI == (int)Epi::Bias) && !VAR_K;
-            U4s<CW / 8> h0, h1, bnext;
+            U4s<CW / 8> h0, h1;
             if (kAux) {
                 h0 = load_aux(0);
                 if (ES::NCH > 1) h1 = load_aux(1);
             }
-            if (kBias) bnext = load_bias(0);
+            float* bias_s = bias_base + ew * ES::COLS;
+            if (kBias && p.bias) {
+                const __nv_bfloat16* bp = (const __nv_bfloat16*)p.bias + (int64_t)ti.e * p.N;
+                #pragma unroll
+                for (int i = lane; i < ES::COLS; i += 32)
+                    bias_s[i] = colw + i < p.N ? __bfloat162float(bp[colw + i]) : 0.f;
+                __syncwarp();
+            }
             if (mma_tile) {
                 if (!mbar_wait_warp(smem_u32(&c.tfull[acc]), acc_phase, p.limit_ns,
                                     &c.abort_flag)) {
@@ -751,21 +755,13 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                             out[(grow0 + r) * p.N + col0 + lane] = sf[r * 32 + (lane ^ r)];
                     __syncwarp();
                 } else if (!VAR_K) {
-                    if (kBias) {
-                        const U4s<CW / 8> bcur = bnext;
-                        if (ch + 1 < ES::NCH) bnext = load_bias(ch + 1);
-                        if (p.bias) {
-                            #pragma unroll
-                            for (int u = 0; u < CW; u += 8) {
-                                const __nv_bfloat162* h =
-                                    reinterpret_cast<const __nv_bfloat162*>(&bcur.u[u / 8]);
-                                #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const float2 f = __bfloat1622float2(h[i]);
-                                    v[u + 2 * i] += f.x;
-                                    v[u + 2 * i + 1] += f.y;
-                                }
-                            }
+                    if (kBias && p.bias) {
+                        const float4* b4 = reinterpret_cast<const float4*>(bias_s + ch * CW);
+                        #pragma unroll
+                        for (int u = 0; u < CW / 4; ++u) {
+                            const float4 b = b4[u];
+                            v[4 * u] += b.x; v[4 * u + 1] += b.y;
+                            v[4 * u + 2] += b.z; v[4 * u + 3] += b.w;
                         }
                     }
                     if (kAux) {
@@ -799,8 +795,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         float gd[CW];
                         #pragma unroll
                         for (int i = 0; i < CW; ++i) {
-                            const PhiFast r = phi_fast(v[i]);
-                            gd[i] = fmaf(v[i] * 0.39894228040143268f, r.g, r.Phi);
+                            const GeluParts r = gelu_parts_fast(v[i]);
+                            gd[i] = r.Phi + r.xphi;
                             v[i] *= r.Phi;
                         }
                         uint4 pg[CW / 8], pa[CW / 8];

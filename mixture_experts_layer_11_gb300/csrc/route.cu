@@ -535,7 +535,7 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
     const float* __restrict__ w, const TIn* __restrict__ Wg,
     const TIn* __restrict__ dx_perm, const int32_t* __restrict__ pos, TIn* __restrict__ dx,
-    float* __restrict__ dL) {
+    float* __restrict__ dL, int dl_only) {
     __shared__ float g_s[8][256];
     __shared__ int e_s[8][256];
     using V = Vec<TIn>;
@@ -628,6 +628,7 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
         }
         ng = E;
     }
+    if (dl_only) return;   // dx by the tiled dense kernel
     __syncwarp();
     for (int c0 = lane * VN; c0 < d; c0 += 32 * VN * U) {
         float acc[U][VN], wv[VN];
@@ -669,54 +670,178 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     }
 }
 
-// Dense (softmax Jacobian) partial sums: partial[tc][e][c] over kDwgChunk
-// consecutive tokens, 8 experts per block.
+// ---- A10, dense gate Jacobian (renorm off): two tiled products ------------------
+// With renorm off every expert's logit gets a gradient, so dx's router term
+// is the product dL [T, E] x Wg [E, d] and dWg = dL^T x: fp32 CUDA-core
+// products tiled through shared memory (64 x 128 outputs per block, 8 x 4 per
+// thread), with the reduction dimension in order.
+
+template <typename T> struct Four;   // four consecutive elements
+template <> struct Four<__nv_bfloat16> {
+    static __device__ __forceinline__ float4 load(const __nv_bfloat16* p) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, float4 v) {
+        uint2 u;
+        *reinterpret_cast<__nv_bfloat162*>(&u.x) = __floats2bfloat162_rn(v.x, v.y);
+        *reinterpret_cast<__nv_bfloat162*>(&u.y) = __floats2bfloat162_rn(v.z, v.w);
+        *reinterpret_cast<uint2*>(p) = u;
+    }
+};
+template <> struct Four<float> {
+    static __device__ __forceinline__ float4 load(const float* p) {
+        return *reinterpret_cast<const float4*>(p);
+    }
+    static __device__ __forceinline__ void store(float* p, float4 v) {
+        *reinterpret_cast<float4*>(p) = v;
+    }
+};
+
+// dx[t, :] = sum_j dx_perm[pos[t, j], :] (or dx[t, :] as given when dx_perm is
+// null) + sum_e dL[t, e] Wg[e, :]; experts in steps of 32.
 template <typename TIn>
-__global__ void __launch_bounds__(256) dwg_partial_dense_kernel(
-    int64_t T, int d, int E, const float* __restrict__ dL, const TIn* __restrict__ x,
-    float* __restrict__ partial) {
-    using V = Vec<TIn>;
-    constexpr int VN = V::N;
-    const int tc = blockIdx.x;
-    const int e0 = blockIdx.z * 8;
-    const int c = (blockIdx.y * 256 + threadIdx.x) * VN;
-    if (c >= d) return;
-    const int64_t t0 = (int64_t)tc * kDwgChunk;
-    const int64_t t1 = min(T, t0 + kDwgChunk);
-    float a[8][VN], xv[VN];
+__global__ void __launch_bounds__(256) route_bwd_dx_dense_kernel(
+    int64_t T, int d, int E, int k, const float* __restrict__ dL, const TIn* __restrict__ Wg,
+    const TIn* __restrict__ dx_perm, const int32_t* __restrict__ pos, TIn* __restrict__ dx) {
+    __shared__ float dl_s[64][33];
+    __shared__ __align__(16) float wg_s[32][128];
+    const int tid = threadIdx.x, lane = tid & 31, ty = tid >> 5;
+    const int64_t t0 = (int64_t)blockIdx.x * 64;
+    const int c0 = blockIdx.y * 128;
+    float acc[8][4];
     #pragma unroll
     for (int i = 0; i < 8; ++i)
         #pragma unroll
-        for (int u = 0; u < VN; ++u) a[i][u] = 0.f;
-    for (int64_t t = t0; t < t1; ++t) {
-        V::load(x + t * d + c, xv);
-        #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float g = (e0 + i < E) ? dL[t * E + e0 + i] : 0.f;
-            #pragma unroll
-            for (int u = 0; u < VN; ++u) a[i][u] = fmaf(g, xv[u], a[i][u]);
+        for (int u = 0; u < 4; ++u) acc[i][u] = 0.f;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+        for (int i = tid; i < 64 * 32; i += 256) {
+            const int r = i >> 5, q = i & 31;
+            const int64_t t = t0 + r;
+            dl_s[r][q] = (t < T && e0 + q < E) ? dL[t * E + e0 + q] : 0.f;
         }
+        for (int i = tid; i < 32 * 32; i += 256) {
+            const int q = i >> 5, cc = (i & 31) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e0 + q < E && c0 + cc < d) v = Four<TIn>::load(Wg + (int64_t)(e0 + q) * d + c0 + cc);
+            *reinterpret_cast<float4*>(&wg_s[q][cc]) = v;
+        }
+        __syncthreads();
+        #pragma unroll 8
+        for (int q = 0; q < 32; ++q) {
+            const float4 b = *reinterpret_cast<const float4*>(&wg_s[q][lane * 4]);
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float a = dl_s[ty * 8 + i][q];
+                acc[i][0] = fmaf(a, b.x, acc[i][0]);
+                acc[i][1] = fmaf(a, b.y, acc[i][1]);
+                acc[i][2] = fmaf(a, b.z, acc[i][2]);
+                acc[i][3] = fmaf(a, b.w, acc[i][3]);
+            }
+        }
+        __syncthreads();
     }
+    const int c = c0 + lane * 4;
+    if (c >= d) return;
     #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        if (e0 + i >= E) break;
-        float* out = partial + ((int64_t)tc * E + e0 + i) * d + c;
-        #pragma unroll
-        for (int u = 0; u < VN; ++u) out[u] = a[i][u];
+        const int64_t t = t0 + ty * 8 + i;
+        if (t >= T) break;
+        float4 base = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (dx_perm) {
+            for (int j = 0; j < k; ++j) {
+                const float4 v = Four<TIn>::load(dx_perm + (int64_t)pos[t * k + j] * d + c);
+                base.x += v.x; base.y += v.y; base.z += v.z; base.w += v.w;
+            }
+        } else {
+            base = Four<TIn>::load(dx + t * d + c);
+        }
+        base.x += acc[i][0]; base.y += acc[i][1]; base.z += acc[i][2]; base.w += acc[i][3];
+        Four<TIn>::store(dx + t * d + c, base);
     }
 }
 
-__global__ void __launch_bounds__(256) dwg_reduce_dense_kernel(int d, int E, int ntc,
-                                                              const float* __restrict__ partial,
-                                                              float* __restrict__ dWg,
-                                                              int accumulate) {
-    const int e = blockIdx.x;
-    const int c = blockIdx.y * 256 + threadIdx.x;
+constexpr int kDwgDenseTokens = 256;   // tokens per dWg partial
+
+// partial[tc][e][c] = sum over the tokens t of chunk tc of dL[t, e] x[t, c];
+// block tile 64 experts x 128 columns, tokens in steps of 32.
+template <typename TIn>
+__global__ void __launch_bounds__(256) dwg_dense_partial_kernel(
+    int64_t T, int d, int E, const float* __restrict__ dL, const TIn* __restrict__ x,
+    float* __restrict__ partial) {
+    __shared__ float dl_s[32][65];
+    __shared__ __align__(16) float x_s[32][128];
+    const int tid = threadIdx.x, lane = tid & 31, ty = tid >> 5;
+    const int64_t tbase = (int64_t)blockIdx.x * kDwgDenseTokens;
+    const int c0 = blockIdx.y * 128, e0 = blockIdx.z * 64;
+    float acc[8][4];
+    #pragma unroll
+    for (int i = 0; i < 8; ++i)
+        #pragma unroll
+        for (int u = 0; u < 4; ++u) acc[i][u] = 0.f;
+    for (int ts = 0; ts < kDwgDenseTokens; ts += 32) {
+        for (int i = tid; i < 32 * 64; i += 256) {
+            const int r = i >> 6, q = i & 63;
+            const int64_t t = tbase + ts + r;
+            dl_s[r][q] = (t < T && e0 + q < E) ? dL[t * E + e0 + q] : 0.f;
+        }
+        for (int i = tid; i < 32 * 32; i += 256) {
+            const int r = i >> 5, cc = (i & 31) * 4;
+            const int64_t t = tbase + ts + r;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < T && c0 + cc < d) v = Four<TIn>::load(x + t * d + c0 + cc);
+            *reinterpret_cast<float4*>(&x_s[r][cc]) = v;
+        }
+        __syncthreads();
+        #pragma unroll 8
+        for (int r = 0; r < 32; ++r) {
+            const float4 b = *reinterpret_cast<const float4*>(&x_s[r][lane * 4]);
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float a = dl_s[r][ty * 8 + i];
+                acc[i][0] = fmaf(a, b.x, acc[i][0]);
+                acc[i][1] = fmaf(a, b.y, acc[i][1]);
+                acc[i][2] = fmaf(a, b.z, acc[i][2]);
+                acc[i][3] = fmaf(a, b.w, acc[i][3]);
+            }
+        }
+        __syncthreads();
+    }
+    const int c = c0 + lane * 4;
     if (c >= d) return;
-    float s = 0.f;
-    for (int i = 0; i < ntc; ++i) s += partial[((int64_t)i * E + e) * d + c];
-    float* o = dWg + (int64_t)e * d + c;
-    *o = accumulate ? *o + s : s;
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = e0 + ty * 8 + i;
+        if (e >= E) break;
+        *reinterpret_cast<float4*>(partial + ((int64_t)blockIdx.x * E + e) * d + c) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    }
+}
+
+// dWg[e][c] (+)= sum over chunks of partial[tc][e][c]: a block takes one expert
+// and 32 columns, its 8 warps every 8th chunk, added in warp order.
+__global__ void __launch_bounds__(256) dwg_dense_reduce_kernel(int d, int E, int ntc,
+                                                               const float* __restrict__ partial,
+                                                               float* __restrict__ dWg,
+                                                               int accumulate) {
+    __shared__ float red[8][32];
+    const int e = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.y * 32 + lane;
+    float sum = 0.f;
+    if (c < d)
+        for (int i = warp; i < ntc; i += 8) sum += partial[((int64_t)i * E + e) * d + c];
+    red[warp][lane] = sum;
+    __syncthreads();
+    if (warp == 0 && c < d) {
+        float s = 0.f;
+        #pragma unroll
+        for (int w = 0; w < 8; ++w) s += red[w][lane];
+        float* o = dWg + (int64_t)e * d + c;
+        *o = accumulate ? *o + s : s;
+    }
 }
 
 template <typename TIn>
@@ -729,10 +854,14 @@ cudaError_t route_bwd_typed(const moe_shape& s, const float* dw, const float* lo
     const int d = s.d, E = s.E, k = s.k;
     const unsigned gx = (unsigned)((T + 7) / 8);
     // KMAX: compile-time bound on k for the fused permute backward (1 when not fused)
-    const int kb = dx_perm == nullptr ? 1 : (k <= 1 ? 1 : k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 16);
+    const int kb = (dx_perm == nullptr || !s.renorm)
+                       ? 1 : (k <= 1 ? 1 : k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 16);
+    // renorm off: dL is dense; dx's router term and dWg are tiled products
+    const bool dense = !s.renorm;
 #define MOE_RBWD(EPLV, KMV)                                                                    \
     route_bwd_dx_kernel<TIn, EPLV, KMV><<<gx, 256, 0, st>>>(T, d, E, k, s.renorm, dw, logits, \
-                                                           idx, w, Wg, dx_perm, pos, dx, dL)
+                                                           idx, w, Wg, dense ? nullptr : dx_perm, \
+                                                           pos, dx, dL, (int)dense)
 #define MOE_RBWD_K(EPLV)                                                                       \
     switch (kb) {                                                                              \
         case 1: MOE_RBWD(EPLV, 1); break;                                                      \
@@ -749,19 +878,18 @@ cudaError_t route_bwd_typed(const moe_shape& s, const float* dw, const float* lo
 #undef MOE_RBWD
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    constexpr int VN = Vec<TIn>::N;
-    const unsigned gy = (unsigned)((d + 256 * VN - 1) / (256 * VN));
-    const unsigned gy_red = (unsigned)((d + 255) / 256);
     if (s.renorm) {
         // dWg[e] = sum over e's selected slots of dL(slot) x[token(slot)]
         return launch_segment_rowsum(s, x, d, offsets, perm, dL, dWg, accumulate, partial, st);
-    } else {
-        const int ntc = (int)((T + kDwgChunk - 1) / kDwgChunk);
-        dwg_partial_dense_kernel<TIn><<<dim3(ntc, gy, (E + 7) / 8), 256, 0, st>>>(T, d, E, dL, x,
-                                                                                  partial);
-        dwg_reduce_dense_kernel<<<dim3(E, gy_red), 256, 0, st>>>(d, E, ntc, partial, dWg,
-                                                                accumulate);
     }
+    const unsigned gc = (unsigned)((d + 127) / 128);
+    route_bwd_dx_dense_kernel<TIn><<<dim3((unsigned)((T + 63) / 64), gc), 256, 0, st>>>(
+        T, d, E, k, dL, Wg, dx_perm, pos, dx);
+    const int ntc = (int)((T + kDwgDenseTokens - 1) / kDwgDenseTokens);
+    dwg_dense_partial_kernel<TIn><<<dim3((unsigned)ntc, gc, (unsigned)((E + 63) / 64)), 256, 0,
+                                    st>>>(T, d, E, dL, x, partial);
+    dwg_dense_reduce_kernel<<<dim3((unsigned)E, (unsigned)((d + 31) / 32)), 256, 0, st>>>(
+        d, E, ntc, partial, dWg, accumulate);
     return cudaGetLastError();
 }
 

@@ -28,6 +28,7 @@ CASES = [  # dtype, T, d, f, E, k, zipf
     ("bf16", 700, 192, 320, 16, 1, 1.2),     # empty experts, partial N tiles
     ("bf16", 2048, 768, 1024, 4, 2, None),
     ("bf16", 600, 128, 64, 64, 4, 1.1),
+    ("bf16", 4096, 128, 256, 8, 1, 2.0),     # one expert takes most rows: split K ranges
     ("f32", 256, 64, 128, 4, 1, None),
     ("f32", 333, 96, 40, 6, 2, 1.2),
 ]

@@ -14,7 +14,8 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 CASES = [("f32", 256, 64, 4, 1, 0), ("bf16", 1000, 768, 8, 2, 1), ("bf16", 777, 256, 64, 1, 0),
-         ("bf16", 513, 512, 128, 8, 1), ("f32", 300, 96, 16, 4, 0)]
+         ("bf16", 513, 512, 128, 8, 1), ("f32", 300, 96, 16, 4, 0),
+         ("bf16", 333, 200, 40, 3, 0), ("f32", 129, 136, 72, 2, 0)]
 
 
 @pytest.mark.parametrize("dtype,T,d,E,k,renorm", CASES)
