@@ -660,41 +660,57 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
         }
         int acc = 0, ecur = 0, sbuf = 0;
         uint32_t acc_phase = 0;
-        for (int t = unit0; t < num_units; t += nunits) {
-            const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
-            const bool mma_tile = ti.num_kb > 0;
-            const int64_t grow_lane = (int64_t)ti.row0 + q * 32 + lane;
-            const bool row_ok = (q * 32 + lane) < ti.rows;
-            const int colw = ti.nt * BN + cq * ES::COLS;   // first global column of this warp
-            // Operands of the epilogue read from global memory are fetched ahead
-            // of the accumulator: the saved GELU'(h) of this thread's row
-            // (ScaleAux) two chunks ahead; the bias of the warp's columns once
-            // per tile, as fp32 into shared memory.
-            auto load_aux = [&](int ch) {
-                U4s<CW / 8> r;
-                const int col = colw + ch * CW;
-                #pragma unroll
-                for (int u = 0; u < CW / 8; ++u)
-                    r.u[u] = (row_ok && col < p.N)
-                                 ? __ldg(reinterpret_cast<const uint4*>(
-                                       (const __nv_bfloat16*)p.aux + grow_lane * p.N + col + u * 8))
-                                 : make_uint4(0, 0, 0, 0);
-                return r;
-            };
-            constexpr bool kAux = EPI == (int)Epi::ScaleAux && !VAR_K;
-            constexpr bool kBias = (EPI == (int)Epi::BiasGelu || EPI == (int)Epi::Bias) && !VAR_K;
-            U4s<CW / 8> h0, h1;
-            if (kAux) {
-                h0 = load_aux(0);
-                if (ES::NCH > 1) h1 = load_aux(1);
+        // Operands of the epilogue read from global memory stream ahead of the
+        // accumulators, across tile boundaries (the next tile of this CTA is
+        // known): the saved GELU'(h) of this thread's row (ScaleAux) two chunks
+        // ahead; the bias of the warp's columns one tile ahead, held in
+        // registers and written to shared memory as fp32 when its tile starts.
+        constexpr bool kAux = EPI == (int)Epi::ScaleAux && !VAR_K;
+        constexpr bool kBias = (EPI == (int)Epi::BiasGelu || EPI == (int)Epi::Bias) && !VAR_K;
+        constexpr int BW = ES::COLS / 32;   // bias values per lane
+        auto load_aux = [&](const Tile& tt, int ch) {
+            U4s<CW / 8> r;
+            const int64_t gl = (int64_t)tt.row0 + q * 32 + lane;
+            const bool ok = (q * 32 + lane) < tt.rows;
+            const int col = tt.nt * BN + cq * ES::COLS + ch * CW;
+            #pragma unroll
+            for (int u = 0; u < CW / 8; ++u)
+                r.u[u] = (ok && col < p.N)
+                             ? __ldg(reinterpret_cast<const uint4*>(
+                                   (const __nv_bfloat16*)p.aux + gl * p.N + col + u * 8))
+                             : make_uint4(0, 0, 0, 0);
+            return r;
+        };
+        auto load_bias = [&](const Tile& tt, float (&b)[BW]) {
+            const int cw = tt.nt * BN + cq * ES::COLS;
+            const __nv_bfloat16* bp = (const __nv_bfloat16*)p.bias + (int64_t)tt.e * p.N;
+            #pragma unroll
+            for (int i = 0; i < BW; ++i) {
+                const int col = cw + lane * BW + i;
+                b[i] = (p.bias && col < p.N) ? __bfloat162float(bp[col]) : 0.f;
             }
+        };
+        Tile tcur;
+        if (unit0 < num_units) tcur = get_tile<VAR_K, PAIR>(c, p, unit0, ecur, rank);
+        U4s<CW / 8> h0, h1;
+        float bnext[BW];
+        if (kAux && unit0 < num_units) {
+            h0 = load_aux(tcur, 0);
+            if (ES::NCH > 1) h1 = load_aux(tcur, 1);
+        }
+        if (kBias && unit0 < num_units) load_bias(tcur, bnext);
+        for (int t = unit0; t < num_units; t += nunits) {
+            const Tile ti = tcur;
+            const bool has_next = t + nunits < num_units;
+            if (has_next) tcur = get_tile<VAR_K, PAIR>(c, p, t + nunits, ecur, rank);
+            const bool mma_tile = ti.num_kb > 0;
+            const bool row_ok = (q * 32 + lane) < ti.rows;   // this thread's row in the segment
             float* bias_s = bias_base + ew * ES::COLS;
-            if (kBias && p.bias) {
-                const __nv_bfloat16* bp = (const __nv_bfloat16*)p.bias + (int64_t)ti.e * p.N;
+            if (kBias) {
                 #pragma unroll
-                for (int i = lane; i < ES::COLS; i += 32)
-                    bias_s[i] = colw + i < p.N ? __bfloat162float(bp[colw + i]) : 0.f;
+                for (int i = 0; i < BW; ++i) bias_s[lane * BW + i] = bnext[i];
                 __syncwarp();
+                if (has_next) load_bias(tcur, bnext);
             }
             if (mma_tile) {
                 if (!mbar_wait_warp(smem_u32(&c.tfull[acc]), acc_phase, p.limit_ns,
@@ -755,7 +771,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                             out[(grow0 + r) * p.N + col0 + lane] = sf[r * 32 + (lane ^ r)];
                     __syncwarp();
                 } else if (!VAR_K) {
-                    if (kBias && p.bias) {
+                    if (kBias) {
                         const float4* b4 = reinterpret_cast<const float4*>(bias_s + ch * CW);
                         #pragma unroll
                         for (int u = 0; u < CW / 4; ++u) {
@@ -767,7 +783,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     if (kAux) {
                         const U4s<CW / 8> hcur = h0;
                         h0 = h1;
-                        if (ch + 2 < ES::NCH) h1 = load_aux(ch + 2);
+                        if (ch + 2 < ES::NCH) h1 = load_aux(ti, ch + 2);
+                        else if (has_next) h1 = load_aux(tcur, ch + 2 - ES::NCH);
                         #pragma unroll
                         for (int cc = 0; cc < CW / 8; ++cc) {
                             const __nv_bfloat162* h =
@@ -868,6 +885,12 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         __syncwarp();
                     }
                 }
+            }
+            // a warp whose columns all lie past N processed no chunk of this tile
+            // and did not advance the GELU' stream: restart it on the next tile
+            if (kAux && has_next && ti.nt * BN + cq * ES::COLS >= p.N) {
+                h0 = load_aux(tcur, 0);
+                if (ES::NCH > 1) h1 = load_aux(tcur, 1);
             }
             if (!mma_tile) continue;
             tc_fence_before();
