@@ -334,24 +334,6 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Column sums over a warp's 32 rows (one row per lane) of 16 values: five
-// butterfly steps, each lane keeping half of the columns still open;
-// afterwards lanes 2c and 2c+1 both hold the sum of column c.
-__device__ __forceinline__ float warp_colsum16(float (&a)[16], int lane) {
-    #pragma unroll
-    for (int h = 8; h >= 1; h >>= 1) {
-        const int m = 2 * h;                 // lane bit deciding which half stays
-        const bool up = (lane & m) != 0;
-        #pragma unroll
-        for (int j = 0; j < h; ++j) {
-            const float send = up ? a[j] : a[j + h];
-            const float keep = up ? a[j + h] : a[j];
-            a[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-        }
-    }
-    return a[0] + __shfl_xor_sync(0xffffffffu, a[0], 1);
-}
-
 template <int CW>
 __device__ __forceinline__ void tmem_ld_cw(uint32_t taddr, float (&v)[CW]) {
     if constexpr (CW == 32) tmem_ld32(taddr, v);
@@ -704,7 +686,6 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             const bool has_next = t + nunits < num_units;
             if (has_next) tcur = get_tile<VAR_K, PAIR>(c, p, t + nunits, ecur, rank);
             const bool mma_tile = ti.num_kb > 0;
-            const bool row_ok = (q * 32 + lane) < ti.rows;   // this thread's row in the segment
             float* bias_s = bias_base + ew * ES::COLS;
             if (kBias) {
                 #pragma unroll
@@ -832,23 +813,32 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         sbuf ^= 1;
                         if (EPI == (int)Epi::ScaleAux && CW == 16 && p.cpart) {
                             // column sums of the stored (bf16) values of this warp's
-                            // rows inside the segment -> one partial row per
+                            // rows inside the segment, read back from the staging
+                            // box: lane (w, g) sums word w (columns 2w, 2w+1) over
+                            // rows 8g..8g+7 (rotated by g: conflict-free), then the
+                            // four row groups are added; one partial row per
                             // (m-tile, CTA, lane quarter)
-                            float a[16];
+                            const uint8_t* sb = stg + (sbuf ^ 1) * ES::CHUNK_BYTES;
+                            const int w = lane & 7, g = lane >> 3;
+                            float s0 = 0.f, s1 = 0.f;
                             #pragma unroll
-                            for (int u = 0; u < CW / 8; ++u) {
-                                const uint32_t* wd = reinterpret_cast<const uint32_t*>(&pk[u]);
-                                #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    a[8 * u + 2 * i] =
-                                        row_ok ? __uint_as_float(wd[i] << 16) : 0.f;
-                                    a[8 * u + 2 * i + 1] =
-                                        row_ok ? __uint_as_float(wd[i] & 0xffff0000u) : 0.f;
+                            for (int i = 0; i < 8; ++i) {
+                                const int r = g * 8 + ((i + g) & 7);
+                                if (r < valid) {
+                                    const uint32_t wd = *reinterpret_cast<const uint32_t*>(
+                                        sb + stg_off<16>(r, w >> 2) + (w & 3) * 4);
+                                    s0 += __uint_as_float(wd << 16);
+                                    s1 += __uint_as_float(wd & 0xffff0000u);
                                 }
                             }
-                            const float cs = warp_colsum16(a, lane);
+                            s0 += __shfl_xor_sync(0xffffffffu, s0, 8);
+                            s1 += __shfl_xor_sync(0xffffffffu, s1, 8);
+                            s0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+                            s1 += __shfl_xor_sync(0xffffffffu, s1, 16);
                             const int64_t prow = ((int64_t)(t / NT) * S::CTAS + rank) * 4 + q;
-                            if ((lane & 1) == 0) p.cpart[prow * p.N + col0 + (lane >> 1)] = cs;
+                            if (g == 0)
+                                *reinterpret_cast<float2*>(p.cpart + prow * p.N + col0 + 2 * w) =
+                                    make_float2(s0, s1);
                         }
                     }
                     if (lane == 0) bulk_commit();
