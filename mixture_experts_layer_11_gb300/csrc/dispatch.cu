@@ -228,9 +228,13 @@ __global__ void __launch_bounds__(256) seg_partial_kernel(int n, int E, int k,
     using V = V16<T>;
     constexpr int TILE = 32 * kSegCPL * V::N;      // columns of one tile
     __shared__ __align__(16) float red[8][TILE];
+    __shared__ int off_s[257];
+    // the segment bounds, loaded in one step (not a chain of dependent loads)
+    for (int i = threadIdx.x; i <= E; i += 256) off_s[i] = offsets[i];
+    __syncthreads();
     int e = 0, acc = 0, sub = -1;
     for (; e < E; ++e) {
-        const int cnt = offsets[e + 1] - offsets[e];
+        const int cnt = off_s[e + 1] - off_s[e];
         const int nc = (cnt + kDwgChunk - 1) / kDwgChunk;
         if ((int)blockIdx.x < acc + nc) { sub = blockIdx.x - acc; break; }
         acc += nc;
@@ -238,8 +242,8 @@ __global__ void __launch_bounds__(256) seg_partial_kernel(int n, int E, int k,
     if (sub < 0) return;   // block-uniform
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ct0 = blockIdx.y * TILE;
-    const int p0 = offsets[e] + sub * kDwgChunk;
-    const int p1 = min(offsets[e + 1], p0 + kDwgChunk);
+    const int p0 = off_s[e] + sub * kDwgChunk;
+    const int p1 = min(off_s[e + 1], p0 + kDwgChunk);
     float a[kSegCPL][V::N];
     #pragma unroll
     for (int i = 0; i < kSegCPL; ++i)
@@ -290,15 +294,18 @@ __global__ void __launch_bounds__(256) seg_reduce_kernel(int n, int E,
                                                          const float* __restrict__ partial,
                                                          float* __restrict__ out, int accumulate) {
     __shared__ float red[8][32];
+    __shared__ int off_s[257];
     const int e = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.y * 32 + lane;
+    for (int i = threadIdx.x; i <= e + 1; i += 256) off_s[i] = offsets[i];
+    __syncthreads();
     int start = 0;
     for (int q = 0; q < e; ++q) {
-        const int cnt = offsets[q + 1] - offsets[q];
+        const int cnt = off_s[q + 1] - off_s[q];
         start += (cnt + kDwgChunk - 1) / kDwgChunk;
     }
-    const int cnt = offsets[e + 1] - offsets[e];
+    const int cnt = off_s[e + 1] - off_s[e];
     const int nc = (cnt + kDwgChunk - 1) / kDwgChunk;
     float sum = 0.f;
     if (c < n) {

@@ -72,12 +72,16 @@ template <bool PAIR> struct Shape {
 // Operand pipeline depth and epilogue staging.  The bf16 epilogues stage two
 // 32-row chunks per warp (32 KB in all), so that the TMA store of one chunk
 // runs while the next is computed; that leaves room for 5 (pair) or 3
-// (single CTA) operand stages under the 227 KB per-CTA limit.  The fp32
-// weight-gradient epilogue stages one chunk per warp (16 KB).
-template <bool PAIR, bool VAR_K> struct Pipe {
+// (single CTA) operand stages under the 227 KB per-CTA limit.  The GELU'
+// scaling epilogue also receives its saved GELU'(h) by TMA into a two-chunk
+// ring per warp (32 KB), for one stage less.  The fp32 weight-gradient
+// epilogue stages one chunk per warp (16 KB).
+template <bool PAIR, bool VAR_K, int EPI> struct Pipe {
+    static constexpr bool AUX = !VAR_K && EPI == (int)Epi::ScaleAux;
     static constexpr int STAGING = VAR_K ? 16 * 1024 : 32 * 1024;
     static constexpr int BIAS = VAR_K ? 0 : 4 * 1024;   // fp32 bias of each warp's columns
-    static constexpr int STAGES = PAIR ? (VAR_K ? 6 : 5) : (VAR_K ? 4 : 3);
+    static constexpr int AUXBUF = AUX ? 32 * 1024 : 0;  // GELU'(h) ring, 2 x 1 KB per warp
+    static constexpr int STAGES = PAIR ? (VAR_K ? 6 : (AUX ? 4 : 5)) : (VAR_K ? 4 : 3);
 };
 
 // Epilogue shape.  The epilogue warps drain a 128 x 256 accumulator, each
@@ -119,6 +123,7 @@ template <int STAGES> struct Ctrl {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t gbar[16][2];        // ScaleAux: GELU'(h) ring, per epilogue warp
     uint32_t tmem_base;
     int abort_flag;
     int nactive;
@@ -127,12 +132,12 @@ template <int STAGES> struct Ctrl {
     int order[MAX_E];            // VarK: experts by descending row count
 };
 
-template <bool PAIR, bool VAR_K>
+template <bool PAIR, bool VAR_K, int EPI>
 constexpr size_t smem_bytes() {
     using S = Shape<PAIR>;
-    using PP = Pipe<PAIR, VAR_K>;
+    using PP = Pipe<PAIR, VAR_K, EPI>;
     return 1024 + (size_t)PP::STAGES * S::STAGE_BYTES + (size_t)PP::STAGING + (size_t)PP::BIAS +
-           sizeof(Ctrl<PP::STAGES>);
+           (size_t)PP::AUXBUF + sizeof(Ctrl<PP::STAGES>);
 }
 
 struct Tile {
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                    const __grid_constant__ CUtensorMap mapO1, const TcParams p) {
     using S = Shape<PAIR>;
     using ES = EpiShape<EPI, VAR_K>;
-    using PP = Pipe<PAIR, VAR_K>;
+    using PP = Pipe<PAIR, VAR_K, EPI>;
     constexpr int THREADS = ES::THREADS;
     constexpr int CW = ES::CW;
     constexpr int STAGES = PP::STAGES;
@@ -358,7 +363,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
     uint8_t* staging_base = base + (size_t)STAGES * S::STAGE_BYTES;
     using CtrlT = Ctrl<STAGES>;
     float* bias_base = reinterpret_cast<float*>(staging_base + (size_t)PP::STAGING);
-    CtrlT& c = *reinterpret_cast<CtrlT*>(staging_base + (size_t)PP::STAGING + (size_t)PP::BIAS);
+    uint8_t* aux_base = staging_base + (size_t)PP::STAGING + (size_t)PP::BIAS;
+    CtrlT& c = *reinterpret_cast<CtrlT*>(aux_base + (size_t)PP::AUXBUF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
@@ -381,6 +387,11 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             mbar_init(smem_u32(&c.tempty[b]), ES::WARPS * S::CTAS);
         }
         mbar_init(smem_u32(&c.drain), 1);
+        if (PP::AUX)
+            for (int w = 0; w < ES::WARPS; ++w) {
+                mbar_init(smem_u32(&c.gbar[w][0]), 1);
+                mbar_init(smem_u32(&c.gbar[w][1]), 1);
+            }
         c.abort_flag = 0;
         fence_barrier_init();
     }
@@ -638,30 +649,34 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
         const uint32_t tempty_local1 = smem_u32(&c.tempty[1]);
         if (!VAR_K && EPI != (int)Epi::Logits && lane == 0) {
             tma_prefetch_map(&mapO0);
-            if (EPI == (int)Epi::BiasGelu) tma_prefetch_map(&mapO1);
+            // second output (BiasGelu) or the saved GELU'(h) input (ScaleAux)
+            if (EPI == (int)Epi::BiasGelu || EPI == (int)Epi::ScaleAux) tma_prefetch_map(&mapO1);
         }
         int acc = 0, ecur = 0, sbuf = 0;
         uint32_t acc_phase = 0;
         // Operands of the epilogue read from global memory stream ahead of the
         // accumulators, across tile boundaries (the next tile of this CTA is
-        // known): the saved GELU'(h) of this thread's row (ScaleAux) two chunks
-        // ahead; the bias of the warp's columns one tile ahead, held in
+        // known).  The saved GELU'(h) (ScaleAux): TMA boxes of the warp's 32
+        // rows x 16 columns (the staging box's shape and swizzle) into a
+        // two-chunk ring, issued two chunks ahead by lane 0 (gi chunks issued,
+        // gc consumed).  The bias of the warp's columns: one tile ahead, held in
         // registers and written to shared memory as fp32 when its tile starts.
-        constexpr bool kAux = EPI == (int)Epi::ScaleAux && !VAR_K;
+        constexpr bool kAux = PP::AUX;
         constexpr bool kBias = (EPI == (int)Epi::BiasGelu || EPI == (int)Epi::Bias) && !VAR_K;
         constexpr int BW = ES::COLS / 32;   // bias values per lane
-        auto load_aux = [&](const Tile& tt, int ch) {
-            U4s<CW / 8> r;
-            const int64_t gl = (int64_t)tt.row0 + q * 32 + lane;
-            const bool ok = (q * 32 + lane) < tt.rows;
-            const int col = tt.nt * BN + cq * ES::COLS + ch * CW;
-            #pragma unroll
-            for (int u = 0; u < CW / 8; ++u)
-                r.u[u] = (ok && col < p.N)
-                             ? __ldg(reinterpret_cast<const uint4*>(
-                                   (const __nv_bfloat16*)p.aux + gl * p.N + col + u * 8))
-                             : make_uint4(0, 0, 0, 0);
-            return r;
+        uint8_t* gring = aux_base + ew * 2 * ES::CHUNK_BYTES;
+        int gi = 0, gc = 0;
+        auto aux_col = [&](const Tile& tt, int ch) { return tt.nt * BN + cq * ES::COLS + ch * CW; };
+        auto issue_aux = [&](const Tile& tt, int ch) {   // every lane; lane 0 issues
+            if (aux_col(tt, ch) >= p.N) return;           // no such chunk: never consumed
+            const int slot = gi & 1;
+            if (lane == 0) {
+                const uint32_t bar = smem_u32(&c.gbar[ew][slot]);
+                mbar_arrive_expect_tx(bar, ES::CHUNK_BYTES);
+                tma_load_2d(smem_u32(gring + slot * ES::CHUNK_BYTES), &mapO1, bar,
+                            aux_col(tt, ch), tt.row0 + q * 32);
+            }
+            ++gi;
         };
         auto load_bias = [&](const Tile& tt, float (&b)[BW]) {
             const int cw = tt.nt * BN + cq * ES::COLS;
@@ -674,11 +689,11 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
         };
         Tile tcur;
         if (unit0 < num_units) tcur = get_tile<VAR_K, PAIR>(c, p, unit0, ecur, rank);
-        U4s<CW / 8> h0, h1;
         float bnext[BW];
+        bool aborted = false;
         if (kAux && unit0 < num_units) {
-            h0 = load_aux(tcur, 0);
-            if (ES::NCH > 1) h1 = load_aux(tcur, 1);
+            issue_aux(tcur, 0);
+            if (ES::NCH > 1) issue_aux(tcur, 1);
         }
         if (kBias && unit0 < num_units) load_bias(tcur, bnext);
         for (int t = unit0; t < num_units; t += nunits) {
@@ -686,6 +701,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             const bool has_next = t + nunits < num_units;
             if (has_next) tcur = get_tile<VAR_K, PAIR>(c, p, t + nunits, ecur, rank);
             const bool mma_tile = ti.num_kb > 0;
+            const int gc_tile = gc;   // GELU' chunks consumed before this tile
             float* bias_s = bias_base + ew * ES::COLS;
             if (kBias) {
                 #pragma unroll
@@ -762,10 +778,24 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         }
                     }
                     if (kAux) {
-                        const U4s<CW / 8> hcur = h0;
-                        h0 = h1;
-                        if (ch + 2 < ES::NCH) h1 = load_aux(ti, ch + 2);
-                        else if (has_next) h1 = load_aux(tcur, ch + 2 - ES::NCH);
+                        const int slot = gc & 1;
+                        if (!mbar_wait_warp(smem_u32(&c.gbar[ew][slot]), (uint32_t)(gc >> 1) & 1u,
+                                            p.limit_ns, &c.abort_flag)) {
+                            raise_abort(c, p);
+                            aborted = true;
+                            break;
+                        }
+                        U4s<CW / 8> hcur;
+                        #pragma unroll
+                        for (int u = 0; u < CW / 8; ++u)
+                            hcur.u[u] = *reinterpret_cast<const uint4*>(
+                                gring + slot * ES::CHUNK_BYTES + stg_off<CW>(lane, u));
+                        ++gc;
+                        // the slot is refilled (async proxy) after every lane has read it
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (ch + 2 < ES::NCH) issue_aux(ti, ch + 2);
+                        else if (has_next) issue_aux(tcur, ch + 2 - ES::NCH);
                         #pragma unroll
                         for (int cc = 0; cc < CW / 8; ++cc) {
                             const __nv_bfloat162* h =
@@ -876,11 +906,12 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     }
                 }
             }
-            // a warp whose columns all lie past N processed no chunk of this tile
-            // and did not advance the GELU' stream: restart it on the next tile
-            if (kAux && has_next && ti.nt * BN + cq * ES::COLS >= p.N) {
-                h0 = load_aux(tcur, 0);
-                if (ES::NCH > 1) h1 = load_aux(tcur, 1);
+            if (aborted) break;
+            // a warp whose columns all lie past N consumed no GELU' chunk of this
+            // tile, so the next tile's first chunks are not in flight yet
+            if (kAux && has_next && gc == gc_tile) {
+                issue_aux(tcur, 0);
+                if (ES::NCH > 1) issue_aux(tcur, 1);
             }
             if (!mma_tile) continue;
             tc_fence_before();
@@ -892,9 +923,12 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
-        // every TMA store has written global memory (and read its staging)
-        // before the CTA exits
+        // every TMA store has written global memory (and read its staging), and
+        // every GELU' load issued has landed, before the CTA exits
         if (!VAR_K && lane == 0) bulk_wait_all();
+        for (; kAux && gc < gi; ++gc)
+            mbar_wait_warp(smem_u32(&c.gbar[ew][gc & 1]), (uint32_t)(gc >> 1) & 1u, p.limit_ns,
+                           nullptr);
         __syncwarp();
     }
 
@@ -956,7 +990,7 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
                       const CUtensorMap& o1, const TcParams& p, int64_t units_upper,
                       cudaStream_t st) {
     auto kern = gemm_tc_kernel<VAR_K, A_MN, B_MN, EPI, PAIR>;
-    constexpr size_t SMEM = smem_bytes<PAIR, VAR_K>();
+    constexpr size_t SMEM = smem_bytes<PAIR, VAR_K, EPI>();
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
     constexpr int THREADS = EpiShape<EPI, VAR_K>::THREADS;
     static std::once_flag once;
@@ -1022,12 +1056,16 @@ __global__ void __launch_bounds__(256) colsum_mtile_reduce_kernel(
     int N, int E, const int32_t* __restrict__ offsets, int tile_m, int rows_per_mtile,
     const float* __restrict__ part, float* __restrict__ out, int accumulate) {
     __shared__ float red[8][32];
+    __shared__ int off_s[MAX_E + 1];
     const int e = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.y * 32 + lane;
+    // the segment bounds, loaded in one step (not a chain of dependent loads)
+    for (int i = threadIdx.x; i <= e + 1; i += 256) off_s[i] = offsets[i];
+    __syncthreads();
     int64_t m0 = 0;
-    for (int q = 0; q < e; ++q) m0 += (offsets[q + 1] - offsets[q] + tile_m - 1) / tile_m;
-    const int R = ((offsets[e + 1] - offsets[e] + tile_m - 1) / tile_m) * rows_per_mtile;
+    for (int q = 0; q < e; ++q) m0 += (off_s[q + 1] - off_s[q] + tile_m - 1) / tile_m;
+    const int R = ((off_s[e + 1] - off_s[e] + tile_m - 1) / tile_m) * rows_per_mtile;
     const float* src = part + m0 * rows_per_mtile * N + c;
     float s = 0.f;
     if (c < N) {
@@ -1113,6 +1151,8 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     if (!make_out_map(&mo0, g.out0, g.P, g.N, cw)) return cudaErrorInvalidValue;
     if (g.epi == Epi::BiasGelu) {
         if (!make_out_map(&mo1, g.out1, g.P, g.N, cw)) return cudaErrorInvalidValue;
+    } else if (g.epi == Epi::ScaleAux) {   // the saved GELU'(h), read in the same boxes
+        if (!make_out_map(&mo1, const_cast<void*>(g.aux), g.P, g.N, cw)) return cudaErrorInvalidValue;
     } else {
         mo1 = mo0;
     }

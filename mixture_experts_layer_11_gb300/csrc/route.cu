@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(kRouteBlockTokens) dispatch_rank_kernel(
 // dtype, fp32 arithmetic).
 
 template <typename TIn, int EPL, int KMAX>
-__global__ void __launch_bounds__(256) route_bwd_dx_kernel(
+__global__ void __launch_bounds__(256, KMAX <= 4 ? 3 : 1) route_bwd_dx_kernel(
     int64_t T, int d, int E, int k, int renorm, const float* __restrict__ dw,
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
     const float* __restrict__ w, const TIn* __restrict__ Wg,
@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(256) route_bwd_dx_kernel(
     if (t >= T) return;
     constexpr int VN = V::N;
     // vectors per lane in flight: U * KMAX row loads before any use
-    constexpr int U = KMAX >= 8 ? 1 : (KMAX >= 2 ? 8 / KMAX : 4);
+    constexpr int U = KMAX >= 4 ? 1 : (KMAX == 2 ? 2 : 4);
     // The gather of the permute backward (rows pos[t, j] of dx_perm) does not
     // depend on dL: its first loads are issued before dL is computed.
     int32_t p[KMAX];
