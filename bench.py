@@ -45,14 +45,14 @@ def launches_per_chunk(cfg) -> int:
     scan and the rank (4); otherwise logits + gate fused for E <= 32 (3) or
     separate (4).  Permute (1); two expert GEMMs (2); combine (1); combine
     backward (1).  Expert backward: bf16 has the dH GEMM + its db1 reduction,
-    the dX GEMM, two weight-gradient GEMMs and the db2 row sum (2 kernels) = 7;
+    the dX GEMM and two weight-gradient GEMMs (db2 inside the dW2 one) = 5;
     fp32 has four GEMMs and two column sums of two kernels each = 8.  Router
     backward: with renorm, dx with the permute backward fused in and dWg (2
     kernels) = 3; without (dense gate Jacobian), dL, the tiled dx product
     with the permute backward, and dWg (2 kernels) = 4."""
     bf16_tc = cfg.dtype == "bf16" and cfg.d % 64 == 0
     route = 4 if (bf16_tc or cfg.E > 32) else 3
-    ffn_bwd = 7 if cfg.dtype == "bf16" else 8
+    ffn_bwd = 5 if cfg.dtype == "bf16" else 8
     route_bwd = 3 if cfg.renorm else 4
     return route + 1 + 2 + 1 + 1 + ffn_bwd + route_bwd
 

@@ -81,6 +81,7 @@ template <bool PAIR, bool VAR_K, int EPI> struct Pipe {
     static constexpr int STAGING = VAR_K ? 16 * 1024 : 32 * 1024;
     static constexpr int BIAS = VAR_K ? 0 : 4 * 1024;   // fp32 bias of each warp's columns
     static constexpr int AUXBUF = AUX ? 32 * 1024 : 0;  // GELU'(h) ring, 2 x 1 KB per warp
+    static constexpr int ONES = VAR_K ? 64 * BK * 2 : 0; // all-ones MN-major B slab (row sums)
     static constexpr int STAGES = PAIR ? (VAR_K ? 6 : (AUX ? 4 : 5)) : (VAR_K ? 4 : 3);
 };
 
@@ -112,6 +113,7 @@ struct TcParams {
     void* out1;
     float* outf;
     float* cpart;            // ScaleAux: column-sum partial rows [rows][N], or null
+    float* bsum;             // VarK: per-expert row sums of act_a [E][M], or null
     int accumulate;
     int32_t* status;
     uint64_t limit_ns;
@@ -137,13 +139,14 @@ constexpr size_t smem_bytes() {
     using S = Shape<PAIR>;
     using PP = Pipe<PAIR, VAR_K, EPI>;
     return 1024 + (size_t)PP::STAGES * S::STAGE_BYTES + (size_t)PP::STAGING + (size_t)PP::BIAS +
-           (size_t)PP::AUXBUF + sizeof(Ctrl<PP::STAGES>);
+           (size_t)PP::AUXBUF + (size_t)PP::ONES + sizeof(Ctrl<PP::STAGES>);
 }
 
 struct Tile {
     int e, mt, nt, num_kb;
     int row0;     // VarM: first row of this CTA's part; VarK: first row of the segment
     int rows;     // VarM: valid rows of this CTA's part (may be <= 0); VarK: segment rows
+    bool ones;    // VarK: the extra tile against the all-ones B (row sums of act_a)
 };
 
 template <bool VAR_K, bool PAIR, typename C>
@@ -161,13 +164,17 @@ __device__ __forceinline__ Tile get_tile(const C& c, const TcParams& p, int t, i
         ti.row0 = c.off[ecur] + ti.mt * S::TILE_M + rank * BM;
         ti.rows = min(BM, c.off[ecur + 1] - ti.row0);
         ti.num_kb = p.K / BK;
+        ti.ones = false;
     } else {
+        // n-tiles per m-tile: NT, plus the all-ones tile when row sums are wanted
+        const int NTX = NT + (p.bsum ? 1 : 0);
         const int MT = (p.M + S::TILE_M - 1) / S::TILE_M;
-        const int per = MT * NT;
+        const int per = MT * NTX;
         ti.e = c.order[t / per];
         const int local = t % per;
-        ti.mt = local / NT;
-        ti.nt = local % NT;
+        ti.mt = local / NTX;
+        ti.nt = local % NTX;
+        ti.ones = ti.nt == NT;
         ti.row0 = c.off[ti.e];
         ti.rows = c.off[ti.e + 1] - ti.row0;
         ti.num_kb = (ti.rows + BK - 1) / BK;
@@ -364,7 +371,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
     using CtrlT = Ctrl<STAGES>;
     float* bias_base = reinterpret_cast<float*>(staging_base + (size_t)PP::STAGING);
     uint8_t* aux_base = staging_base + (size_t)PP::STAGING + (size_t)PP::BIAS;
-    CtrlT& c = *reinterpret_cast<CtrlT*>(aux_base + (size_t)PP::AUXBUF);
+    uint8_t* ones_base = aux_base + (size_t)PP::AUXBUF;
+    CtrlT& c = *reinterpret_cast<CtrlT*>(ones_base + (size_t)PP::ONES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
@@ -406,6 +414,13 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
     }
     for (int i = threadIdx.x; i <= E; i += THREADS)
         c.off[i] = p.offsets ? p.offsets[i] : (i == 0 ? 0 : (int)p.P);   // null: rows [0, P)
+    if (VAR_K && p.bsum) {
+        // bf16 ones for the row-sum tile's B operand, read by the tensor core
+        for (int i = threadIdx.x; i < PP::ONES / 16; i += THREADS)
+            reinterpret_cast<uint4*>(ones_base)[i] =
+                make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        fence_proxy_async_smem();
+    }
     __syncthreads();
     if (!VAR_K) {
         if (threadIdx.x == 0) {
@@ -437,7 +452,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             int act = 0;
             for (int e = 0; e < E; ++e) act += (c.off[e + 1] - c.off[e]) > 0;
             const int MT = (p.M + S::TILE_M - 1) / S::TILE_M;
-            c.nactive = (p.accumulate ? act : E) * MT * NT;  // number of work units
+            const int NTX = NT + (p.bsum ? 1 : 0);
+            c.nactive = (p.accumulate ? act : E) * MT * NTX;  // number of work units
         }
     }
     tc_fence_before();
@@ -476,8 +492,9 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         bytes += S::A_BYTES;
                         bytes += S::B_BYTES;   // whole box (columns past N zero-filled)
                     } else {
-                        // whole boxes (slabs past the M / N edge are zero-filled)
-                        bytes = S::A_BYTES + S::B_BYTES;
+                        // whole boxes (slabs past the M / N edge are zero-filled); the
+                        // row-sum tile reads only A
+                        bytes = S::A_BYTES + (ti.ones ? 0 : S::B_BYTES);
                     }
                     // a weight-gradient pair's odd CTA loads a segment's last K block
                     // onto its own barrier, for its relay warp to zero the tail first
@@ -508,7 +525,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         const int r = ti.row0 + kb * BK;
                         const int mA = ti.mt * S::TILE_M + rank * BM;
                         load3(sA, &mapA, 0, r, mA / 64);
-                        load3(sB, &mapB, 0, r, nB / 64);
+                        if (!ti.ones) load3(sB, &mapB, 0, r, nB / 64);
                     }
                     issued_parity[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -569,6 +586,12 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
         // ---- MMA issuer (the even CTA of a pair issues for both) ---------------------
         if (leader) {
             constexpr uint32_t IDESC = idesc_bf16_f32(S::TILE_M, BN, A_MN, B_MN);
+            // row-sum tile: N = 32 against the all-ones slab (the same slab for every
+            // stage and K block)
+            constexpr uint32_t IDESC_ONES = idesc_bf16_f32(S::TILE_M, 32, A_MN, B_MN);
+            const uint64_t ones_desc =
+                smem_desc_sw128(smem_u32(ones_base), B_MN ? SLAB_BYTES : 16, 1024);
+            const uint32_t o_lo0 = (uint32_t)ones_desc;
             // Descriptors of stage 0's A and B; a stage or K step only moves the
             // start address (bits 0-13, in 16-byte units; shared addresses stay
             // below 256 KB, so the field never carries into the next one).
@@ -611,11 +634,13 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             const uint64_t ad =
                                 ((uint64_t)a_hi << 32) | (uint64_t)(a_lo0 + so + kk * A_KSTEP);
-                            const uint64_t bd =
-                                ((uint64_t)b_hi << 32) | (uint64_t)(b_lo0 + so + kk * B_KSTEP);
+                            const uint32_t blo = ti.ones ? o_lo0 + kk * B_KSTEP
+                                                         : b_lo0 + so + kk * B_KSTEP;
+                            const uint64_t bd = ((uint64_t)b_hi << 32) | (uint64_t)blo;
                             const uint32_t accum = (kk != 0 || kb != 0) ? 1u : 0u;
-                            if (PAIR) tc_mma2_bf16(d_tmem, ad, bd, IDESC, accum);
-                            else tc_mma_bf16(d_tmem, ad, bd, IDESC, accum);
+                            const uint32_t idesc = ti.ones ? IDESC_ONES : IDESC;
+                            if (PAIR) tc_mma2_bf16(d_tmem, ad, bd, idesc, accum);
+                            else tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
                         }
                         if (PAIR) tc_commit2_both(smem_u32(&c.empty[stage]));
                         else tc_commit(smem_u32(&c.empty[stage]));
@@ -734,6 +759,17 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     store_tile_bf16<CW>(buf, lane, (__nv_bfloat16*)out, grow0, valid, p.N, col0);
                 }
             };
+            if (VAR_K && ti.ones && cq == 0) {
+                // row sums of act_a: column 0 of the all-ones tile's accumulator
+                float v[32];
+                if (mma_tile) tmem_ld32(trow, v);
+                else v[0] = 0.f;
+                const int m = ti.mt * S::TILE_M + rank * BM + q * 32 + lane;
+                if (m < p.M) {
+                    float* o = p.bsum + (int64_t)ti.e * p.M + m;
+                    *o = p.accumulate ? *o + v[0] : v[0];
+                }
+            }
             #pragma unroll 1
             for (int ch = 0; ch < ES::NCH; ++ch) {
                 const int cl = cq * ES::COLS + ch * CW;       // column inside the tile
@@ -1213,7 +1249,8 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
     p.E = g.E; p.M = g.M; p.N = g.N; p.K = 0; p.P = g.P;
     p.offsets = g.offsets; p.outf = g.out; p.accumulate = g.accumulate;
     p.status = status; p.limit_ns = wait_limit_ns();
-    const int64_t NT = (g.N + BN - 1) / BN;
+    p.bsum = g.bsum;
+    const int64_t NT = (g.N + BN - 1) / BN + (g.bsum ? 1 : 0);
     const int64_t u1 = (int64_t)g.E * ((g.M + BM - 1) / BM) * NT;
     const int64_t u2 = (int64_t)g.E * ((g.M + 2 * BM - 1) / (2 * BM)) * NT;
     CUtensorMap unused;   // no bf16 output: the fp32 epilogue stores directly

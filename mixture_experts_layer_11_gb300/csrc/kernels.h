@@ -103,6 +103,10 @@ struct GemmVarK {
     const void* act_b;      // [P, N]
     float* out;             // [E, M, N]
     int accumulate;
+    // tensor-core path: when non-null, also bsum[e][m] (+)= sum over expert e's
+    // rows of act_a[row][m] (a bias gradient), from one extra tile per
+    // (expert, m-tile) whose B operand is a constant all-ones block
+    float* bsum = nullptr;
 };
 
 cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t st);

@@ -233,6 +233,7 @@ moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const voi
     GemmVarM g_dx{E, d, f, P, offsets, dH, W1, false, Epi::Plain, nullptr, nullptr, dx_perm, nullptr};
     // dW2[e] = dY^T A  ([d, f]);  dW1[e] = dH^T X  ([f, d])
     GemmVarK g_w2{E, d, f, P, offsets, dy_perm, A, dW2, accumulate};
+    if (tc) g_w2.bsum = db2;   // db2 = column sums of dY_perm, by the dW2 GEMM
     GemmVarK g_w1{E, f, d, P, offsets, dH, x_perm, dW1, accumulate};
     cudaError_t e = tc ? launch_gemm_varm_tc(g_dh, dev_status, st) : launch_gemm_varm_simt(g_dh, st);
     if (e == cudaSuccess)
@@ -241,7 +242,8 @@ moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const voi
         e = tc ? launch_gemm_vark_tc(g_w2, dev_status, st) : launch_gemm_vark_simt(g_w2, st);
     if (e == cudaSuccess)
         e = tc ? launch_gemm_vark_tc(g_w1, dev_status, st) : launch_gemm_vark_simt(g_w1, st);
-    if (e == cudaSuccess) e = launch_segment_colsum(*s, dy_perm, d, offsets, db2, accumulate, partial, st);
+    if (e == cudaSuccess && !tc)
+        e = launch_segment_colsum(*s, dy_perm, d, offsets, db2, accumulate, partial, st);
     if (e == cudaSuccess && !tc)
         e = launch_segment_colsum(*s, dH, f, offsets, db1, accumulate, partial, st);
     return cuda_status(e);
