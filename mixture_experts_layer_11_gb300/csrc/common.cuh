@@ -61,31 +61,79 @@ __device__ __forceinline__ float gelu_grad_f(float x) {
 // and one exponential, phi(x) = 2^(-x^2 log2(e) / 2 - log2(sqrt(2 pi))), gives
 // GELU(x) = x Phi(x) and GELU'(x) = Phi(x) + x phi(x).  Used only where the
 // result is rounded to bf16 (relative spacing 2^-8), far above the
-// approximation error.
-struct GeluParts {
-    float Phi;    // standard normal CDF at x
-    float xphi;   // x times the standard normal density at x
-};
+// approximation error.  Evaluated for two values at a time (below).
 __device__ __forceinline__ float ex2_approx(float v) {
     float r;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
     return r;
 }
-__device__ __forceinline__ GeluParts gelu_parts_fast(float x) {
-    const float z = fabsf(x) * 0.70710678118654752f;
-    const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
-    const float phi = ex2_approx(fmaf(x * x, -0.72134752044448170f, -1.32574806473615950f));
-    const float q =
-        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.33027442958912330f, -1.82125597917760770f),
-                                 1.78147793656981300f),
-                         -0.35656378124891563f),
-                 0.31938153025994090f) * phi;   // Phi(-|x|)
-    return {x >= 0.f ? 1.0f - q : q, x * phi};
+
+// Packed fp32 pairs (fma/mul/add .f32x2: one instruction for two lanes, each
+// rounded like its scalar form).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
 }
-__device__ __forceinline__ float gelu_fast(float x) { return x * gelu_parts_fast(x).Phi; }
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Phi(x) and x phi(x) for two values at once: the reciprocal, the exponential
+// and the sign select per value, the polynomial and the products as packed
+// pairs (each lane rounded as its scalar form would be).
+struct GeluParts2 {
+    uint64_t Phi;    // (Phi(x0), Phi(x1))
+    uint64_t xphi;   // (x0 phi(x0), x1 phi(x1))
+};
+__device__ __forceinline__ GeluParts2 gelu_parts_fast2(float x0, float x1) {
+    const float t0 = __fdividef(1.0f, fmaf(0.3275911f, fabsf(x0) * 0.70710678118654752f, 1.0f));
+    const float t1 = __fdividef(1.0f, fmaf(0.3275911f, fabsf(x1) * 0.70710678118654752f, 1.0f));
+    const uint64_t x = f2_pack(x0, x1), t = f2_pack(t0, t1);
+    const uint64_t arg = f2_fma(f2_mul(x, x), f2_pack(-0.72134752044448170f, -0.72134752044448170f),
+                                f2_pack(-1.32574806473615950f, -1.32574806473615950f));
+    float a0, a1;
+    f2_unpack(arg, a0, a1);
+    const uint64_t phi = f2_pack(ex2_approx(a0), ex2_approx(a1));
+    uint64_t poly = f2_fma(t, f2_pack(1.33027442958912330f, 1.33027442958912330f),
+                           f2_pack(-1.82125597917760770f, -1.82125597917760770f));
+    poly = f2_fma(t, poly, f2_pack(1.78147793656981300f, 1.78147793656981300f));
+    poly = f2_fma(t, poly, f2_pack(-0.35656378124891563f, -0.35656378124891563f));
+    poly = f2_fma(t, poly, f2_pack(0.31938153025994090f, 0.31938153025994090f));
+    const uint64_t q = f2_mul(f2_mul(t, poly), phi);                              // Phi(-|x|)
+    const uint64_t omq = f2_fma(q, f2_pack(-1.0f, -1.0f), f2_pack(1.0f, 1.0f));  // 1 - q
+    float q0, q1, o0, o1;
+    f2_unpack(q, q0, q1);
+    f2_unpack(omq, o0, o1);
+    return {f2_pack(x0 >= 0.f ? o0 : q0, x1 >= 0.f ? o1 : q1), f2_mul(x, phi)};
+}
+
+// Single values through the paired evaluation (as the epilogue computes them).
+__device__ __forceinline__ float gelu_fast(float x) {
+    float a, b;
+    f2_unpack(f2_mul(f2_pack(x, x), gelu_parts_fast2(x, x).Phi), a, b);
+    return a;
+}
 __device__ __forceinline__ float gelu_grad_fast(float x) {
-    const GeluParts r = gelu_parts_fast(x);
-    return r.Phi + r.xphi;
+    const GeluParts2 r = gelu_parts_fast2(x, x);
+    float a, b;
+    f2_unpack(f2_add(r.Phi, r.xphi), a, b);
+    return a;
 }
 
 // ---- shared-memory addresses and mbarriers ---------------------------------------
@@ -235,7 +283,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
         : "memory");
 }
 
-// Load 32 consecutive fp32 columns of this thread's TMEM lane.
 // Load 16 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
@@ -251,6 +298,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Load 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
     asm volatile(

@@ -809,8 +809,10 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         #pragma unroll
                         for (int u = 0; u < CW / 4; ++u) {
                             const float4 b = b4[u];
-                            v[4 * u] += b.x; v[4 * u + 1] += b.y;
-                            v[4 * u + 2] += b.z; v[4 * u + 3] += b.w;
+                            f2_unpack(f2_add(f2_pack(v[4 * u], v[4 * u + 1]), f2_pack(b.x, b.y)),
+                                      v[4 * u], v[4 * u + 1]);
+                            f2_unpack(f2_add(f2_pack(v[4 * u + 2], v[4 * u + 3]), f2_pack(b.z, b.w)),
+                                      v[4 * u + 2], v[4 * u + 3]);
                         }
                     }
                     if (kAux) {
@@ -858,10 +860,10 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         // and GELU'(h) (stored for the backward)
                         float gd[CW];
                         #pragma unroll
-                        for (int i = 0; i < CW; ++i) {
-                            const GeluParts r = gelu_parts_fast(v[i]);
-                            gd[i] = r.Phi + r.xphi;
-                            v[i] *= r.Phi;
+                        for (int i = 0; i < CW; i += 2) {
+                            const GeluParts2 r = gelu_parts_fast2(v[i], v[i + 1]);
+                            f2_unpack(f2_add(r.Phi, r.xphi), gd[i], gd[i + 1]);
+                            f2_unpack(f2_mul(f2_pack(v[i], v[i + 1]), r.Phi), v[i], v[i + 1]);
                         }
                         uint4 pg[CW / 8], pa[CW / 8];
                         #pragma unroll
