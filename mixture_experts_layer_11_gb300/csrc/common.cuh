@@ -68,6 +68,12 @@ __device__ __forceinline__ float ex2_approx(float v) {
     return r;
 }
 
+__device__ __forceinline__ float rcp_approx(float v) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 // Packed fp32 pairs (fma/mul/add .f32x2: one instruction for two lanes, each
 // rounded like its scalar form).
 __device__ __forceinline__ uint64_t f2_pack(float a, float b) {
@@ -102,8 +108,8 @@ struct GeluParts2 {
     uint64_t xphi;   // (x0 phi(x0), x1 phi(x1))
 };
 __device__ __forceinline__ GeluParts2 gelu_parts_fast2(float x0, float x1) {
-    const float t0 = __fdividef(1.0f, fmaf(0.3275911f, fabsf(x0) * 0.70710678118654752f, 1.0f));
-    const float t1 = __fdividef(1.0f, fmaf(0.3275911f, fabsf(x1) * 0.70710678118654752f, 1.0f));
+    const float t0 = rcp_approx(fmaf(0.23164360308456421f, fabsf(x0), 1.0f));
+    const float t1 = rcp_approx(fmaf(0.23164360308456421f, fabsf(x1), 1.0f));
     const uint64_t x = f2_pack(x0, x1), t = f2_pack(t0, t1);
     const uint64_t arg = f2_fma(f2_mul(x, x), f2_pack(-0.72134752044448170f, -0.72134752044448170f),
                                 f2_pack(-1.32574806473615950f, -1.32574806473615950f));
@@ -116,11 +122,9 @@ __device__ __forceinline__ GeluParts2 gelu_parts_fast2(float x0, float x1) {
     poly = f2_fma(t, poly, f2_pack(-0.35656378124891563f, -0.35656378124891563f));
     poly = f2_fma(t, poly, f2_pack(0.31938153025994090f, 0.31938153025994090f));
     const uint64_t q = f2_mul(f2_mul(t, poly), phi);                              // Phi(-|x|)
-    const uint64_t omq = f2_fma(q, f2_pack(-1.0f, -1.0f), f2_pack(1.0f, 1.0f));  // 1 - q
-    float q0, q1, o0, o1;
-    f2_unpack(q, q0, q1);
-    f2_unpack(omq, o0, o1);
-    return {f2_pack(x0 >= 0.f ? o0 : q0, x1 >= 0.f ? o1 : q1), f2_mul(x, phi)};
+    const uint64_t w = f2_fma(q, f2_pack(-2.0f, -2.0f), f2_pack(1.0f, 1.0f));  // 1 - 2q
+    const uint64_t st = f2_pack(x0 >= 0.f ? 1.0f : 0.0f, x1 >= 0.f ? 1.0f : 0.0f);
+    return {f2_fma(st, w, q), f2_mul(x, phi)};
 }
 
 // Single values through the paired evaluation (as the epilogue computes them).

@@ -69,20 +69,29 @@ template <bool PAIR> struct Shape {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 };
 
-// Operand pipeline depth and epilogue staging.  The bf16 epilogues stage two
-// 32-row chunks per warp (32 KB in all), so that the TMA store of one chunk
-// runs while the next is computed; that leaves room for 5 (pair) or 3
-// (single CTA) operand stages under the 227 KB per-CTA limit.  The GELU'
-// scaling epilogue also receives its saved GELU'(h) by TMA into a two-chunk
-// ring per warp (32 KB), for one stage less.  The fp32 weight-gradient
-// epilogue stages one chunk per warp (16 KB).
+// Operand pipeline depth and epilogue staging, under the 227 KB per-CTA limit.
+// The operand loads mostly come from L2 or DRAM with a latency of a few
+// microseconds under load, so the stages take whatever the epilogue leaves:
+// - bias + GELU stages G and A (one 32-row chunk each per warp, 32 KB) and
+//   holds the fp32 bias (4 KB): 5 pair stages;
+// - the one-output bf16 epilogues stage one chunk per warp (16 KB; the TMA
+//   store of a chunk has read it long before the next chunk is written):
+//   6 pair stages, or 5 for the GELU' scaling epilogue, which also receives
+//   its saved GELU'(h) by TMA into a two-chunk ring per warp (32 KB);
+// - the fp32 weight-gradient epilogue stages one chunk per warp (16 KB), next
+//   to the all-ones slab (8 KB): 6 pair stages;
+// - the router-logit epilogue stages 32 x 32 fp32 per warp (32 KB): 5.
+// Single CTAs (48 KB stages) get 3, or 4 for the weight gradients.
 template <bool PAIR, bool VAR_K, int EPI> struct Pipe {
     static constexpr bool AUX = !VAR_K && EPI == (int)Epi::ScaleAux;
-    static constexpr int STAGING = VAR_K ? 16 * 1024 : 32 * 1024;
-    static constexpr int BIAS = VAR_K ? 0 : 4 * 1024;   // fp32 bias of each warp's columns
-    static constexpr int AUXBUF = AUX ? 32 * 1024 : 0;  // GELU'(h) ring, 2 x 1 KB per warp
-    static constexpr int ONES = VAR_K ? 64 * BK * 2 : 0; // all-ones MN-major B slab (row sums)
-    static constexpr int STAGES = PAIR ? (VAR_K ? 6 : (AUX ? 4 : 5)) : (VAR_K ? 4 : 3);
+    static constexpr bool GELU = !VAR_K && EPI == (int)Epi::BiasGelu;
+    static constexpr bool HAS_BIAS = !VAR_K && (EPI == (int)Epi::BiasGelu || EPI == (int)Epi::Bias);
+    static constexpr bool LOGITS = !VAR_K && EPI == (int)Epi::Logits;
+    static constexpr int STAGING = (GELU || LOGITS) ? 32 * 1024 : 16 * 1024;
+    static constexpr int BIAS = HAS_BIAS ? 4 * 1024 : 0;  // fp32 bias of each warp's columns
+    static constexpr int AUXBUF = AUX ? 32 * 1024 : 0;    // GELU'(h) ring, 2 x 1 KB per warp
+    static constexpr int ONES = VAR_K ? 64 * BK * 2 : 0;  // all-ones MN-major B slab (row sums)
+    static constexpr int STAGES = PAIR ? ((GELU || AUX || LOGITS) ? 5 : 6) : (VAR_K ? 4 : 3);
 };
 
 // Epilogue shape.  The epilogue warps drain a 128 x 256 accumulator, each
@@ -677,7 +686,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             // second output (BiasGelu) or the saved GELU'(h) input (ScaleAux)
             if (EPI == (int)Epi::BiasGelu || EPI == (int)Epi::ScaleAux) tma_prefetch_map(&mapO1);
         }
-        int acc = 0, ecur = 0, sbuf = 0;
+        int acc = 0, ecur = 0;
         uint32_t acc_phase = 0;
         // Operands of the epilogue read from global memory stream ahead of the
         // accumulators, across tile boundaries (the next tile of this CTA is
@@ -846,14 +855,9 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                             }
                         }
                     }
-                    // The staging buffers written below were last read by the TMA
-                    // stores committed two chunks ago (one-output epilogues,
-                    // alternating buffers) or one chunk ago (BiasGelu, which
-                    // stages two outputs per chunk).
-                    if (lane == 0) {
-                        if (EPI == (int)Epi::BiasGelu) bulk_wait_read<0>();
-                        else bulk_wait_read<1>();
-                    }
+                    // The staging written below was last read by the TMA stores
+                    // of the previous chunk.
+                    if (lane == 0) bulk_wait_read<0>();
                     __syncwarp();
                     if (EPI == (int)Epi::BiasGelu) {
                         // one Phi / exp evaluation gives both GELU(h) (kept in v)
@@ -877,8 +881,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         uint4 pk[CW / 8];
                         #pragma unroll
                         for (int u = 0; u < CW / 8; ++u) pk[u] = pack8_bf16(v + 8 * u);
-                        emit(stg + sbuf * ES::CHUNK_BYTES, pk, &mapO0, p.out0, col0);
-                        sbuf ^= 1;
+                        emit(stg, pk, &mapO0, p.out0, col0);
                         if (EPI == (int)Epi::ScaleAux && CW == 16 && p.cpart) {
                             // column sums of the stored (bf16) values of this warp's
                             // rows inside the segment, read back from the staging
@@ -886,7 +889,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                             // rows 8g..8g+7 (rotated by g: conflict-free), then the
                             // four row groups are added; one partial row per
                             // (m-tile, CTA, lane quarter)
-                            const uint8_t* sb = stg + (sbuf ^ 1) * ES::CHUNK_BYTES;
+                            const uint8_t* sb = stg;
                             const int w = lane & 7, g = lane >> 3;
                             float s0 = 0.f, s1 = 0.f;
                             #pragma unroll
