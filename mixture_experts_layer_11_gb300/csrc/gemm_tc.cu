@@ -343,6 +343,21 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                  ::"l"(map), "r"(src), "r"(c0), "r"(c1)
                  : "memory");
 }
+// The same for a 3-D box, stored as is or added element by element to what
+// global memory holds (fp32 weight gradients).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
+                                             int32_t c1, int32_t c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(map), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
+                                                  int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%2, %3, %4}], [%1];" ::"l"(map), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -681,7 +696,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
         uint8_t* stg = staging_base + ew * (PP::STAGING / ES::WARPS);
         const uint32_t tempty_local0 = smem_u32(&c.tempty[0]);
         const uint32_t tempty_local1 = smem_u32(&c.tempty[1]);
-        if (!VAR_K && EPI != (int)Epi::Logits && lane == 0) {
+        if (EPI != (int)Epi::Logits && lane == 0) {
             tma_prefetch_map(&mapO0);
             // second output (BiasGelu) or the saved GELU'(h) input (ScaleAux)
             if (EPI == (int)Epi::BiasGelu || EPI == (int)Epi::ScaleAux) tma_prefetch_map(&mapO1);
@@ -915,35 +930,35 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     if (lane == 0) bulk_commit();
                     __syncwarp();
                 } else {
-                    // fp32 weight gradient, 16 columns (64 B per row) at a time
+                    // fp32 weight gradient, 32 rows x 16 columns (64-byte rows) at a
+                    // time: staged like the bf16 boxes (64-byte swizzle) and sent
+                    // by one TMA store, or, when accumulating, by one TMA
+                    // reduction that adds it to what global memory holds.  The
+                    // tensor map clips the rows past M.
                     static_assert(!VAR_K || CW == 32, "fp32 epilogue drains 32-column chunks");
                     const int m0 = ti.mt * S::TILE_M + rank * BM + q * 32;
-                    const int valid_m = p.M - m0;
-                    #pragma unroll
-                    for (int hh = 0; hh < CW / 16; ++hh) {
+                    if (m0 < p.M) {
                         #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc)
-                            *reinterpret_cast<float4*>(stg + stg_off<32>(lane, cc)) =
-                                make_float4(v[hh * 16 + cc * 4], v[hh * 16 + cc * 4 + 1],
-                                            v[hh * 16 + cc * 4 + 2], v[hh * 16 + cc * 4 + 3]);
-                        __syncwarp();
-                        #pragma unroll
-                        for (int it = 0; it < 4; ++it) {
-                            const int rr = it * 8 + (lane >> 2), cc = lane & 3;
-                            if (rr < valid_m) {
-                                float4 o =
-                                    *reinterpret_cast<const float4*>(stg + stg_off<32>(rr, cc));
-                                float4* dst = reinterpret_cast<float4*>(
-                                    p.outf + ((int64_t)ti.e * p.M + m0 + rr) * p.N + col0 +
-                                    hh * 16 + cc * 4);
-                                if (p.accumulate) {
-                                    const float4 old = *dst;
-                                    o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
-                                }
-                                *dst = o;
+                        for (int hh = 0; hh < CW / 16; ++hh) {
+                            // the staging's previous box has been read by its TMA op
+                            if (lane == 0) bulk_wait_read<0>();
+                            __syncwarp();
+                            #pragma unroll
+                            for (int cc = 0; cc < 4; ++cc)
+                                *reinterpret_cast<float4*>(stg + stg_off<32>(lane, cc)) =
+                                    make_float4(v[hh * 16 + cc * 4], v[hh * 16 + cc * 4 + 1],
+                                                v[hh * 16 + cc * 4 + 2], v[hh * 16 + cc * 4 + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if (p.accumulate)
+                                    tma_reduce_add_3d(&mapO0, smem_u32(stg), col0 + hh * 16, m0,
+                                                      ti.e);
+                                else
+                                    tma_store_3d(&mapO0, smem_u32(stg), col0 + hh * 16, m0, ti.e);
+                                bulk_commit();
                             }
                         }
-                        __syncwarp();
                     }
                 }
             }
@@ -966,7 +981,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
         }
         // every TMA store has written global memory (and read its staging), and
         // every GELU' load issued has landed, before the CTA exits
-        if (!VAR_K && lane == 0) bulk_wait_all();
+        if (lane == 0) bulk_wait_all();
         for (; kAux && gc < gi; ++gc)
             mbar_wait_warp(smem_u32(&c.gbar[ew][gc & 1]), (uint32_t)(gc >> 1) & 1u, p.limit_ns,
                            nullptr);
@@ -1003,7 +1018,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // dims/box innermost first; strides in bytes for dims 1.. .
 bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
               const uint64_t* strides, const uint32_t* box,
-              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (!fn) return false;
     if (rank < 1 || rank > 5) return false;
@@ -1011,7 +1027,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
     cuuint32_t bx[5], es[5] = {1, 1, 1, 1, 1};
     for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; }
     for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr),
+    CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(ptr),
                     gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -1258,9 +1274,17 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
     const int64_t NT = (g.N + BN - 1) / BN + (g.bsum ? 1 : 0);
     const int64_t u1 = (int64_t)g.E * ((g.M + BM - 1) / BM) * NT;
     const int64_t u2 = (int64_t)g.E * ((g.M + 2 * BM - 1) / (2 * BM)) * NT;
-    CUtensorMap unused;   // no bf16 output: the fp32 epilogue stores directly
-    memset(&unused, 0, sizeof(unused));
-    return launch_either<true, true, true, (int)Epi::Plain>(ma, mb, unused, unused, p, u1, u2, st);
+    // fp32 output [E, M, N]: boxes of 32 rows x 16 columns, 64-byte swizzle
+    CUtensorMap mo;
+    {
+        const uint64_t dims[3] = {(uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.E};
+        const uint64_t strides[2] = {(uint64_t)g.N * 4, (uint64_t)g.M * g.N * 4};
+        const uint32_t box[3] = {16, 32, 1};
+        if (!make_map(&mo, g.out, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B,
+                      CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+            return cudaErrorInvalidValue;
+    }
+    return launch_either<true, true, true, (int)Epi::Plain>(ma, mb, mo, mo, p, u1, u2, st);
 }
 
 }  // namespace moe
