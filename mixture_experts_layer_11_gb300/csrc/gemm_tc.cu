@@ -858,15 +858,17 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         __syncwarp();
                         if (ch + 2 < ES::NCH) issue_aux(ti, ch + 2);
                         else if (has_next) issue_aux(tcur, ch + 2 - ES::NCH);
+                        // bf16 pair word -> fp32 pair (low half first), packed multiply
                         #pragma unroll
                         for (int cc = 0; cc < CW / 8; ++cc) {
-                            const __nv_bfloat162* h =
-                                reinterpret_cast<const __nv_bfloat162*>(&hcur.u[cc]);
+                            const uint32_t* wd = reinterpret_cast<const uint32_t*>(&hcur.u[cc]);
                             #pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                const float2 f = __bfloat1622float2(h[i]);
-                                v[cc * 8 + 2 * i] *= f.x;
-                                v[cc * 8 + 2 * i + 1] *= f.y;
+                                const int j = cc * 8 + 2 * i;
+                                f2_unpack(f2_mul(f2_pack(v[j], v[j + 1]),
+                                                 f2_pack(__uint_as_float(wd[i] << 16),
+                                                         __uint_as_float(wd[i] & 0xffff0000u))),
+                                          v[j], v[j + 1]);
                             }
                         }
                     }
@@ -898,33 +900,30 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         for (int u = 0; u < CW / 8; ++u) pk[u] = pack8_bf16(v + 8 * u);
                         emit(stg, pk, &mapO0, p.out0, col0);
                         if (EPI == (int)Epi::ScaleAux && CW == 16 && p.cpart) {
-                            // column sums of the stored (bf16) values of this warp's
-                            // rows inside the segment, read back from the staging
-                            // box: lane (w, g) sums word w (columns 2w, 2w+1) over
-                            // rows 8g..8g+7 (rotated by g: conflict-free), then the
-                            // four row groups are added; one partial row per
-                            // (m-tile, CTA, lane quarter)
-                            const uint8_t* sb = stg;
-                            const int w = lane & 7, g = lane >> 3;
-                            float s0 = 0.f, s1 = 0.f;
+                            // column sums of this warp's rows inside the segment (rows
+                            // past its end are masked), one partial row per (m-tile,
+                            // CTA, lane quarter): a halving butterfly over the lanes,
+                            // after which the even lanes hold one column each
+                            float a[16];
+                            const bool row_in = lane < valid;
                             #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int r = g * 8 + ((i + g) & 7);
-                                if (r < valid) {
-                                    const uint32_t wd = *reinterpret_cast<const uint32_t*>(
-                                        sb + stg_off<16>(r, w >> 2) + (w & 3) * 4);
-                                    s0 += __uint_as_float(wd << 16);
-                                    s1 += __uint_as_float(wd & 0xffff0000u);
+                            for (int i = 0; i < 16; ++i) a[i] = (valid >= 32 || row_in) ? v[i] : 0.f;
+                            #pragma unroll
+                            for (int h = 8; h >= 1; h >>= 1) {
+                                const bool up = (lane & (2 * h)) != 0;   // keeps the upper half
+                                #pragma unroll
+                                for (int j = 0; j < h; ++j) {
+                                    const float send = up ? a[j] : a[j + h];
+                                    const float keep = up ? a[j + h] : a[j];
+                                    a[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * h);
                                 }
                             }
-                            s0 += __shfl_xor_sync(0xffffffffu, s0, 8);
-                            s1 += __shfl_xor_sync(0xffffffffu, s1, 8);
-                            s0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-                            s1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+                            const float cs = a[0] + __shfl_xor_sync(0xffffffffu, a[0], 1);
+                            // lane bits 4..1 select the column: 8, 4, 2, 1
+                            const int c = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 +
+                                          ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
                             const int64_t prow = ((int64_t)(t / NT) * S::CTAS + rank) * 4 + q;
-                            if (g == 0)
-                                *reinterpret_cast<float2*>(p.cpart + prow * p.N + col0 + 2 * w) =
-                                    make_float2(s0, s1);
+                            if ((lane & 1) == 0) p.cpart[prow * p.N + col0 + c] = cs;
                         }
                     }
                     if (lane == 0) bulk_commit();

@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(kRouteBlockTokens) dispatch_rank_kernel(
 // dtype, fp32 arithmetic).
 
 template <typename TIn, int EPL, int KMAX>
-__global__ void __launch_bounds__(256, KMAX <= 4 ? 3 : 1) route_bwd_dx_kernel(
+__global__ void __launch_bounds__(256, KMAX <= 4 ? 3 : (KMAX <= 8 ? 2 : 1)) route_bwd_dx_kernel(
     int64_t T, int d, int E, int k, int renorm, const float* __restrict__ dw,
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
     const float* __restrict__ w, const TIn* __restrict__ Wg,
@@ -634,7 +634,7 @@ __global__ void __launch_bounds__(256, KMAX <= 4 ? 3 : 1) route_bwd_dx_kernel(
         float acc[U][VN], wv[VN];
         if (dx_perm) {
             // permute backward fused in: dx = sum_j dx_perm[pos[t,j]] + router term
-            if (c0 != lane * VN) gather(c0);
+            // (the rows of this step were gathered one step ahead)
             #pragma unroll
             for (int u = 0; u < U; ++u) {
                 #pragma unroll
@@ -648,20 +648,45 @@ __global__ void __launch_bounds__(256, KMAX <= 4 ? 3 : 1) route_bwd_dx_kernel(
                     for (int e = 0; e < VN; ++e) acc[u][e] += xr[e];
                 }
             }
+            if (c0 + 32 * VN * U < d) gather(c0 + 32 * VN * U);
         } else {
             #pragma unroll
             for (int u = 0; u < U; ++u)
                 if (c0 + 32 * VN * u < d) V::load(dx + t * d + c0 + 32 * VN * u, acc[u]);
         }
-        for (int i = 0; i < ng; ++i) {
-            const float g = g_s[warp][i];
-            const TIn* wrow = Wg + (int64_t)e_s[warp][i] * d;
+        if (KMAX > 1 && ng <= KMAX) {
+            // the gate rows of all terms are requested before the first is used
+            uint4 wr[KMAX][U];
             #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (c0 + 32 * VN * u >= d) break;
-                V::load(wrow + c0 + 32 * VN * u, wv);
+            for (int i = 0; i < KMAX; ++i)
                 #pragma unroll
-                for (int e = 0; e < VN; ++e) acc[u][e] = fmaf(g, wv[e], acc[u][e]);
+                for (int u = 0; u < U; ++u)
+                    if (i < ng && c0 + 32 * VN * u < d)
+                        wr[i][u] = __ldg(reinterpret_cast<const uint4*>(
+                            Wg + (int64_t)e_s[warp][i] * d + c0 + 32 * VN * u));
+            #pragma unroll
+            for (int i = 0; i < KMAX; ++i) {
+                if (i >= ng) break;
+                const float g = g_s[warp][i];
+                #pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (c0 + 32 * VN * u >= d) break;
+                    V::unpack(wr[i][u], wv);
+                    #pragma unroll
+                    for (int e = 0; e < VN; ++e) acc[u][e] = fmaf(g, wv[e], acc[u][e]);
+                }
+            }
+        } else {
+            for (int i = 0; i < ng; ++i) {
+                const float g = g_s[warp][i];
+                const TIn* wrow = Wg + (int64_t)e_s[warp][i] * d;
+                #pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (c0 + 32 * VN * u >= d) break;
+                    V::load(wrow + c0 + 32 * VN * u, wv);
+                    #pragma unroll
+                    for (int e = 0; e < VN; ++e) acc[u][e] = fmaf(g, wv[e], acc[u][e]);
+                }
             }
         }
         #pragma unroll
