@@ -249,25 +249,43 @@ __global__ void __launch_bounds__(256) seg_partial_kernel(int n, int E, int k,
     for (int i = 0; i < kSegCPL; ++i)
         #pragma unroll
         for (int u = 0; u < V::N; ++u) a[i][u] = 0.f;
-    #pragma unroll 2
-    for (int r = p0 + warp; r < p1; r += 8) {
-        int64_t row = r;
-        float g = 1.f;
-        if (perm) {
-            const int sl = __ldg(perm + r);
-            g = __ldg(wsel + sl);
-            row = sl / k;
+    // The warp's rows p0 + warp + 8 j (j < kDwgChunk / 8): their slot, weight
+    // and source row are fetched by lane j in one step, then every row's
+    // vectors are requested before the first is used.
+    constexpr int RPW = kDwgChunk / 8;   // rows per warp
+    static_assert(RPW <= 32, "one lane per row");
+    int my_row = 0;
+    float my_g = 1.f;
+    {
+        const int r = p0 + warp + 8 * lane;
+        if (lane < RPW && r < p1) {
+            my_row = r;
+            if (perm) {
+                const int sl = __ldg(perm + r);
+                my_g = __ldg(wsel + sl);
+                my_row = sl / k;
+            }
         }
-        uint4 raw[kSegCPL];
+    }
+    uint4 raw[RPW][kSegCPL];
+    #pragma unroll
+    for (int j = 0; j < RPW; ++j) {
+        const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
+        const bool in = p0 + warp + 8 * j < p1;
         #pragma unroll
         for (int i = 0; i < kSegCPL; ++i) {
             const int c = ct0 + (lane + 32 * i) * V::N;
-            raw[i] = c < n ? ldg16(src + row * n + c) : make_uint4(0, 0, 0, 0);
+            raw[j][i] = (in && c < n) ? ldg16(src + row * n + c) : make_uint4(0, 0, 0, 0);
         }
+    }
+    #pragma unroll
+    for (int j = 0; j < RPW; ++j) {
+        const float g = __shfl_sync(0xffffffffu, my_g, j);
+        if (p0 + warp + 8 * j >= p1) break;   // warp-uniform
         #pragma unroll
         for (int i = 0; i < kSegCPL; ++i) {
             float v[V::N];
-            V::unpack(raw[i], v);
+            V::unpack(raw[j][i], v);
             #pragma unroll
             for (int u = 0; u < V::N; ++u) a[i][u] = fmaf(g, v[u], a[i][u]);
         }

@@ -455,8 +455,16 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nblk, in
     const int per = (n + 1023) / 1024;
     const int b = threadIdx.x * per;
     const int e_ = min(n, b + per);
+    // each thread's run of consecutive entries, kScanU loads in flight at a time
+    constexpr int kScanU = 16;
     int s = 0;
-    for (int i = b; i < e_; ++i) s += data[i];
+    for (int i0 = b; i0 < e_; i0 += kScanU) {
+        int v[kScanU];
+        #pragma unroll
+        for (int u = 0; u < kScanU; ++u) v[u] = (i0 + u < e_) ? data[i0 + u] : 0;
+        #pragma unroll
+        for (int u = 0; u < kScanU; ++u) s += v[u];
+    }
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     int incl = s;
     #pragma unroll
@@ -479,10 +487,16 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nblk, in
     }
     __syncthreads();
     int run = warp_tot[wid] + incl - s;
-    for (int i = b; i < e_; ++i) {
-        const int c = data[i];
-        data[i] = run;
-        run += c;
+    for (int i0 = b; i0 < e_; i0 += kScanU) {
+        int v[kScanU];
+        #pragma unroll
+        for (int u = 0; u < kScanU; ++u) v[u] = (i0 + u < e_) ? data[i0 + u] : 0;
+        #pragma unroll
+        for (int u = 0; u < kScanU; ++u)
+            if (i0 + u < e_) {
+                data[i0 + u] = run;
+                run += v[u];
+            }
     }
     __syncthreads();
     for (int e = threadIdx.x; e <= E; e += 1024) {
