@@ -11,9 +11,20 @@ chunk's backward needs (X_perm, G = GELU'(h), A, Y_perm) stay resident in HBM be
 the forward and the backward; the backward's transient buffers (dY_perm,
 dX_perm and the library workspace) are shared by all chunks.
 
+With more than one chunk the chunks are pipelined on two streams (the
+micro-batch overlap of MPipeMoE, "research method", and ES-MoE's overlap of
+the permutation with compute): a side stream routes and permutes chunk i+1
+while the current stream runs chunk i's expert GEMMs, and in the backward it
+runs chunk i+1's combine backward and chunk i's router backward next to chunk
+i's expert backward.  The side stream has its own library workspace, dY_perm
+and dX_perm are double-buffered, and events order every reuse.  Each fp32
+gradient still accumulates in chunk order on one stream (dW, db on the current
+one, dWg on the side one), so the results equal the serial loop's bit for bit.
+
 All buffers are allocated once, up front, by ``LayerPass``; ``forward`` and
-``backward`` only launch work on the current CUDA stream (no allocation, no
-host synchronisation).  This module does no arithmetic of its own.
+``backward`` only launch work on the current CUDA stream and the side stream
+joined to it (no allocation, no host synchronisation).  This module does no
+arithmetic of its own.
 """
 from __future__ import annotations
 
@@ -34,10 +45,12 @@ class LayerPass:
 
     Parameters: T tokens, d model width, f expert hidden width, E experts,
     k experts per token, dtype (torch.bfloat16 or torch.float32), renorm,
-    chunk (dispatch chunk cap; None = one chunk)."""
+    chunk (dispatch chunk cap; None = one chunk), pipeline (two-stream chunk
+    pipelining when there is more than one chunk; False keeps one stream)."""
 
     def __init__(self, T: int, d: int, f: int, E: int, k: int, dtype: torch.dtype,
-                 renorm: int, chunk: Optional[int] = None, device="cuda"):
+                 renorm: int, chunk: Optional[int] = None, device="cuda",
+                 pipeline: bool = True):
         self.T, self.d, self.f, self.E, self.k = T, d, f, E, k
         self.dtype, self.renorm = dtype, int(renorm)
         C = chunk if chunk else T
@@ -46,6 +59,7 @@ class LayerPass:
         self.C = C
         self.chunks = [(c0, min(T, c0 + C)) for c0 in range(0, T, C)] or [(0, 0)]
         nch = len(self.chunks)
+        self.pipeline = bool(pipeline) and nch > 1
         dev = torch.device(device)
         f32, i32 = torch.float32, torch.int32
         z = lambda *s, dt=dtype: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
@@ -67,8 +81,9 @@ class LayerPass:
         # backward
         self.dw = z(T, k, dt=f32)
         self.dx = z(T, d)
-        self.dY_perm = z(C * k, d)
-        self.dX_perm = z(C * k, d)
+        nbuf = 2 if self.pipeline else 1
+        self.dY_perm = z(nbuf, C * k, d)
+        self.dX_perm = z(nbuf, C * k, d)
         self.dW1 = z(E, f, d, dt=f32)
         self.db1 = z(E, f, dt=f32)
         self.dW2 = z(E, d, f, dt=f32)
@@ -77,6 +92,12 @@ class LayerPass:
         ws = max(ops.moe_workspace_size(s) for s in self.shapes)
         self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=i32, device=dev)
+        if self.pipeline:
+            self.side = torch.cuda.Stream(device=dev)
+            self.ws2 = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+            ev = lambda: [torch.cuda.Event() for _ in range(nch)]  # noqa: E731
+            self._ev_routed, self._ev_cb, self._ev_ffn, self._ev_rb = ev(), ev(), ev(), ev()
+            self._ev_fork, self._ev_join = torch.cuda.Event(), torch.cuda.Event()
 
     # -- per-chunk views ------------------------------------------------------------
     def _rows(self, t: torch.Tensor, c0: int, c1: int, mult: int = 1) -> torch.Tensor:
@@ -91,6 +112,10 @@ class LayerPass:
         k = self.k
         if not compute_logits:
             self.logits.copy_(logits)
+        main = torch.cuda.current_stream()
+        if self.pipeline:
+            self._ev_fork.record(main)
+            self.side.wait_event(self._ev_fork)
         for ci, ((c0, c1), s) in enumerate(zip(self.chunks, self.shapes)):
             if c1 == c0:
                 continue
@@ -98,42 +123,94 @@ class LayerPass:
             pos = self._rows(self.pos, c0, c1)
             perm = self._rows(self.perm, c0, c1, k)
             offs = self.offsets[ci]
-            ops.moe_route(s, xc, Wg, beta, self._rows(self.logits, c0, c1), int(compute_logits),
-                          self._rows(self.idx, c0, c1), self._rows(self.w, c0, c1),
-                          self.counts[ci], offs, pos, perm, self.ws, self.status)
             Xp = self._rows(self.X_perm, c0, c1, k)
-            ops.moe_permute(s, xc, pos, Xp)
+            # routing and permute of this chunk: on the side stream when
+            # pipelined (chunks are independent there: own rows, own workspace)
+            with torch.cuda.stream(self.side if self.pipeline else main):
+                ops.moe_route(s, xc, Wg, beta, self._rows(self.logits, c0, c1),
+                              int(compute_logits), self._rows(self.idx, c0, c1),
+                              self._rows(self.w, c0, c1), self.counts[ci], offs, pos, perm,
+                              self.ws2 if self.pipeline else self.ws, self.status)
+                ops.moe_permute(s, xc, pos, Xp)
+                if self.pipeline:
+                    self._ev_routed[ci].record(self.side)
+            if self.pipeline:
+                main.wait_event(self._ev_routed[ci])
             Yp = self._rows(self.Y_perm, c0, c1, k)
             ops.moe_expert_ffn_fwd(s, Xp, offs, W1, b1, W2, b2, self._rows(self.G, c0, c1, k),
                                    self._rows(self.A, c0, c1, k), Yp, self.ws, self.status)
             ops.moe_combine_fwd(s, Yp, pos, self._rows(self.w, c0, c1), self._rows(self.y, c0, c1))
+        if self.pipeline:
+            self._ev_join.record(self.side)
+            main.wait_event(self._ev_join)
         return self.y
 
     def backward(self, dy, x, Wg, W1, W2):
         """Backward of the last ``forward``: dy [T,d].  Fills dx, dw, dW1, db1,
         dW2, db2, dWg (buffers owned by this object)."""
         k = self.k
-        for ci, ((c0, c1), s) in enumerate(zip(self.chunks, self.shapes)):
-            acc = int(ci > 0)
-            if c1 == c0:
-                continue
+        main = torch.cuda.current_stream()
+        live = [ci for ci, (c0, c1) in enumerate(self.chunks) if c1 > c0]
+
+        def views(ci):
+            c0, c1 = self.chunks[ci]
             n = (c1 - c0) * k
-            pos = self._rows(self.pos, c0, c1)
-            w = self._rows(self.w, c0, c1)
-            offs = self.offsets[ci]
-            dYp = self.dY_perm[:n]
-            dXp = self.dX_perm[:n]
-            ops.moe_combine_bwd(s, self._rows(dy, c0, c1), self._rows(self.Y_perm, c0, c1, k), pos,
-                                w, dYp, self._rows(self.dw, c0, c1))
-            ops.moe_expert_ffn_bwd(s, dYp, self._rows(self.X_perm, c0, c1, k),
+            b = ci % 2 if self.pipeline else 0
+            return c0, c1, self.dY_perm[b, :n], self.dX_perm[b, :n]
+
+        def combine_bwd(ci):   # A7: dY_perm and dw of chunk ci
+            c0, c1, dYp, _ = views(ci)
+            ops.moe_combine_bwd(self.shapes[ci], self._rows(dy, c0, c1),
+                                self._rows(self.Y_perm, c0, c1, k), self._rows(self.pos, c0, c1),
+                                self._rows(self.w, c0, c1), dYp, self._rows(self.dw, c0, c1))
+
+        def ffn_bwd(ci):       # A8: dX_perm of chunk ci; dW1, db1, dW2, db2 accumulate
+            c0, c1, dYp, dXp = views(ci)
+            ops.moe_expert_ffn_bwd(self.shapes[ci], dYp, self._rows(self.X_perm, c0, c1, k),
                                    self._rows(self.G, c0, c1, k), self._rows(self.A, c0, c1, k),
-                                   offs, W1, W2, dXp, self.dW1, self.db1, self.dW2, self.db2, acc,
-                                   self.ws, self.status)
-            # permute backward (A9) fused into the router backward (A10)
-            ops.moe_route_bwd(s, self._rows(self.dw, c0, c1), self._rows(self.logits, c0, c1),
-                              self._rows(self.idx, c0, c1), w, self._rows(self.perm, c0, c1, k),
-                              offs, self._rows(x, c0, c1), Wg, dXp, pos,
-                              self._rows(self.dx, c0, c1), self.dWg, acc, self.ws, self.status)
+                                   self.offsets[ci], W1, W2, dXp, self.dW1, self.db1, self.dW2,
+                                   self.db2, int(ci > 0), self.ws, self.status)
+
+        def route_bwd(ci, ws):  # A9 (permute backward) fused into A10; dWg accumulates
+            c0, c1, _, dXp = views(ci)
+            ops.moe_route_bwd(self.shapes[ci], self._rows(self.dw, c0, c1),
+                              self._rows(self.logits, c0, c1), self._rows(self.idx, c0, c1),
+                              self._rows(self.w, c0, c1), self._rows(self.perm, c0, c1, k),
+                              self.offsets[ci], self._rows(x, c0, c1), Wg, dXp,
+                              self._rows(self.pos, c0, c1), self._rows(self.dx, c0, c1),
+                              self.dWg, int(ci > 0), ws, self.status)
+
+        if not self.pipeline:
+            for ci in live:
+                combine_bwd(ci)
+                ffn_bwd(ci)
+                route_bwd(ci, self.ws)
+            return self.dx
+        # two streams: the side stream runs combine backward one chunk ahead and
+        # router backward one chunk behind the current stream's expert backward
+        side = self.side
+        self._ev_fork.record(main)
+        side.wait_event(self._ev_fork)
+        with torch.cuda.stream(side):
+            combine_bwd(live[0])
+            self._ev_cb[live[0]].record(side)
+        for i, ci in enumerate(live):
+            main.wait_event(self._ev_cb[ci])
+            if i >= 2:
+                main.wait_event(self._ev_rb[live[i - 2]])   # its dX_perm buffer is free
+            ffn_bwd(ci)
+            self._ev_ffn[ci].record(main)
+            with torch.cuda.stream(side):
+                if i + 1 < len(live):
+                    if i >= 1:
+                        side.wait_event(self._ev_ffn[live[i - 1]])   # its dY_perm buffer is free
+                    combine_bwd(live[i + 1])
+                    self._ev_cb[live[i + 1]].record(side)
+                side.wait_event(self._ev_ffn[ci])
+                route_bwd(ci, self.ws2)
+                self._ev_rb[ci].record(side)
+        self._ev_join.record(side)
+        main.wait_event(self._ev_join)
         return self.dx
 
     def offsets_of(self, ci: int) -> torch.Tensor:

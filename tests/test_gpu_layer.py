@@ -29,10 +29,10 @@ SMALL = {
 }
 
 
-def _run(cfg, inp, logits=None):
+def _run(cfg, inp, logits=None, pipeline=True):
     g = to_dev(inp, DEV)
     lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
-                   chunk=cfg.chunk, device=DEV)
+                   chunk=cfg.chunk, device=DEV, pipeline=pipeline)
     lp.forward(g["x"], g["Wg"], g["W1"], g["b1"], g["W2"], g["b2"], g["beta"],
                compute_logits=logits is None,
                logits=None if logits is None else logits.to(DEV))
@@ -97,3 +97,40 @@ def test_layer_deterministic():
     a, b = _run(cfg, inp), _run(cfg, inp)
     for n in ("idx", "pos", "perm", "y", "dx", "dW1", "db1", "dW2", "db2", "dWg", "dw"):
         assert torch.equal(getattr(a, n), getattr(b, n)), n
+
+
+OUTPUTS = ("idx", "w", "pos", "perm", "y", "dx", "dw", "dW1", "db1", "dW2", "db2", "dWg")
+
+
+def test_layer_pipelined_equals_serial():
+    """Two-stream chunk pipelining (5 chunks, the last one ragged) gives the
+    one-stream loop's results bit for bit, eagerly and replayed from a CUDA
+    graph captured with its side stream."""
+    cfg = synth.CONFIGS["longctx128_bf16"].scaled(T=2300, d=512, f=256, chunk=512)
+    inp = synth.make_inputs(cfg, seed=9, random_bias=True)
+    ser = _run(cfg, inp, pipeline=False)
+    pip = _run(cfg, inp, pipeline=True)
+    assert not ser.pipeline and pip.pipeline and len(pip.chunks) == 5
+    for n in OUTPUTS:
+        assert torch.equal(getattr(ser, n), getattr(pip, n)), n
+    # the same pass captured in a CUDA graph (as the benchmark runs it)
+    g = to_dev(inp, DEV)
+    lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
+                   chunk=cfg.chunk, device=DEV)
+
+    def step():
+        lp.forward(g["x"], g["Wg"], g["W1"], g["b1"], g["W2"], g["b2"], g["beta"])
+        lp.backward(g["dy"], g["x"], g["Wg"], g["W1"], g["W2"])
+
+    step()   # eager warm-up on the side stream's first use
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for n in ("y", "dx", "dW1", "dWg"):
+        getattr(lp, n).zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    lp.check_status()
+    for n in OUTPUTS:
+        assert torch.equal(getattr(ser, n), getattr(lp, n)), n
