@@ -11,6 +11,7 @@ namespace moe {
 
 // Tokens handled by one block of the gate / rank kernels: the per-block
 // histogram is a bitmask of 64 tokens (two 32-bit words) per expert.
+constexpr int kMaxExperts = 256;   // largest moe_shape::E the entry points accept
 constexpr int kRouteBlockTokens = 64;
 constexpr int kRouteWords = kRouteBlockTokens / 32;
 // Rows summed per partial of the router weight gradient and of the bias

@@ -449,64 +449,87 @@ cudaError_t router_gate_small(const moe_shape& s, const TIn* x, const TIn* Wg, c
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int E, int nblk, int32_t* data,
                                                             int32_t* counts,
                                                             int32_t* offsets) {
-    __shared__ int warp_tot[32];
+    // data: the expert-major table [E][nblk] of per-block counts, replaced by its
+    // exclusive prefix sums in that order.  A warp takes whole experts and reads
+    // their rows 32 consecutive entries at a time (coalesced): their totals,
+    // then one scan of the E totals, then each row's prefixes from its base.
+    __shared__ int base_s[kMaxExperts];
     __shared__ int grand;
-    const int n = E * nblk;
-    const int per = (n + 1023) / 1024;
-    const int b = threadIdx.x * per;
-    const int e_ = min(n, b + per);
-    // each thread's run of consecutive entries, kScanU loads in flight at a time
-    constexpr int kScanU = 16;
-    int s = 0;
-    for (int i0 = b; i0 < e_; i0 += kScanU) {
-        int v[kScanU];
-        #pragma unroll
-        for (int u = 0; u < kScanU; ++u) v[u] = (i0 + u < e_) ? data[i0 + u] : 0;
-        #pragma unroll
-        for (int u = 0; u < kScanU; ++u) s += v[u];
-    }
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    int incl = s;
-    #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += v;
+    constexpr int U = 8;   // 32-entry loads in flight per lane
+    for (int e = wid; e < E; e += 32) {
+        const int32_t* row = data + (int64_t)e * nblk;
+        int s = 0;
+        for (int j0 = 0; j0 < nblk; j0 += 32 * U) {
+            int v[U];
+            #pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + 32 * u + lane;
+                v[u] = j < nblk ? row[j] : 0;
+            }
+            #pragma unroll
+            for (int u = 0; u < U; ++u) s += v[u];
+        }
+        #pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+        if (lane == 0) base_s[e] = s;
     }
-    if (lane == 31) warp_tot[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-        const int v = warp_tot[lane];
-        int iv = v;
+        // exclusive scan of the E <= kMaxExperts (256) totals: 8 consecutive per lane
+        int t[8], sum = 0;
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            t[i] = e < E ? base_s[e] : 0;
+            sum += t[i];
+        }
+        int incl = sum;
         #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(kFull, iv, o);
-            if (lane >= o) iv += u;
+            const int v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
         }
-        warp_tot[lane] = iv - v;
-        if (lane == 31) grand = iv;
+        int run = incl - sum;
+        __syncwarp();
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            if (e < E) base_s[e] = run;
+            run += t[i];
+        }
+        if (lane == 31) grand = incl;
     }
     __syncthreads();
-    int run = warp_tot[wid] + incl - s;
-    for (int i0 = b; i0 < e_; i0 += kScanU) {
-        int v[kScanU];
-        #pragma unroll
-        for (int u = 0; u < kScanU; ++u) v[u] = (i0 + u < e_) ? data[i0 + u] : 0;
-        #pragma unroll
-        for (int u = 0; u < kScanU; ++u)
-            if (i0 + u < e_) {
-                data[i0 + u] = run;
-                run += v[u];
+    for (int e = wid; e < E; e += 32) {
+        int32_t* row = data + (int64_t)e * nblk;
+        int run = base_s[e];
+        for (int j0 = 0; j0 < nblk; j0 += 32 * U) {
+            int v[U];
+            #pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + 32 * u + lane;
+                v[u] = j < nblk ? row[j] : 0;
             }
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e <= E; e += 1024) {
-        const int off = (e == E) ? grand : data[e * nblk];
-        offsets[e] = off;
-        if (e < E) {
-            const int nxt = (e + 1 == E) ? grand : data[(e + 1) * nblk];
-            counts[e] = nxt - off;
+            #pragma unroll
+            for (int u = 0; u < U; ++u) {
+                int incl = v[u];
+                #pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int x = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += x;
+                }
+                const int j = j0 + 32 * u + lane;
+                if (j < nblk) row[j] = run + incl - v[u];
+                run += __shfl_sync(kFull, incl, 31);
+            }
+        }
+        if (lane == 0) {
+            offsets[e] = base_s[e];
+            counts[e] = (e + 1 < E ? base_s[e + 1] : grand) - base_s[e];
         }
     }
+    if (threadIdx.x == 0) offsets[E] = grand;
 }
 
 // ---- A3: stable rank inside each block -> pos, perm ------------------------------
