@@ -61,7 +61,7 @@ def launches_per_chunk(cfg) -> int:
 # GEMM launches of one step, from one ncu capture (profiles/gemm_tc_moe_s_bf16.md),
 # valid only for the grouped-GEMM source it was taken on (first 16 hex digits of
 # its SHA-256); any other source or workload reports null.
-GEMM_TRAFFIC = {"moe_s_bf16": (1087.9e6, "54a2ca30758f7416")}
+GEMM_TRAFFIC = {"moe_s_bf16": (1087.1e6, "14e8d341c1309f45")}
 
 
 def gemm_traffic(cfg):

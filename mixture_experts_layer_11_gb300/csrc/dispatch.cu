@@ -327,15 +327,18 @@ __global__ void __launch_bounds__(256) seg_reduce_kernel(int n, int E,
     const int nc = (cnt + kDwgChunk - 1) / kDwgChunk;
     float sum = 0.f;
     if (c < n) {
-        int i = warp;
-        for (; i + 24 < nc; i += 32) {   // 4 loads in flight, added in partial order
-            float v[4];
+        // the warp's partials warp, warp + 8, ...: 16 loads in flight, added in order
+        constexpr int UN = 16;
+        for (int i0 = warp; i0 < nc; i0 += 8 * UN) {
+            float v[UN];
             #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = partial[(int64_t)(start + i + 8 * u) * n + c];
+            for (int u = 0; u < UN; ++u) {
+                const int i = i0 + 8 * u;
+                v[u] = i < nc ? partial[(int64_t)(start + i) * n + c] : 0.f;
+            }
             #pragma unroll
-            for (int u = 0; u < 4; ++u) sum += v[u];
+            for (int u = 0; u < UN; ++u) sum += v[u];   // past the end: + 0
         }
-        for (; i < nc; i += 8) sum += partial[(int64_t)(start + i) * n + c];
     }
     red[warp][lane] = sum;
     __syncthreads();

@@ -1125,15 +1125,18 @@ __global__ void __launch_bounds__(256) colsum_mtile_reduce_kernel(
     const float* src = part + m0 * rows_per_mtile * N + c;
     float s = 0.f;
     if (c < N) {
-        int i = warp;
-        for (; i + 24 < R; i += 32) {   // 4 loads in flight, added in row order
-            float v[4];
+        // the warp's rows warp, warp + 8, ...: 16 loads in flight, added in row order
+        constexpr int UN = 16;
+        for (int i0 = warp; i0 < R; i0 += 8 * UN) {
+            float v[UN];
             #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = src[(int64_t)(i + 8 * u) * N];
+            for (int u = 0; u < UN; ++u) {
+                const int i = i0 + 8 * u;
+                v[u] = i < R ? src[(int64_t)i * N] : 0.f;
+            }
             #pragma unroll
-            for (int u = 0; u < 4; ++u) s += v[u];
+            for (int u = 0; u < UN; ++u) s += v[u];   // past the end: + 0
         }
-        for (; i < R; i += 8) s += src[(int64_t)i * N];
     }
     red[warp][lane] = s;
     __syncthreads();
