@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int64_t Tn, int nv, in
 // Phase 1: one partial per (expert, chunk of kDwgChunk segment rows) and
 // column tile; the block's 8 warps take every 8th row of the chunk, lanes
 // consecutive 16-byte column vectors, and are added in warp order through
-// shared memory.  Phase 2: per expert and 128 columns (4 per lane), 8 warps take
-// every 8th partial, added in warp order.  Deterministic.
+// shared memory.  Phase 2: per expert and 32 or 128 columns (1 or 4 per lane), 8
+// warps take every 8th partial, added in warp order.  Deterministic.
 constexpr int kSegCPL = 4;   // 16-byte vectors per lane in a column tile
 
 template <typename T>
@@ -307,16 +307,17 @@ __global__ void __launch_bounds__(256) seg_partial_kernel(int n, int E, int k,
     }
 }
 
+// VL consecutive columns per lane (1, or 4 when n % 4 == 0), 32 * VL per block
+template <int VL>
 __global__ void __launch_bounds__(256) seg_reduce_kernel(int n, int E,
                                                          const int32_t* __restrict__ offsets,
                                                          const float* __restrict__ partial,
                                                          float* __restrict__ out, int accumulate) {
-    // 4 consecutive columns per lane (n % 4 == 0), 128 per block
-    __shared__ float4 red[8][32];
+    __shared__ float red[8][32 * VL];
     __shared__ int off_s[257];
     const int e = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = (blockIdx.y * 32 + lane) * 4;
+    const int c = (blockIdx.y * 32 + lane) * VL;
     for (int i = threadIdx.x; i <= e + 1; i += 256) off_s[i] = offsets[i];
     __syncthreads();
     int start = 0;
@@ -326,39 +327,44 @@ __global__ void __launch_bounds__(256) seg_reduce_kernel(int n, int E,
     }
     const int cnt = off_s[e + 1] - off_s[e];
     const int nc = (cnt + kDwgChunk - 1) / kDwgChunk;
-    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    float sum[VL];
+    #pragma unroll
+    for (int x = 0; x < VL; ++x) sum[x] = 0.f;
     if (c < n) {
-        // the warp's partials warp, warp + 8, ...: 8 loads in flight, added in order
-        constexpr int UN = 8;
+        // the warp's partials warp, warp + 8, ...: UN loads in flight, added in order
+        constexpr int UN = VL == 1 ? 16 : 8;
         for (int i0 = warp; i0 < nc; i0 += 8 * UN) {
-            float4 v[UN];
+            float v[UN][VL];
             #pragma unroll
             for (int u = 0; u < UN; ++u) {
                 const int i = i0 + 8 * u;
-                v[u] = i < nc ? *reinterpret_cast<const float4*>(partial + (int64_t)(start + i) * n + c)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float* src = partial + (int64_t)(start + i) * n + c;
+                if (VL == 4) {
+                    const float4 f = i < nc ? *reinterpret_cast<const float4*>(src)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[u][0] = f.x; v[u][1 % VL] = f.y; v[u][2 % VL] = f.z; v[u][3 % VL] = f.w;
+                } else {
+                    v[u][0] = i < nc ? *src : 0.f;
+                }
             }
             #pragma unroll
-            for (int u = 0; u < UN; ++u) {   // past the end: + 0
-                sum.x += v[u].x; sum.y += v[u].y; sum.z += v[u].z; sum.w += v[u].w;
-            }
+            for (int u = 0; u < UN; ++u)   // past the end: + 0
+                #pragma unroll
+                for (int x = 0; x < VL; ++x) sum[x] += v[u][x];
         }
     }
-    red[warp][lane] = sum;
+    #pragma unroll
+    for (int x = 0; x < VL; ++x) red[warp][lane * VL + x] = sum[x];
     __syncthreads();
     if (warp == 0 && c < n) {
-        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const float4 r = red[w][lane];
-            s.x += r.x; s.y += r.y; s.z += r.z; s.w += r.w;
+        for (int x = 0; x < VL; ++x) {
+            float t = 0.f;
+            #pragma unroll
+            for (int w = 0; w < 8; ++w) t += red[w][lane * VL + x];
+            float* o = out + (int64_t)e * n + c + x;
+            *o = accumulate ? *o + t : t;
         }
-        float4* o = reinterpret_cast<float4*>(out + (int64_t)e * n + c);
-        if (accumulate) {
-            const float4 old = *o;
-            s.x = old.x + s.x; s.y = old.y + s.y; s.z = old.z + s.z; s.w = old.w + s.w;
-        }
-        *o = s;
     }
 }
 
@@ -442,8 +448,14 @@ cudaError_t launch_segment_rowsum(const moe_shape& s, const void* src, int n,
     else
         seg_partial_kernel<float><<<grid, 256, 0, st>>>(n, s.E, s.k, offsets, perm, wsel,
                                                         (const float*)src, partial);
-    seg_reduce_kernel<<<dim3(s.E, (unsigned)((n + 127) / 128)), 256, 0, st>>>(
-        n, s.E, offsets, partial, out, accumulate);
+    // 4 columns per lane when that still leaves two blocks per SM (wide
+    // outputs, many experts), else 1 (more blocks for small problems)
+    if (n % 4 == 0 && (int64_t)s.E * ((n + 127) / 128) >= 2 * (int64_t)device_sm_count())
+        seg_reduce_kernel<4><<<dim3(s.E, (unsigned)((n + 127) / 128)), 256, 0, st>>>(
+            n, s.E, offsets, partial, out, accumulate);
+    else
+        seg_reduce_kernel<1><<<dim3(s.E, (unsigned)((n + 31) / 32)), 256, 0, st>>>(
+            n, s.E, offsets, partial, out, accumulate);
     return cudaGetLastError();
 }
 
