@@ -224,7 +224,7 @@ def run_ours(args, cfg):
 
     inp = synth.make_inputs(cfg, seed=rank, device=str(dev))
     lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
-                   chunk=cfg.chunk, device=dev)
+                   chunk=cfg.chunk, device=dev, recompute=args.recompute)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ev = lambda **kw: torch.cuda.Event(enable_timing=True, **kw)  # noqa: E731
     x_buf, dy_buf = inp["x"], inp["dy"]   # fixed input buffers (the graph reads these)
@@ -409,7 +409,8 @@ def run_ours(args, cfg):
     achieved = gemm_flops / (gemm_ms / 1e3) / 1e12
     peak = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
     chunks = len(lp.chunks)
-    launches = launches_per_chunk(cfg) * chunks * args.steps
+    # recompute: the backward re-runs each chunk's permute and two expert GEMMs
+    launches = (launches_per_chunk(cfg) + (3 if args.recompute else 0)) * chunks * args.steps
     elem = 2 if cfg.dtype == "bf16" else 4
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -417,10 +418,13 @@ def run_ours(args, cfg):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.dtype, "data": "synthetic (seeded N(0,1) inputs, N(0,1/fan_in) weights)",
         "tflops": flops * args.steps * world / (total_ms / 1e3) / 1e12,
+        "device_memory_gib": torch.cuda.max_memory_allocated(dev) / 2**30,
         "config": {"workload": workload_desc(cfg), "T": cfg.T, "d_model": cfg.d,
                    "d_ffn": cfg.f, "E": cfg.E, "k": cfg.k,
                    "l2": "flushed between steps (256 MiB write, outside the step timing)",
                    "launch": "one CUDA graph per step" if graph is not None else "eager",
+                   "activations": ("recomputed in the backward (routing kept)" if args.recompute
+                                   else "kept from the forward for the backward"),
                    "parallelism": f"replicas x{world}"},
         "roofline": {
             "bound": "tensor", "kernel": "grouped expert GEMM (tcgen05), all expert FFN calls",
@@ -457,6 +461,9 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--recompute", action="store_true",
+                    help="keep only the routing between forward and backward; the backward "
+                         "re-runs each chunk's permute and expert forward")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's kernels one by one instead of as one CUDA graph")
     args = ap.parse_args()

@@ -21,6 +21,13 @@ and dX_perm are double-buffered, and events order every reuse.  Each fp32
 gradient still accumulates in chunk order on one stream (dW, db on the current
 one, dWg on the side one), so the results equal the serial loop's bit for bit.
 
+With ``recompute`` the activations are not kept between the forward and the
+backward (MPipeMoE, "research method": recomputation to cut activation
+memory): only the routing results are, and the backward re-runs each chunk's
+permute and expert forward into one chunk's buffers before its backward, for
+the cost of those kernels again.  The results are the saved mode's, bit for
+bit (the same kernels on the same inputs).  This mode runs on one stream.
+
 All buffers are allocated once, up front, by ``LayerPass``; ``forward`` and
 ``backward`` only launch work on the current CUDA stream and the side stream
 joined to it (no allocation, no host synchronisation).  This module does no
@@ -46,11 +53,13 @@ class LayerPass:
     Parameters: T tokens, d model width, f expert hidden width, E experts,
     k experts per token, dtype (torch.bfloat16 or torch.float32), renorm,
     chunk (dispatch chunk cap; None = one chunk), pipeline (two-stream chunk
-    pipelining when there is more than one chunk; False keeps one stream)."""
+    pipelining when there is more than one chunk; False keeps one stream),
+    recompute (keep only the routing between forward and backward and re-run
+    each chunk's permute and expert forward in the backward; one stream)."""
 
     def __init__(self, T: int, d: int, f: int, E: int, k: int, dtype: torch.dtype,
                  renorm: int, chunk: Optional[int] = None, device="cuda",
-                 pipeline: bool = True):
+                 pipeline: bool = True, recompute: bool = False):
         self.T, self.d, self.f, self.E, self.k = T, d, f, E, k
         self.dtype, self.renorm = dtype, int(renorm)
         C = chunk if chunk else T
@@ -59,7 +68,8 @@ class LayerPass:
         self.C = C
         self.chunks = [(c0, min(T, c0 + C)) for c0 in range(0, T, C)] or [(0, 0)]
         nch = len(self.chunks)
-        self.pipeline = bool(pipeline) and nch > 1
+        self.recompute = bool(recompute)
+        self.pipeline = bool(pipeline) and nch > 1 and not self.recompute
         dev = torch.device(device)
         f32, i32 = torch.float32, torch.int32
         z = lambda *s, dt=dtype: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
@@ -72,11 +82,14 @@ class LayerPass:
         self.perm = z(T * k, dt=i32)
         self.counts = z(nch, _pad4(E), dt=i32)
         self.offsets = z(nch, _pad4(E + 1), dt=i32)
-        # saved activations of every chunk
-        self.X_perm = z(T * k, d)
-        self.G = z(T * k, f)
-        self.A = z(T * k, f)
-        self.Y_perm = z(T * k, d)
+        # activations: of every chunk (kept for the backward), or of one chunk
+        # (recompute)
+        R = C * k if self.recompute else T * k
+        self.X_perm = z(R, d)
+        self.G = z(R, f)
+        self.A = z(R, f)
+        self.Y_perm = z(R, d)
+        self._params = None   # recompute: the forward's W1, b1, W2, b2
         self.y = z(T, d)
         # backward
         self.dw = z(T, k, dt=f32)
@@ -103,6 +116,12 @@ class LayerPass:
     def _rows(self, t: torch.Tensor, c0: int, c1: int, mult: int = 1) -> torch.Tensor:
         return t[c0 * mult:c1 * mult]
 
+    def _act(self, t: torch.Tensor, c0: int, c1: int) -> torch.Tensor:
+        """A chunk's rows of an activation buffer (X_perm, G, A, Y_perm)."""
+        if self.recompute:
+            return t[:(c1 - c0) * self.k]
+        return t[c0 * self.k:c1 * self.k]
+
     def forward(self, x, Wg, W1, b1, W2, b2, beta=None, compute_logits: bool = True,
                 logits: Optional[torch.Tensor] = None):
         """x [T,d]; Wg [E,d]; W1 [E,f,d]; b1 [E,f]; W2 [E,d,f]; b2 [E,d]
@@ -112,6 +131,8 @@ class LayerPass:
         k = self.k
         if not compute_logits:
             self.logits.copy_(logits)
+        if self.recompute:
+            self._params = (W1, b1, W2, b2)
         main = torch.cuda.current_stream()
         if self.pipeline:
             self._ev_fork.record(main)
@@ -123,7 +144,7 @@ class LayerPass:
             pos = self._rows(self.pos, c0, c1)
             perm = self._rows(self.perm, c0, c1, k)
             offs = self.offsets[ci]
-            Xp = self._rows(self.X_perm, c0, c1, k)
+            Xp = self._act(self.X_perm, c0, c1)
             # routing and permute of this chunk: on the side stream when
             # pipelined (chunks are independent there: own rows, own workspace)
             with torch.cuda.stream(self.side if self.pipeline else main):
@@ -136,9 +157,9 @@ class LayerPass:
                     self._ev_routed[ci].record(self.side)
             if self.pipeline:
                 main.wait_event(self._ev_routed[ci])
-            Yp = self._rows(self.Y_perm, c0, c1, k)
-            ops.moe_expert_ffn_fwd(s, Xp, offs, W1, b1, W2, b2, self._rows(self.G, c0, c1, k),
-                                   self._rows(self.A, c0, c1, k), Yp, self.ws, self.status)
+            Yp = self._act(self.Y_perm, c0, c1)
+            ops.moe_expert_ffn_fwd(s, Xp, offs, W1, b1, W2, b2, self._act(self.G, c0, c1),
+                                   self._act(self.A, c0, c1), Yp, self.ws, self.status)
             ops.moe_combine_fwd(s, Yp, pos, self._rows(self.w, c0, c1), self._rows(self.y, c0, c1))
         if self.pipeline:
             self._ev_join.record(self.side)
@@ -161,13 +182,13 @@ class LayerPass:
         def combine_bwd(ci):   # A7: dY_perm and dw of chunk ci
             c0, c1, dYp, _ = views(ci)
             ops.moe_combine_bwd(self.shapes[ci], self._rows(dy, c0, c1),
-                                self._rows(self.Y_perm, c0, c1, k), self._rows(self.pos, c0, c1),
+                                self._act(self.Y_perm, c0, c1), self._rows(self.pos, c0, c1),
                                 self._rows(self.w, c0, c1), dYp, self._rows(self.dw, c0, c1))
 
         def ffn_bwd(ci):       # A8: dX_perm of chunk ci; dW1, db1, dW2, db2 accumulate
             c0, c1, dYp, dXp = views(ci)
-            ops.moe_expert_ffn_bwd(self.shapes[ci], dYp, self._rows(self.X_perm, c0, c1, k),
-                                   self._rows(self.G, c0, c1, k), self._rows(self.A, c0, c1, k),
+            ops.moe_expert_ffn_bwd(self.shapes[ci], dYp, self._act(self.X_perm, c0, c1),
+                                   self._act(self.G, c0, c1), self._act(self.A, c0, c1),
                                    self.offsets[ci], W1, W2, dXp, self.dW1, self.db1, self.dW2,
                                    self.db2, int(ci > 0), self.ws, self.status)
 
@@ -180,8 +201,22 @@ class LayerPass:
                               self._rows(self.pos, c0, c1), self._rows(self.dx, c0, c1),
                               self.dWg, int(ci > 0), ws, self.status)
 
+        def refill(ci):        # recompute: A4 and A5 of chunk ci again
+            c0, c1 = self.chunks[ci]
+            W1_, b1_, W2_, b2_ = self._params
+            s = self.shapes[ci]
+            Xp = self._act(self.X_perm, c0, c1)
+            ops.moe_permute(s, self._rows(x, c0, c1), self._rows(self.pos, c0, c1), Xp)
+            ops.moe_expert_ffn_fwd(s, Xp, self.offsets[ci], W1_, b1_, W2_, b2_,
+                                   self._act(self.G, c0, c1), self._act(self.A, c0, c1),
+                                   self._act(self.Y_perm, c0, c1), self.ws, self.status)
+
+        if self.recompute and self._params is None:
+            raise RuntimeError("recompute: backward needs the forward's parameters")
         if not self.pipeline:
             for ci in live:
+                if self.recompute:
+                    refill(ci)
                 combine_bwd(ci)
                 ffn_bwd(ci)
                 route_bwd(ci, self.ws)

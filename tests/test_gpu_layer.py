@@ -134,3 +134,26 @@ def test_layer_pipelined_equals_serial():
     lp.check_status()
     for n in OUTPUTS:
         assert torch.equal(getattr(ser, n), getattr(lp, n)), n
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("longctx128_bf16", dict(T=2300, d=512, f=256, chunk=512)),
+    ("moe_s_bf16", dict(T=700, d=256, f=512)),
+])
+def test_layer_recompute_equals_saved(name, kw):
+    """Recomputing the permute and expert forward in the backward (only the
+    routing kept) gives the saved-activation pass's results bit for bit."""
+    cfg = synth.CONFIGS[name].scaled(**kw)
+    inp = synth.make_inputs(cfg, seed=11, random_bias=True)
+    saved = _run(cfg, inp, pipeline=False)
+    g = to_dev(inp, DEV)
+    lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
+                   chunk=cfg.chunk, device=DEV, recompute=True)
+    assert lp.recompute and not lp.pipeline
+    assert lp.G.shape[0] == (cfg.chunk or cfg.T) * cfg.k   # one chunk's activations
+    lp.forward(g["x"], g["Wg"], g["W1"], g["b1"], g["W2"], g["b2"], g["beta"])
+    lp.backward(g["dy"], g["x"], g["Wg"], g["W1"], g["W2"])
+    torch.cuda.synchronize()
+    lp.check_status()
+    for n in OUTPUTS:
+        assert torch.equal(getattr(saved, n), getattr(lp, n)), n
