@@ -196,7 +196,8 @@ def run_reference(args, cfg):
         "ms_per_step": cfg.T / v * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "tflops": v * flops_per_token / 1e12,
-        "config": {"workload": workload_desc(cfg), "T": cfg.T},
+        "config": {"workload": workload_desc(cfg), "T": cfg.T, "d_model": cfg.d,
+                   "d_ffn": cfg.f, "E": cfg.E, "k": cfg.k},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
