@@ -206,6 +206,23 @@ def run_reference(args, cfg):
     return 0
 
 
+# ---- replicas: the slowest rank's times and the whole job's rate ---------------------------
+
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of a list of times over all ranks (the values
+    unchanged with one process).  dist: torch.distributed or None."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_rate(tokens_per_rank_step: int, steps: int, world: int, ms: float) -> float:
+    """Tokens per second of all replicas together: every rank processed
+    tokens_per_rank_step tokens per step, over the slowest rank's time."""
+    return tokens_per_rank_step * steps * world / (ms / 1e3)
+
+
 # ---- our arm -----------------------------------------------------------------------------
 
 def run_ours(args, cfg):
@@ -391,18 +408,14 @@ def run_ours(args, cfg):
     if not torch.equal(out_h[(n - 1) % 2][0], out_bufs[(n - 1) % 2][0].cpu()):
         raise RuntimeError("end-to-end output differs from the device-resident step")
 
-    # max over ranks
-    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return 0
 
     tokens = cfg.T * args.steps * world
-    value = tokens / (total_ms / 1e3)
+    value = whole_job_rate(cfg.T, args.steps, world, total_ms)
     flops = cfg.expert_flops() + cfg.router_flops()
     pk, pk_kind = peaks()
     gemm_flops = cfg.expert_flops() * args.steps
@@ -437,7 +450,7 @@ def run_ours(args, cfg):
             "ffn_ms_per_step": {k: v / args.steps for k, v in ffn_ms.items()},
         },
         "gpu_launches": launches,
-        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(cfg.T, args.steps, world, e2e_ms), "unit": "tokens/s",
                 "pipeline": "H2D of step i+1 and D2H of step i on copy streams, overlapping step i",
                 "h2d_bytes_per_step": 2 * cfg.T * cfg.d * elem,
                 "d2h_bytes_per_step": 2 * cfg.T * cfg.d * elem},
