@@ -166,7 +166,11 @@ def permute(x, pos) -> np.ndarray:
     return out
 
 
-def expert_ffn_fwd(X, offsets, W1, b1, W2, b2, round_bf16: bool):
+def expert_ffn_fwd(X, offsets, W1, b1, W2, b2, round_bf16: bool, store_h: bool = False):
+    """Returns G = GELU'(h), A = GELU(h), Y.  With ``round_bf16`` the stored
+    activations are rounded to bf16: G itself, or with ``store_h`` the
+    pre-activation h that G is then taken of (the two readings of where a
+    bf16 forward rounds; A and Y are the same in both)."""
     X, offsets = _f64(X), _i32(offsets)
     W1, b1, W2, b2 = _f64(W1), _f64(b1), _f64(W2), _f64(b2)
     P, d = X.shape
@@ -175,7 +179,8 @@ def expert_ffn_fwd(X, offsets, W1, b1, W2, b2, round_bf16: bool):
     A = np.zeros((P, f), np.float64)
     Y = np.zeros((P, d), np.float64)
     lib().oracle_expert_ffn_fwd(d, f, E, _pi(offsets), _pd(X), _pd(W1), _pd(b1),
-                                _pd(W2), _pd(b2), _pd(G), _pd(A), _pd(Y), int(round_bf16))
+                                _pd(W2), _pd(b2), _pd(G), _pd(A), _pd(Y),
+                                (2 if store_h else 1) if round_bf16 else 0)
     return G, A, Y
 
 
@@ -241,7 +246,7 @@ def router_bwd(dw, logits, idx, w, x, Wg, renorm: int, dWg=None):
 # ---- the whole layer -------------------------------------------------------------
 
 def layer(inp: dict, k: int, renorm: int, round_bf16: bool, chunk: int | None = None,
-          logits=None, backward: bool = True) -> dict:
+          logits=None, backward: bool = True, store_h: bool = False) -> dict:
     """Forward and backward of the MoE layer, steps A1..A10 in order.
 
     ``inp`` holds x, Wg, W1, b1, W2, b2, dy and beta (see ``synth``).
@@ -250,7 +255,8 @@ def layer(inp: dict, k: int, renorm: int, round_bf16: bool, chunk: int | None = 
     consecutive dispatch chunks; routing is per token, the histogram,
     offsets and positions are per chunk, and the weight gradients accumulate
     over chunks in chunk order.  Returns every intermediate, per chunk for the
-    dispatch tensors."""
+    dispatch tensors.  ``store_h`` selects the other reading of where the
+    bf16 forward rounds (see ``expert_ffn_fwd``)."""
     x = _f64(inp["x"])
     T = x.shape[0]
     Wg, W1, b1, W2, b2 = (_f64(inp[n]) for n in ("Wg", "W1", "b1", "W2", "b2"))
@@ -269,7 +275,7 @@ def layer(inp: dict, k: int, renorm: int, round_bf16: bool, chunk: int | None = 
         idx, w = gate(Lc, k, renorm)
         counts, offsets, pos, perm = dispatch(idx, E)
         X = permute(xc, pos)
-        G, A, Y = expert_ffn_fwd(X, offsets, W1, b1, W2, b2, round_bf16)
+        G, A, Y = expert_ffn_fwd(X, offsets, W1, b1, W2, b2, round_bf16, store_h)
         y = combine(Y, pos, w, round_bf16)
         for name, v in (("logits", Lc), ("idx", idx), ("w", w), ("counts", counts),
                         ("offsets", offsets), ("pos", pos), ("perm", perm), ("y", y)):

@@ -197,7 +197,13 @@ ORACLE_API void oracle_permute(int64_t T, int d, int k, const double* x,
  *   h      = W1[e] x_p + b1[e]          (W1: [E][f][d], b1: [E][f])
  *   A[p]   = GELU(h)
  *   G[p]   = GELU'(h)   (kept for the backward, which needs only this of h)
- *   Y[p]   = W2[e] A[p] + b2[e]         (W2: [E][d][f], b2: [E][d]) */
+ *   Y[p]   = W2[e] A[p] + b2[e]         (W2: [E][d][f], b2: [E][d])
+ * round_bf16 selects where a bf16 configuration rounds (the pages fix no
+ * precision, so both plain readings are kept):
+ *   1  G = GELU'(h) and A are what the forward stores, each rounded to bf16;
+ *   2  the pre-activation h itself is what the forward stores (in bf16), so the
+ *      backward's G = GELU'(bf16(h)), exact; A is rounded as in 1.
+ * A and Y always come from the unrounded h. */
 ORACLE_API void oracle_expert_ffn_fwd(int d, int f, int E, const int32_t* offsets,
                                       const double* X, const double* W1,
                                       const double* b1, const double* W2,
@@ -211,7 +217,10 @@ ORACLE_API void oracle_expert_ffn_fwd(int d, int f, int E, const int32_t* offset
             for (int n = 0; n < f; ++n) {
                 double h = b1[(int64_t)e * f + n];
                 for (int c = 0; c < d; ++c) h += W1e[(int64_t)n * d + c] * X[p * d + c];
-                G[p * f + n] = rnd(oracle_gelu_grad(h), round_bf16);
+                if (round_bf16 == 2)
+                    G[p * f + n] = oracle_gelu_grad(oracle_round_bf16(h));
+                else
+                    G[p * f + n] = rnd(oracle_gelu_grad(h), round_bf16);
                 A[p * f + n] = rnd(oracle_gelu(h), round_bf16);
             }
             for (int m = 0; m < d; ++m) {

@@ -232,3 +232,40 @@ def test_bf16_storage_rounds_only_stored_activations():
     # rounding moves results by about bf16 precision, not more
     for n in ("y", "dx", "dW1", "dW2", "dWg"):
         _close(r[n], full[n], 2e-2)
+
+
+def test_h_storage_reading_single_expert_against_library():
+    """The second reading of where the bf16 forward rounds: h itself is stored
+    in bf16 and the backward takes GELU' of it.  With one expert the forward
+    is a dense layer: G must equal torch's float64 autograd derivative of the
+    exact GELU at bf16(h) (h from torch's float64 linear), while A and Y are
+    those of the first reading (both come from the unrounded h)."""
+    cfg = synth.MoEConfig("t", T=48, d=32, f=40, E=1, k=1, renorm=0, dtype="bf16")
+    inp = _inputs(cfg, seed=13)
+    X = inp["x"]
+    offsets = np.array([0, cfg.T], np.int32)
+    G2, A2, Y2 = oracle.expert_ffn_fwd(X, offsets, inp["W1"], inp["b1"], inp["W2"], inp["b2"],
+                                       round_bf16=True, store_h=True)
+    G1, A1, Y1 = oracle.expert_ffn_fwd(X, offsets, inp["W1"], inp["b1"], inp["W2"], inp["b2"],
+                                       round_bf16=True)
+    h = F.linear(X, inp["W1"][0], inp["b1"][0])
+    hr = torch.from_numpy(oracle.round_bf16_array(h.numpy())).requires_grad_(True)
+    F.gelu(hr, approximate="none").sum().backward()
+    _close(G2, hr.grad.numpy(), 1e-13)
+    # G of the first reading is a bf16 value, of the second in general not
+    np.testing.assert_array_equal(oracle.round_bf16_array(G1), G1)
+    assert not np.array_equal(oracle.round_bf16_array(G2), G2)
+    np.testing.assert_array_equal(A2, A1)
+    np.testing.assert_array_equal(Y2, Y1)
+
+
+def test_h_storage_reading_changes_only_the_backward():
+    cfg = synth.MoEConfig("t", T=40, d=16, f=32, E=4, k=2, renorm=1, dtype="bf16")
+    inp = _inputs(cfg, seed=14)
+    a = oracle.layer(inp, 2, 1, round_bf16=True)
+    b = oracle.layer(inp, 2, 1, round_bf16=True, store_h=True)
+    for n in ("y", "dw"):
+        np.testing.assert_array_equal(a[n], b[n])
+    # the two readings differ by about bf16 precision in the gradients
+    for n in ("dx", "dW1", "db1", "dWg"):
+        _close(b[n], a[n], 2e-2)
