@@ -55,8 +55,31 @@
  *    accumulates in fp32; the expert GEMMs run on the tcgen05 tensor cores and
  *    need d % 64 == 0 and f % 64 == 0.  dtype MOE_F32: everything fp32 with
  *    fp32 arithmetic on CUDA cores (no TF32).  Logits, gate weights, dw and
- *    every weight / bias gradient are fp32 in both.
+ *    every weight / bias gradient are fp32 in both.  The router (logits and
+ *    its backward) runs on CUDA cores in fp32: the tensor cores are used only
+ *    for the expert GEMMs unless MOE_ROUTER_TENSOR_CORES=1 (below).
  *  - Limits: T * k < 2^31, 1 <= k <= min(E, 16), 1 <= E <= 256.
+ *
+ * Environment variables (all optional)
+ * ------------------------------------
+ *  MOE_WAIT_TIMEOUT_NS      bound on every device-side wait, ns (default 1e9;
+ *                           read once per process).
+ *  The rest are read at every call:
+ *  MOE_ROUTER_TENSOR_CORES  "1": bf16 router logits (d % 64 == 0) as one more
+ *                           segment of the tcgen05 grouped GEMM with an fp32
+ *                           epilogue instead of the CUDA-core kernel.
+ *  MOE_GEMM_PAIR            "0": the expert GEMMs use single CTAs (128 x 256
+ *                           tiles) instead of CTA pairs (256 x 256).
+ *  MOE_GEMM_MAX_UNITS       n > 0: at most n CTAs (or CTA pairs) per expert
+ *                           GEMM launch; each then walks more tiles.  For
+ *                           tests; results are the same for every n.
+ *  MOE_DEBUG_GEMM_WITHHOLD  "u:kb", for tests of the timeout path only: in
+ *                           every expert GEMM launch, the producer of the CTA
+ *                           (pair) holding work unit u stops before K block kb
+ *                           and issues nothing more; that CTA's bounded wait
+ *                           runs out, it writes MOE_ERR_TIMEOUT to *dev_status,
+ *                           drains what it issued, frees its tensor memory and
+ *                           exits.  The call's outputs are then incomplete.
  */
 #ifndef MOE_H_
 #define MOE_H_
@@ -108,6 +131,11 @@ MOE_API const char* moe_status_string(moe_status s);
 MOE_API size_t moe_workspace_size(const moe_shape* s);
 
 /* A1 + A2 + A3: router logits, softmax top-k gate and stable dispatch.
+ * Source: the gating network decides each token's experts, and tokens are
+ * assigned to their target experts in order with no dispatch mask ("ES-MoE",
+ * review, section 3 "dynamic expert placement" and "expert-wise offloading
+ * and processing"); the gate formula and tie rule are this library's reading
+ * (header above).
  *   x       [T,d] dtype            tokens
  *   Wg      [E,d] dtype            router weight
  *   logit_bias [E] fp32 or NULL    fixed per-expert additive logit shift
@@ -135,12 +163,19 @@ MOE_API moe_status moe_route(const moe_shape* s, const void* x, const void* Wg,
                      int32_t* pos, int32_t* perm, void* ws, int32_t* dev_status,
                      moe_stream_t stream);
 
-/* A4: X_perm[pos[t*k+j]] = x[t].   x [T,d], X_perm [T*k,d], dtype. */
+/* A4: X_perm[pos[t*k+j]] = x[t].   x [T,d], X_perm [T*k,d], dtype.
+ * Source: the scatter half of the scatter/gather layout that batches the
+ * inputs by expert ("FastMoE", review, "proposed method"); the token
+ * permutation stage of "ES-MoE", review, section 3. */
 MOE_API moe_status moe_permute(const moe_shape* s, const void* x, const int32_t* pos,
                        void* x_perm, moe_stream_t stream);
 
 /* A5: expert FFN forward over the contiguous expert segments
  * [offsets[e], offsets[e+1]) of X_perm (offsets as produced by moe_route).
+ * Source: each expert runs over only its own tokens, with no zero padding
+ * ("ES-MoE", review, section 3 and section 4 table row "sequential
+ * processing"); the per-expert Linear-GELU-Linear of FMoETransformerMLP /
+ * FMoELinear ("FastMoE", review, "proposed method").
  *   W1 [E,f,d], b1 [E,f] (or NULL = 0), W2 [E,d,f], b2 [E,d] (or NULL), dtype
  *   with h = X W1[e]^T + b1[e], the pre-activation (not stored):
  *   G  [T*k,f] out  GELU'(h), kept for the backward (the only use of h there)
@@ -154,19 +189,22 @@ MOE_API moe_status moe_expert_ffn_fwd(const moe_shape* s, const void* x_perm,
                               moe_stream_t stream);
 
 /* A6 (w != NULL): y[t] = sum_j w[t,j] * y_perm[pos[t,j]], j ascending, fp32
- * accumulation.  A9 (w == NULL): the permute backward, y[t] = sum_j
+ * accumulation.  Source: the gather half of the scatter/gather layout
+ * ("FastMoE", review, "proposed method"), weighted by the gate.  A9 (w == NULL): the permute backward, y[t] = sum_j
  * y_perm[pos[t,j]].   y_perm [T*k,d], y [T,d], dtype. */
 MOE_API moe_status moe_combine_fwd(const moe_shape* s, const void* y_perm, const int32_t* pos,
                            const float* w, void* y, moe_stream_t stream);
 
-/* A7: combine backward.
+/* A7: combine backward (the chain rule through A6; the pages describe the
+ * backward only as each expert's backward pass, "ES-MoE", review, section 3).
  *   dy_perm[pos[t,j]] = w[t,j] * dy[t]            [T*k,d] dtype out
  *   dw[t,j]           = <dy[t], y_perm[pos[t,j]]> [T,k]   fp32  out */
 MOE_API moe_status moe_combine_bwd(const moe_shape* s, const void* dy, const void* y_perm,
                            const int32_t* pos, const float* w, void* dy_perm, float* dw,
                            moe_stream_t stream);
 
-/* A8: expert FFN backward over the same segments.
+/* A8: expert FFN backward over the same segments (each expert's backward
+ * pass over its own tokens, "ES-MoE", review, section 3).
  *   dA = dY W2[e];  dH = dA * G (G = GELU'(h) from moe_expert_ffn_fwd);
  *   dx_perm = dH W1[e]
  *   dW2[e] (+)= dY^T A,  db2[e] (+)= sum_rows dY
@@ -182,7 +220,9 @@ MOE_API moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, c
                               float* db1, float* dW2, float* db2, int accumulate, void* ws,
                               int32_t* dev_status, moe_stream_t stream);
 
-/* A10: router backward.  dL = d(gate weights)/d(logits)^T dw:
+/* A10: router backward (the gating network is trained with the model,
+ * "ES-MoE", review, section 3; the formulas are the chain rule through this
+ * library's gate).  dL = d(gate weights)/d(logits)^T dw:
  *   renorm: dL[idx_j] = w_j (dw_j - sum_i w_i dw_i), zero elsewhere;
  *   else:   dL[e] = sum_j dw_j p[idx_j] (delta(e, idx_j) - p[e]), p = softmax(L).
  *   dx[t]   = [sum_j dx_perm[pos[t,j]]]  +  sum_e dL[t,e] Wg[e]
@@ -215,7 +255,9 @@ MOE_API moe_status moe_route_bwd(const moe_shape* s, const float* dw, const floa
  *     larger shapes return MOE_ERR_UNSUPPORTED without launching anything.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.  A failure there returns MOE_ERR_CUDA.
+ *     before any stream capture.  A failure there returns MOE_ERR_CUDA.  The
+ *     address is looked up again when the device's context has changed since
+ *     (after cudaDeviceReset), so that a new context never gets a stale one.
  *   - The library allocates and frees nothing on this path.
  *   - All calls share the one array and leave their contents in it; every
  *     entry a call reads is written earlier by the same call, so nothing needs

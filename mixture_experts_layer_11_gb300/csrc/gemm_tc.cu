@@ -126,6 +126,11 @@ struct TcParams {
     int accumulate;
     int32_t* status;
     uint64_t limit_ns;
+    // Test hook (MOE_DEBUG_GEMM_WITHHOLD): the even CTA's producer stops before
+    // issuing K block withhold_kb of work unit withhold_unit (neither its
+    // expect_tx nor its loads), so the MMA warp's bounded wait on that stage
+    // runs out and the CTA takes its timeout teardown.  -1: off.
+    int withhold_unit, withhold_kb;
 };
 
 template <int STAGES> struct Ctrl {
@@ -499,6 +504,13 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             for (int t = unit0; t < num_units && ok; t += nunits) {
                 const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
                 for (int kb = 0; kb < ti.num_kb; ++kb) {
+                    if (leader && t == p.withhold_unit && kb == p.withhold_kb) {
+                        // test hook: issue nothing more (no copy is left in
+                        // flight for this stage); the copies already issued are
+                        // waited for below
+                        ok = false;
+                        break;
+                    }
                     if (!mbar_wait_bounded(smem_u32(&c.empty[stage]), phase ^ 1, p.limit_ns,
                                            &c.abort_flag)) {
                         raise_abort(c, p);
@@ -1032,13 +1044,36 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
     return r == CUDA_SUCCESS;
 }
 
-// Which CTA shape to use: CTA pairs unless MOE_GEMM_PAIR=0 selects single CTAs.
+// Launch options read from the environment at every launch (so that a test
+// can change them between calls):
+//   MOE_GEMM_PAIR=0        single CTAs (128 x 256 tiles) instead of CTA pairs;
+//   MOE_GEMM_MAX_UNITS=n   at most n CTAs (or pairs) per launch, so that each
+//                          walks more tiles of the static tile list;
+//   MOE_DEBUG_GEMM_WITHHOLD=u:kb  test hook, see TcParams::withhold_unit.
 bool use_pairs() {
-    static const bool v = [] {
-        const char* s = getenv("MOE_GEMM_PAIR");
-        return !(s && s[0] == '0');
-    }();
-    return v;
+    const char* s = getenv("MOE_GEMM_PAIR");
+    return !(s && s[0] == '0');
+}
+
+int64_t max_units_override() {
+    const char* s = getenv("MOE_GEMM_MAX_UNITS");
+    if (!s || !*s) return 0;
+    const long long v = strtoll(s, nullptr, 10);
+    return v > 0 ? (int64_t)v : 0;
+}
+
+void withhold_hook(TcParams& p) {
+    p.withhold_unit = -1;
+    p.withhold_kb = -1;
+    const char* s = getenv("MOE_DEBUG_GEMM_WITHHOLD");
+    if (!s || !*s) return;
+    char* end = nullptr;
+    const long u = strtol(s, &end, 10);
+    if (end == s || *end != ':') return;
+    const long kb = strtol(end + 1, nullptr, 10);
+    if (u < 0 || kb < 0) return;
+    p.withhold_unit = (int)u;
+    p.withhold_kb = (int)kb;
 }
 
 template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool PAIR>
@@ -1076,7 +1111,10 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
         }
     });
     if (attr_err != cudaSuccess) return attr_err;
-    const int64_t units = units_upper < max_units ? (units_upper > 0 ? units_upper : 1) : max_units;
+    int64_t cap = max_units;
+    const int64_t ov = max_units_override();
+    if (ov > 0 && ov < cap) cap = ov;
+    const int64_t units = units_upper < cap ? (units_upper > 0 ? units_upper : 1) : cap;
     if (!PAIR) {
         kern<<<(unsigned)units, THREADS, SMEM, st>>>(a, b, o0, o1, p);
         return cudaGetLastError();
@@ -1097,10 +1135,10 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
 }
 
 template <bool VAR_K, bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_either(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
-                          const CUtensorMap& o1, const TcParams& p, int64_t units1,
-                          int64_t units2, cudaStream_t st) {
-    if (use_pairs()) return launch_tc<VAR_K, A_MN, B_MN, EPI, true>(a, b, o0, o1, p, units2, st);
+cudaError_t launch_either(bool pair, const CUtensorMap& a, const CUtensorMap& b,
+                          const CUtensorMap& o0, const CUtensorMap& o1, const TcParams& p,
+                          int64_t units1, int64_t units2, cudaStream_t st) {
+    if (pair) return launch_tc<VAR_K, A_MN, B_MN, EPI, true>(a, b, o0, o1, p, units2, st);
     return launch_tc<VAR_K, A_MN, B_MN, EPI, false>(a, b, o0, o1, p, units1, st);
 }
 
@@ -1191,6 +1229,7 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     p.E = g.E; p.N = g.N; p.K = g.K; p.M = 0; p.P = g.P;
     p.offsets = g.offsets; p.bias = g.bias; p.aux = g.aux; p.out0 = g.out0; p.out1 = g.out1;
     p.outf = nullptr; p.accumulate = 0; p.status = status; p.limit_ns = wait_limit_ns();
+    withhold_hook(p);
     const bool colsum = g.epi == Epi::ScaleAux && g.colsum != nullptr;
     if (colsum && !g.colsum_partial) return cudaErrorInvalidValue;
     p.cpart = colsum ? g.colsum_partial : nullptr;
@@ -1204,7 +1243,7 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     CUtensorMap mo0, mo1;
     if (logits) {   // fp32 output, stored by the epilogue warps
         memset(&mo0, 0, sizeof(mo0));
-        return launch_either<false, false, false, (int)Epi::Logits>(ma, mb, mo0, mo0, p, u1, u2,
+        return launch_either<false, false, false, (int)Epi::Logits>(pair, ma, mb, mo0, mo0, p, u1, u2,
                                                                     st);
     }
     if (!make_out_map(&mo0, g.out0, g.P, g.N, cw)) return cudaErrorInvalidValue;
@@ -1218,16 +1257,16 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     switch (g.epi) {
         case Epi::BiasGelu:
             if (!g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_either<false, false, false, (int)Epi::BiasGelu>(ma, mb, mo0, mo1, p, u1,
+            return launch_either<false, false, false, (int)Epi::BiasGelu>(pair, ma, mb, mo0, mo1, p, u1,
                                                                           u2, st);
         case Epi::Bias:
             if (!g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_either<false, false, false, (int)Epi::Bias>(ma, mb, mo0, mo1, p, u1, u2,
+            return launch_either<false, false, false, (int)Epi::Bias>(pair, ma, mb, mo0, mo1, p, u1, u2,
                                                                       st);
         case Epi::ScaleAux: {
             if (g.weight_kmajor) return cudaErrorInvalidValue;
             cudaError_t e = launch_either<false, false, true, (int)Epi::ScaleAux>(
-                ma, mb, mo0, mo1, p, u1, u2, st);
+                pair, ma, mb, mo0, mo1, p, u1, u2, st);
             if (e != cudaSuccess || !colsum) return e;
             colsum_mtile_reduce_kernel<<<dim3((unsigned)g.E, (unsigned)((g.N + 31) / 32)), 256,
                                          0, st>>>(g.N, g.E, g.offsets, pair ? 2 * BM : BM,
@@ -1237,7 +1276,7 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
         }
         case Epi::Plain:
             if (g.weight_kmajor) return cudaErrorInvalidValue;
-            return launch_either<false, false, true, (int)Epi::Plain>(ma, mb, mo0, mo1, p, u1, u2,
+            return launch_either<false, false, true, (int)Epi::Plain>(pair, ma, mb, mo0, mo1, p, u1, u2,
                                                                       st);
     }
     return cudaErrorInvalidValue;
@@ -1272,6 +1311,7 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
     p.E = g.E; p.M = g.M; p.N = g.N; p.K = 0; p.P = g.P;
     p.offsets = g.offsets; p.outf = g.out; p.accumulate = g.accumulate;
     p.status = status; p.limit_ns = wait_limit_ns();
+    withhold_hook(p);
     p.bsum = g.bsum;
     const int64_t NT = (g.N + BN - 1) / BN + (g.bsum ? 1 : 0);
     const int64_t u1 = (int64_t)g.E * ((g.M + BM - 1) / BM) * NT;
@@ -1286,7 +1326,7 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
                       CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
             return cudaErrorInvalidValue;
     }
-    return launch_either<true, true, true, (int)Epi::Plain>(ma, mb, mo, mo, p, u1, u2, st);
+    return launch_either<true, true, true, (int)Epi::Plain>(pair, ma, mb, mo, mo, p, u1, u2, st);
 }
 
 }  // namespace moe

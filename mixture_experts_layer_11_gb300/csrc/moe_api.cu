@@ -1,5 +1,6 @@
 // moe_api.cu -- the C ABI of include/moe.h: argument validation, workspace
 // carving, and the launch sequence of each step on the caller's stream.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -285,18 +286,50 @@ static __device__ __align__(256) int32_t g_route_noalloc_scratch[MOE_ROUTE_NOALL
 
 namespace {
 
-// Device address of the scratch array on the current device, looked up on the
-// first call for that device (nullptr if the lookup fails).
+// Unique id of the calling thread's current CUDA context (0 if none or if the
+// driver cannot tell), through the driver entry points the runtime exposes.
+unsigned long long current_context_id() {
+    typedef CUresult (*GetCurrent)(CUcontext*);
+    typedef CUresult (*GetId)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the scratch array in the current device's context.  It is
+// looked up (cudaGetSymbolAddress, with that device current) on the first call
+// for the device, and again when the context has changed since (after a
+// cudaDeviceReset the old address would be stale).  nullptr if the lookup
+// fails.
 int32_t* route_noalloc_scratch() {
     static std::mutex mu;
     static int32_t* addr[64] = {};
+    static unsigned long long ctx_of[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+    const unsigned long long ctx = current_context_id();
+    if (addr[dev] == nullptr || ctx == 0 || ctx != ctx_of[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_route_noalloc_scratch) != cudaSuccess) return nullptr;
         addr[dev] = static_cast<int32_t*>(p);
+        ctx_of[dev] = current_context_id();   // the lookup made the context current
     }
     return addr[dev];
 }

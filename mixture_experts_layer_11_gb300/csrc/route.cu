@@ -16,6 +16,7 @@
 // Positions are therefore a pure function of idx: deterministic and stable.
 #include <float.h>
 #include <limits.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -992,11 +993,20 @@ cudaError_t launch_debug_gelu(int64_t n, const float* x, float* g, float* gd, in
 
 // ---- launchers -----------------------------------------------------------------------
 
+// The router runs on CUDA cores (fp32 FMA): the tensor cores are kept for the
+// expert GEMMs.  MOE_ROUTER_TENSOR_CORES=1 (read at every call) opts into
+// computing bf16 logits as one more segment of the tcgen05 grouped GEMM with
+// an fp32 epilogue (d % 64 == 0), which costs little more than the read of x.
+static bool router_on_tensor_cores() {
+    const char* v = getenv("MOE_ROUTER_TENSOR_CORES");
+    return v && v[0] == '1';
+}
+
 cudaError_t launch_route_gate(const moe_shape& s, const void* x, const void* Wg,
                              const float* beta, float* logits, int compute_logits, int32_t* idx,
                              float* w, int32_t* block_counts, int32_t* status, cudaStream_t st) {
     const bool bf = s.dtype == MOE_BF16;
-    if (compute_logits && bf && s.d % 64 == 0) {
+    if (compute_logits && bf && s.d % 64 == 0 && router_on_tensor_cores()) {
         // bf16 logits on the tensor cores (fp32 accumulation), then the gate
         GemmVarM g{1, s.E, s.d, s.T, nullptr, x, Wg, true, Epi::Logits, beta, nullptr, logits,
                    nullptr};

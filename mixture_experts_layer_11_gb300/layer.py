@@ -35,7 +35,6 @@ arithmetic of its own.
 """
 from __future__ import annotations
 
-import math
 from typing import Optional
 
 import torch
@@ -260,15 +259,3 @@ class LayerPass:
         if code != ops.MOE_OK:
             raise ops.MoEError("device", code, ops.moe_status_string(code))
 
-
-def expert_flops(T: int, d: int, f: int, k: int) -> float:
-    """Algorithmic expert FLOPs of forward + backward: 12 T k d f."""
-    return 12.0 * T * k * d * f
-
-
-def router_flops(T: int, d: int, E: int) -> float:
-    return 6.0 * T * d * E
-
-
-def _ceil(a: int, b: int) -> int:
-    return math.ceil(a / b)

@@ -1,7 +1,13 @@
 """GPU parity of the grouped expert FFN, forward (A5) and backward (A8),
 against the oracle: tcgen05 tensor-core path for bf16, CUDA-core path for
 fp32.  Segments come from the oracle's dispatch of a seeded routing and
-include empty experts, ragged segment ends and partial N / K tiles."""
+include empty experts, ragged segment ends and partial N / K tiles.
+
+The bf16 cases run in three launch shapes: CTA pairs with the full grid;
+CTA pairs capped at two per launch (MOE_GEMM_MAX_UNITS=2), so that each pair
+walks many tiles of the static tile list and the epilogue's cross-tile state
+(bias and GELU' operands streamed one tile ahead, the GELU' ring) is used
+at every tile boundary; and single CTAs (MOE_GEMM_PAIR=0)."""
 import numpy as np
 import pytest
 import torch
@@ -28,14 +34,23 @@ CASES = [  # dtype, T, d, f, E, k, zipf
     ("bf16", 700, 192, 320, 16, 1, 1.2),     # empty experts, partial N tiles
     ("bf16", 2048, 768, 1024, 4, 2, None),
     ("bf16", 600, 128, 64, 64, 4, 1.1),
-    ("bf16", 4096, 128, 256, 8, 1, 2.0),     # one expert takes most rows: split K ranges
+    ("bf16", 4096, 128, 256, 8, 1, 2.0),     # one expert takes most rows: long K in wgrad
     ("f32", 256, 64, 128, 4, 1, None),
     ("f32", 333, 96, 40, 6, 2, 1.2),
 ]
 
 
+SHAPES = {"pairs": {}, "pairs_2_units": {"MOE_GEMM_MAX_UNITS": "2"},
+          "single_cta": {"MOE_GEMM_PAIR": "0"}}
+
+
+@pytest.mark.parametrize("shape", list(SHAPES))
 @pytest.mark.parametrize("dtype,T,d,f,E,k,zipf", CASES)
-def test_expert_ffn_fwd_bwd(dtype, T, d, f, E, k, zipf):
+def test_expert_ffn_fwd_bwd(dtype, T, d, f, E, k, zipf, shape, monkeypatch):
+    if dtype != "bf16" and shape != "pairs":
+        pytest.skip("the launch shapes are those of the tensor-core path")
+    for n, v in SHAPES[shape].items():
+        monkeypatch.setenv(n, v)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     rb = dtype == "bf16"
     counts, offsets = _segments(T, E, k, zipf, seed=T * 7 + E)

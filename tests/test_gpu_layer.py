@@ -157,3 +157,50 @@ def test_layer_recompute_equals_saved(name, kw):
     lp.check_status()
     for n in OUTPUTS:
         assert torch.equal(getattr(saved, n), getattr(lp, n)), n
+
+
+@pytest.mark.parametrize("name", [n for n in SMALL if n != "tiny_f32"])
+def test_layer_identical_logits_many_tiles_per_pair(name, monkeypatch):
+    """The small workloads with every expert GEMM launch capped at three CTA
+    pairs, so that each pair walks several tiles (the full-size launch paths
+    at sizes the oracle finishes in seconds)."""
+    monkeypatch.setenv("MOE_GEMM_MAX_UNITS", "3")
+    test_layer_identical_logits(name)
+
+
+def test_layer_recompute_identical_logits():
+    """Recompute mode (only the routing kept; the backward re-runs each chunk's
+    permute and expert forward) against the oracle, on five dispatch chunks."""
+    cfg = synth.CONFIGS["longctx128_bf16"].scaled(T=2300, d=512, f=256, chunk=512)
+    inp = synth.make_inputs(cfg, seed=12, random_bias=True)
+    L = torch.from_numpy(oracle.router_logits(inp["x"], inp["Wg"], inp["beta"])).float()
+    ref = oracle.layer(inp, cfg.k, cfg.renorm, True, chunk=cfg.chunk, logits=L.double().numpy())
+    g = to_dev(inp, DEV)
+    lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
+                   chunk=cfg.chunk, device=DEV, recompute=True)
+    assert lp.recompute and len(lp.chunks) == 5
+    lp.forward(g["x"], g["Wg"], g["W1"], g["b1"], g["W2"], g["b2"], g["beta"],
+               compute_logits=False, logits=L.to(DEV))
+    lp.backward(g["dy"], g["x"], g["Wg"], g["W1"], g["W2"])
+    torch.cuda.synchronize()
+    lp.check_status()
+    assert_equal("idx", lp.idx, ref["idx"])
+    for ci, (c0, c1) in enumerate(lp.chunks):
+        assert_equal(f"perm[{ci}]", lp.perm[c0 * cfg.k:c1 * cfg.k], ref["perm"][ci])
+    for n in ("y", "dx", "dw", "dW1", "db1", "dW2", "db2", "dWg"):
+        assert_close(n, getattr(lp, n), ref[n], cfg.dtype)
+
+
+@pytest.mark.parametrize("name", ["moe_s_bf16", "longctx128_bf16"])
+def test_layer_meets_the_h_storage_reading(name):
+    """The kernels store G = GELU'(h) in bf16.  The other plain reading of the
+    bf16 configurations stores h itself and takes GELU' of it in the backward;
+    the GPU's results must meet the same tolerance against that oracle too."""
+    cfg = synth.CONFIGS[name].scaled(**SMALL[name])
+    inp = synth.make_inputs(cfg, seed=4, random_bias=True)
+    L = torch.from_numpy(oracle.router_logits(inp["x"], inp["Wg"], inp["beta"])).float()
+    ref = oracle.layer(inp, cfg.k, cfg.renorm, True, chunk=cfg.chunk, logits=L.double().numpy(),
+                       store_h=True)
+    lp = _run(cfg, inp, logits=L)
+    for n in ("y", "dx", "dw", "dW1", "db1", "dW2", "db2", "dWg"):
+        assert_close(n, getattr(lp, n), ref[n], cfg.dtype)
