@@ -547,6 +547,12 @@ def dispatch_roofline(cfg, res, pk):
         byt = dispatch_bytes(cfg, kind, T)
         per[kind] = {"ms_per_step": ms, "bytes_per_step": byt,
                      "gbs": byt / (ms / 1e3) / 1e9, "frac": byt / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+    if "moe_route" in calls:
+        ms, T = calls["moe_route"]
+        fl = 2.0 * T * cfg.d * cfg.E
+        per["route"] = {"ms_per_step": ms, "logits_flops_per_step": fl,
+                        "tflops": fl / (ms / 1e3) / 1e12,
+                        "note": "router logits (CUDA cores), gate, histogram, scan, rank"}
     main = [per[k] for k in ("permute", "combine", "combine_bwd") if k in per]
     byt = sum(p["bytes_per_step"] for p in main)
     ms = sum(p["ms_per_step"] for p in main)
