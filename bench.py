@@ -48,23 +48,32 @@ L2_FLUSH_BYTES = 256 << 20
 ROUTER_TC_ENV = "MOE_ROUTER_TENSOR_CORES"
 
 
-def launches_per_chunk(cfg, router_tc: bool) -> int:
-    """Library kernels one dispatch chunk of a step launches.
-    Route: the tensor-core logits (bf16, d_model % 64 == 0, opt-in) or the
-    CUDA-core logits kernel, then the gate, the scan and the rank (4); the
-    CUDA-core router fuses logits and gate for E <= 32 (3).  Permute (1); two
-    expert GEMMs (2); combine (1); combine backward (1).  Expert backward: bf16
-    has the dH GEMM + its db1 reduction, the dX GEMM and two weight-gradient
-    GEMMs (db2 inside the dW2 one) = 5; fp32 has four GEMMs and two column
-    sums of two kernels each = 8.  Router backward: with renorm, dx with the
-    permute backward fused in and dWg (2 kernels) = 3; without (dense gate
-    Jacobian), dL, the tiled dx product with the permute backward, and dWg (2
-    kernels) = 4."""
-    tc = router_tc and cfg.dtype == "bf16" and cfg.d % 64 == 0
+def launches_per_step(cfg, nchunks: int, router_tc: bool, recompute: bool, defer: bool) -> int:
+    """Library kernels one step launches.
+    Per dispatch chunk.  Route: the tensor-core logits (bf16, d_model % 64 ==
+    0, opt-in) or the CUDA-core logits kernel, then the gate, the scan and the
+    rank (4); the CUDA-core router fuses logits and gate for E <= 32 (3).
+    Permute (1); two expert GEMMs (2); combine (1); combine backward (1).
+    Expert backward, bf16: the dH GEMM + its db1 reduction and the dX GEMM (3),
+    and unless the weight gradients are deferred, the two weight-gradient
+    GEMMs (db2 inside the dW2 one) (2); fp32: dH and dX GEMMs and db1's column
+    sum of two kernels (4), plus two weight-gradient GEMMs and db2's column sum
+    (4).  Router backward: with renorm, dx with the permute backward fused in
+    and dWg (2 kernels) = 3; without (dense gate Jacobian), dL, the tiled dx
+    product with the permute backward, and dWg (2 kernels) = 4.  Recompute
+    re-runs the permute and the two forward GEMMs (3).
+    Deferred weight gradients: once per step, the two weight-gradient GEMMs
+    (bf16), or per chunk two GEMMs and db2's column sum (fp32)."""
+    bf = cfg.dtype == "bf16"
+    tc = router_tc and bf and cfg.d % 64 == 0
     route = 4 if (tc or cfg.E > 32) else 3
-    ffn_bwd = 5 if cfg.dtype == "bf16" else 8
+    data = 3 if bf else 4
+    wgrad = 2 if bf else 4
     route_bwd = 3 if cfg.renorm else 4
-    return route + 1 + 2 + 1 + 1 + ffn_bwd + route_bwd
+    per_chunk = route + 1 + 2 + 1 + 1 + data + (0 if defer else wgrad) + route_bwd
+    per_chunk += 3 if recompute else 0
+    per_step = (2 if bf else 4 * nchunks) if defer else 0
+    return per_chunk * nchunks + per_step
 
 
 def workload_desc(cfg) -> str:
@@ -280,7 +289,10 @@ def whole_job_rate(tokens_per_rank_step: int, steps: int, world: int, ms: float)
 # ---- device timing of one workload ---------------------------------------------------------
 
 CALLS = ("moe_route", "moe_permute", "moe_expert_ffn_fwd", "moe_combine_fwd",
-         "moe_combine_bwd", "moe_expert_ffn_bwd", "moe_route_bwd")
+         "moe_combine_bwd", "moe_expert_ffn_bwd", "moe_expert_ffn_bwd_data",
+         "moe_expert_ffn_bwd_weights", "moe_route_bwd")
+GEMM_CALLS = ("moe_expert_ffn_fwd", "moe_expert_ffn_bwd", "moe_expert_ffn_bwd_data",
+              "moe_expert_ffn_bwd_weights")
 
 
 class CallTimer:
@@ -332,7 +344,7 @@ def _sum_ms(marks):
 
 
 def measure(cfg, dev, steps, warmup, *, pipeline=True, graph=True, router_tc=False,
-            recompute=False, sampler=None, e2e=False, dist=None, seed=0):
+            recompute=False, defer_wgrad=None, sampler=None, e2e=False, dist=None, seed=0):
     """Times `steps` layer steps of one workload.  Returns a dict of measured
     values; with e2e also the end-to-end rate through host buffers."""
     from mixture_experts_layer_11_gb300.layer import LayerPass
@@ -342,8 +354,8 @@ def measure(cfg, dev, steps, warmup, *, pipeline=True, graph=True, router_tc=Fal
     else:
         os.environ.pop(ROUTER_TC_ENV, None)
     try:
-        return _measure(cfg, dev, steps, warmup, pipeline, graph, router_tc, recompute, sampler,
-                        e2e, dist, seed, LayerPass)
+        return _measure(cfg, dev, steps, warmup, pipeline, graph, router_tc, recompute,
+                        defer_wgrad, sampler, e2e, dist, seed, LayerPass)
     finally:
         if prev is None:
             os.environ.pop(ROUTER_TC_ENV, None)
@@ -351,12 +363,13 @@ def measure(cfg, dev, steps, warmup, *, pipeline=True, graph=True, router_tc=Fal
             os.environ[ROUTER_TC_ENV] = prev
 
 
-def _measure(cfg, dev, steps, warmup, pipeline, graph_on, router_tc, recompute, sampler, e2e,
-             dist, seed, LayerPass):
+def _measure(cfg, dev, steps, warmup, pipeline, graph_on, router_tc, recompute, defer_wgrad,
+             sampler, e2e, dist, seed, LayerPass):
     torch.cuda.reset_peak_memory_stats(dev)
     inp = synth.make_inputs(cfg, seed=seed, device=str(dev))
     lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
-                   chunk=cfg.chunk, device=dev, pipeline=pipeline, recompute=recompute)
+                   chunk=cfg.chunk, device=dev, pipeline=pipeline, recompute=recompute,
+                   defer_wgrad=defer_wgrad)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     x_buf, dy_buf = inp["x"], inp["dy"]
@@ -420,10 +433,9 @@ def _measure(cfg, dev, steps, warmup, pipeline, graph_on, router_tc, recompute, 
     res.update(total_ms=sum(step_ms), steps=steps, wall_s=wall, chunks=len(lp.chunks),
                calls={n: (ms / steps, tok // steps) for n, (ms, tok) in calls.items()},
                device_memory_gib=torch.cuda.max_memory_allocated(dev) / 2**30,
-               pipelined=lp.pipeline,
-               # recompute: the backward re-runs each chunk's permute and two expert GEMMs
-               launches=(launches_per_chunk(cfg, router_tc) + (3 if recompute else 0))
-               * len(lp.chunks) * steps)
+               pipelined=lp.pipeline, defer_wgrad=lp.defer_wgrad,
+               launches=launches_per_step(cfg, len(lp.chunks), router_tc, recompute,
+                                          lp.defer_wgrad) * steps)
     if e2e:
         res["e2e_ms"], res["e2e_steps"] = _end_to_end(cfg, lp, inp, graph, flush, steps, warmup,
                                                       dev)
@@ -522,7 +534,7 @@ def summarize(cfg, res, pk):
            "tflops": (cfg.expert_flops() + cfg.router_flops()) / (ms / 1e3) / 1e12,
            "device_memory_gib": res["device_memory_gib"]}
     calls = res["calls"]
-    gemm_ms = sum(calls.get(n, (0.0, 0))[0] for n in ("moe_expert_ffn_fwd", "moe_expert_ffn_bwd"))
+    gemm_ms = sum(calls.get(n, (0.0, 0))[0] for n in GEMM_CALLS)
     if gemm_ms > 0:
         ach = cfg.expert_flops() / (gemm_ms / 1e3) / 1e12
         out["gemm"] = {"ms_per_step": gemm_ms, "tflops": ach,
@@ -587,7 +599,8 @@ def run_ours(args, cfg):
     # pipelining, one CUDA graph per step; clocks sampled over the timed steps
     sampler = ClockSampler(local)
     main = measure(cfg, dev, args.steps, args.warmup, sampler=sampler, e2e=True, dist=dist,
-                   seed=rank, graph=not args.no_graph, recompute=args.recompute)
+                   seed=rank, graph=not args.no_graph, recompute=args.recompute,
+                   defer_wgrad=False if args.per_chunk_wgrad else None)
     total_ms, e2e_ms = max_over_ranks([main["total_ms"], main["e2e_ms"]], dist, dev)
     if rank != 0:
         if dist:
@@ -605,8 +618,12 @@ def run_ours(args, cfg):
               "note": "router logits as one segment of the tcgen05 grouped GEMM "
                       f"({ROUTER_TC_ENV}=1); not the default: the tensor cores are reserved "
                       "for the expert GEMMs"}
-    # ---- dispatch kernels timed on one stream
-    disp = dispatch_roofline(cfg, measure(cfg, dev, sub_steps, sub_warm, pipeline=False), pk)
+    # ---- every call timed on one stream (the dispatch kernels' HBM fraction)
+    serial = measure(cfg, dev, sub_steps, sub_warm, pipeline=False,
+                     defer_wgrad=False if args.per_chunk_wgrad else None)
+    disp = dispatch_roofline(cfg, serial, pk)
+    disp["serial_step_ms"] = serial["total_ms"] / serial["steps"]
+    disp["serial_calls_ms_per_step"] = {n: v[0] for n, v in serial["calls"].items()}
     # ---- the other workloads
     per_config = {}
     if not args.no_sub_configs:
@@ -645,6 +662,8 @@ def run_ours(args, cfg):
                               else f"{main['chunks']}, one stream"),
                    "activations": ("recomputed in the backward (routing kept)" if args.recompute
                                    else "kept from the forward for the backward"),
+                   "weight_gradients": ("one pass over all chunks after the backward"
+                                        if main["defer_wgrad"] else "accumulated per chunk"),
                    "parallelism": f"replicas x{world}"},
         "roofline": {
             "bound": "tensor", "kernel": "grouped expert GEMM (tcgen05), all expert FFN calls",
@@ -690,6 +709,9 @@ def main():
     ap.add_argument("--recompute", action="store_true",
                     help="keep only the routing between forward and backward; the backward "
                          "re-runs each chunk's permute and expert forward")
+    ap.add_argument("--per-chunk-wgrad", action="store_true",
+                    help="accumulate the weight gradients chunk by chunk instead of one pass "
+                         "over all chunks after the backward")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's kernels one by one instead of as one CUDA graph")
     ap.add_argument("--no-sub-configs", action="store_true",

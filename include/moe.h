@@ -220,6 +220,61 @@ MOE_API moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, c
                               float* db1, float* dW2, float* db2, int accumulate, void* ws,
                               int32_t* dev_status, moe_stream_t stream);
 
+/* A8, data half, for one dispatch chunk: the activation gradients and db1.
+ *   dA = dY W2[e];  dH = dA * G (G = GELU'(h) from moe_expert_ffn_fwd);
+ *   dx_perm = dH W1[e];  db1[e] (+)= sum_rows dH
+ * dy_perm [T*k,d], G [T*k,f] dtype in; dH [T*k,f] and dx_perm [T*k,d] dtype
+ * out (dH is the caller's, for moe_expert_ffn_bwd_weights); db1 [E,f] fp32,
+ * overwritten (accumulate == 0; experts with no tokens get zeros) or added to.
+ * ws: workspace as for moe_expert_ffn_bwd.  Source: each expert's backward
+ * pass over its own tokens ("ES-MoE", review, section 3). */
+MOE_API moe_status moe_expert_ffn_bwd_data(const moe_shape* s, const void* dy_perm,
+                                           const void* G, const int32_t* offsets,
+                                           const void* W1, const void* W2, void* dH,
+                                           void* dx_perm, float* db1, int accumulate, void* ws,
+                                           int32_t* dev_status, moe_stream_t stream);
+
+/* A8, weight half, over one or more dispatch chunks in one call.
+ *   dW2[e] (+)= dY^T A,  db2[e] (+)= sum_rows dY,  dW1[e] (+)= dH^T X
+ * summed over expert e's rows in every chunk.  For a pass split into dispatch
+ * chunks ("Flattening Every Memory Peak in Long-Context Mixture-of-Experts
+ * Training", abstract: a cap on the tokens of a dispatch chunk) whose rows the
+ * caller keeps, this writes each gradient tile once per pass instead of once
+ * per chunk, and each expert's reduction runs over its rows of all chunks in
+ * chunk order (fp32 accumulation).
+ *   s              d, f, E, k, dtype of the layer (s->T is not used)
+ *   nchunks >= 1, chunk_T  HOST array [nchunks]: tokens of each chunk (>= 0)
+ *   offsets        device int32 [nchunks][offsets_stride]: chunk c's expert
+ *                  offsets (from its moe_route) at c * offsets_stride;
+ *                  offsets_stride >= E+1 and a multiple of 4
+ *   dy_perm, x_perm [R,d], dH, A [R,f] dtype, R = k * sum(chunk_T): chunk c's
+ *                  rows follow chunk c-1's (chunk c holds chunk_T[c] * k rows,
+ *                  in the expert-sorted order of its dispatch)
+ *   dW1 [E,f,d], dW2 [E,d,f], db2 [E,d] fp32: overwritten (accumulate == 0;
+ *                  experts with no rows get zeros) or added to
+ *   ws, ws_bytes   device workspace and its size.  bf16: scratch for the
+ *                  partial tiles of long reductions, which are cut into parts
+ *                  so that a few long (expert, tile) reductions do not leave
+ *                  most SMs idle; the parts are added in a fixed order, so the
+ *                  result is deterministic for a given ws_bytes (any size works,
+ *                  NULL / 0 included; less scratch means coarser parts; the
+ *                  finest split needs moe_expert_ffn_bwd_weights_workspace_size
+ *                  bytes).  fp32: at least moe_expert_ffn_bwd_weights_workspace_size.
+ * R < 2^31. */
+MOE_API moe_status moe_expert_ffn_bwd_weights(const moe_shape* s, int nchunks,
+                                              const int64_t* chunk_T, const int32_t* offsets,
+                                              int offsets_stride, const void* dy_perm,
+                                              const void* x_perm, const void* dH, const void* A,
+                                              float* dW1, float* dW2, float* db2, int accumulate,
+                                              void* ws, size_t ws_bytes, int32_t* dev_status,
+                                              moe_stream_t stream);
+
+/* Workspace bytes for moe_expert_ffn_bwd_weights with these chunks (0 on bad
+ * arguments): the finest split of its reductions (bf16), the column-sum
+ * partials (fp32). */
+MOE_API size_t moe_expert_ffn_bwd_weights_workspace_size(const moe_shape* s, int nchunks,
+                                                         const int64_t* chunk_T);
+
 /* A10: router backward (the gating network is trained with the model,
  * "ES-MoE", review, section 3; the formulas are the chain rule through this
  * library's gate).  dL = d(gate weights)/d(logits)^T dw:

@@ -161,8 +161,19 @@ cudaError_t launch_gemm_varm_simt(const GemmVarM& g, cudaStream_t st) {
 
 cudaError_t launch_gemm_vark_simt(const GemmVarK& g, cudaStream_t st) {
     dim3 grid((unsigned)((g.M + SB - 1) / SB), (unsigned)((g.N + SB - 1) / SB), (unsigned)g.E);
-    gemm_vark_f32_kernel<<<grid, 256, 0, st>>>(g);
-    return cudaGetLastError();
+    // one launch per dispatch chunk, each adding to the previous ones
+    for (int s = 0; s < g.nseg; ++s) {
+        GemmVarK c = g;
+        c.nseg = 1;
+        c.offsets = g.offsets + (int64_t)s * g.ostride;
+        c.act_a = (const float*)g.act_a + g.seg_base[s] * g.M;
+        c.act_b = (const float*)g.act_b + g.seg_base[s] * g.N;
+        c.accumulate = g.accumulate || s > 0;
+        gemm_vark_f32_kernel<<<grid, 256, 0, st>>>(c);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace moe

@@ -15,9 +15,11 @@
 //     the weight stored [E,N,K] (K-major) or [E,K,N] (MN-major); the segment
 //     length varies per expert.  Rows past the segment are computed from
 //     whatever TMA loads there and never stored.
-//   VarK (weight gradient): C_e[M, N] (+)= act_a[seg_e, M]^T act_b[seg_e, N];
-//     the reduction runs over the segment's rows, so rows past the segment in
-//     the last K block are zeroed in shared memory before the MMA reads them.
+//   VarK (weight gradient): C_e[M, N] (+)= act_a[rows_e, M]^T act_b[rows_e, N];
+//     the reduction runs over the expert's rows, which are its segments in one
+//     or more dispatch chunks (chunk s holds the rows seg_base[s] + offsets of
+//     that chunk), walked segment after segment.  Rows past a segment's end
+//     in its last K block are zeroed in shared memory before the MMA reads them.
 //     On a CTA pair each CTA zeroes its own operands: for a segment's last K
 //     block the odd CTA's loads complete on its own stage barrier, its
 //     otherwise idle MMA warp zeroes the tail and then arrives on the even
@@ -59,6 +61,14 @@ constexpr int BK = 64;             // K per stage: one 128-byte swizzle row of b
 constexpr int SLAB_BYTES = 64 * BK * 2;    // one 64-wide MN slab of BK rows
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_E = 256;
+// Weight-gradient split: a (m-tile, n-tile) of an expert whose reduction spans
+// many K blocks is cut into parts of at most kb_part K blocks, so that a few
+// long tiles do not leave most CTA pairs idle at the end of the launch.  The
+// parts aim at kSplitUnitsPerPair work units per pair and have at least
+// kKbPartMin K blocks (about 0.15 ms of MMAs per pair), so that the partial
+// tiles' extra traffic stays small beside their MMA time.
+constexpr int kKbPartMin = 512;
+constexpr int kSplitUnitsPerPair = 32;
 
 template <bool PAIR> struct Shape {
     static constexpr int CTAS = PAIR ? 2 : 1;
@@ -131,7 +141,47 @@ struct TcParams {
     // expect_tx nor its loads), so the MMA warp's bounded wait on that stage
     // runs out and the CTA takes its timeout teardown.  -1: off.
     int withhold_unit, withhold_kb;
+    // VarK: expert e's rows in dispatch chunk s are
+    // [seg_base[s] + offsets[s*ostride + e], seg_base[s] + offsets[s*ostride + e + 1]).
+    int nseg, ostride;
+    int64_t seg_base[kMaxWgradChunks];
+    // VarK split: slots for partial tiles in the scratch map (0: no split),
+    // and the number of CTA pairs of the launch (the split's unit target)
+    int64_t part_cap;
+    int split_units;
+    float* bpart;            // VarK split: row sums of all-ones tiles of parts > 0
 };
+
+// K blocks per part of the split weight-gradient tiles (INT_MAX: no split):
+// the smallest power of two >= kKbPartMin giving about kSplitUnitsPerPair
+// units per pair, doubled until the partial tiles fit in `cap` slots.  kbs[e]
+// is expert e's K-block count; MT x NT real tiles per expert.  Every kernel
+// that needs the split computes it with this same function.
+__device__ __forceinline__ int vark_kb_part(const int* kbs, int E, int MT, int NT, int nunits,
+                                            int64_t cap) {
+    if (cap <= 0) return INT_MAX;
+    int64_t tot = 0;
+    int kmax = 0;
+    for (int e = 0; e < E; ++e) {
+        tot += kbs[e];
+        kmax = kbs[e] > kmax ? kbs[e] : kmax;
+    }
+    tot *= (int64_t)MT * NT;
+    const int64_t want = tot / ((int64_t)kSplitUnitsPerPair * (nunits > 0 ? nunits : 1));
+    int kp = kKbPartMin;
+    while (kp < want && kp < kmax) kp *= 2;
+    while (kp < kmax) {
+        int64_t slots = 0;
+        for (int e = 0; e < E; ++e)
+            if (kbs[e] > kp) slots += (int64_t)((kbs[e] + kp - 1) / kp - 1) * MT * NT;
+        if (slots <= cap) break;
+        kp *= 2;
+    }
+    return kp >= kmax ? INT_MAX : kp;
+}
+__device__ __forceinline__ int vark_nsplit(int kb, int kp) {
+    return kb > kp ? (kb + kp - 1) / kp : 1;
+}
 
 template <int STAGES> struct Ctrl {
     uint64_t full[STAGES];
@@ -144,8 +194,11 @@ template <int STAGES> struct Ctrl {
     int abort_flag;
     int nactive;
     int off[MAX_E + 1];
-    int tile_start[MAX_E + 1];   // VarM: first tile of each expert
+    int tile_start[MAX_E + 1];   // VarM: first tile of each expert; VarK: K blocks of each
     int order[MAX_E];            // VarK: experts by descending row count
+    int ustart[MAX_E + 1];       // VarK: first unit of each position of `order`
+    int sbase[MAX_E];            // VarK: first scratch slot of each expert's split parts
+    int kb_part;                 // VarK: K blocks per split part (INT_MAX: none)
 };
 
 template <bool PAIR, bool VAR_K, int EPI>
@@ -158,9 +211,53 @@ constexpr size_t smem_bytes() {
 
 struct Tile {
     int e, mt, nt, num_kb;
-    int row0;     // VarM: first row of this CTA's part; VarK: first row of the segment
-    int rows;     // VarM: valid rows of this CTA's part (may be <= 0); VarK: segment rows
+    int row0;     // VarM: first row of this CTA's part; VarK: unused
+    int rows;     // VarM: valid rows of this CTA's part (may be <= 0); VarK: the expert's rows
     bool ones;    // VarK: the extra tile against the all-ones B (row sums of act_a)
+    int kb0;      // VarK: first K block of this part
+    int slot;     // VarK: scratch slot of a split part > 0, else -1 (written to the output)
+    int bslot;    // VarK: scratch row-sum slot of an all-ones tile of a part > 0, else -1
+};
+
+// VarK: walks an expert's K blocks segment after segment (dispatch chunks with
+// rows for the expert), one BK-row block at a time.
+struct SegCursor {
+    int seg, kl, rows;   // current segment, K block inside it, the segment's rows
+    int row0;            // first row of the segment (global row coordinate)
+    __device__ __forceinline__ void next_segment(const TcParams& p, int e) {
+        for (++seg; seg < p.nseg; ++seg) {
+            const int32_t* o = p.offsets + (int64_t)seg * p.ostride;
+            const int a = __ldg(o + e), b = __ldg(o + e + 1);
+            if (b > a) {
+                rows = b - a;
+                row0 = (int)(p.seg_base[seg] + a);
+                kl = 0;
+                return;
+            }
+        }
+        rows = 0;
+        row0 = 0;
+        kl = 0;
+    }
+    // position at K block kb0 of the expert's blocks, counted over its segments
+    __device__ __forceinline__ void start(const TcParams& p, int e, int kb0) {
+        seg = -1;
+        next_segment(p, e);
+        while (seg < p.nseg) {
+            const int nkb = (rows + BK - 1) / BK;
+            if (kb0 < nkb) {
+                kl = kb0;
+                return;
+            }
+            kb0 -= nkb;
+            next_segment(p, e);
+        }
+    }
+    __device__ __forceinline__ void advance(const TcParams& p, int e) {
+        if (++kl * BK >= rows) next_segment(p, e);
+    }
+    __device__ __forceinline__ int row() const { return row0 + kl * BK; }
+    __device__ __forceinline__ int valid() const { return rows - kl * BK; }   // rows of this block
 };
 
 template <bool VAR_K, bool PAIR, typename C>
@@ -179,19 +276,45 @@ __device__ __forceinline__ Tile get_tile(const C& c, const TcParams& p, int t, i
         ti.rows = min(BM, c.off[ecur + 1] - ti.row0);
         ti.num_kb = p.K / BK;
         ti.ones = false;
+        ti.kb0 = 0;
+        ti.slot = -1;
+        ti.bslot = -1;
     } else {
-        // n-tiles per m-tile: NT, plus the all-ones tile when row sums are wanted
-        const int NTX = NT + (p.bsum ? 1 : 0);
+        // An expert's units, part after part of its split K range (the units of
+        // one part run at about the same time and share operand rows in L2):
+        // its MT x NT tiles, ordered so that neighbouring units share the
+        // operand with more slabs (m-tile groups when MT >= NT, each followed by
+        // its all-ones tile; else n-tile groups, the all-ones tiles last), plus
+        // an all-ones tile per m-tile when row sums are wanted.  ecur: position
+        // in c.order.
         const int MT = (p.M + S::TILE_M - 1) / S::TILE_M;
-        const int per = MT * NTX;
-        ti.e = c.order[t / per];
-        const int local = t % per;
-        ti.mt = local / NTX;
-        ti.nt = local % NTX;
+        const int NTX = NT + (p.bsum ? 1 : 0);
+        while (c.ustart[ecur + 1] <= t) ++ecur;
+        ti.e = c.order[ecur];
+        const int local = t - c.ustart[ecur];
+        const int kb = c.tile_start[ti.e];   // K blocks over all of the expert's segments
+        const int nparts = vark_nsplit(kb, c.kb_part);
+        const int part = local / (MT * NTX);
+        const int rem = local - part * MT * NTX;
+        if (MT >= NT) {
+            ti.mt = rem / NTX;
+            ti.nt = rem % NTX;
+        } else if (rem < MT * NT) {
+            ti.nt = rem / MT;
+            ti.mt = rem % MT;
+        } else {
+            ti.mt = rem - MT * NT;
+            ti.nt = NT;
+        }
         ti.ones = ti.nt == NT;
-        ti.row0 = c.off[ti.e];
-        ti.rows = c.off[ti.e + 1] - ti.row0;
-        ti.num_kb = (ti.rows + BK - 1) / BK;
+        const int ks = nparts > 1 ? (kb + nparts - 1) / nparts : kb;
+        ti.kb0 = part * ks;
+        ti.num_kb = min(ks, kb - ti.kb0);
+        ti.slot = (part > 0 && !ti.ones)
+                      ? c.sbase[ti.e] + (part - 1) * MT * NT + ti.mt * NT + ti.nt : -1;
+        ti.bslot = (part > 0 && ti.ones) ? c.sbase[ti.e] / NT + (part - 1) * MT + ti.mt : -1;
+        ti.row0 = 0;
+        ti.rows = c.off[ti.e + 1] - c.off[ti.e];
     }
     return ti;
 }
@@ -441,8 +564,30 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             tmem_relinquish();
         }
     }
-    for (int i = threadIdx.x; i <= E; i += THREADS)
-        c.off[i] = p.offsets ? p.offsets[i] : (i == 0 ? 0 : (int)p.P);   // null: rows [0, P)
+    if (!VAR_K) {
+        for (int i = threadIdx.x; i <= E; i += THREADS)
+            c.off[i] = p.offsets ? p.offsets[i] : (i == 0 ? 0 : (int)p.P);   // null: rows [0, P)
+    } else {
+        // per expert: rows and K blocks summed over its segments; c.off becomes
+        // the prefix sum of the rows (so that off[e+1] - off[e] is expert e's
+        // total), c.tile_start[e] its K-block count
+        for (int e = threadIdx.x; e < E; e += THREADS) {
+            int tot = 0, kbs = 0;
+            for (int sg = 0; sg < p.nseg; ++sg) {
+                const int32_t* o = p.offsets + (int64_t)sg * p.ostride;
+                const int n = o[e + 1] - o[e];
+                tot += n;
+                kbs += (n + BK - 1) / BK;
+            }
+            c.off[e + 1] = tot;
+            c.tile_start[e] = kbs;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            c.off[0] = 0;
+            for (int e = 0; e < E; ++e) c.off[e + 1] += c.off[e];
+        }
+    }
     if (VAR_K && p.bsum) {
         // bf16 ones for the row-sum tile's B operand, read by the tensor core
         for (int i = threadIdx.x; i < PP::ONES / 16; i += THREADS)
@@ -477,12 +622,28 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             }
             c.order[r] = e;
         }
+        __syncthreads();
         if (threadIdx.x == 0) {
             int act = 0;
             for (int e = 0; e < E; ++e) act += (c.off[e + 1] - c.off[e]) > 0;
             const int MT = (p.M + S::TILE_M - 1) / S::TILE_M;
-            const int NTX = NT + (p.bsum ? 1 : 0);
-            c.nactive = (p.accumulate ? act : E) * MT * NTX;  // number of work units
+            const int ONES = p.bsum ? 1 : 0;
+            const int kp = vark_kb_part(c.tile_start, E, MT, NT, p.split_units, p.part_cap);
+            c.kb_part = kp;
+            int slots = 0;
+            for (int e = 0; e < E; ++e) {
+                c.sbase[e] = slots;
+                slots += (vark_nsplit(c.tile_start[e], kp) - 1) * MT * NT;
+            }
+            int u = 0;
+            for (int r = 0; r < E; ++r) {
+                c.ustart[r] = u;
+                u += MT * (NT + ONES) * vark_nsplit(c.tile_start[c.order[r]], kp);
+            }
+            c.ustart[E] = u;
+            // number of work units: without accumulation every expert (the empty
+            // ones write zeros), else the experts with rows (first in the order)
+            c.nactive = p.accumulate ? c.ustart[act] : u;
         }
     }
     tc_fence_before();
@@ -503,6 +664,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             bool ok = true;
             for (int t = unit0; t < num_units && ok; t += nunits) {
                 const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
+                SegCursor cur;
+                if (VAR_K) cur.start(p, ti.e, ti.kb0);
                 for (int kb = 0; kb < ti.num_kb; ++kb) {
                     if (leader && t == p.withhold_unit && kb == p.withhold_kb) {
                         // test hook: issue nothing more (no copy is left in
@@ -534,7 +697,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     }
                     // a weight-gradient pair's odd CTA loads a segment's last K block
                     // onto its own barrier, for its relay warp to zero the tail first
-                    const bool relay = PAIR && VAR_K && !leader && ti.rows - kb * BK < BK;
+                    const bool relay = PAIR && VAR_K && !leader && cur.valid() < BK;
                     if (PAIR && !leader && !relay) mbar_arrive_expect_tx_cluster(fbc, bytes);
                     else mbar_arrive_expect_tx(fb, bytes);
                     auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
@@ -558,10 +721,11 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     } else {
                         // one box per operand: this CTA's 64-column slabs of BK rows
                         // (maps: {column in slab, row, slab})
-                        const int r = ti.row0 + kb * BK;
+                        const int r = cur.row();
                         const int mA = ti.mt * S::TILE_M + rank * BM;
                         load3(sA, &mapA, 0, r, mA / 64);
                         if (!ti.ones) load3(sB, &mapB, 0, r, nB / 64);
+                        cur.advance(p, ti.e);
                     }
                     issued_parity[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -600,8 +764,11 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             bool ok = true;
             for (int t = unit0; t < num_units && ok; t += nunits) {
                 const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
+                SegCursor cur;
+                cur.start(p, ti.e, ti.kb0);
                 for (int kb = 0; kb < ti.num_kb; ++kb) {
-                    const int valid = ti.rows - kb * BK;
+                    const int valid = cur.valid();
+                    cur.advance(p, ti.e);
                     if (valid < BK) {
                         if (!mbar_wait_warp(smem_u32(&c.full[stage]), (local_phase >> stage) & 1u,
                                             p.limit_ns, &c.abort_flag)) {
@@ -645,6 +812,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             for (int t = unit0; t < num_units && ok; t += nunits) {
                 const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
                 if (ti.num_kb == 0) continue;
+                SegCursor cur;
+                if (VAR_K) cur.start(p, ti.e, ti.kb0);
                 if (!mbar_wait_warp(smem_u32(&c.tempty[acc]), acc_phase ^ 1, p.limit_ns,
                                     &c.abort_flag)) {
                     raise_abort(c, p);
@@ -661,7 +830,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     }
                     tc_fence_after();
                     if (VAR_K) {
-                        zero_tail(stage, ti.rows - kb * BK);
+                        zero_tail(stage, cur.valid());
+                        cur.advance(p, ti.e);
                         __syncwarp();
                     }
                     if (lane == 0) {
@@ -801,7 +971,9 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                 if (mma_tile) tmem_ld32(trow, v);
                 else v[0] = 0.f;
                 const int m = ti.mt * S::TILE_M + rank * BM + q * 32 + lane;
-                if (m < p.M) {
+                if (ti.bslot >= 0) {   // a split part > 0: its scratch row
+                    p.bpart[(int64_t)ti.bslot * S::TILE_M + rank * BM + q * 32 + lane] = v[0];
+                } else if (m < p.M) {
                     float* o = p.bsum + (int64_t)ti.e * p.M + m;
                     *o = p.accumulate ? *o + v[0] : v[0];
                 }
@@ -962,7 +1134,10 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                if (p.accumulate)
+                                if (ti.slot >= 0)   // a split part > 0: its scratch slot
+                                    tma_store_3d(&mapO1, smem_u32(stg), cl + hh * 16,
+                                                 rank * BM + q * 32, ti.slot);
+                                else if (p.accumulate)
                                     tma_reduce_add_3d(&mapO0, smem_u32(stg), col0 + hh * 16, m0,
                                                       ti.e);
                                 else
@@ -1078,8 +1253,8 @@ void withhold_hook(TcParams& p) {
 
 template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool PAIR>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
-                      const CUtensorMap& o1, const TcParams& p, int64_t units_upper,
-                      cudaStream_t st) {
+                      const CUtensorMap& o1, const TcParams& p_in, int64_t units_upper,
+                      cudaStream_t st, int* units_out) {
     auto kern = gemm_tc_kernel<VAR_K, A_MN, B_MN, EPI, PAIR>;
     constexpr size_t SMEM = smem_bytes<PAIR, VAR_K, EPI>();
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
@@ -1115,6 +1290,9 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
     const int64_t ov = max_units_override();
     if (ov > 0 && ov < cap) cap = ov;
     const int64_t units = units_upper < cap ? (units_upper > 0 ? units_upper : 1) : cap;
+    TcParams p = p_in;
+    p.split_units = (int)units;
+    if (units_out) *units_out = (int)units;
     if (!PAIR) {
         kern<<<(unsigned)units, THREADS, SMEM, st>>>(a, b, o0, o1, p);
         return cudaGetLastError();
@@ -1137,9 +1315,74 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
 template <bool VAR_K, bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_either(bool pair, const CUtensorMap& a, const CUtensorMap& b,
                           const CUtensorMap& o0, const CUtensorMap& o1, const TcParams& p,
-                          int64_t units1, int64_t units2, cudaStream_t st) {
-    if (pair) return launch_tc<VAR_K, A_MN, B_MN, EPI, true>(a, b, o0, o1, p, units2, st);
-    return launch_tc<VAR_K, A_MN, B_MN, EPI, false>(a, b, o0, o1, p, units1, st);
+                          int64_t units1, int64_t units2, cudaStream_t st,
+                          int* units_out = nullptr) {
+    if (pair)
+        return launch_tc<VAR_K, A_MN, B_MN, EPI, true>(a, b, o0, o1, p, units2, st, units_out);
+    return launch_tc<VAR_K, A_MN, B_MN, EPI, false>(a, b, o0, o1, p, units1, st, units_out);
+}
+
+// Adds the split parts > 0 of the weight-gradient tiles (scratch slots, fp32
+// [slot][tile_m][BN]) to the output [E, M, N] in part order, so that the result
+// is out + part 0 (written by the GEMM) + part 1 + part 2 + ... whatever the
+// order the GEMM's CTAs finished in.  Recomputes the GEMM's split from the same
+// inputs.  A block takes one expert (blockIdx.y) and strides over its elements,
+// four columns per thread.
+__global__ void __launch_bounds__(256) vark_split_reduce_kernel(
+    int E, int M, int N, int tile_m, int nseg, int ostride, const int32_t* __restrict__ offsets,
+    int split_units, int64_t cap, const float* __restrict__ part, float* __restrict__ out,
+    const float* __restrict__ bpart, float* __restrict__ bsum) {
+    __shared__ int kbs[MAX_E];
+    __shared__ int sb[MAX_E];
+    __shared__ int kp_s;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int kb = 0;
+        for (int sg = 0; sg < nseg; ++sg) {
+            const int32_t* o = offsets + (int64_t)sg * ostride;
+            kb += (o[e + 1] - o[e] + BK - 1) / BK;
+        }
+        kbs[e] = kb;
+    }
+    __syncthreads();
+    const int MT = (M + tile_m - 1) / tile_m, NT = (N + BN - 1) / BN;
+    if (threadIdx.x == 0) {
+        const int kp = vark_kb_part(kbs, E, MT, NT, split_units, cap);
+        kp_s = kp;
+        int slots = 0;
+        for (int e = 0; e < E; ++e) {
+            sb[e] = slots;
+            slots += (vark_nsplit(kbs[e], kp) - 1) * MT * NT;
+        }
+    }
+    __syncthreads();
+    const int e = blockIdx.y;
+    const int S = vark_nsplit(kbs[e], kp_s);
+    if (S <= 1) return;
+    const int64_t n4 = (int64_t)M * N / 4;
+    float4* o4 = reinterpret_cast<float4*>(out + (int64_t)e * M * N);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int m = (int)(i * 4 / N), n = (int)(i * 4 % N);
+        const int mt = m / tile_m, nt = n / BN;
+        float4 a = o4[i];
+        for (int q = 1; q < S; ++q) {
+            const int64_t slot = sb[e] + (int64_t)(q - 1) * MT * NT + mt * NT + nt;
+            const float4 b = *reinterpret_cast<const float4*>(
+                part + (slot * tile_m + (m % tile_m)) * BN + (n % BN));
+            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+        }
+        o4[i] = a;
+    }
+    if (bsum && blockIdx.x == 0) {
+        // row sums: bsum[e][m] + part 1 + part 2 + ... (block 0 of the expert)
+        for (int m = threadIdx.x; m < M; m += blockDim.x) {
+            const int mt = m / tile_m;
+            float a = bsum[(int64_t)e * M + m];
+            for (int q = 1; q < S; ++q)
+                a += bpart[((int64_t)sb[e] / NT + (int64_t)(q - 1) * MT + mt) * tile_m + m % tile_m];
+            bsum[(int64_t)e * M + m] = a;
+        }
+    }
 }
 
 // Column sums from the ScaleAux epilogue's partial rows: expert e owns the
@@ -1282,6 +1525,15 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     return cudaErrorInvalidValue;
 }
 
+size_t vark_split_workspace(int64_t rows, int E, int M, int N) {
+    // parts of >= kKbPartMin K blocks: at most (rows / 64 + E) / kKbPartMin parts
+    // beyond the first over all experts, each needing MT x NT slots of 256 x 256
+    // fp32 (+ a row-sum row); one more for rounding
+    const int64_t parts = (rows / BK + E) / kKbPartMin + 1;
+    const int64_t MT = (M + 2 * BM - 1) / (2 * BM), NT = (N + BN - 1) / BN;
+    return (size_t)(parts * MT * NT) * (size_t)(2 * BM * BN * 4 + 2 * BM * 4);
+}
+
 size_t gemm_colsum_workspace(int64_t P, int E, int N) {
     // 4 partial rows per 128-row CTA tile.  Single CTAs: at most ceil(P/128) + E
     // tiles; pairs: 2 (ceil(P/256) + E) <= ceil(P/128) + 1 + 2E.
@@ -1307,15 +1559,40 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
         const uint32_t box[3] = {64, BK, (uint32_t)(pair ? BN / 2 : BN) / 64};
         if (!make_map(&mb, g.act_b, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
+    if (g.nseg < 1 || g.nseg > kMaxWgradChunks) return cudaErrorInvalidValue;
+    if (g.P >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;   // TMA row coordinate
     TcParams p{};
     p.E = g.E; p.M = g.M; p.N = g.N; p.K = 0; p.P = g.P;
     p.offsets = g.offsets; p.outf = g.out; p.accumulate = g.accumulate;
+    p.nseg = g.nseg; p.ostride = g.ostride;
+    for (int i = 0; i < g.nseg; ++i) p.seg_base[i] = g.seg_base[i];
     p.status = status; p.limit_ns = wait_limit_ns();
     withhold_hook(p);
     p.bsum = g.bsum;
     const int64_t NT = (g.N + BN - 1) / BN + (g.bsum ? 1 : 0);
+    // without a split; the grid is capped at the co-resident CTAs (pairs) anyway
     const int64_t u1 = (int64_t)g.E * ((g.M + BM - 1) / BM) * NT;
     const int64_t u2 = (int64_t)g.E * ((g.M + 2 * BM - 1) / (2 * BM)) * NT;
+    // scratch for the split parts: fp32 tiles [slot][tile_m][BN], stored by TMA
+    // in the epilogue's 32 x 16 boxes
+    const int tile_m = pair ? 2 * BM : BM;
+    const int64_t slot_bytes = (int64_t)tile_m * BN * 4;
+    // each partial tile's slot also reserves one row-sum row (tile_m floats)
+    // after the tiles; the row sums of a split need at most one per N tiles
+    int64_t cap = g.part ? (int64_t)(g.part_bytes / (size_t)(slot_bytes + tile_m * 4)) : 0;
+    if (cap > ((int64_t)1 << 30)) cap = (int64_t)1 << 30;
+    float* bpart = g.part ? g.part + cap * tile_m * BN : nullptr;
+    CUtensorMap mpart;
+    if (cap > 0) {
+        const uint64_t dims[3] = {(uint64_t)BN, (uint64_t)tile_m, (uint64_t)cap};
+        const uint64_t strides[2] = {(uint64_t)BN * 4, (uint64_t)slot_bytes};
+        const uint32_t box[3] = {16, 32, 1};
+        if (!make_map(&mpart, g.part, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B,
+                      CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+            return cudaErrorInvalidValue;
+    }
+    p.part_cap = cap;
+    p.bpart = bpart;
     // fp32 output [E, M, N]: boxes of 32 rows x 16 columns, 64-byte swizzle
     CUtensorMap mo;
     {
@@ -1326,7 +1603,19 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
                       CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
             return cudaErrorInvalidValue;
     }
-    return launch_either<true, true, true, (int)Epi::Plain>(pair, ma, mb, mo, mo, p, u1, u2, st);
+    if (cap == 0) mpart = mo;
+    // u1 / u2 bound the grid only; with a split there are more units than that
+    const int64_t big = (int64_t)1 << 30;
+    int units = 0;
+    cudaError_t e = launch_either<true, true, true, (int)Epi::Plain>(
+        pair, ma, mb, mo, mpart, p, cap > 0 ? big : u1, cap > 0 ? big : u2, st, &units);
+    if (e != cudaSuccess || cap == 0) return e;
+    const int64_t n4 = (int64_t)g.M * g.N / 4;
+    const unsigned gx = (unsigned)(n4 / 256 < 64 ? (n4 + 255) / 256 : 64);
+    vark_split_reduce_kernel<<<dim3(gx, (unsigned)g.E), 256, 0, st>>>(
+        g.E, g.M, g.N, tile_m, g.nseg, g.ostride, g.offsets, units, cap, g.part, g.out, bpart,
+        g.bsum);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -17,6 +17,9 @@ constexpr int kRouteWords = kRouteBlockTokens / 32;
 // Rows summed per partial of the router weight gradient and of the bias
 // gradients (column sums).
 constexpr int kDwgChunk = 32;
+// Dispatch chunks one weight-gradient GEMM launch walks (more are split over
+// several launches that accumulate).
+constexpr int kMaxWgradChunks = 16;
 
 inline int64_t route_blocks(int64_t T) { return (T + kRouteBlockTokens - 1) / kRouteBlockTokens; }
 
@@ -98,8 +101,8 @@ struct GemmVarM {
 size_t gemm_colsum_workspace(int64_t P, int E, int N);
 struct GemmVarK {
     int E, M, N;
-    int64_t P;
-    const int32_t* offsets;
+    int64_t P;              // rows of act_a / act_b (all segments)
+    const int32_t* offsets; // [nseg][ostride]: each chunk's expert offsets (E+1 used)
     const void* act_a;      // [P, M]
     const void* act_b;      // [P, N]
     float* out;             // [E, M, N]
@@ -108,7 +111,19 @@ struct GemmVarK {
     // rows of act_a[row][m] (a bias gradient), from one extra tile per
     // (expert, m-tile) whose B operand is a constant all-ones block
     float* bsum = nullptr;
+    // expert e's rows are, in each dispatch chunk s < nseg,
+    // [seg_base[s] + offsets[s*ostride + e], seg_base[s] + offsets[s*ostride + e + 1])
+    int nseg = 1;
+    int ostride = 0;
+    int64_t seg_base[kMaxWgradChunks] = {};
+    // tensor-core path: scratch for the partial tiles of long reductions split
+    // into parts (none when null or too small for one tile)
+    float* part = nullptr;
+    size_t part_bytes = 0;
 };
+// Scratch bytes that let the weight-gradient GEMMs over `rows` rows split their
+// long reductions as finely as they would (parts of >= 512 K blocks of 64 rows).
+size_t vark_split_workspace(int64_t rows, int E, int M, int N);
 
 cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t st);
 cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t st);

@@ -80,13 +80,25 @@ size_t route_ws(const moe_shape& s) {
     return align_up((size_t)s.E * (size_t)route_blocks(s.T) * sizeof(int32_t));
 }
 
-size_t ffn_bwd_ws(const moe_shape& s) {
-    const size_t dh = align_up((size_t)s.T * s.k * s.f * esize(s));
+// column-sum partial rows of the bias gradients (either path)
+size_t ffn_partial_bytes(const moe_shape& s) {
     const int n = s.d > s.f ? s.d : s.f;
     size_t part = segment_colsum_workspace(s, n);
     const size_t fused = gemm_colsum_workspace(s.T * s.k, s.E, s.f);   // db1 in the dH GEMM
-    if (fused > part) part = fused;
-    return dh + align_up(part);
+    return align_up(fused > part ? fused : part);
+}
+
+// scratch of the split weight-gradient reductions over `rows` rows (bf16)
+size_t split_bytes(const moe_shape& s, int64_t rows) {
+    if (s.dtype != MOE_BF16) return 0;
+    const size_t a = vark_split_workspace(rows, s.E, s.d, s.f);
+    const size_t b = vark_split_workspace(rows, s.E, s.f, s.d);
+    return align_up(a > b ? a : b);
+}
+
+size_t ffn_bwd_ws(const moe_shape& s) {
+    const size_t dh = align_up((size_t)s.T * s.k * s.f * esize(s));
+    return dh + ffn_partial_bytes(s) + split_bytes(s, s.T * s.k);
 }
 
 }  // namespace
@@ -197,6 +209,103 @@ moe_status moe_combine_bwd(const moe_shape* s, const void* dy, const void* y_per
                                           (cudaStream_t)stream));
 }
 
+}  // extern "C"
+
+namespace {
+
+// A8, data half: dH = (dY W2[e]) * G, db1 (+)= sum_rows dH, dX = dH W1[e].
+// `partial` holds the column-sum partial rows (ffn_partial_bytes).
+cudaError_t ffn_bwd_data(const moe_shape& s, const void* dy_perm, const void* G,
+                         const int32_t* offsets, const void* W1, const void* W2, void* dH,
+                         void* dx_perm, float* db1, int accumulate, float* partial,
+                         int32_t* status, cudaStream_t st) {
+    const int E = s.E, d = s.d, f = s.f;
+    const int64_t P = s.T * s.k;
+    const bool tc = s.dtype == MOE_BF16;
+    // dA = dY W2[e] (W2 stored [E,d,f] = [E,K,N]); dH = dA * G, G = GELU'(h)
+    GemmVarM g_dh{E, f, d, P, offsets, dy_perm, W2, false, Epi::ScaleAux, nullptr, G, dH, nullptr};
+    if (tc) {   // db1 = column sums of dH, taken in the dH GEMM's epilogue
+        g_dh.colsum = db1;
+        g_dh.colsum_partial = partial;
+        g_dh.colsum_accumulate = accumulate;
+    }
+    // dX = dH W1[e] (W1 stored [E,f,d] = [E,K,N])
+    GemmVarM g_dx{E, d, f, P, offsets, dH, W1, false, Epi::Plain, nullptr, nullptr, dx_perm, nullptr};
+    cudaError_t e = tc ? launch_gemm_varm_tc(g_dh, status, st) : launch_gemm_varm_simt(g_dh, st);
+    if (e == cudaSuccess)
+        e = tc ? launch_gemm_varm_tc(g_dx, status, st) : launch_gemm_varm_simt(g_dx, st);
+    if (e == cudaSuccess && !tc)
+        e = launch_segment_colsum(s, dH, f, offsets, db1, accumulate, partial, st);
+    return e;
+}
+
+// A8, weight half over nchunks dispatch chunks whose rows follow one another in
+// dy_perm, x_perm, dH and A (chunk c holds chunk_T[c] * k rows, its expert
+// offsets at offsets + c * ostride):
+//   dW2[e] (+)= dY^T A,  db2[e] (+)= sum_rows dY,  dW1[e] (+)= dH^T X
+// summed over every chunk's rows of expert e.  Chunks beyond what one launch
+// walks go to further launches that accumulate.  `partial`: column-sum
+// partial rows of the fp32 path (ffn_partial_bytes of the largest chunk).
+cudaError_t ffn_bwd_weights(const moe_shape& s, int nchunks, const int64_t* chunk_T,
+                            const int32_t* offsets, int ostride, const void* dy_perm,
+                            const void* x_perm, const void* dH, const void* A, float* dW1,
+                            float* dW2, float* db2, int accumulate, float* partial,
+                            void* split, size_t split_size, int32_t* status, cudaStream_t st) {
+    const int E = s.E, d = s.d, f = s.f, k = s.k;
+    const bool tc = s.dtype == MOE_BF16;
+    int64_t P = 0;
+    for (int c = 0; c < nchunks; ++c) P += chunk_T[c] * k;
+    int64_t base = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += kMaxWgradChunks) {
+        const int n = nchunks - c0 < kMaxWgradChunks ? nchunks - c0 : kMaxWgradChunks;
+        const int acc = accumulate || c0 > 0;
+        // dW2[e] = dY^T A  ([d, f]);  dW1[e] = dH^T X  ([f, d])
+        GemmVarK g_w2{E, d, f, P, offsets + (int64_t)c0 * ostride, dy_perm, A, dW2, acc};
+        if (tc) g_w2.bsum = db2;   // db2 = column sums of dY_perm, by the dW2 GEMM
+        GemmVarK g_w1{E, f, d, P, offsets + (int64_t)c0 * ostride, dH, x_perm, dW1, acc};
+        int64_t b = base;
+        for (int i = 0; i < n; ++i) {
+            g_w2.seg_base[i] = g_w1.seg_base[i] = b;
+            b += chunk_T[c0 + i] * k;
+        }
+        g_w2.nseg = g_w1.nseg = n;
+        g_w2.ostride = g_w1.ostride = ostride;
+        g_w2.part = g_w1.part = (float*)split;   // used by one launch after the other
+        g_w2.part_bytes = g_w1.part_bytes = split ? split_size : 0;
+        cudaError_t e = tc ? launch_gemm_vark_tc(g_w2, status, st) : launch_gemm_vark_simt(g_w2, st);
+        if (e == cudaSuccess)
+            e = tc ? launch_gemm_vark_tc(g_w1, status, st) : launch_gemm_vark_simt(g_w1, st);
+        if (e != cudaSuccess) return e;
+        if (!tc) {
+            // db2 per chunk, in chunk order
+            for (int i = 0; i < n; ++i) {
+                moe_shape sc = s;
+                sc.T = chunk_T[c0 + i];
+                const int64_t rb = g_w2.seg_base[i];
+                e = launch_segment_colsum(sc, (const float*)dy_perm + rb * d, d,
+                                          offsets + (int64_t)(c0 + i) * ostride, db2,
+                                          acc || i > 0, partial, st);
+                if (e != cudaSuccess) return e;
+            }
+        }
+        base = b;
+    }
+    return cudaSuccess;
+}
+
+// zero the weight / bias gradients of an empty call (accumulate == 0)
+cudaError_t zero_grads(const moe_shape& s, float* a, size_t na, float* b, size_t nb,
+                       cudaStream_t st) {
+    cudaError_t e = a ? cudaMemsetAsync(a, 0, sizeof(float) * na, st) : cudaSuccess;
+    if (e == cudaSuccess && b) e = cudaMemsetAsync(b, 0, sizeof(float) * nb, st);
+    (void)s;
+    return e;
+}
+
+}  // namespace
+
+extern "C" {
+
 moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const void* x_perm,
                               const void* G, const void* A, const int32_t* offsets,
                               const void* W1, const void* W2, void* dx_perm, float* dW1,
@@ -209,45 +318,105 @@ moe_status moe_expert_ffn_bwd(const moe_shape* s, const void* dy_perm, const voi
     const int E = s->E, d = s->d, f = s->f;
     if (s->T == 0) {
         if (accumulate) return MOE_OK;
-        cudaError_t e = cudaMemsetAsync(dW1, 0, sizeof(float) * (size_t)E * f * d, st);
-        if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, sizeof(float) * (size_t)E * d * f, st);
-        if (e == cudaSuccess) e = cudaMemsetAsync(db1, 0, sizeof(float) * (size_t)E * f, st);
-        if (e == cudaSuccess) e = cudaMemsetAsync(db2, 0, sizeof(float) * (size_t)E * d, st);
+        cudaError_t e = zero_grads(*s, dW1, (size_t)E * f * d, db1, (size_t)E * f, st);
+        if (e == cudaSuccess) e = zero_grads(*s, dW2, (size_t)E * d * f, db2, (size_t)E * d, st);
         return cuda_status(e);
     }
     if (!ok_ptr(dy_perm) || !ok_ptr(x_perm) || !ok_ptr(G) || !ok_ptr(A) || !ok_ptr(offsets) ||
         !ok_ptr(W1) || !ok_ptr(W2) || !ok_ptr(dx_perm) || !ok_ptr(ws) || !ok_status(dev_status))
         return MOE_ERR_INVALID;
     const int64_t P = s->T * s->k;
+    // workspace: dH | column-sum partials | split scratch
     uint8_t* wsb = (uint8_t*)ws;
     void* dH = wsb;
-    float* partial = (float*)(wsb + align_up((size_t)P * f * esize(*s)));
-    // dA = dY W2[e] (W2 stored [E,d,f] = [E,K,N]); dH = dA * G, G = GELU'(h)
-    GemmVarM g_dh{E, f, d, P, offsets, dy_perm, W2, false, Epi::ScaleAux, nullptr, G, dH, nullptr};
-    const bool tc = s->dtype == MOE_BF16;
-    if (tc) {   // db1 = column sums of dH, taken in the dH GEMM's epilogue
-        g_dh.colsum = db1;
-        g_dh.colsum_partial = partial;
-        g_dh.colsum_accumulate = accumulate;
-    }
-    // dX = dH W1[e] (W1 stored [E,f,d] = [E,K,N])
-    GemmVarM g_dx{E, d, f, P, offsets, dH, W1, false, Epi::Plain, nullptr, nullptr, dx_perm, nullptr};
-    // dW2[e] = dY^T A  ([d, f]);  dW1[e] = dH^T X  ([f, d])
-    GemmVarK g_w2{E, d, f, P, offsets, dy_perm, A, dW2, accumulate};
-    if (tc) g_w2.bsum = db2;   // db2 = column sums of dY_perm, by the dW2 GEMM
-    GemmVarK g_w1{E, f, d, P, offsets, dH, x_perm, dW1, accumulate};
-    cudaError_t e = tc ? launch_gemm_varm_tc(g_dh, dev_status, st) : launch_gemm_varm_simt(g_dh, st);
+    const size_t dh_bytes = align_up((size_t)P * f * esize(*s));
+    float* partial = (float*)(wsb + dh_bytes);
+    uint8_t* split = wsb + dh_bytes + ffn_partial_bytes(*s);
+    cudaError_t e = ffn_bwd_data(*s, dy_perm, G, offsets, W1, W2, dH, dx_perm, db1, accumulate,
+                                 partial, dev_status, st);
+    const int64_t T = s->T;
     if (e == cudaSuccess)
-        e = tc ? launch_gemm_varm_tc(g_dx, dev_status, st) : launch_gemm_varm_simt(g_dx, st);
-    if (e == cudaSuccess)
-        e = tc ? launch_gemm_vark_tc(g_w2, dev_status, st) : launch_gemm_vark_simt(g_w2, st);
-    if (e == cudaSuccess)
-        e = tc ? launch_gemm_vark_tc(g_w1, dev_status, st) : launch_gemm_vark_simt(g_w1, st);
-    if (e == cudaSuccess && !tc)
-        e = launch_segment_colsum(*s, dy_perm, d, offsets, db2, accumulate, partial, st);
-    if (e == cudaSuccess && !tc)
-        e = launch_segment_colsum(*s, dH, f, offsets, db1, accumulate, partial, st);
+        e = ffn_bwd_weights(*s, 1, &T, offsets, E + 1, dy_perm, x_perm, dH, A, dW1, dW2, db2,
+                            accumulate, partial, split, split_bytes(*s, P), dev_status, st);
     return cuda_status(e);
+}
+
+moe_status moe_expert_ffn_bwd_data(const moe_shape* s, const void* dy_perm, const void* G,
+                                   const int32_t* offsets, const void* W1, const void* W2,
+                                   void* dH, void* dx_perm, float* db1, int accumulate, void* ws,
+                                   int32_t* dev_status, moe_stream_t stream) {
+    moe_status r = check_gemm_shape(s);
+    if (r != MOE_OK) return r;
+    if (!ok_ptr(db1)) return MOE_ERR_INVALID;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (s->T == 0)
+        return accumulate ? MOE_OK
+                          : cuda_status(zero_grads(*s, db1, (size_t)s->E * s->f, nullptr, 0, st));
+    if (!ok_ptr(dy_perm) || !ok_ptr(G) || !ok_ptr(offsets) || !ok_ptr(W1) || !ok_ptr(W2) ||
+        !ok_ptr(dH) || !ok_ptr(dx_perm) || !ok_ptr(ws) || !ok_status(dev_status))
+        return MOE_ERR_INVALID;
+    return cuda_status(ffn_bwd_data(*s, dy_perm, G, offsets, W1, W2, dH, dx_perm, db1,
+                                    accumulate, (float*)ws, dev_status, st));
+}
+
+size_t moe_expert_ffn_bwd_weights_workspace_size(const moe_shape* s, int nchunks,
+                                                 const int64_t* chunk_T) {
+    if (check_gemm_shape(s) != MOE_OK || nchunks < 1 || chunk_T == nullptr) return 0;
+    int64_t T = 0, Tmax = 0;
+    for (int c = 0; c < nchunks; ++c) {
+        if (chunk_T[c] < 0) return 0;
+        T += chunk_T[c];
+        Tmax = chunk_T[c] > Tmax ? chunk_T[c] : Tmax;
+    }
+    moe_shape big = *s;
+    big.T = Tmax;
+    const size_t part = s->dtype == MOE_BF16 ? 0 : ffn_partial_bytes(big);
+    const size_t split = split_bytes(*s, T * s->k);
+    const size_t n = part + split;
+    return n > 0 ? n : 256;
+}
+
+moe_status moe_expert_ffn_bwd_weights(const moe_shape* s, int nchunks, const int64_t* chunk_T,
+                                      const int32_t* offsets, int offsets_stride,
+                                      const void* dy_perm, const void* x_perm, const void* dH,
+                                      const void* A, float* dW1, float* dW2, float* db2,
+                                      int accumulate, void* ws, size_t ws_bytes,
+                                      int32_t* dev_status, moe_stream_t stream) {
+    moe_status r = check_gemm_shape(s);
+    if (r != MOE_OK) return r;
+    if (nchunks < 1 || chunk_T == nullptr || offsets_stride < s->E + 1 || offsets_stride % 4)
+        return MOE_ERR_INVALID;
+    if (!ok_ptr(dW1) || !ok_ptr(dW2) || !ok_ptr(db2)) return MOE_ERR_INVALID;
+    int64_t T = 0, Tmax = 0;
+    for (int c = 0; c < nchunks; ++c) {
+        if (chunk_T[c] < 0) return MOE_ERR_INVALID;
+        T += chunk_T[c];
+        if (chunk_T[c] > Tmax) Tmax = chunk_T[c];
+    }
+    if (T * (int64_t)s->k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int E = s->E, d = s->d, f = s->f;
+    if (T == 0) {
+        if (accumulate) return MOE_OK;
+        cudaError_t e = zero_grads(*s, dW1, (size_t)E * f * d, dW2, (size_t)E * d * f, st);
+        if (e == cudaSuccess) e = zero_grads(*s, db2, (size_t)E * d, nullptr, 0, st);
+        return cuda_status(e);
+    }
+    if (!ok_ptr(dy_perm) || !ok_ptr(x_perm) || !ok_ptr(dH) || !ok_ptr(A) || !ok_ptr(offsets) ||
+        !ok_status(dev_status) || !ok_opt(ws) || (ws == nullptr && ws_bytes != 0))
+        return MOE_ERR_INVALID;
+    moe_shape big = *s;
+    big.T = Tmax;
+    if (s->dtype != MOE_BF16) {
+        // fp32: the column-sum partials of db2 (no split)
+        if (ws == nullptr || ws_bytes < ffn_partial_bytes(big)) return MOE_ERR_INVALID;
+        return cuda_status(ffn_bwd_weights(*s, nchunks, chunk_T, offsets, offsets_stride, dy_perm,
+                                           x_perm, dH, A, dW1, dW2, db2, accumulate, (float*)ws,
+                                           nullptr, 0, dev_status, st));
+    }
+    return cuda_status(ffn_bwd_weights(*s, nchunks, chunk_T, offsets, offsets_stride, dy_perm,
+                                       x_perm, dH, A, dW1, dW2, db2, accumulate, nullptr, ws,
+                                       ws_bytes, dev_status, st));
 }
 
 moe_status moe_route_bwd(const moe_shape* s, const float* dw, const float* logits,

@@ -21,6 +21,15 @@ and dX_perm are double-buffered, and events order every reuse.  Each fp32
 gradient still accumulates in chunk order on one stream (dW, db on the current
 one, dWg on the side one), so the results equal the serial loop's bit for bit.
 
+With more than one chunk (and the activations kept) the weight gradients are
+not accumulated chunk by chunk: dY_perm and dH of every chunk are kept, each
+chunk's backward computes only its activation gradients (and db1), and one
+weight-gradient pass after the last chunk sums each expert's rows over all
+chunks (``moe_expert_ffn_bwd_weights``).  Every dW tile is then written once
+per pass instead of being read, added to and written back once per chunk, and
+experts with few rows per chunk get one longer reduction instead of many
+short ones.  ``defer_wgrad=False`` keeps the per-chunk accumulation.
+
 With ``recompute`` the activations are not kept between the forward and the
 backward (MPipeMoE, "research method": recomputation to cut activation
 memory): only the routing results are, and the backward re-runs each chunk's
@@ -54,11 +63,14 @@ class LayerPass:
     chunk (dispatch chunk cap; None = one chunk), pipeline (two-stream chunk
     pipelining when there is more than one chunk; False keeps one stream),
     recompute (keep only the routing between forward and backward and re-run
-    each chunk's permute and expert forward in the backward; one stream)."""
+    each chunk's permute and expert forward in the backward; one stream),
+    defer_wgrad (one weight-gradient pass over all chunks after the last
+    chunk's backward; default: with more than one chunk, unless recompute)."""
 
     def __init__(self, T: int, d: int, f: int, E: int, k: int, dtype: torch.dtype,
                  renorm: int, chunk: Optional[int] = None, device="cuda",
-                 pipeline: bool = True, recompute: bool = False):
+                 pipeline: bool = True, recompute: bool = False,
+                 defer_wgrad: Optional[bool] = None):
         self.T, self.d, self.f, self.E, self.k = T, d, f, E, k
         self.dtype, self.renorm = dtype, int(renorm)
         C = chunk if chunk else T
@@ -69,6 +81,9 @@ class LayerPass:
         nch = len(self.chunks)
         self.recompute = bool(recompute)
         self.pipeline = bool(pipeline) and nch > 1 and not self.recompute
+        if defer_wgrad is None:
+            defer_wgrad = nch > 1
+        self.defer_wgrad = bool(defer_wgrad) and not self.recompute
         dev = torch.device(device)
         f32, i32 = torch.float32, torch.int32
         z = lambda *s, dt=dtype: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
@@ -94,7 +109,17 @@ class LayerPass:
         self.dw = z(T, k, dt=f32)
         self.dx = z(T, d)
         nbuf = 2 if self.pipeline else 1
-        self.dY_perm = z(nbuf, C * k, d)
+        if self.defer_wgrad:
+            # every chunk's rows, kept for the one weight-gradient pass
+            self.dY_perm = z(T * k, d)
+            self.dH = z(T * k, f)
+            self.chunk_T = [c1 - c0 for c0, c1 in self.chunks]
+            self.wshape = ops.make_shape(T, d, f, E, k, dtype, renorm)
+            # scratch of the weight-gradient pass (split reductions; fp32 partials)
+            wn = ops.moe_expert_ffn_bwd_weights_workspace_size(self.wshape, self.chunk_T)
+            self.wws = torch.empty(max(wn, 256), dtype=torch.uint8, device=dev)
+        else:
+            self.dY_perm = z(nbuf, C * k, d)
         self.dX_perm = z(nbuf, C * k, d)
         self.dW1 = z(E, f, d, dt=f32)
         self.db1 = z(E, f, dt=f32)
@@ -176,7 +201,8 @@ class LayerPass:
             c0, c1 = self.chunks[ci]
             n = (c1 - c0) * k
             b = ci % 2 if self.pipeline else 0
-            return c0, c1, self.dY_perm[b, :n], self.dX_perm[b, :n]
+            dYp = self.dY_perm[c0 * k:c1 * k] if self.defer_wgrad else self.dY_perm[b, :n]
+            return c0, c1, dYp, self.dX_perm[b, :n]
 
         def combine_bwd(ci):   # A7: dY_perm and dw of chunk ci
             c0, c1, dYp, _ = views(ci)
@@ -186,6 +212,11 @@ class LayerPass:
 
         def ffn_bwd(ci):       # A8: dX_perm of chunk ci; dW1, db1, dW2, db2 accumulate
             c0, c1, dYp, dXp = views(ci)
+            if self.defer_wgrad:   # the activation half; db1 accumulates here
+                ops.moe_expert_ffn_bwd_data(self.shapes[ci], dYp, self._act(self.G, c0, c1),
+                                            self.offsets[ci], W1, W2, self.dH[c0 * k:c1 * k],
+                                            dXp, self.db1, int(ci > 0), self.ws, self.status)
+                return
             ops.moe_expert_ffn_bwd(self.shapes[ci], dYp, self._act(self.X_perm, c0, c1),
                                    self._act(self.G, c0, c1), self._act(self.A, c0, c1),
                                    self.offsets[ci], W1, W2, dXp, self.dW1, self.db1, self.dW2,
@@ -212,6 +243,13 @@ class LayerPass:
 
         if self.recompute and self._params is None:
             raise RuntimeError("recompute: backward needs the forward's parameters")
+        def weights():         # A8, weight half: every chunk's rows in one pass
+            if self.defer_wgrad:
+                ops.moe_expert_ffn_bwd_weights(self.wshape, self.chunk_T, self.offsets,
+                                               self.dY_perm, self.X_perm, self.dH, self.A,
+                                               self.dW1, self.dW2, self.db2, 0, self.wws,
+                                               self.status)
+
         if not self.pipeline:
             for ci in live:
                 if self.recompute:
@@ -219,6 +257,7 @@ class LayerPass:
                 combine_bwd(ci)
                 ffn_bwd(ci)
                 route_bwd(ci, self.ws)
+            weights()
             return self.dx
         # two streams: the side stream runs combine backward one chunk ahead and
         # router backward one chunk behind the current stream's expert backward
@@ -236,13 +275,14 @@ class LayerPass:
             self._ev_ffn[ci].record(main)
             with torch.cuda.stream(side):
                 if i + 1 < len(live):
-                    if i >= 1:
+                    if i >= 1 and not self.defer_wgrad:
                         side.wait_event(self._ev_ffn[live[i - 1]])   # its dY_perm buffer is free
                     combine_bwd(live[i + 1])
                     self._ev_cb[live[i + 1]].record(side)
                 side.wait_event(self._ev_ffn[ci])
                 route_bwd(ci, self.ws2)
                 self._ev_rb[ci].record(side)
+        weights()
         self._ev_join.record(side)
         main.wait_event(self._ev_join)
         return self.dx

@@ -24,7 +24,8 @@ MOE_F32, MOE_BF16 = 0, 1
 ENTRY_POINTS = ("moe_status_string", "moe_workspace_size", "moe_route", "moe_permute",
                 "moe_expert_ffn_fwd", "moe_combine_fwd", "moe_combine_bwd",
                 "moe_expert_ffn_bwd", "moe_route_bwd", "moe_debug_bounded_wait",
-                "moe_debug_gelu", "moe_route_noalloc")
+                "moe_debug_gelu", "moe_route_noalloc", "moe_expert_ffn_bwd_data",
+                "moe_expert_ffn_bwd_weights", "moe_expert_ffn_bwd_weights_workspace_size")
 
 
 class MoEError(RuntimeError):
@@ -84,8 +85,18 @@ def lib() -> ctypes.CDLL:
             L.moe_debug_gelu.argtypes = [ctypes.c_int64, _P, _P, _P, ctypes.c_int, _P]
             L.moe_route_noalloc.argtypes = [_SP, _P, _P, _P, _P, ctypes.c_int, _P, _P, _P, _P,
                                             _P, _P, _P, _P]
+            L.moe_expert_ffn_bwd_data.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                  ctypes.c_int, _P, _P, _P]
+            L.moe_expert_ffn_bwd_weights.argtypes = [_SP, ctypes.c_int,
+                                                     ctypes.POINTER(ctypes.c_int64), _P,
+                                                     ctypes.c_int, _P, _P, _P, _P, _P, _P, _P,
+                                                     ctypes.c_int, _P, ctypes.c_size_t, _P, _P]
+            L.moe_expert_ffn_bwd_weights_workspace_size.restype = ctypes.c_size_t
+            L.moe_expert_ffn_bwd_weights_workspace_size.argtypes = [
+                _SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64)]
             for fn in ENTRY_POINTS[2:]:
-                getattr(L, fn).restype = ctypes.c_int
+                if not fn.endswith("_workspace_size"):
+                    getattr(L, fn).restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -177,6 +188,42 @@ def moe_expert_ffn_bwd(s, dy_perm, x_perm, G, A, offsets, W1, W2, dx_perm, dW1, 
         _ptr(A, _act(s)), _ptr(offsets, _I32), _ptr(W1, _act(s)), _ptr(W2, _act(s)),
         _ptr(dx_perm, _act(s)), _ptr(dW1, _F32), _ptr(db1, _F32), _ptr(dW2, _F32),
         _ptr(db2, _F32), int(accumulate), _ptr(ws), _ptr(dev_status, _I32), _stream(stream)))
+
+
+def moe_expert_ffn_bwd_data(s, dy_perm, G, offsets, W1, W2, dH, dx_perm, db1, accumulate, ws,
+                            dev_status, stream=None):
+    _check("moe_expert_ffn_bwd_data", lib().moe_expert_ffn_bwd_data(
+        ctypes.byref(s), _ptr(dy_perm, _act(s)), _ptr(G, _act(s)), _ptr(offsets, _I32),
+        _ptr(W1, _act(s)), _ptr(W2, _act(s)), _ptr(dH, _act(s)), _ptr(dx_perm, _act(s)),
+        _ptr(db1, _F32), int(accumulate), _ptr(ws), _ptr(dev_status, _I32), _stream(stream)))
+
+
+def moe_expert_ffn_bwd_weights_workspace_size(s, chunk_T) -> int:
+    n = len(chunk_T)
+    arr = (ctypes.c_int64 * n)(*[int(t) for t in chunk_T])
+    return int(lib().moe_expert_ffn_bwd_weights_workspace_size(ctypes.byref(s), n, arr))
+
+
+def moe_expert_ffn_bwd_weights(s, chunk_T, offsets, dy_perm, x_perm, dH, A, dW1, dW2, db2,
+                               accumulate, ws, dev_status, stream=None):
+    """chunk_T: tokens of each dispatch chunk (a host sequence of ints);
+    offsets: int32 [nchunks, stride] (stride >= E+1, a multiple of 4); ws: a
+    uint8 device tensor (its size is passed) or None."""
+    n = len(chunk_T)
+    arr = (ctypes.c_int64 * n)(*[int(t) for t in chunk_T])
+    if isinstance(offsets, torch.Tensor):
+        if offsets.dim() != 2 or offsets.shape[0] != n:
+            raise MoEError("moe_expert_ffn_bwd_weights", MOE_ERR_INVALID,
+                           "offsets must be [nchunks, stride]")
+        stride = int(offsets.shape[1])
+    else:
+        raise MoEError("moe_expert_ffn_bwd_weights", MOE_ERR_INVALID, "offsets must be a tensor")
+    _check("moe_expert_ffn_bwd_weights", lib().moe_expert_ffn_bwd_weights(
+        ctypes.byref(s), n, arr, _ptr(offsets, _I32), stride, _ptr(dy_perm, _act(s)),
+        _ptr(x_perm, _act(s)), _ptr(dH, _act(s)), _ptr(A, _act(s)), _ptr(dW1, _F32),
+        _ptr(dW2, _F32), _ptr(db2, _F32), int(accumulate), _ptr(ws),
+        0 if ws is None else int(ws.numel() * ws.element_size()), _ptr(dev_status, _I32),
+        _stream(stream)))
 
 
 def moe_route_bwd(s, dw, logits, idx, w, perm, offsets, x, Wg, dx_perm, pos, dx, dWg,

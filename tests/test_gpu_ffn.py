@@ -101,3 +101,59 @@ def test_expert_ffn_fwd_bwd(dtype, T, d, f, E, k, zipf, shape, monkeypatch):
     torch.cuda.synchronize()
     for n in grads:
         assert torch.equal(grads[n], 2 * first[n]), n
+
+
+@pytest.mark.parametrize("dtype,nchunks,T,d,f,E,k", [
+    ("bf16", 3, 700, 256, 384, 8, 2),
+    ("bf16", 19, 100, 128, 192, 16, 3),    # more chunks than one launch walks: two launches
+    ("f32", 4, 150, 64, 96, 6, 2),
+])
+def test_expert_ffn_bwd_data_and_weights_over_chunks(dtype, nchunks, T, d, f, E, k):
+    """moe_expert_ffn_bwd_data per chunk, then moe_expert_ffn_bwd_weights over
+    all chunks in one call, against the oracle's per-chunk backward with the
+    weight gradients accumulated over the chunks."""
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    rb = dtype == "bf16"
+    cfg = synth.MoEConfig("t", T=T, d=d, f=f, E=E, k=k, renorm=1, dtype=dtype)
+    inp = synth.make_inputs(cfg, seed=E + nchunks, random_bias=True)
+    W = {n: inp[n].to(DEV) for n in ("W1", "b1", "W2", "b2")}
+    s = ops.make_shape(T, d, f, E, k, dtype, 1)
+    ws = torch.empty(ops.moe_workspace_size(s), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    P = T * k
+    stride = (E + 1 + 3) // 4 * 4
+    offs_all = torch.zeros(nchunks, stride, dtype=torch.int32)
+    g = torch.Generator().manual_seed(nchunks)
+    X_all, dY_all, G_all, A_all, dH_all = [], [], [], [], []
+    grads = None
+    db1_dev = torch.full((E, f), float("nan"), device=DEV)
+    dX_dev = torch.empty(P, d, dtype=tdt, device=DEV)
+    for c in range(nchunks):
+        # chunk c's routing: Zipf-shifted logits, a different shift per chunk
+        counts, offsets = _segments(T, E, k, 1.0 + 0.1 * c, seed=100 + c)
+        offs_all[c, :E + 1] = torch.from_numpy(offsets)
+        X = torch.randn(P, d, generator=g).to(tdt)
+        dY = torch.randn(P, d, generator=g).to(tdt)
+        rG, rA, _ = oracle.expert_ffn_fwd(X, offsets, inp["W1"], inp["b1"], inp["W2"], inp["b2"], rb)
+        res = oracle.expert_ffn_bwd(dY, X, rG, rA, offsets, inp["W1"], inp["W2"], rb, grads)
+        grads = dict(zip(("dW1", "db1", "dW2", "db2"), res[2:]))
+        G = torch.from_numpy(rG).to(tdt).to(DEV)
+        dH = torch.empty(P, f, dtype=tdt, device=DEV)
+        ops.moe_expert_ffn_bwd_data(s, dY.to(DEV), G, offs_all[c, :E + 1].to(DEV), W["W1"],
+                                    W["W2"], dH, dX_dev, db1_dev, int(c > 0), ws, st)
+        torch.cuda.synchronize()
+        assert_close(f"dX_perm[{c}]", dX_dev, res[1], dtype)
+        X_all.append(X)
+        dY_all.append(dY)
+        A_all.append(torch.from_numpy(rA).to(tdt))
+        dH_all.append(dH)
+    dW1 = torch.full((E, f, d), float("nan"), device=DEV)
+    dW2 = torch.full((E, d, f), float("nan"), device=DEV)
+    db2 = torch.full((E, d), float("nan"), device=DEV)
+    ops.moe_expert_ffn_bwd_weights(s, [T] * nchunks, offs_all.to(DEV), torch.cat(dY_all).to(DEV),
+                                   torch.cat(X_all).to(DEV), torch.cat(dH_all),
+                                   torch.cat(A_all).to(DEV), dW1, dW2, db2, 0, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for n, t in (("dW1", dW1), ("db1", db1_dev), ("dW2", dW2), ("db2", db2)):
+        assert_close(n, t, grads[n], dtype)

@@ -29,10 +29,10 @@ SMALL = {
 }
 
 
-def _run(cfg, inp, logits=None, pipeline=True):
+def _run(cfg, inp, logits=None, pipeline=True, defer_wgrad=None):
     g = to_dev(inp, DEV)
     lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
-                   chunk=cfg.chunk, device=DEV, pipeline=pipeline)
+                   chunk=cfg.chunk, device=DEV, pipeline=pipeline, defer_wgrad=defer_wgrad)
     lp.forward(g["x"], g["Wg"], g["W1"], g["b1"], g["W2"], g["b2"], g["beta"],
                compute_logits=logits is None,
                logits=None if logits is None else logits.to(DEV))
@@ -142,10 +142,11 @@ def test_layer_pipelined_equals_serial():
 ])
 def test_layer_recompute_equals_saved(name, kw):
     """Recomputing the permute and expert forward in the backward (only the
-    routing kept) gives the saved-activation pass's results bit for bit."""
+    routing kept) gives the saved-activation pass's results bit for bit (both
+    accumulate the weight gradients chunk by chunk)."""
     cfg = synth.CONFIGS[name].scaled(**kw)
     inp = synth.make_inputs(cfg, seed=11, random_bias=True)
-    saved = _run(cfg, inp, pipeline=False)
+    saved = _run(cfg, inp, pipeline=False, defer_wgrad=False)
     g = to_dev(inp, DEV)
     lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
                    chunk=cfg.chunk, device=DEV, recompute=True)
@@ -202,5 +203,20 @@ def test_layer_meets_the_h_storage_reading(name):
     ref = oracle.layer(inp, cfg.k, cfg.renorm, True, chunk=cfg.chunk, logits=L.double().numpy(),
                        store_h=True)
     lp = _run(cfg, inp, logits=L)
+    for n in ("y", "dx", "dw", "dW1", "db1", "dW2", "db2", "dWg"):
+        assert_close(n, getattr(lp, n), ref[n], cfg.dtype)
+
+
+@pytest.mark.parametrize("defer", [True, False])
+def test_layer_weight_gradient_modes_identical_logits(defer):
+    """The one weight-gradient pass over all chunks (default with several
+    chunks) and the chunk-by-chunk accumulation, each against the oracle, on
+    five dispatch chunks with a ragged last one, pipelined."""
+    cfg = synth.CONFIGS["longctx128_bf16"].scaled(T=2300, d=512, f=256, chunk=512)
+    inp = synth.make_inputs(cfg, seed=15, random_bias=True)
+    L = torch.from_numpy(oracle.router_logits(inp["x"], inp["Wg"], inp["beta"])).float()
+    ref = oracle.layer(inp, cfg.k, cfg.renorm, True, chunk=cfg.chunk, logits=L.double().numpy())
+    lp = _run(cfg, inp, logits=L, defer_wgrad=defer)
+    assert lp.defer_wgrad == defer and lp.pipeline
     for n in ("y", "dx", "dw", "dW1", "db1", "dW2", "db2", "dWg"):
         assert_close(n, getattr(lp, n), ref[n], cfg.dtype)
