@@ -29,9 +29,13 @@ int device_sm_count();
 
 // A1 (when compute_logits) + A2 + per-block histogram (block_counts laid out
 // [E][nblk]).  E <= 32 fuses all three in one kernel.
+// `part` (optional, part_bytes): scratch for the CUDA-core logits' split tiles
 cudaError_t launch_route_gate(const moe_shape& s, const void* x, const void* Wg,
                              const float* beta, float* logits, int compute_logits, int32_t* idx,
-                             float* w, int32_t* block_counts, int32_t* status, cudaStream_t st);
+                             float* w, int32_t* block_counts, float* part, size_t part_bytes,
+                             int32_t* status, cudaStream_t st);
+// scratch bytes of the CUDA-core router logits' split tiles
+size_t router_logits_workspace(const moe_shape& s);
 // A3 scan: block_counts -> block_base in place, counts, offsets
 cudaError_t launch_dispatch_scan(const moe_shape& s, int32_t* block_counts,
                                  int32_t* counts, int32_t* offsets, cudaStream_t st);

@@ -76,8 +76,12 @@ inline moe_status cuda_status(cudaError_t e) {
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-size_t route_ws(const moe_shape& s) {
+// block histograms, then the router logits' split tiles
+size_t route_counts_ws(const moe_shape& s) {
     return align_up((size_t)s.E * (size_t)route_blocks(s.T) * sizeof(int32_t));
+}
+size_t route_ws(const moe_shape& s) {
+    return route_counts_ws(s) + align_up(router_logits_workspace(s));
 }
 
 // column-sum partial rows of the bias gradients (either path)
@@ -143,10 +147,11 @@ moe_status moe_route(const moe_shape* s, const void* x, const void* Wg, const fl
     }
     cudaStream_t st = (cudaStream_t)stream;
     int32_t* block_counts = (int32_t*)ws;
+    float* part = (float*)((uint8_t*)ws + route_counts_ws(*s));
     cudaError_t e = cudaSuccess;
     if (s->T > 0)
         e = launch_route_gate(*s, x, Wg, logit_bias, logits, compute_logits, idx, w, block_counts,
-                              dev_status, st);
+                              part, router_logits_workspace(*s), dev_status, st);
     if (e == cudaSuccess) e = launch_dispatch_scan(*s, block_counts, counts, offsets, st);
     if (e == cudaSuccess && s->T > 0) e = launch_dispatch_rank(*s, idx, block_counts, pos, perm, st);
     return cuda_status(e);
@@ -528,9 +533,9 @@ moe_status moe_route_noalloc(const moe_shape* s, const void* x, const void* Wg,
     if (block_counts == nullptr) return MOE_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
-    if (s->T > 0)
+    if (s->T > 0)   // no scratch for split logits tiles here: whole tiles
         e = launch_route_gate(*s, x, Wg, logit_bias, logits, compute_logits, idx, w, block_counts,
-                              dev_status, st);
+                              nullptr, 0, dev_status, st);
     if (e == cudaSuccess) e = launch_dispatch_scan(*s, block_counts, counts, offsets, st);
     if (e == cudaSuccess && s->T > 0) e = launch_dispatch_rank(*s, idx, block_counts, pos, perm, st);
     return cuda_status(e);

@@ -87,140 +87,251 @@ template <> struct Vec<float> {
 // ---- A1: router logits for many experts: register-tiled SIMT GEMM ------------------
 //
 // logits[t][e] = sum_c x[t][c] Wg[e][c] + beta[e] with fp32 accumulation on the
-// CUDA cores.  Block tile 128 tokens x BN experts, K in steps of 16 through
-// double-buffered shared memory (fp32, K-major so that a thread reads 4
-// consecutive rows / columns as one float4); each of the 256 threads owns an
-// 8 x (BN/16) register tile: rows ty*4+i and 64+ty*4+i, columns tx*4+j (and
-// 64+tx*4+j when BN = 128).  Summation over K runs in index order.
+// CUDA cores.  Tile 128 tokens x 128 experts per block of 128 threads; each
+// thread owns 8 rows x 16 columns (rows ty*4+i and 64+ty*4+i, columns
+// g*32+tx*4+w), accumulated as packed fp32 pairs (fma.rn.f32x2: one issue slot
+// for two FMAs, each rounded as the scalar FMA).  K in steps of 16 through
+// double-buffered shared memory (fp32, K-major, so that a thread reads its 4
+// consecutive rows or columns as one 16-byte load).
+//
+// Work split ("stream-K"): the grid holds as many blocks as are co-resident,
+// and the (tile, K step) iterations of the whole problem are cut into equal
+// contiguous ranges, one per block, so every SM gets the same work whatever
+// the tile count.  A block whose range holds a whole tile writes its logits;
+// the pieces of a tile split between consecutive blocks go to scratch as fp32
+// partial tiles, and a fix-up kernel adds them in block order (= K order) and
+// adds beta: deterministic.  Without scratch (part == nullptr) every block
+// takes whole tiles.
 
-template <typename TIn, int BN>
-__global__ void __launch_bounds__(256, 2) router_logits_tiled_kernel(
+constexpr int kRtM = 128, kRtN = 128, kRtK = 16, kRtThreads = 128;
+
+__device__ __forceinline__ uint64_t rt_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void rt_unpack(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t rt_fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+struct RouterSplit {
+    int G;              // blocks
+    int64_t iters;      // tiles * ksteps
+    int ksteps;         // K steps of 16 per tile
+    int ntn;            // expert tiles
+    int maxp;           // pieces per block (scratch slots)
+};
+
+// first iteration of block b
+__device__ __forceinline__ int64_t rt_it0(const RouterSplit& sp, int b) {
+    return (int64_t)b * sp.iters / sp.G;
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(kRtThreads, 2) router_logits_tiled_kernel(
     int64_t T, int d, int E, const TIn* __restrict__ x, const TIn* __restrict__ Wg,
-    const float* __restrict__ beta, float* __restrict__ logits) {
-    constexpr int BM = 128, BK = 16;
-    constexpr int TN = BN / 16;          // 8 or 4 columns per thread
-    constexpr int VN = Vec<TIn>::N;      // elements per 16-byte load
-    constexpr int LA = BM * BK / VN / 256;  // 16-byte loads per thread per tile
-    constexpr int LB = BN * BK / VN / 256 > 0 ? BN * BK / VN / 256 : 1;
-    __shared__ __align__(16) float As[2][BK][BM];
-    __shared__ __align__(16) float Bs[2][BK][BN];
+    const float* __restrict__ beta, float* __restrict__ logits, float* __restrict__ part,
+    RouterSplit sp) {
+    constexpr int VN = Vec<TIn>::N;            // elements per 16-byte load
+    constexpr int LPR = kRtK / VN;             // 16-byte loads per row per K step
+    __shared__ __align__(16) float As[2][kRtK][kRtM];
+    __shared__ __align__(16) float Bs[2][kRtK][kRtN];
     const int tid = threadIdx.x;
-    const int tx = tid & 15, ty = tid >> 4;
-    const int64_t m0 = (int64_t)blockIdx.x * BM;
-    const int n0 = blockIdx.y * BN;
-    constexpr int CPR = BK / VN;         // 16-byte chunks per row of a tile
-
-    float ra[LA][VN], rb[LB][VN];
-    auto load_tiles = [&](int k0) {
-        #pragma unroll
-        for (int l = 0; l < LA; ++l) {
-            const int i = tid + 256 * l;
-            const int r = i / CPR, c = (i % CPR) * VN;
-            const int64_t gm = m0 + r;
-            if (gm < T && k0 + c < d) Vec<TIn>::load(x + gm * d + k0 + c, ra[l]);
-            else
-                #pragma unroll
-                for (int u = 0; u < VN; ++u) ra[l][u] = 0.f;
-        }
-        #pragma unroll
-        for (int l = 0; l < LB; ++l) {
-            const int i = tid + 256 * l;
-            const int r = i / CPR, c = (i % CPR) * VN;
-            const int gn = n0 + r;
-            if (r < BN && gn < E && k0 + c < d) Vec<TIn>::load(Wg + (int64_t)gn * d + k0 + c, rb[l]);
-            else
-                #pragma unroll
-                for (int u = 0; u < VN; ++u) rb[l][u] = 0.f;
-        }
-    };
-    auto store_tiles = [&](int buf) {
-        #pragma unroll
-        for (int l = 0; l < LA; ++l) {
-            const int i = tid + 256 * l;
-            const int r = i / CPR, c = (i % CPR) * VN;
+    const int ty = tid >> 3, tx = tid & 7;
+    const int b = blockIdx.x;
+    int64_t it = rt_it0(sp, b);
+    const int64_t it_end = rt_it0(sp, b + 1);
+    int piece = 0;
+    while (it < it_end) {
+        const int64_t tile = it / sp.ksteps;
+        const int ks0 = (int)(it % sp.ksteps);
+        const int64_t rem = it_end - it;
+        const int ks1 = (int)((int64_t)sp.ksteps < ks0 + rem ? (int64_t)sp.ksteps : ks0 + rem);
+        const int64_t m0 = (tile / sp.ntn) * kRtM;
+        const int n0 = (int)(tile % sp.ntn) * kRtN;
+        // this thread's row of the A tile (token m0 + tid) and of the B tile
+        // (expert n0 + tid), K columns [k, k + 16), kept packed until stored
+        uint4 ra[LPR], rb[LPR];
+        auto load = [&](int ks) {
+            const int k = ks * kRtK;
+            const int64_t gm = m0 + tid;
+            const int gn = n0 + tid;
             #pragma unroll
-            for (int u = 0; u < VN; ++u) As[buf][c + u][r] = ra[l][u];
-        }
-        #pragma unroll
-        for (int l = 0; l < LB; ++l) {
-            const int i = tid + 256 * l;
-            const int r = i / CPR, c = (i % CPR) * VN;
-            if (r < BN)
-                #pragma unroll
-                for (int u = 0; u < VN; ++u) Bs[buf][c + u][r] = rb[l][u];
-        }
-    };
-
-    float acc[8][TN];
-    #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        #pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
-
-    load_tiles(0);
-    store_tiles(0);
-    __syncthreads();
-    int buf = 0;
-    for (int k0 = 0; k0 < d; k0 += BK) {
-        const bool more = k0 + BK < d;
-        if (more) load_tiles(k0 + BK);
-        #pragma unroll
-        for (int kk = 0; kk < BK; ++kk) {
-            float a[8], b[TN];
-            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
-            a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
-            a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
-            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
-            b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
-            if (TN == 8) {
-                const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
-                b[TN - 4] = b1.x; b[TN - 3] = b1.y; b[TN - 2] = b1.z; b[TN - 1] = b1.w;
+            for (int l = 0; l < LPR; ++l) {
+                const int c = k + l * VN;
+                ra[l] = (gm < T && c < d) ? *reinterpret_cast<const uint4*>(x + gm * d + c)
+                                          : make_uint4(0, 0, 0, 0);
+                rb[l] = (gn < E && c < d)
+                            ? *reinterpret_cast<const uint4*>(Wg + (int64_t)gn * d + c)
+                            : make_uint4(0, 0, 0, 0);
             }
+        };
+        auto store = [&](int buf) {
             #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int l = 0; l < LPR; ++l) {
+                float va[VN], vb[VN];
+                Vec<TIn>::unpack(ra[l], va);
+                Vec<TIn>::unpack(rb[l], vb);
                 #pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
-        if (more) {
-            store_tiles(buf ^ 1);
-            __syncthreads();
-            buf ^= 1;
-        }
-    }
-    #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int64_t t = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
-        if (t >= T) continue;
+                for (int u = 0; u < VN; ++u) {
+                    As[buf][l * VN + u][tid] = va[u];
+                    Bs[buf][l * VN + u][tid] = vb[u];
+                }
+            }
+        };
+        uint64_t acc[8][8];
         #pragma unroll
-        for (int jj = 0; jj < TN; jj += 4) {
-            const int e0 = n0 + (jj < 4 ? tx * 4 : 64 + tx * 4);
-            float o[4];
+        for (int i = 0; i < 8; ++i)
             #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                o[j] = acc[i][jj + j] + ((beta && e0 + j < E) ? beta[e0 + j] : 0.f);
-            if ((E & 3) == 0 && e0 + 3 < E) {
-                *reinterpret_cast<float4*>(logits + t * E + e0) = make_float4(o[0], o[1], o[2], o[3]);
-            } else {
+            for (int j = 0; j < 8; ++j) acc[i][j] = 0;
+        __syncthreads();   // the previous piece's last reads of the buffers are done
+        load(ks0);
+        store(0);
+        __syncthreads();
+        int buf = 0;
+        for (int ks = ks0; ks < ks1; ++ks) {
+            const bool more = ks + 1 < ks1;
+            if (more) load(ks + 1);
+            #pragma unroll
+            for (int kk = 0; kk < kRtK; ++kk) {
+                const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+                uint64_t bp[8];
                 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (e0 + j < E) logits[t * E + e0 + j] = o[j];
+                for (int g = 0; g < 4; ++g) {
+                    const ulonglong2 v =
+                        *reinterpret_cast<const ulonglong2*>(&Bs[buf][kk][g * 32 + tx * 4]);
+                    bp[2 * g] = v.x;
+                    bp[2 * g + 1] = v.y;
+                }
+                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint64_t sa = rt_pack(a[i], a[i]);
+                    #pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[i][j] = rt_fma2(sa, bp[j], acc[i][j]);
+                }
+            }
+            if (more) {
+                store(buf ^ 1);
+                __syncthreads();
+                buf ^= 1;
             }
         }
+        const bool whole = ks0 == 0 && ks1 == sp.ksteps;
+        float* pt = whole ? nullptr : part + ((int64_t)b * sp.maxp + piece) * (kRtM * kRtN);
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4);
+            const int64_t t = m0 + r;
+            #pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int cl = g * 32 + tx * 4;   // column inside the tile
+                float o[4];
+                rt_unpack(acc[i][2 * g], o[0], o[1]);
+                rt_unpack(acc[i][2 * g + 1], o[2], o[3]);
+                if (!whole) {
+                    *reinterpret_cast<float4*>(pt + r * kRtN + cl) = make_float4(o[0], o[1], o[2], o[3]);
+                    continue;
+                }
+                if (t >= T) continue;
+                const int e0 = n0 + cl;
+                #pragma unroll
+                for (int j = 0; j < 4; ++j) o[j] += (beta && e0 + j < E) ? beta[e0 + j] : 0.f;
+                if ((E & 3) == 0 && e0 + 3 < E) {
+                    *reinterpret_cast<float4*>(logits + t * E + e0) = make_float4(o[0], o[1], o[2], o[3]);
+                } else {
+                    #pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (e0 + j < E) logits[t * E + e0 + j] = o[j];
+                }
+            }
+        }
+        it += ks1 - ks0;
+        ++piece;
     }
+}
+
+// Tiles split between blocks: logits = the pieces in block order + beta.  One
+// block per tile; tiles held whole by one block were written by it.
+__global__ void __launch_bounds__(256) router_logits_fixup_kernel(
+    int64_t T, int E, const float* __restrict__ beta, float* __restrict__ logits,
+    const float* __restrict__ part, RouterSplit sp) {
+    const int64_t tile = blockIdx.x;
+    const int64_t first = tile * sp.ksteps, last = first + sp.ksteps;   // iterations [first, last)
+    // the block holding iteration `first`: the last b with it0(b) <= first
+    int b = (int)(first * sp.G / sp.iters);
+    while (b + 1 < sp.G && rt_it0(sp, b + 1) <= first) ++b;
+    while (b > 0 && rt_it0(sp, b) > first) --b;
+    if (rt_it0(sp, b + 1) >= last && rt_it0(sp, b) <= first) return;   // whole in one block
+    const int64_t m0 = (tile / sp.ntn) * kRtM;
+    const int n0 = (int)(tile % sp.ntn) * kRtN;
+    for (int i = threadIdx.x; i < kRtM * kRtN; i += blockDim.x) {
+        const int r = i / kRtN, c = i % kRtN;
+        const int64_t t = m0 + r;
+        const int e = n0 + c;
+        if (t >= T || e >= E) continue;
+        float a = 0.f;
+        for (int bb = b; bb < sp.G && rt_it0(sp, bb) < last; ++bb) {
+            // the piece of block bb holding this tile: tiles counted from its first
+            const int64_t it0 = rt_it0(sp, bb);
+            if (rt_it0(sp, bb + 1) <= it0) continue;   // an empty block
+            const int pc = (int)(tile - it0 / sp.ksteps);
+            a += part[((int64_t)bb * sp.maxp + pc) * (kRtM * kRtN) + i];
+        }
+        logits[t * E + e] = a + (beta ? beta[e] : 0.f);
+    }
+}
+
+// Blocks of the router logits kernel that fit on the device at once.
+int router_logits_slots() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return device_sm_count() * 2;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, router_logits_tiled_kernel<__nv_bfloat16>, kRtThreads, 0);
+        cache[dev] = device_sm_count() * (n > 0 ? n : 1);
+    }
+    return cache[dev];
 }
 
 template <typename TIn>
 cudaError_t router_logits_dispatch(const moe_shape& s, const TIn* x, const TIn* Wg,
-                                   const float* beta, float* logits, cudaStream_t st) {
-    const int64_t T = s.T;
-    const unsigned gx = (unsigned)((T + 127) / 128);
-    if (s.E <= 64)
-        router_logits_tiled_kernel<TIn, 64><<<dim3(gx, (s.E + 63) / 64), 256, 0, st>>>(
-            T, s.d, s.E, x, Wg, beta, logits);
-    else
-        router_logits_tiled_kernel<TIn, 128><<<dim3(gx, (s.E + 127) / 128), 256, 0, st>>>(
-            T, s.d, s.E, x, Wg, beta, logits);
+                                   const float* beta, float* logits, float* part,
+                                   size_t part_bytes, cudaStream_t st) {
+    RouterSplit sp;
+    const int64_t mt = (s.T + kRtM - 1) / kRtM;
+    sp.ntn = (s.E + kRtN - 1) / kRtN;
+    sp.ksteps = (s.d + kRtK - 1) / kRtK;
+    const int64_t tiles = mt * sp.ntn;
+    sp.iters = tiles * sp.ksteps;
+    const int64_t slots = router_logits_slots();
+    const size_t tile_bytes = (size_t)kRtM * kRtN * sizeof(float);
+    bool split = part != nullptr && tiles % slots != 0;
+    if (split) {
+        sp.G = (int)(slots < sp.iters ? slots : sp.iters);
+        const int64_t per = (sp.iters + sp.G - 1) / sp.G;
+        sp.maxp = (int)(per / sp.ksteps + 2);
+        if ((size_t)sp.G * sp.maxp * tile_bytes > part_bytes) split = false;
+    }
+    if (!split) {   // whole tiles, one per block
+        sp.G = (int)tiles;
+        sp.maxp = 1;
+        part = nullptr;
+    }
+    if (sp.G <= 0) return cudaSuccess;
+    router_logits_tiled_kernel<TIn><<<sp.G, kRtThreads, 0, st>>>(s.T, s.d, s.E, x, Wg, beta,
+                                                                logits, part, sp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !split) return e;
+    router_logits_fixup_kernel<<<(unsigned)tiles, 256, 0, st>>>(s.T, s.E, beta, logits, part, sp);
     return cudaGetLastError();
 }
 
@@ -1002,9 +1113,17 @@ static bool router_on_tensor_cores() {
     return v && v[0] == '1';
 }
 
+size_t router_logits_workspace(const moe_shape& s) {
+    if (s.E <= 32) return 0;   // the fused small-E kernel
+    const int64_t tiles = ((s.T + kRtM - 1) / kRtM) * ((s.E + kRtN - 1) / kRtN);
+    // at most (tiles / G + 2) pieces per block, G <= 4 blocks per SM
+    return (size_t)(tiles + 8 * (int64_t)device_sm_count()) * kRtM * kRtN * sizeof(float);
+}
+
 cudaError_t launch_route_gate(const moe_shape& s, const void* x, const void* Wg,
                              const float* beta, float* logits, int compute_logits, int32_t* idx,
-                             float* w, int32_t* block_counts, int32_t* status, cudaStream_t st) {
+                             float* w, int32_t* block_counts, float* part, size_t part_bytes,
+                             int32_t* status, cudaStream_t st) {
     const bool bf = s.dtype == MOE_BF16;
     if (compute_logits && bf && s.d % 64 == 0 && router_on_tensor_cores()) {
         // bf16 logits on the tensor cores (fp32 accumulation), then the gate
@@ -1023,9 +1142,10 @@ cudaError_t launch_route_gate(const moe_shape& s, const void* x, const void* Wg,
     }
     if (compute_logits) {
         cudaError_t e = bf ? router_logits_dispatch(s, (const __nv_bfloat16*)x,
-                                                    (const __nv_bfloat16*)Wg, beta, logits, st)
+                                                    (const __nv_bfloat16*)Wg, beta, logits, part,
+                                                    part_bytes, st)
                            : router_logits_dispatch(s, (const float*)x, (const float*)Wg, beta,
-                                                    logits, st);
+                                                    logits, part, part_bytes, st);
         if (e != cudaSuccess) return e;
     }
     const int nblk = (int)route_blocks(s.T);
