@@ -445,6 +445,54 @@ def _measure(cfg, dev, steps, warmup, pipeline, graph_on, router_tc, recompute, 
     return res
 
 
+def measure_streaming(cfg, dev, steps, warmup, group, sampler=None, seed=0):
+    """Times `steps` layer steps with the expert weights in pinned host memory,
+    streamed one group of experts at a time (eager launches: the host copies
+    run on their own stream)."""
+    from mixture_experts_layer_11_gb300.streaming import ExpertStreamingPass
+    torch.cuda.reset_peak_memory_stats(dev)
+    inp = synth.make_inputs(cfg, seed=seed, device=str(dev))
+    host = {n: inp.pop(n).cpu().pin_memory() for n in ("W1", "b1", "W2", "b2")}
+    sp = ExpertStreamingPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
+                             chunk=cfg.chunk, group=group, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        sp.forward(inp["x"], inp["Wg"], host["W1"], host["b1"], host["W2"], host["b2"],
+                   inp["beta"])
+        sp.backward(inp["dy"], inp["x"], inp["Wg"], host["W1"], host["W2"])
+
+    for _ in range(warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    sp.check_status()
+    st = torch.cuda.current_stream()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ms = []
+    for _ in range(steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        step()
+        e1.record(st)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    clocks = sampler.stop() if sampler else None
+    sp.check_status()
+    esize = elem_bytes(cfg)
+    wbytes = 2 * cfg.E * cfg.d * cfg.f * esize
+    res = {"total_ms": sum(ms), "steps": steps, "group": group, "groups": len(sp.groups),
+           "device_memory_gib": torch.cuda.max_memory_allocated(dev) / 2**30,
+           "h2d_weight_bytes_per_step": 2 * wbytes + cfg.E * (cfg.d + cfg.f) * esize,
+           "d2h_grad_bytes_per_step": 2 * cfg.E * cfg.d * cfg.f * 4, "clocks": clocks}
+    del sp, host, inp
+    torch.cuda.empty_cache()
+    return res
+
+
 def _end_to_end(cfg, lp, inp, graph, flush, steps, warmup, dev):
     """A training loop's input pipeline through the public API: two device
     sets of inputs (x, dy) and outputs (y, dx), one CUDA graph per set.  The
@@ -595,6 +643,8 @@ def run_ours(args, cfg):
     ops.lib()  # fail loudly if the library is missing
     pk, pk_kind = peaks()
 
+    if args.weights_on_host:
+        return run_streaming(args, cfg, dev, rank, world, dist)
     # ---- the headline: the default router (CUDA cores), two-stream chunk
     # pipelining, one CUDA graph per step; clocks sampled over the timed steps
     sampler = ClockSampler(local)
@@ -698,6 +748,39 @@ def run_ours(args, cfg):
     return 0
 
 
+def run_streaming(args, cfg, dev, rank, world, dist):
+    """--weights-on-host: the step with the expert weights streamed from host
+    memory.  Prints one JSON line like the default mode (no per-workload table,
+    no end-to-end leg: the weights already cross the host link every step)."""
+    pk, pk_kind = peaks()
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    r = measure_streaming(cfg, dev, args.steps, args.warmup, args.group, sampler=sampler,
+                          seed=rank)
+    total_ms, = max_over_ranks([r["total_ms"]], dist, dev)
+    if rank != 0:
+        return 0
+    ms = total_ms / args.steps
+    line = {
+        "metric": METRIC, "value": whole_job_rate(cfg.T, args.steps, world, total_ms),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg.dtype, "data": "synthetic (seeded N(0,1) inputs, N(0,1/fan_in) weights)",
+        "tflops": (cfg.expert_flops() + cfg.router_flops()) / (ms / 1e3) / 1e12,
+        "config": {"workload": workload_desc(cfg), "T": cfg.T, "d_model": cfg.d,
+                   "d_ffn": cfg.f, "E": cfg.E, "k": cfg.k,
+                   "weights": f"pinned host memory, streamed in groups of {args.group} experts "
+                              f"({r['groups']} groups) per pass, fp32 weight gradients read back",
+                   "launch": "eager", "parallelism": f"replicas x{world}"},
+        "streaming": {k: r[k] for k in ("h2d_weight_bytes_per_step", "d2h_grad_bytes_per_step",
+                                         "device_memory_gib", "groups")},
+        "link_gbs_needed": (r["h2d_weight_bytes_per_step"] + r["d2h_grad_bytes_per_step"])
+        / (ms / 1e3) / 1e9,
+        "clocks": r["clocks"],
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -714,6 +797,11 @@ def main():
                          "over all chunks after the backward")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's kernels one by one instead of as one CUDA graph")
+    ap.add_argument("--weights-on-host", action="store_true",
+                    help="keep the expert weights in pinned host memory and stream them to "
+                         "the GPU one group of experts at a time")
+    ap.add_argument("--group", type=int, default=16,
+                    help="experts per streamed group (--weights-on-host)")
     ap.add_argument("--no-sub-configs", action="store_true",
                     help="time only the chosen workload (no per-workload table, no router "
                          "variant)")

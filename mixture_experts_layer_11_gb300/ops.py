@@ -207,19 +207,20 @@ def moe_expert_ffn_bwd_weights_workspace_size(s, chunk_T) -> int:
 def moe_expert_ffn_bwd_weights(s, chunk_T, offsets, dy_perm, x_perm, dH, A, dW1, dW2, db2,
                                accumulate, ws, dev_status, stream=None):
     """chunk_T: tokens of each dispatch chunk (a host sequence of ints);
-    offsets: int32 [nchunks, stride] (stride >= E+1, a multiple of 4); ws: a
+    offsets: int32 device tensor [nchunks, >= E+1] whose rows are the chunks'
+    expert offsets; it may be a column slice of a wider array (row stride a
+    multiple of 4 elements, columns contiguous), for a range of experts.  ws: a
     uint8 device tensor (its size is passed) or None."""
     n = len(chunk_T)
     arr = (ctypes.c_int64 * n)(*[int(t) for t in chunk_T])
-    if isinstance(offsets, torch.Tensor):
-        if offsets.dim() != 2 or offsets.shape[0] != n:
-            raise MoEError("moe_expert_ffn_bwd_weights", MOE_ERR_INVALID,
-                           "offsets must be [nchunks, stride]")
-        stride = int(offsets.shape[1])
-    else:
-        raise MoEError("moe_expert_ffn_bwd_weights", MOE_ERR_INVALID, "offsets must be a tensor")
-    _check("moe_expert_ffn_bwd_weights", lib().moe_expert_ffn_bwd_weights(
-        ctypes.byref(s), n, arr, _ptr(offsets, _I32), stride, _ptr(dy_perm, _act(s)),
+    fn = "moe_expert_ffn_bwd_weights"
+    if not isinstance(offsets, torch.Tensor) or offsets.dim() != 2 or offsets.shape[0] != n:
+        raise MoEError(fn, MOE_ERR_INVALID, "offsets must be a [nchunks, stride] tensor")
+    if not offsets.is_cuda or offsets.dtype != _I32 or offsets.stride(1) != 1:
+        raise MoEError(fn, MOE_ERR_INVALID, "offsets must be int32 CUDA rows")
+    stride = int(offsets.stride(0)) if n > 1 else max(int(offsets.shape[1]) + 3 & ~3, 4)
+    _check(fn, lib().moe_expert_ffn_bwd_weights(
+        ctypes.byref(s), n, arr, offsets.data_ptr(), stride, _ptr(dy_perm, _act(s)),
         _ptr(x_perm, _act(s)), _ptr(dH, _act(s)), _ptr(A, _act(s)), _ptr(dW1, _F32),
         _ptr(dW2, _F32), _ptr(db2, _F32), int(accumulate), _ptr(ws),
         0 if ws is None else int(ws.numel() * ws.element_size()), _ptr(dev_status, _I32),
