@@ -87,10 +87,10 @@ template <> struct Vec<float> {
 // ---- A1: router logits for many experts: register-tiled SIMT GEMM ------------------
 //
 // logits[t][e] = sum_c x[t][c] Wg[e][c] + beta[e] with fp32 accumulation on the
-// CUDA cores.  Tile 128 tokens x 128 experts per block of 128 threads; each
-// thread owns 8 rows x 16 columns (rows ty*4+i and 64+ty*4+i, columns
-// g*32+tx*4+w), accumulated as packed fp32 pairs (fma.rn.f32x2: one issue slot
-// for two FMAs, each rounded as the scalar FMA).  K in steps of 16 through
+// CUDA cores.  Tile 128 tokens x 32*NG experts (NG = 4, or 2 when E <= 64) per
+// block of 128 threads; each thread owns 8 rows x 4*NG columns (rows ty*4+i
+// and 64+ty*4+i, columns g*32+tx*4+w), accumulated as packed fp32 pairs
+// (fma.rn.f32x2: one issue slot for two FMAs, each rounded as the scalar FMA).  K in steps of 16 through
 // double-buffered shared memory (fp32, K-major, so that a thread reads its 4
 // consecutive rows or columns as one 16-byte load).
 //
@@ -103,7 +103,7 @@ template <> struct Vec<float> {
 // adds beta: deterministic.  Without scratch (part == nullptr) every block
 // takes whole tiles.
 
-constexpr int kRtM = 128, kRtN = 128, kRtK = 16, kRtThreads = 128;
+constexpr int kRtM = 128, kRtK = 16, kRtThreads = 128;
 
 __device__ __forceinline__ uint64_t rt_pack(float a, float b) {
     uint64_t r;
@@ -125,6 +125,7 @@ struct RouterSplit {
     int ksteps;         // K steps of 16 per tile
     int ntn;            // expert tiles
     int maxp;           // pieces per block (scratch slots)
+    int bn;             // experts per tile (32 * NG)
 };
 
 // first iteration of block b
@@ -132,15 +133,16 @@ __device__ __forceinline__ int64_t rt_it0(const RouterSplit& sp, int b) {
     return (int64_t)b * sp.iters / sp.G;
 }
 
-template <typename TIn>
+template <typename TIn, int NG>
 __global__ void __launch_bounds__(kRtThreads, 2) router_logits_tiled_kernel(
     int64_t T, int d, int E, const TIn* __restrict__ x, const TIn* __restrict__ Wg,
     const float* __restrict__ beta, float* __restrict__ logits, float* __restrict__ part,
     RouterSplit sp) {
     constexpr int VN = Vec<TIn>::N;            // elements per 16-byte load
     constexpr int LPR = kRtK / VN;             // 16-byte loads per row per K step
+    constexpr int BNT = 32 * NG;               // experts per tile
     __shared__ __align__(16) float As[2][kRtK][kRtM];
-    __shared__ __align__(16) float Bs[2][kRtK][kRtN];
+    __shared__ __align__(16) float Bs[2][kRtK][BNT];
     const int tid = threadIdx.x;
     const int ty = tid >> 3, tx = tid & 7;
     const int b = blockIdx.x;
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(kRtThreads, 2) router_logits_tiled_kernel(
         const int64_t rem = it_end - it;
         const int ks1 = (int)((int64_t)sp.ksteps < ks0 + rem ? (int64_t)sp.ksteps : ks0 + rem);
         const int64_t m0 = (tile / sp.ntn) * kRtM;
-        const int n0 = (int)(tile % sp.ntn) * kRtN;
+        const int n0 = (int)(tile % sp.ntn) * BNT;
         // this thread's row of the A tile (token m0 + tid) and of the B tile
         // (expert n0 + tid), K columns [k, k + 16), kept packed until stored
         uint4 ra[LPR], rb[LPR];
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(kRtThreads, 2) router_logits_tiled_kernel(
                 const int c = k + l * VN;
                 ra[l] = (gm < T && c < d) ? *reinterpret_cast<const uint4*>(x + gm * d + c)
                                           : make_uint4(0, 0, 0, 0);
-                rb[l] = (gn < E && c < d)
+                rb[l] = (tid < BNT && gn < E && c < d)
                             ? *reinterpret_cast<const uint4*>(Wg + (int64_t)gn * d + c)
                             : make_uint4(0, 0, 0, 0);
             }
@@ -180,15 +182,15 @@ __global__ void __launch_bounds__(kRtThreads, 2) router_logits_tiled_kernel(
                 #pragma unroll
                 for (int u = 0; u < VN; ++u) {
                     As[buf][l * VN + u][tid] = va[u];
-                    Bs[buf][l * VN + u][tid] = vb[u];
+                    if (tid < BNT) Bs[buf][l * VN + u][tid] = vb[u];
                 }
             }
         };
-        uint64_t acc[8][8];
+        uint64_t acc[8][2 * NG];
         #pragma unroll
         for (int i = 0; i < 8; ++i)
             #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = 0;
+            for (int j = 0; j < 2 * NG; ++j) acc[i][j] = 0;
         __syncthreads();   // the previous piece's last reads of the buffers are done
         load(ks0);
         store(0);
@@ -201,9 +203,9 @@ __global__ void __launch_bounds__(kRtThreads, 2) router_logits_tiled_kernel(
             for (int kk = 0; kk < kRtK; ++kk) {
                 const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
                 const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
-                uint64_t bp[8];
+                uint64_t bp[2 * NG];
                 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
+                for (int g = 0; g < NG; ++g) {
                     const ulonglong2 v =
                         *reinterpret_cast<const ulonglong2*>(&Bs[buf][kk][g * 32 + tx * 4]);
                     bp[2 * g] = v.x;
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(kRtThreads, 2) router_logits_tiled_kernel(
                 for (int i = 0; i < 8; ++i) {
                     const uint64_t sa = rt_pack(a[i], a[i]);
                     #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][j] = rt_fma2(sa, bp[j], acc[i][j]);
+                    for (int j = 0; j < 2 * NG; ++j) acc[i][j] = rt_fma2(sa, bp[j], acc[i][j]);
                 }
             }
             if (more) {
@@ -224,19 +226,19 @@ __global__ void __launch_bounds__(kRtThreads, 2) router_logits_tiled_kernel(
             }
         }
         const bool whole = ks0 == 0 && ks1 == sp.ksteps;
-        float* pt = whole ? nullptr : part + ((int64_t)b * sp.maxp + piece) * (kRtM * kRtN);
+        float* pt = whole ? nullptr : part + ((int64_t)b * sp.maxp + piece) * (kRtM * BNT);
         #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4);
             const int64_t t = m0 + r;
             #pragma unroll
-            for (int g = 0; g < 4; ++g) {
+            for (int g = 0; g < NG; ++g) {
                 const int cl = g * 32 + tx * 4;   // column inside the tile
                 float o[4];
                 rt_unpack(acc[i][2 * g], o[0], o[1]);
                 rt_unpack(acc[i][2 * g + 1], o[2], o[3]);
                 if (!whole) {
-                    *reinterpret_cast<float4*>(pt + r * kRtN + cl) = make_float4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<float4*>(pt + r * BNT + cl) = make_float4(o[0], o[1], o[2], o[3]);
                     continue;
                 }
                 if (t >= T) continue;
@@ -258,48 +260,81 @@ __global__ void __launch_bounds__(kRtThreads, 2) router_logits_tiled_kernel(
 }
 
 // Tiles split between blocks: logits = the pieces in block order + beta.  One
-// block per tile; tiles held whole by one block were written by it.
+// block per tile; tiles held whole by one block were written by it.  The
+// tile's pieces (block, piece index) are listed once in shared memory.
 __global__ void __launch_bounds__(256) router_logits_fixup_kernel(
     int64_t T, int E, const float* __restrict__ beta, float* __restrict__ logits,
     const float* __restrict__ part, RouterSplit sp) {
+    constexpr int kMaxPieces = 32;   // > the 16 blocks a tile is shared by, plus its ends
+    __shared__ int npc;
+    __shared__ int64_t pslot[kMaxPieces];
     const int64_t tile = blockIdx.x;
-    const int64_t first = tile * sp.ksteps, last = first + sp.ksteps;   // iterations [first, last)
-    // the block holding iteration `first`: the last b with it0(b) <= first
-    int b = (int)(first * sp.G / sp.iters);
-    while (b + 1 < sp.G && rt_it0(sp, b + 1) <= first) ++b;
-    while (b > 0 && rt_it0(sp, b) > first) --b;
-    if (rt_it0(sp, b + 1) >= last && rt_it0(sp, b) <= first) return;   // whole in one block
-    const int64_t m0 = (tile / sp.ntn) * kRtM;
-    const int n0 = (int)(tile % sp.ntn) * kRtN;
-    for (int i = threadIdx.x; i < kRtM * kRtN; i += blockDim.x) {
-        const int r = i / kRtN, c = i % kRtN;
-        const int64_t t = m0 + r;
-        const int e = n0 + c;
-        if (t >= T || e >= E) continue;
-        float a = 0.f;
-        for (int bb = b; bb < sp.G && rt_it0(sp, bb) < last; ++bb) {
-            // the piece of block bb holding this tile: tiles counted from its first
-            const int64_t it0 = rt_it0(sp, bb);
-            if (rt_it0(sp, bb + 1) <= it0) continue;   // an empty block
-            const int pc = (int)(tile - it0 / sp.ksteps);
-            a += part[((int64_t)bb * sp.maxp + pc) * (kRtM * kRtN) + i];
+    if (threadIdx.x == 0) {
+        const int64_t first = tile * sp.ksteps, last = first + sp.ksteps;   // iterations
+        // the block holding iteration `first`: the last b with it0(b) <= first
+        int b = (int)(first * sp.G / sp.iters);
+        while (b + 1 < sp.G && rt_it0(sp, b + 1) <= first) ++b;
+        while (b > 0 && rt_it0(sp, b) > first) --b;
+        int n = 0;
+        if (!(rt_it0(sp, b) <= first && rt_it0(sp, b + 1) >= last)) {   // not whole
+            for (int bb = b; bb < sp.G && n < kMaxPieces; ++bb) {
+                const int64_t it0 = rt_it0(sp, bb);
+                if (it0 >= last) break;
+                if (rt_it0(sp, bb + 1) <= it0) continue;   // an empty block
+                // the piece of block bb holding this tile: tiles counted from its first
+                pslot[n++] = ((int64_t)bb * sp.maxp + (tile - it0 / sp.ksteps)) *
+                             ((int64_t)kRtM * sp.bn);
+            }
         }
-        logits[t * E + e] = a + (beta ? beta[e] : 0.f);
+        npc = n;
+    }
+    __syncthreads();
+    const int n = npc;
+    if (n == 0) return;
+    const int64_t m0 = (tile / sp.ntn) * kRtM;
+    const int n0 = (int)(tile % sp.ntn) * sp.bn;
+    const int vpr = sp.bn / 4;   // float4 per tile row
+    for (int i = threadIdx.x; i < kRtM * vpr; i += blockDim.x) {
+        const int r = i / vpr, c = (i % vpr) * 4;
+        const int64_t t = m0 + r;
+        if (t >= T) continue;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < n; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(part + pslot[q] + r * sp.bn + c);
+            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+        }
+        const int e0 = n0 + c;
+        float o[4] = {a.x, a.y, a.z, a.w};
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] += (beta && e0 + j < E) ? beta[e0 + j] : 0.f;
+        if ((E & 3) == 0 && e0 + 3 < E) {
+            *reinterpret_cast<float4*>(logits + t * E + e0) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+            #pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (e0 + j < E) logits[t * E + e0 + j] = o[j];
+        }
     }
 }
 
-// Blocks of the router logits kernel that fit on the device at once.
-int router_logits_slots() {
-    static int cache[64] = {0};
+// Blocks of the router logits kernel (64- or 128-expert tiles) that fit on the
+// device at once.
+int router_logits_slots(bool narrow) {
+    static int cache[64][2] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return device_sm_count() * 2;
-    if (cache[dev] == 0) {
+    int& c = cache[dev][narrow ? 1 : 0];
+    if (c == 0) {
         int n = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, router_logits_tiled_kernel<__nv_bfloat16>, kRtThreads, 0);
-        cache[dev] = device_sm_count() * (n > 0 ? n : 1);
+        if (narrow)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &n, router_logits_tiled_kernel<__nv_bfloat16, 2>, kRtThreads, 0);
+        else
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &n, router_logits_tiled_kernel<__nv_bfloat16, 4>, kRtThreads, 0);
+        c = device_sm_count() * (n > 0 ? n : 1);
     }
-    return cache[dev];
+    return c;
 }
 
 template <typename TIn>
@@ -307,16 +342,21 @@ cudaError_t router_logits_dispatch(const moe_shape& s, const TIn* x, const TIn* 
                                    const float* beta, float* logits, float* part,
                                    size_t part_bytes, cudaStream_t st) {
     RouterSplit sp;
+    const bool narrow = s.E <= 64;   // 64-expert tiles
+    sp.bn = narrow ? 64 : 128;
     const int64_t mt = (s.T + kRtM - 1) / kRtM;
-    sp.ntn = (s.E + kRtN - 1) / kRtN;
+    sp.ntn = (s.E + sp.bn - 1) / sp.bn;
     sp.ksteps = (s.d + kRtK - 1) / kRtK;
     const int64_t tiles = mt * sp.ntn;
     sp.iters = tiles * sp.ksteps;
-    const int64_t slots = router_logits_slots();
-    const size_t tile_bytes = (size_t)kRtM * kRtN * sizeof(float);
+    const int64_t slots = router_logits_slots(narrow);
+    const size_t tile_bytes = (size_t)kRtM * sp.bn * sizeof(float);
     bool split = part != nullptr && tiles % slots != 0;
     if (split) {
-        sp.G = (int)(slots < sp.iters ? slots : sp.iters);
+        // at most 16 blocks share a tile (the fix-up lists a tile's pieces)
+        int64_t g = slots < sp.iters ? slots : sp.iters;
+        if (g > 16 * tiles) g = 16 * tiles;
+        sp.G = (int)g;
         const int64_t per = (sp.iters + sp.G - 1) / sp.G;
         sp.maxp = (int)(per / sp.ksteps + 2);
         if ((size_t)sp.G * sp.maxp * tile_bytes > part_bytes) split = false;
@@ -327,8 +367,12 @@ cudaError_t router_logits_dispatch(const moe_shape& s, const TIn* x, const TIn* 
         part = nullptr;
     }
     if (sp.G <= 0) return cudaSuccess;
-    router_logits_tiled_kernel<TIn><<<sp.G, kRtThreads, 0, st>>>(s.T, s.d, s.E, x, Wg, beta,
-                                                                logits, part, sp);
+    if (narrow)
+        router_logits_tiled_kernel<TIn, 2><<<sp.G, kRtThreads, 0, st>>>(s.T, s.d, s.E, x, Wg,
+                                                                       beta, logits, part, sp);
+    else
+        router_logits_tiled_kernel<TIn, 4><<<sp.G, kRtThreads, 0, st>>>(s.T, s.d, s.E, x, Wg,
+                                                                       beta, logits, part, sp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !split) return e;
     router_logits_fixup_kernel<<<(unsigned)tiles, 256, 0, st>>>(s.T, s.E, beta, logits, part, sp);
@@ -1115,9 +1159,10 @@ static bool router_on_tensor_cores() {
 
 size_t router_logits_workspace(const moe_shape& s) {
     if (s.E <= 32) return 0;   // the fused small-E kernel
-    const int64_t tiles = ((s.T + kRtM - 1) / kRtM) * ((s.E + kRtN - 1) / kRtN);
+    const int bn = s.E <= 64 ? 64 : 128;
+    const int64_t tiles = ((s.T + kRtM - 1) / kRtM) * ((s.E + bn - 1) / bn);
     // at most (tiles / G + 2) pieces per block, G <= 4 blocks per SM
-    return (size_t)(tiles + 8 * (int64_t)device_sm_count()) * kRtM * kRtN * sizeof(float);
+    return (size_t)(tiles + 8 * (int64_t)device_sm_count()) * kRtM * bn * sizeof(float);
 }
 
 cudaError_t launch_route_gate(const moe_shape& s, const void* x, const void* Wg,
