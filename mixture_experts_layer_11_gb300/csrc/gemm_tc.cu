@@ -224,10 +224,18 @@ struct Tile {
 struct SegCursor {
     int seg, kl, rows;   // current segment, K block inside it, the segment's rows
     int row0;            // first row of the segment (global row coordinate)
+    const int* soff;     // one segment: its offsets in shared memory (else null)
     __device__ __forceinline__ void next_segment(const TcParams& p, int e) {
         for (++seg; seg < p.nseg; ++seg) {
-            const int32_t* o = p.offsets + (int64_t)seg * p.ostride;
-            const int a = __ldg(o + e), b = __ldg(o + e + 1);
+            int a, b;
+            if (soff) {
+                a = soff[e];
+                b = soff[e + 1];
+            } else {
+                const int32_t* o = p.offsets + (int64_t)seg * p.ostride;
+                a = __ldg(o + e);
+                b = __ldg(o + e + 1);
+            }
             if (b > a) {
                 rows = b - a;
                 row0 = (int)(p.seg_base[seg] + a);
@@ -239,8 +247,11 @@ struct SegCursor {
         row0 = 0;
         kl = 0;
     }
-    // position at K block kb0 of the expert's blocks, counted over its segments
-    __device__ __forceinline__ void start(const TcParams& p, int e, int kb0) {
+    // position at K block kb0 of the expert's blocks, counted over its segments;
+    // off: the per-expert row prefix in shared memory, which for one segment
+    // (seg_base 0) is that segment's offsets
+    __device__ __forceinline__ void start(const TcParams& p, int e, int kb0, const int* off) {
+        soff = p.nseg == 1 && p.seg_base[0] == 0 ? off : nullptr;
         seg = -1;
         next_segment(p, e);
         while (seg < p.nseg) {
@@ -260,7 +271,7 @@ struct SegCursor {
     __device__ __forceinline__ int valid() const { return rows - kl * BK; }   // rows of this block
 };
 
-template <bool VAR_K, bool PAIR, typename C>
+template <bool VAR_K, bool PAIR, bool MULTI, typename C>
 __device__ __forceinline__ Tile get_tile(const C& c, const TcParams& p, int t, int& ecur,
                                          int rank) {
     using S = Shape<PAIR>;
@@ -276,6 +287,23 @@ __device__ __forceinline__ Tile get_tile(const C& c, const TcParams& p, int t, i
         ti.rows = min(BM, c.off[ecur + 1] - ti.row0);
         ti.num_kb = p.K / BK;
         ti.ones = false;
+        ti.kb0 = 0;
+        ti.slot = -1;
+        ti.bslot = -1;
+    } else if (!MULTI) {
+        // one segment, no split: an expert's MT x (NT + all-ones) units, m-tile
+        // groups each followed by its all-ones tile
+        const int NTX = NT + (p.bsum ? 1 : 0);
+        const int MT = (p.M + S::TILE_M - 1) / S::TILE_M;
+        const int per = MT * NTX;
+        ti.e = c.order[t / per];
+        const int local = t % per;
+        ti.mt = local / NTX;
+        ti.nt = local % NTX;
+        ti.ones = ti.nt == NT;
+        ti.row0 = c.off[ti.e];
+        ti.rows = c.off[ti.e + 1] - ti.row0;
+        ti.num_kb = (ti.rows + BK - 1) / BK;
         ti.kb0 = 0;
         ti.slot = -1;
         ti.bslot = -1;
@@ -504,7 +532,7 @@ __device__ __forceinline__ void tmem_ld_cw(uint32_t taddr, float (&v)[CW]) {
     else tmem_ld16(taddr, v);
 }
 
-template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool PAIR>
+template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool PAIR, bool MULTI>
 __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB,
@@ -564,7 +592,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             tmem_relinquish();
         }
     }
-    if (!VAR_K) {
+    if (!VAR_K || !MULTI) {
         for (int i = threadIdx.x; i <= E; i += THREADS)
             c.off[i] = p.offsets ? p.offsets[i] : (i == 0 ? 0 : (int)p.P);   // null: rows [0, P)
     } else {
@@ -622,8 +650,15 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             }
             c.order[r] = e;
         }
-        __syncthreads();
-        if (threadIdx.x == 0) {
+        if (!MULTI && threadIdx.x == 0) {
+            int act = 0;
+            for (int e = 0; e < E; ++e) act += (c.off[e + 1] - c.off[e]) > 0;
+            const int MT = (p.M + S::TILE_M - 1) / S::TILE_M;
+            const int NTX = NT + (p.bsum ? 1 : 0);
+            c.nactive = (p.accumulate ? act : E) * MT * NTX;  // number of work units
+        }
+        if (MULTI) __syncthreads();
+        if (MULTI && threadIdx.x == 0) {
             int act = 0;
             for (int e = 0; e < E; ++e) act += (c.off[e + 1] - c.off[e]) > 0;
             const int MT = (p.M + S::TILE_M - 1) / S::TILE_M;
@@ -663,9 +698,9 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
             bool ok = true;
             for (int t = unit0; t < num_units && ok; t += nunits) {
-                const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
+                const Tile ti = get_tile<VAR_K, PAIR, MULTI>(c, p, t, ecur, rank);
                 SegCursor cur;
-                if (VAR_K) cur.start(p, ti.e, ti.kb0);
+                if (VAR_K && MULTI) cur.start(p, ti.e, ti.kb0, c.off);
                 for (int kb = 0; kb < ti.num_kb; ++kb) {
                     if (leader && t == p.withhold_unit && kb == p.withhold_kb) {
                         // test hook: issue nothing more (no copy is left in
@@ -697,7 +732,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     }
                     // a weight-gradient pair's odd CTA loads a segment's last K block
                     // onto its own barrier, for its relay warp to zero the tail first
-                    const bool relay = PAIR && VAR_K && !leader && cur.valid() < BK;
+                    const int kvalid = MULTI ? cur.valid() : ti.rows - kb * BK;
+                    const bool relay = PAIR && VAR_K && !leader && kvalid < BK;
                     if (PAIR && !leader && !relay) mbar_arrive_expect_tx_cluster(fbc, bytes);
                     else mbar_arrive_expect_tx(fb, bytes);
                     auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
@@ -721,11 +757,11 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     } else {
                         // one box per operand: this CTA's 64-column slabs of BK rows
                         // (maps: {column in slab, row, slab})
-                        const int r = cur.row();
+                        const int r = MULTI ? cur.row() : ti.row0 + kb * BK;
                         const int mA = ti.mt * S::TILE_M + rank * BM;
                         load3(sA, &mapA, 0, r, mA / 64);
                         if (!ti.ones) load3(sB, &mapB, 0, r, nB / 64);
-                        cur.advance(p, ti.e);
+                        if (MULTI) cur.advance(p, ti.e);
                     }
                     issued_parity[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -763,12 +799,12 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             uint32_t local_phase = 0;   // bit s: parity of stage s's next own phase
             bool ok = true;
             for (int t = unit0; t < num_units && ok; t += nunits) {
-                const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
+                const Tile ti = get_tile<VAR_K, PAIR, MULTI>(c, p, t, ecur, rank);
                 SegCursor cur;
-                cur.start(p, ti.e, ti.kb0);
+                if (MULTI) cur.start(p, ti.e, ti.kb0, c.off);
                 for (int kb = 0; kb < ti.num_kb; ++kb) {
-                    const int valid = cur.valid();
-                    cur.advance(p, ti.e);
+                    const int valid = MULTI ? cur.valid() : ti.rows - kb * BK;
+                    if (MULTI) cur.advance(p, ti.e);
                     if (valid < BK) {
                         if (!mbar_wait_warp(smem_u32(&c.full[stage]), (local_phase >> stage) & 1u,
                                             p.limit_ns, &c.abort_flag)) {
@@ -810,10 +846,10 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int t = unit0; t < num_units && ok; t += nunits) {
-                const Tile ti = get_tile<VAR_K, PAIR>(c, p, t, ecur, rank);
+                const Tile ti = get_tile<VAR_K, PAIR, MULTI>(c, p, t, ecur, rank);
                 if (ti.num_kb == 0) continue;
                 SegCursor cur;
-                if (VAR_K) cur.start(p, ti.e, ti.kb0);
+                if (VAR_K && MULTI) cur.start(p, ti.e, ti.kb0, c.off);
                 if (!mbar_wait_warp(smem_u32(&c.tempty[acc]), acc_phase ^ 1, p.limit_ns,
                                     &c.abort_flag)) {
                     raise_abort(c, p);
@@ -830,8 +866,8 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     }
                     tc_fence_after();
                     if (VAR_K) {
-                        zero_tail(stage, cur.valid());
-                        cur.advance(p, ti.e);
+                        zero_tail(stage, MULTI ? cur.valid() : ti.rows - kb * BK);
+                        if (MULTI) cur.advance(p, ti.e);
                         __syncwarp();
                     }
                     if (lane == 0) {
@@ -919,7 +955,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             }
         };
         Tile tcur;
-        if (unit0 < num_units) tcur = get_tile<VAR_K, PAIR>(c, p, unit0, ecur, rank);
+        if (unit0 < num_units) tcur = get_tile<VAR_K, PAIR, MULTI>(c, p, unit0, ecur, rank);
         float bnext[BW];
         bool aborted = false;
         if (kAux && unit0 < num_units) {
@@ -930,7 +966,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
         for (int t = unit0; t < num_units; t += nunits) {
             const Tile ti = tcur;
             const bool has_next = t + nunits < num_units;
-            if (has_next) tcur = get_tile<VAR_K, PAIR>(c, p, t + nunits, ecur, rank);
+            if (has_next) tcur = get_tile<VAR_K, PAIR, MULTI>(c, p, t + nunits, ecur, rank);
             const bool mma_tile = ti.num_kb > 0;
             const int gc_tile = gc;   // GELU' chunks consumed before this tile
             float* bias_s = bias_base + ew * ES::COLS;
@@ -971,7 +1007,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                 if (mma_tile) tmem_ld32(trow, v);
                 else v[0] = 0.f;
                 const int m = ti.mt * S::TILE_M + rank * BM + q * 32 + lane;
-                if (ti.bslot >= 0) {   // a split part > 0: its scratch row
+                if (MULTI && ti.bslot >= 0) {   // a split part > 0: its scratch row
                     p.bpart[(int64_t)ti.bslot * S::TILE_M + rank * BM + q * 32 + lane] = v[0];
                 } else if (m < p.M) {
                     float* o = p.bsum + (int64_t)ti.e * p.M + m;
@@ -1134,7 +1170,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                if (ti.slot >= 0)   // a split part > 0: its scratch slot
+                                if (MULTI && ti.slot >= 0)   // a split part > 0: its scratch slot
                                     tma_store_3d(&mapO1, smem_u32(stg), cl + hh * 16,
                                                  rank * BM + q * 32, ti.slot);
                                 else if (p.accumulate)
@@ -1251,11 +1287,11 @@ void withhold_hook(TcParams& p) {
     p.withhold_kb = (int)kb;
 }
 
-template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool PAIR>
+template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool PAIR, bool MULTI>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
                       const CUtensorMap& o1, const TcParams& p_in, int64_t units_upper,
                       cudaStream_t st, int* units_out) {
-    auto kern = gemm_tc_kernel<VAR_K, A_MN, B_MN, EPI, PAIR>;
+    auto kern = gemm_tc_kernel<VAR_K, A_MN, B_MN, EPI, PAIR, MULTI>;
     constexpr size_t SMEM = smem_bytes<PAIR, VAR_K, EPI>();
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
     constexpr int THREADS = EpiShape<EPI, VAR_K>::THREADS;
@@ -1312,14 +1348,16 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
     return cudaLaunchKernelEx(&cfg, kern, a, b, o0, o1, p);
 }
 
-template <bool VAR_K, bool A_MN, bool B_MN, int EPI>
+template <bool VAR_K, bool A_MN, bool B_MN, int EPI, bool MULTI = false>
 cudaError_t launch_either(bool pair, const CUtensorMap& a, const CUtensorMap& b,
                           const CUtensorMap& o0, const CUtensorMap& o1, const TcParams& p,
                           int64_t units1, int64_t units2, cudaStream_t st,
                           int* units_out = nullptr) {
     if (pair)
-        return launch_tc<VAR_K, A_MN, B_MN, EPI, true>(a, b, o0, o1, p, units2, st, units_out);
-    return launch_tc<VAR_K, A_MN, B_MN, EPI, false>(a, b, o0, o1, p, units1, st, units_out);
+        return launch_tc<VAR_K, A_MN, B_MN, EPI, true, MULTI>(a, b, o0, o1, p, units2, st,
+                                                              units_out);
+    return launch_tc<VAR_K, A_MN, B_MN, EPI, false, MULTI>(a, b, o0, o1, p, units1, st,
+                                                           units_out);
 }
 
 // Adds the split parts > 0 of the weight-gradient tiles (scratch slots, fp32
@@ -1577,9 +1615,14 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
     // in the epilogue's 32 x 16 boxes
     const int tile_m = pair ? 2 * BM : BM;
     const int64_t slot_bytes = (int64_t)tile_m * BN * 4;
+    // The segment walk and the split are compiled into a kernel of their own
+    // (MULTI): a one-segment call whose experts cannot exceed kKbPartMin K blocks
+    // takes the lean kernel, without their code and set-up.
+    const bool multi = g.nseg > 1 || g.P > (int64_t)kKbPartMin * BK;
     // each partial tile's slot also reserves one row-sum row (tile_m floats)
     // after the tiles; the row sums of a split need at most one per N tiles
-    int64_t cap = g.part ? (int64_t)(g.part_bytes / (size_t)(slot_bytes + tile_m * 4)) : 0;
+    int64_t cap = (multi && g.part) ? (int64_t)(g.part_bytes / (size_t)(slot_bytes + tile_m * 4))
+                                    : 0;
     if (cap > ((int64_t)1 << 30)) cap = (int64_t)1 << 30;
     float* bpart = g.part ? g.part + cap * tile_m * BN : nullptr;
     CUtensorMap mpart;
@@ -1607,8 +1650,11 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
     // u1 / u2 bound the grid only; with a split there are more units than that
     const int64_t big = (int64_t)1 << 30;
     int units = 0;
-    cudaError_t e = launch_either<true, true, true, (int)Epi::Plain>(
-        pair, ma, mb, mo, mpart, p, cap > 0 ? big : u1, cap > 0 ? big : u2, st, &units);
+    cudaError_t e =
+        multi ? launch_either<true, true, true, (int)Epi::Plain, true>(
+                    pair, ma, mb, mo, mpart, p, cap > 0 ? big : u1, cap > 0 ? big : u2, st, &units)
+              : launch_either<true, true, true, (int)Epi::Plain, false>(pair, ma, mb, mo, mo, p,
+                                                                        u1, u2, st, &units);
     if (e != cudaSuccess || cap == 0) return e;
     const int64_t n4 = (int64_t)g.M * g.N / 4;
     const unsigned gx = (unsigned)(n4 / 256 < 64 ? (n4 + 255) / 256 : 64);
