@@ -117,7 +117,8 @@ template <int EPI, bool VAR_K> struct EpiShape {
     static constexpr int COLS = BN / (WARPS / 4);          // columns per warp
     static constexpr int NCH = COLS / CW;                  // chunks per warp
     static constexpr int CHUNK_BYTES = 32 * CW * 2;        // one staged bf16 chunk
-    static constexpr int THREADS = 32 * (2 + WARPS);
+    // + the tail-relay warp of the weight gradients (see the kernel)
+    static constexpr int THREADS = 32 * (2 + WARPS + (VAR_K ? 1 : 0));
 };
 
 template <int N> struct U4s { uint4 u[N]; };
@@ -186,6 +187,7 @@ __device__ __forceinline__ int vark_nsplit(int kb, int kp) {
 template <int STAGES> struct Ctrl {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
+    uint64_t tail[STAGES];       // VarK, even / single CTA: a segment's last K block lands here
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -569,6 +571,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             // weight-gradient relay); odd CTA of a weight-gradient pair: its producer
             mbar_init(smem_u32(&c.full[s]), leader ? S::CTAS : 1);
             mbar_init(smem_u32(&c.empty[s]), 1);
+            mbar_init(smem_u32(&c.tail[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&c.tfull[b]), 1);
@@ -694,8 +697,11 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             tma_prefetch_map(&mapB);
             int stage = 0, ecur = 0;
             uint32_t phase = 0;
-            int issued_parity[STAGES];
-            for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+            // per stage, the parity of the last phase this CTA's copies count on
+            // (of full[], or of tail[] for a segment's last K block), else -1
+            int issued_parity[STAGES], issued_tail[STAGES];
+            for (int s = 0; s < STAGES; ++s) issued_parity[s] = issued_tail[s] = -1;
+            uint32_t tail_phase = 0;   // bit s: parity of tail[s]'s next phase
             bool ok = true;
             for (int t = unit0; t < num_units && ok; t += nunits) {
                 const Tile ti = get_tile<VAR_K, PAIR, MULTI>(c, p, t, ecur, rank);
@@ -730,19 +736,25 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         // row-sum tile reads only A
                         bytes = S::A_BYTES + (ti.ones ? 0 : S::B_BYTES);
                     }
-                    // a weight-gradient pair's odd CTA loads a segment's last K block
-                    // onto its own barrier, for its relay warp to zero the tail first
-                    const int kvalid = MULTI ? cur.valid() : ti.rows - kb * BK;
-                    const bool relay = PAIR && VAR_K && !leader && kvalid < BK;
-                    if (PAIR && !leader && !relay) mbar_arrive_expect_tx_cluster(fbc, bytes);
+                    // A segment's last K block (weight gradients) lands on a barrier
+                    // of this CTA's own, for its relay warp to zero the rows past
+                    // the segment before the MMAs read the stage: the odd CTA's
+                    // stage barrier (which nothing else completes), the even or
+                    // single CTA's tail barrier.
+                    const int kvalid = VAR_K ? (MULTI ? cur.valid() : ti.rows - kb * BK) : BK;
+                    const bool relay = VAR_K && kvalid < BK;
+                    const uint32_t rb = (PAIR && !leader) ? fb : smem_u32(&c.tail[stage]);
+                    if (relay) mbar_arrive_expect_tx(rb, bytes);
+                    else if (PAIR && !leader) mbar_arrive_expect_tx_cluster(fbc, bytes);
                     else mbar_arrive_expect_tx(fb, bytes);
+                    const uint32_t lb = relay ? rb : fb;   // barrier of a CTA-local copy
                     auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
                         if (PAIR && !relay) tma2_load_2d(dst, m, fbc, c0, c1);
-                        else tma_load_2d(dst, m, fb, c0, c1);
+                        else tma_load_2d(dst, m, lb, c0, c1);
                     };
                     auto load3 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2) {
                         if (PAIR && !relay) tma2_load_3d(dst, m, fbc, c0, c1, c2);
-                        else tma_load_3d(dst, m, fb, c0, c1, c2);
+                        else tma_load_3d(dst, m, lb, c0, c1, c2);
                     };
                     if (!VAR_K) {
                         load2(sA, &mapA, kb * BK, ti.row0);
@@ -752,7 +764,7 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                             // this CTA's 64-column slabs of BK rows in one box
                             // (map: {column in slab, K row, slab, expert})
                             if (PAIR && !relay) tma2_load_4d(sB, &mapB, fbc, 0, kb * BK, nB / 64, ti.e);
-                            else tma_load_4d(sB, &mapB, fb, 0, kb * BK, nB / 64, ti.e);
+                            else tma_load_4d(sB, &mapB, lb, 0, kb * BK, nB / 64, ti.e);
                         }
                     } else {
                         // one box per operand: this CTA's 64-column slabs of BK rows
@@ -763,40 +775,45 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                         if (!ti.ones) load3(sB, &mapB, 0, r, nB / 64);
                         if (MULTI) cur.advance(p, ti.e);
                     }
-                    issued_parity[stage] = (int)phase;
+                    if (relay && (!PAIR || leader)) {
+                        issued_tail[stage] = (int)((tail_phase >> stage) & 1u);
+                        issued_parity[stage] = -1;
+                        tail_phase ^= 1u << stage;
+                    } else {
+                        issued_parity[stage] = (int)phase;
+                        issued_tail[stage] = -1;
+                    }
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
             if (!ok && (!PAIR || leader)) {
                 // wait (bounded) for every copy this CTA's barriers are counting
-                for (int s = 0; s < STAGES; ++s)
+                for (int s = 0; s < STAGES; ++s) {
                     if (issued_parity[s] >= 0)
                         mbar_wait_bounded(smem_u32(&c.full[s]), (uint32_t)issued_parity[s],
                                           p.limit_ns, nullptr);
+                    if (issued_tail[s] >= 0)
+                        mbar_wait_bounded(smem_u32(&c.tail[s]), (uint32_t)issued_tail[s],
+                                          p.limit_ns, nullptr);
+                }
             }
         }
-    } else if (warp == 1) {
-        // zero this CTA's K rows past the segment (valid of BK) in every MN slab
-        // of the stage (whole 128-byte rows: the swizzle only permutes chunks
-        // inside a row); the writes are made visible to the tensor core's reads
-        auto zero_tail = [&](int stage, int valid) {
-            if (valid >= BK) return;
-            uint8_t* gA = base + (size_t)stage * S::STAGE_BYTES;
-            const int nz = (BK - valid) * 8;  // 16-byte chunks per slab
-            for (int sl = 0; sl < S::STAGE_BYTES / SLAB_BYTES; ++sl) {
-                uint8_t* slab = gA + sl * SLAB_BYTES;
-                for (int i = lane; i < nz; i += 32)
-                    *reinterpret_cast<uint4*>(slab + (valid + (i >> 3)) * 128 + ((i & 7) << 4)) =
-                        make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-        };
-        if (PAIR && VAR_K && !leader) {
-            // ---- odd CTA of a weight-gradient pair: tail relay ---------------------
-            // Its own stage barriers only complete for segments' last K blocks, so
-            // their phases are tracked per stage.
+    } else if (warp == 1 || (VAR_K && warp == 2 + ES::WARPS)) {
+        // ---- weight gradients: tail relay ---------------------------------------------
+        // A segment's last K block holds rows of the next segment (or past the
+        // end): this warp waits for such a stage on the CTA's own barrier (the
+        // odd CTA's stage barrier, the even / single CTA's tail barrier), zeroes
+        // the CTA's K rows past the segment in every MN slab (whole 128-byte
+        // rows: the swizzle only permutes chunks inside a row), makes the writes
+        // visible to the tensor core's reads and then counts the stage as loaded
+        // on the even CTA's stage barrier.  The barriers it waits on complete only
+        // for such blocks, so their phases are tracked per stage.  The odd CTA's
+        // warp 1 (it issues no MMAs) and the even / single CTA's extra warp relay.
+        const bool relay_warp = VAR_K && (PAIR && !leader ? warp == 1 : warp == 2 + ES::WARPS);
+        if (relay_warp) {
+            const bool odd = PAIR && !leader;
             int stage = 0, ecur = 0;
-            uint32_t local_phase = 0;   // bit s: parity of stage s's next own phase
+            uint32_t local_phase = 0;   // bit s: parity of the own barrier's next phase
             bool ok = true;
             for (int t = unit0; t < num_units && ok; t += nunits) {
                 const Tile ti = get_tile<VAR_K, PAIR, MULTI>(c, p, t, ecur, rank);
@@ -806,24 +823,39 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                     const int valid = MULTI ? cur.valid() : ti.rows - kb * BK;
                     if (MULTI) cur.advance(p, ti.e);
                     if (valid < BK) {
-                        if (!mbar_wait_warp(smem_u32(&c.full[stage]), (local_phase >> stage) & 1u,
-                                            p.limit_ns, &c.abort_flag)) {
+                        const uint32_t own = odd ? smem_u32(&c.full[stage]) : smem_u32(&c.tail[stage]);
+                        if (!mbar_wait_warp(own, (local_phase >> stage) & 1u, p.limit_ns,
+                                            &c.abort_flag)) {
                             raise_abort(c, p);
                             ok = false;
                             break;
                         }
                         local_phase ^= 1u << stage;
-                        zero_tail(stage, valid);
+                        uint8_t* gA = base + (size_t)stage * S::STAGE_BYTES;
+                        const int nz = (BK - valid) * 8;  // 16-byte chunks per slab
+                        for (int sl = 0; sl < S::STAGE_BYTES / SLAB_BYTES; ++sl) {
+                            uint8_t* slab = gA + sl * SLAB_BYTES;
+                            for (int i = lane; i < nz; i += 32)
+                                *reinterpret_cast<uint4*>(slab + (valid + (i >> 3)) * 128 +
+                                                          ((i & 7) << 4)) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive_cluster_release(mapa_rank(smem_u32(&c.full[stage]), 0));
+                        if (lane == 0) {
+                            if (odd) mbar_arrive_cluster_release(mapa_rank(smem_u32(&c.full[stage]), 0));
+                            else mbar_arrive(smem_u32(&c.full[stage]));
+                        }
                     }
                     if (++stage == STAGES) stage = 0;
                 }
             }
         }
         // ---- MMA issuer (the even CTA of a pair issues for both) ---------------------
-        if (leader) {
+        // One thread issues: it waits for a stage, issues its MMAs and their
+        // commit and goes on to the next stage with nothing else in between
+        // (the tensor core queues only a few MMAs, so every cycle spent between
+        // two stages beyond that queue is an idle tensor core).
+        if (leader && warp == 1) {
             constexpr uint32_t IDESC = idesc_bf16_f32(S::TILE_M, BN, A_MN, B_MN);
             // row-sum tile: N = 32 against the all-ones slab (the same slab for every
             // stage and K block)
@@ -842,35 +874,29 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             const uint32_t b_lo0 = (uint32_t)b_desc0, b_hi = (uint32_t)(b_desc0 >> 32);
             constexpr uint32_t A_KSTEP = (A_MN ? 2048u : 32u) >> 4;   // one K step of 16
             constexpr uint32_t B_KSTEP = (B_MN ? 2048u : 32u) >> 4;
-            int stage = 0, acc = 0, ecur = 0;
-            uint32_t phase = 0, acc_phase = 0;
-            bool ok = true;
-            for (int t = unit0; t < num_units && ok; t += nunits) {
-                const Tile ti = get_tile<VAR_K, PAIR, MULTI>(c, p, t, ecur, rank);
-                if (ti.num_kb == 0) continue;
-                SegCursor cur;
-                if (VAR_K && MULTI) cur.start(p, ti.e, ti.kb0, c.off);
-                if (!mbar_wait_warp(smem_u32(&c.tempty[acc]), acc_phase ^ 1, p.limit_ns,
-                                    &c.abort_flag)) {
-                    raise_abort(c, p);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < ti.num_kb; ++kb) {
-                    if (!mbar_wait_warp(smem_u32(&c.full[stage]), phase, p.limit_ns,
-                                        &c.abort_flag)) {
+            if (lane == 0) {
+                int stage = 0, acc = 0, ecur = 0;
+                uint32_t phase = 0, acc_phase = 0;
+                bool ok = true;
+                for (int t = unit0; t < num_units && ok; t += nunits) {
+                    const Tile ti = get_tile<VAR_K, PAIR, MULTI>(c, p, t, ecur, rank);
+                    if (ti.num_kb == 0) continue;
+                    if (!mbar_wait_bounded(smem_u32(&c.tempty[acc]), acc_phase ^ 1, p.limit_ns,
+                                           &c.abort_flag)) {
                         raise_abort(c, p);
-                        ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (VAR_K) {
-                        zero_tail(stage, MULTI ? cur.valid() : ti.rows - kb * BK);
-                        if (MULTI) cur.advance(p, ti.e);
-                        __syncwarp();
-                    }
-                    if (lane == 0) {
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                    const uint32_t idesc = ti.ones ? IDESC_ONES : IDESC;
+                    for (int kb = 0; kb < ti.num_kb; ++kb) {
+                        if (!mbar_wait_bounded(smem_u32(&c.full[stage]), phase, p.limit_ns,
+                                               &c.abort_flag)) {
+                            raise_abort(c, p);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
                         const uint32_t so = (uint32_t)stage * (uint32_t)(S::STAGE_BYTES >> 4);
                         #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk) {
@@ -880,24 +906,20 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                                                          : b_lo0 + so + kk * B_KSTEP;
                             const uint64_t bd = ((uint64_t)b_hi << 32) | (uint64_t)blo;
                             const uint32_t accum = (kk != 0 || kb != 0) ? 1u : 0u;
-                            const uint32_t idesc = ti.ones ? IDESC_ONES : IDESC;
                             if (PAIR) tc_mma2_bf16(d_tmem, ad, bd, idesc, accum);
                             else tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
                         }
                         if (PAIR) tc_commit2_both(smem_u32(&c.empty[stage]));
                         else tc_commit(smem_u32(&c.empty[stage]));
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
-                    __syncwarp();
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
-                }
-                if (!ok) break;
-                if (lane == 0) {
+                    if (!ok) break;
                     if (PAIR) tc_commit2_both(smem_u32(&c.tfull[acc]));
                     else tc_commit(smem_u32(&c.tfull[acc]));
+                    if (++acc == 2) { acc = 0; acc_phase ^= 1; }
                 }
-                __syncwarp();
-                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
+            __syncwarp();
             // drain: every MMA this warp issued has completed before TMEM is freed
             if (lane == 0) {
                 if (PAIR) tc_commit2_local(smem_u32(&c.drain));
