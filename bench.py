@@ -29,6 +29,7 @@ from __future__ import annotations
 
 import argparse
 import json
+from typing import Optional
 import os
 import statistics
 import subprocess
@@ -48,32 +49,61 @@ L2_FLUSH_BYTES = 256 << 20
 ROUTER_TC_ENV = "MOE_ROUTER_TENSOR_CORES"
 
 
-def launches_per_step(cfg, nchunks: int, router_tc: bool, recompute: bool, defer: bool) -> int:
+# weight-gradient GEMM calls over more rows than this (or over several chunks)
+# take the segment-walking kernel, which adds a split-reduction kernel
+VARK_LEAN_MAX_ROWS = 512 * 64
+
+
+def launches_per_step(cfg, nchunks: int, router_tc: bool, recompute: bool, defer: bool,
+                      gather: bool = False) -> int:
     """Library kernels one step launches.
     Per dispatch chunk.  Route: the tensor-core logits (bf16, d_model % 64 ==
     0, opt-in) or the CUDA-core logits kernel, then the gate, the scan and the
     rank (4); the CUDA-core router fuses logits and gate for E <= 32 (3).
-    Permute (1); two expert GEMMs (2); combine (1); combine backward (1).
-    Expert backward, bf16: the dH GEMM + its db1 reduction and the dX GEMM (3),
-    and unless the weight gradients are deferred, the two weight-gradient
-    GEMMs (db2 inside the dW2 one) (2); fp32: dH and dX GEMMs and db1's column
-    sum of two kernels (4), plus two weight-gradient GEMMs and db2's column sum
-    (4).  Router backward: with renorm, dx with the permute backward fused in
-    and dWg (2 kernels) = 3; without (dense gate Jacobian), dL, the tiled dx
-    product with the permute backward, and dWg (2 kernels) = 4.  Recompute
-    re-runs the permute and the two forward GEMMs (3).
-    Deferred weight gradients: once per step, the two weight-gradient GEMMs
-    (bf16), or per chunk two GEMMs and db2's column sum (fp32)."""
+    Permute (1; none when fused into the GEMM loads); two expert GEMMs (2);
+    combine (1); combine backward (1).  Expert backward, bf16: the dH GEMM +
+    its db1 reduction and the dX GEMM (3), and unless the weight gradients are
+    deferred, the two weight-gradient GEMMs (db2 inside the dW2 one) (2), each
+    with its split reduction when it walks more than VARK_LEAN_MAX_ROWS rows
+    (+2); fp32: dH and dX GEMMs and db1's column sum of two kernels (4), plus
+    two weight-gradient GEMMs and db2's column sum (4).  Router backward: with
+    renorm, dx with the permute backward fused in and dWg (2 kernels) = 3;
+    without (dense gate Jacobian), dL, the tiled dx product with the permute
+    backward, and dWg (2 kernels) = 4.  Recompute re-runs the permute (unless
+    fused) and the two forward GEMMs.  Deferred weight gradients: once per
+    step, the two weight-gradient GEMMs and their split reductions (bf16), or
+    per chunk two GEMMs and db2's column sum (fp32)."""
     bf = cfg.dtype == "bf16"
     tc = router_tc and bf and cfg.d % 64 == 0
     route = 4 if (tc or cfg.E > 32) else 3
+    permute = 0 if gather else 1
     data = 3 if bf else 4
-    wgrad = 2 if bf else 4
+    chunk_rows = min(cfg.T, cfg.chunk or cfg.T) * cfg.k
+    wgrad = (2 + (2 if chunk_rows > VARK_LEAN_MAX_ROWS else 0)) if bf else 4
     route_bwd = 3 if cfg.renorm else 4
-    per_chunk = route + 1 + 2 + 1 + 1 + data + (0 if defer else wgrad) + route_bwd
-    per_chunk += 3 if recompute else 0
-    per_step = (2 if bf else 4 * nchunks) if defer else 0
+    per_chunk = route + permute + 2 + 1 + 1 + data + (0 if defer else wgrad) + route_bwd
+    per_chunk += (permute + 2) if recompute else 0
+    multi = nchunks > 1 or cfg.T * cfg.k > VARK_LEAN_MAX_ROWS
+    per_step = ((4 if multi else 2) if bf else 4 * nchunks) if defer else 0
     return per_chunk * nchunks + per_step
+
+
+def count_library_kernels(step) -> Optional[int]:
+    """Kernels of this library (namespace moe) that one eager call of ``step``
+    launches, from the CUDA kernel activity the PyTorch profiler records (None
+    if it records none)."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        torch.cuda.synchronize()
+        # (kernel activity is attributed through the CPU-side launch records)
+        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
+            step()
+            torch.cuda.synchronize()
+        n = sum(1 for e in prof.events()
+                if e.device_type == torch.autograd.DeviceType.CUDA and "moe::" in e.name)
+    except Exception:
+        return None
+    return n or None
 
 
 def workload_desc(cfg) -> str:
@@ -288,11 +318,12 @@ def whole_job_rate(tokens_per_rank_step: int, steps: int, world: int, ms: float)
 
 # ---- device timing of one workload ---------------------------------------------------------
 
-CALLS = ("moe_route", "moe_permute", "moe_expert_ffn_fwd", "moe_combine_fwd",
-         "moe_combine_bwd", "moe_expert_ffn_bwd", "moe_expert_ffn_bwd_data",
-         "moe_expert_ffn_bwd_weights", "moe_route_bwd")
-GEMM_CALLS = ("moe_expert_ffn_fwd", "moe_expert_ffn_bwd", "moe_expert_ffn_bwd_data",
-              "moe_expert_ffn_bwd_weights")
+CALLS = ("moe_route", "moe_permute", "moe_expert_ffn_fwd", "moe_expert_ffn_fwd_gather",
+         "moe_combine_fwd", "moe_combine_bwd", "moe_expert_ffn_bwd", "moe_expert_ffn_bwd_data",
+         "moe_expert_ffn_bwd_weights", "moe_expert_ffn_bwd_weights_gather", "moe_route_bwd")
+GEMM_CALLS = ("moe_expert_ffn_fwd", "moe_expert_ffn_fwd_gather", "moe_expert_ffn_bwd",
+              "moe_expert_ffn_bwd_data", "moe_expert_ffn_bwd_weights",
+              "moe_expert_ffn_bwd_weights_gather")
 
 
 class CallTimer:
@@ -344,7 +375,8 @@ def _sum_ms(marks):
 
 
 def measure(cfg, dev, steps, warmup, *, pipeline=True, graph=True, router_tc=False,
-            recompute=False, defer_wgrad=None, sampler=None, e2e=False, dist=None, seed=0):
+            recompute=False, defer_wgrad=None, sampler=None, e2e=False, dist=None, seed=0,
+            gather=False):
     """Times `steps` layer steps of one workload.  Returns a dict of measured
     values; with e2e also the end-to-end rate through host buffers."""
     from mixture_experts_layer_11_gb300.layer import LayerPass
@@ -355,7 +387,7 @@ def measure(cfg, dev, steps, warmup, *, pipeline=True, graph=True, router_tc=Fal
         os.environ.pop(ROUTER_TC_ENV, None)
     try:
         return _measure(cfg, dev, steps, warmup, pipeline, graph, router_tc, recompute,
-                        defer_wgrad, sampler, e2e, dist, seed, LayerPass)
+                        defer_wgrad, sampler, e2e, dist, seed, LayerPass, gather)
     finally:
         if prev is None:
             os.environ.pop(ROUTER_TC_ENV, None)
@@ -364,12 +396,12 @@ def measure(cfg, dev, steps, warmup, *, pipeline=True, graph=True, router_tc=Fal
 
 
 def _measure(cfg, dev, steps, warmup, pipeline, graph_on, router_tc, recompute, defer_wgrad,
-             sampler, e2e, dist, seed, LayerPass):
+             sampler, e2e, dist, seed, LayerPass, gather):
     torch.cuda.reset_peak_memory_stats(dev)
     inp = synth.make_inputs(cfg, seed=seed, device=str(dev))
     lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
                    chunk=cfg.chunk, device=dev, pipeline=pipeline, recompute=recompute,
-                   defer_wgrad=defer_wgrad)
+                   defer_wgrad=defer_wgrad, gather=gather)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     x_buf, dy_buf = inp["x"], inp["dy"]
@@ -387,6 +419,9 @@ def _measure(cfg, dev, steps, warmup, pipeline, graph_on, router_tc, recompute, 
         lp.check_status()
         graph = None
         graph_marks = []
+        # the library's kernels in one step (the captured graph replays the same)
+        graph_kernels = count_library_kernels(step)
+        lp.check_status()
         if graph_on:
             graph = torch.cuda.CUDAGraph()
             tm.record, tm.external = True, True
@@ -433,9 +468,13 @@ def _measure(cfg, dev, steps, warmup, pipeline, graph_on, router_tc, recompute, 
     res.update(total_ms=sum(step_ms), steps=steps, wall_s=wall, chunks=len(lp.chunks),
                calls={n: (ms / steps, tok // steps) for n, (ms, tok) in calls.items()},
                device_memory_gib=torch.cuda.max_memory_allocated(dev) / 2**30,
-               pipelined=lp.pipeline, defer_wgrad=lp.defer_wgrad,
-               launches=launches_per_step(cfg, len(lp.chunks), router_tc, recompute,
-                                          lp.defer_wgrad) * steps)
+               pipelined=lp.pipeline, defer_wgrad=lp.defer_wgrad, gather=lp.gather,
+               launches_formula=launches_per_step(cfg, len(lp.chunks), router_tc, recompute,
+                                                  lp.defer_wgrad, lp.gather) * steps,
+               launches=(graph_kernels * steps if graph_kernels
+                         else launches_per_step(cfg, len(lp.chunks), router_tc, recompute,
+                                                lp.defer_wgrad, lp.gather) * steps),
+               launches_counted=bool(graph_kernels))
     if e2e:
         res["e2e_ms"], res["e2e_steps"] = _end_to_end(cfg, lp, inp, graph, flush, steps, warmup,
                                                       dev)
@@ -613,11 +652,17 @@ def dispatch_roofline(cfg, res, pk):
         per["route"] = {"ms_per_step": ms, "logits_flops_per_step": fl,
                         "tflops": fl / (ms / 1e3) / 1e12,
                         "note": "router logits (CUDA cores), gate, histogram, scan, rank"}
-    main = [per[k] for k in ("permute", "combine", "combine_bwd") if k in per]
+    names = [k for k in ("permute", "combine", "combine_bwd") if k in per]
+    main = [per[k] for k in names]
     byt = sum(p["bytes_per_step"] for p in main)
     ms = sum(p["ms_per_step"] for p in main)
     ach = byt / (ms / 1e3) / 1e9 if ms > 0 else None
-    return {"bound": "hbm", "kernels": "permute, combine, combine backward (A4, A6, A7)",
+    label = {"permute": "permute (A4)", "combine": "combine (A6)",
+             "combine_bwd": "combine backward (A7)"}
+    kernels = ", ".join(label[k] for k in names)
+    if "permute" not in per:
+        kernels += "; the permute (A4) is fused into the expert GEMMs' operand loads"
+    return {"bound": "hbm", "kernels": kernels,
             "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": ach / pk["hbm_gbs"] if ach else None,
             "algorithmic_bytes_per_step": byt, "ms_per_step": ms,
@@ -668,6 +713,18 @@ def run_ours(args, cfg):
               "note": "router logits as one segment of the tcgen05 grouped GEMM "
                       f"({ROUTER_TC_ENV}=1); not the default: the tensor cores are reserved "
                       "for the expert GEMMs"}
+    # ---- the same workload with the permute fused into the GEMMs' loads (opt-in)
+    fused = None
+    if cfg.dtype == "bf16" and not args.no_sub_configs:
+        r = summarize(cfg, measure(cfg, dev, sub_steps, sub_warm, gather=True), pk)
+        c = r["calls_ms_per_step"]
+        fused = {"tokens_per_s": r["tokens_per_s"], "ms_per_step": r["ms_per_step"],
+                 "expert_ffn_fwd_ms_per_step": c.get("moe_expert_ffn_fwd_gather"),
+                 "expert_ffn_bwd_weights_ms_per_step": c.get("moe_expert_ffn_bwd_weights_gather"),
+                 "device_memory_gib": r["device_memory_gib"],
+                 "note": "no moe_permute and no X_perm: the first expert GEMM and the dW1 GEMM "
+                         "load x rows through the dispatch's perm (TMA tile::gather4); not the "
+                         "default"}
     # ---- every call timed on one stream (the dispatch kernels' HBM fraction)
     serial = measure(cfg, dev, sub_steps, sub_warm, pipeline=False,
                      defer_wgrad=False if args.per_chunk_wgrad else None)
@@ -714,6 +771,10 @@ def run_ours(args, cfg):
                                    else "kept from the forward for the backward"),
                    "weight_gradients": ("one pass over all chunks after the backward"
                                         if main["defer_wgrad"] else "accumulated per chunk"),
+                   "permute": ("fused into the expert GEMMs' operand loads (TMA tile::gather4 "
+                               "of x rows through the dispatch's perm; no X_perm)"
+                               if main["gather"] else "its own kernel (X_perm written, read by "
+                               "the expert GEMMs)"),
                    "parallelism": f"replicas x{world}"},
         "roofline": {
             "bound": "tensor", "kernel": "grouped expert GEMM (tcgen05), all expert FFN calls",
@@ -727,8 +788,13 @@ def run_ours(args, cfg):
         },
         "dispatch_roofline": disp,
         "router_tensor_cores_variant": tc,
+        "fused_permute_variant": fused,
         "per_config": per_config,
         "gpu_launches": main["launches"],
+        "gpu_launches_formula": main["launches_formula"],
+        "gpu_launches_source": ("the library's kernels in one profiled step (PyTorch profiler, "
+                                "CUDA kernel activity) x steps" if main["launches_counted"]
+                                else "launches_per_step() formula x steps"),
         "e2e": {"value": whole_job_rate(cfg.T, main["e2e_steps"], world, e2e_ms),
                 "unit": "tokens/s",
                 "pipeline": "H2D of step i+1 and D2H of step i on copy streams, overlapping step i",

@@ -188,6 +188,23 @@ MOE_API moe_status moe_expert_ffn_fwd(const moe_shape* s, const void* x_perm,
                               void* y_perm, void* ws, int32_t* dev_status,
                               moe_stream_t stream);
 
+/* NEXT-2, permute half: A4 fused into A5.  The same results as moe_permute
+ * followed by moe_expert_ffn_fwd (bit for bit), without X_perm: the first
+ * GEMM's operand loads read row r of the expert-sorted activations straight
+ * from x, as x[perm[r] / k] (four rows per TMA tile::gather4 load on the
+ * tensor-core path).  Source: the scatter half of the scatter/gather layout
+ * ("FastMoE", review, "proposed method") and the token permutation that
+ * "ES-MoE" (review, section 3) overlaps with the experts' compute, here folded
+ * into the compute itself.
+ *   x    [T,d] dtype        tokens of this chunk
+ *   perm [T*k] int32        from moe_route of this chunk
+ *   others as moe_expert_ffn_fwd. */
+MOE_API moe_status moe_expert_ffn_fwd_gather(const moe_shape* s, const void* x,
+                                             const int32_t* perm, const int32_t* offsets,
+                                             const void* W1, const void* b1, const void* W2,
+                                             const void* b2, void* G, void* A, void* y_perm,
+                                             void* ws, int32_t* dev_status, moe_stream_t stream);
+
 /* A6 (w != NULL): y[t] = sum_j w[t,j] * y_perm[pos[t,j]], j ascending, fp32
  * accumulation.  Source: the gather half of the scatter/gather layout
  * ("FastMoE", review, "proposed method"), weighted by the gate.  A9 (w == NULL): the permute backward, y[t] = sum_j
@@ -269,9 +286,27 @@ MOE_API moe_status moe_expert_ffn_bwd_weights(const moe_shape* s, int nchunks,
                                               void* ws, size_t ws_bytes, int32_t* dev_status,
                                               moe_stream_t stream);
 
-/* Workspace bytes for moe_expert_ffn_bwd_weights with these chunks (0 on bad
- * arguments): the finest split of its reductions (bf16), the column-sum
- * partials (fp32). */
+/* NEXT-2, permute half, in the weight gradient: moe_expert_ffn_bwd_weights
+ * with dW1 = dH^T X reading X's rows through each chunk's perm instead of
+ * X_perm (bit for bit the same results).
+ *   x     [sum(chunk_T), d] dtype: the chunks' tokens, chunk c's after those
+ *         of chunks < c
+ *   perm  device int32: chunk c's perm (from its moe_route, chunk_T[c] * k
+ *         entries) at c * perm_stride; perm_stride >= k * max(chunk_T)
+ *   others as moe_expert_ffn_bwd_weights (the same workspace size). */
+MOE_API moe_status moe_expert_ffn_bwd_weights_gather(const moe_shape* s, int nchunks,
+                                                     const int64_t* chunk_T,
+                                                     const int32_t* offsets, int offsets_stride,
+                                                     const void* dy_perm, const void* x,
+                                                     const int32_t* perm, int64_t perm_stride,
+                                                     const void* dH, const void* A, float* dW1,
+                                                     float* dW2, float* db2, int accumulate,
+                                                     void* ws, size_t ws_bytes,
+                                                     int32_t* dev_status, moe_stream_t stream);
+
+/* Workspace bytes for moe_expert_ffn_bwd_weights (and its _gather form) with
+ * these chunks (0 on bad arguments): the finest split of its reductions
+ * (bf16), the column-sum partials (fp32). */
 MOE_API size_t moe_expert_ffn_bwd_weights_workspace_size(const moe_shape* s, int nchunks,
                                                          const int64_t* chunk_T);
 

@@ -42,7 +42,13 @@ __global__ void __launch_bounds__(256) gemm_varm_f32_kernel(GemmVarM g) {
     for (int k0 = 0; k0 < g.K; k0 += SK) {
         for (int i = threadIdx.x; i < SB * SK; i += 256) {
             const int r = i / SK, c = i % SK;
-            As[c][r] = (r < rows && k0 + c < g.K) ? act[(int64_t)(row0 + r) * g.K + k0 + c] : 0.f;
+            float v = 0.f;
+            if (r < rows && k0 + c < g.K) {
+                const int64_t src = g.gather ? (int64_t)(g.gather[row0 + r] / g.gather_k)
+                                             : (int64_t)(row0 + r);
+                v = act[src * g.K + k0 + c];
+            }
+            As[c][r] = v;
         }
         for (int i = threadIdx.x; i < SB * SK; i += 256) {
             int n, c;
@@ -119,7 +125,13 @@ __global__ void __launch_bounds__(256) gemm_vark_f32_kernel(GemmVarK g) {
             const int c = i / SB, r = i % SB;  // c: row of the segment, r: column
             const bool kin = k0 + c < p1;
             As[c][r] = (kin && m0 + r < g.M) ? a[(int64_t)(k0 + c) * g.M + m0 + r] : 0.f;
-            Bs[c][r] = (kin && n0 + r < g.N) ? b[(int64_t)(k0 + c) * g.N + n0 + r] : 0.f;
+            float bv = 0.f;
+            if (kin && n0 + r < g.N) {
+                const int64_t src = g.gather_b ? g.gather_base[0] + g.gather_b[k0 + c] / g.gather_k
+                                               : (int64_t)(k0 + c);
+                bv = b[src * g.N + n0 + r];
+            }
+            Bs[c][r] = bv;
         }
         __syncthreads();
         #pragma unroll
@@ -167,7 +179,12 @@ cudaError_t launch_gemm_vark_simt(const GemmVarK& g, cudaStream_t st) {
         c.nseg = 1;
         c.offsets = g.offsets + (int64_t)s * g.ostride;
         c.act_a = (const float*)g.act_a + g.seg_base[s] * g.M;
-        c.act_b = (const float*)g.act_b + g.seg_base[s] * g.N;
+        if (g.gather_b) {   // rows of the unpermuted source, through chunk s's perm
+            c.gather_b = g.gather_b + (int64_t)s * g.gather_stride;
+            c.gather_base[0] = g.gather_base[s];
+        } else {
+            c.act_b = (const float*)g.act_b + g.seg_base[s] * g.N;
+        }
         c.accumulate = g.accumulate || s > 0;
         gemm_vark_f32_kernel<<<grid, 256, 0, st>>>(c);
         const cudaError_t e = cudaGetLastError();

@@ -122,6 +122,7 @@ template <int EPI, bool VAR_K> struct EpiShape {
 };
 
 template <int N> struct U4s { uint4 u[N]; };
+template <bool B> struct BoolTag { static constexpr bool value = B; };
 
 struct TcParams {
     int E, M, N, K;          // VarM: N, K (M unused); VarK: M, N (K = segment)
@@ -151,6 +152,14 @@ struct TcParams {
     int64_t part_cap;
     int split_units;
     float* bpart;            // VarK split: row sums of all-ones tiles of parts > 0
+    // Row gather (the permute fused into the operand loads), or null: row r of
+    // the expert-sorted operand (VarM: A; VarK: B) is row
+    // gbase[s] + gather[s * gstride + r - seg_base[s]] / gk of the tensor map's
+    // source (s = 0 for VarM), loaded four rows at a time by tile::gather4.
+    const int32_t* gather;
+    int gk;
+    int64_t gstride;
+    int64_t gbase[kMaxWgradChunks];
 };
 
 // K blocks per part of the split weight-gradient tiles (INT_MAX: no split):
@@ -403,6 +412,26 @@ __device__ __forceinline__ void tma2_load_3d(uint32_t dst, const CUtensorMap* ma
         "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(map), "r"(cl_bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+// Four rows (row0..row3, one-row boxes of the map) at column c0, written to
+// shared memory one after the other as a four-row box (the map's swizzle
+// applies by shared address, as for a tiled box).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, const int (&rows)[4]) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(map), "r"(bar), "r"(c0), "r"(rows[0]), "r"(rows[1]), "r"(rows[2]), "r"(rows[3])
+        : "memory");
+}
+// The same, completing on the pair's even CTA (cl_bar: shared::cluster address).
+__device__ __forceinline__ void tma2_gather4(uint32_t dst, const CUtensorMap* map,
+                                             uint32_t cl_bar, int32_t c0, const int (&rows)[4]) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(map), "r"(cl_bar), "r"(c0), "r"(rows[0]), "r"(rows[1]), "r"(rows[2]), "r"(rows[3])
         : "memory");
 }
 __device__ __forceinline__ void tma2_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t cl_bar,
@@ -692,72 +721,125 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
 
     if (warp == 0) {
         // ---- TMA producer ---------------------------------------------------------
+        // Lane 0 waits for free stages, arms the barriers and issues the box
+        // loads.  With a row gather (the permute fused into the loads; GAT) the
+        // whole warp walks the tiles and every lane also issues tile::gather4
+        // loads of four source rows each: VarM, the CTA's 128 A rows per K block
+        // (the rows are the tile's, fetched once per tile); VarK, the BK rows of
+        // every B slab of a K block (fetched one K block ahead).
         if (lane == 0) {
             tma_prefetch_map(&mapA);
             tma_prefetch_map(&mapB);
-            int stage = 0, ecur = 0;
-            uint32_t phase = 0;
-            // per stage, the parity of the last phase this CTA's copies count on
-            // (of full[], or of tail[] for a segment's last K block), else -1
-            int issued_parity[STAGES], issued_tail[STAGES];
-            for (int s = 0; s < STAGES; ++s) issued_parity[s] = issued_tail[s] = -1;
-            uint32_t tail_phase = 0;   // bit s: parity of tail[s]'s next phase
-            bool ok = true;
-            for (int t = unit0; t < num_units && ok; t += nunits) {
-                const Tile ti = get_tile<VAR_K, PAIR, MULTI>(c, p, t, ecur, rank);
-                SegCursor cur;
-                if (VAR_K && MULTI) cur.start(p, ti.e, ti.kb0, c.off);
-                for (int kb = 0; kb < ti.num_kb; ++kb) {
-                    if (leader && t == p.withhold_unit && kb == p.withhold_kb) {
-                        // test hook: issue nothing more (no copy is left in
-                        // flight for this stage); the copies already issued are
-                        // waited for below
-                        ok = false;
-                        break;
-                    }
-                    if (!mbar_wait_bounded(smem_u32(&c.empty[stage]), phase ^ 1, p.limit_ns,
-                                           &c.abort_flag)) {
-                        raise_abort(c, p);
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t sA = smem_u32(base + (size_t)stage * S::STAGE_BYTES);
-                    const uint32_t sB = sA + S::A_BYTES;
-                    const uint32_t fb = smem_u32(&c.full[stage]);
-                    const uint32_t fbc = PAIR ? mapa_rank(fb, 0) : fb;   // even CTA's barrier
-                    const int nB = ti.nt * BN + rank * S::BN_CTA;      // first B column held here
-                    // bytes: full boxes, except MN slabs lying wholly past the edge
-                    uint32_t bytes = 0;
-                    if (!VAR_K) {
-                        bytes += S::A_BYTES;
-                        bytes += S::B_BYTES;   // whole box (columns past N zero-filled)
-                    } else {
-                        // whole boxes (slabs past the M / N edge are zero-filled); the
-                        // row-sum tile reads only A
-                        bytes = S::A_BYTES + (ti.ones ? 0 : S::B_BYTES);
-                    }
-                    // A segment's last K block (weight gradients) lands on a barrier
-                    // of this CTA's own, for its relay warp to zero the rows past
-                    // the segment before the MMAs read the stage: the odd CTA's
-                    // stage barrier (which nothing else completes), the even or
-                    // single CTA's tail barrier.
-                    const int kvalid = VAR_K ? (MULTI ? cur.valid() : ti.rows - kb * BK) : BK;
-                    const bool relay = VAR_K && kvalid < BK;
-                    const uint32_t rb = (PAIR && !leader) ? fb : smem_u32(&c.tail[stage]);
+        }
+        auto producer = [&](auto gather_tag) {
+        constexpr bool gat = decltype(gather_tag)::value;
+        // VarK gather: (slab, four-row group) assignments per lane
+        constexpr int kGatherJ = (S::B_BYTES / SLAB_BYTES) * (BK / 4) / 32;
+        int stage = 0, ecur = 0;
+        uint32_t phase = 0;
+        // per stage, the parity of the last phase this CTA's copies count on
+        // (of full[], or of tail[] for a segment's last K block), else -1
+        int issued_parity[STAGES], issued_tail[STAGES];
+        for (int s = 0; s < STAGES; ++s) issued_parity[s] = issued_tail[s] = -1;
+        uint32_t tail_phase = 0;   // bit s: parity of tail[s]'s next phase
+        bool ok = true;
+        // source row of gathered operand row r of segment seg (r clamped to the
+        // segment's last row: rows past it are never used, or zeroed by the relay)
+        auto gsrc = [&](int seg, int r, int rlast) -> int {
+            const int rr = r < rlast ? r : rlast;
+            const int32_t v =
+                __ldg(p.gather + (int64_t)seg * p.gstride + (rr - p.seg_base[seg]));
+            return (int)(p.gbase[seg] + v / p.gk);
+        };
+        for (int t = unit0; t < num_units && ok; t += nunits) {
+            const Tile ti = get_tile<VAR_K, PAIR, MULTI>(c, p, t, ecur, rank);
+            SegCursor cur;
+            if (VAR_K && MULTI) cur.start(p, ti.e, ti.kb0, c.off);
+            int arow[4];                 // VarM gather: this lane's four A rows
+            int brow[kGatherJ][4];       // VarK gather: this lane's B rows, next K block
+            if (gat && !VAR_K) {
+                // the CTA's part may start past the expert's rows (then no row is used)
+                const int rlast = c.off[ti.e + 1] - 1;
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) arow[q] = gsrc(0, ti.row0 + 4 * lane + q, rlast);
+            }
+            // VarK gather: the rows of the K block the cursor is at
+            auto fetch_b = [&](int kb) {
+                const int seg = MULTI ? cur.seg : 0;
+                const int r0 = MULTI ? cur.row() : ti.row0 + kb * BK;
+                const int rlast = MULTI ? cur.row0 + cur.rows - 1 : ti.row0 + ti.rows - 1;
+                #pragma unroll
+                for (int j = 0; j < kGatherJ; ++j) {
+                    const int g = (lane + 32 * j) & (BK / 4 - 1);
+                    #pragma unroll
+                    for (int q = 0; q < 4; ++q) brow[j][q] = gsrc(seg, r0 + 4 * g + q, rlast);
+                }
+            };
+            if (gat && VAR_K && !ti.ones && ti.num_kb > 0) fetch_b(0);
+            for (int kb = 0; kb < ti.num_kb; ++kb) {
+                if (leader && t == p.withhold_unit && kb == p.withhold_kb) {
+                    // test hook: issue nothing more (no copy is left in
+                    // flight for this stage); the copies already issued are
+                    // waited for below
+                    ok = false;
+                    break;
+                }
+                bool got = true;
+                if (!gat || lane == 0)
+                    got = mbar_wait_bounded(smem_u32(&c.empty[stage]), phase ^ 1, p.limit_ns,
+                                            &c.abort_flag);
+                if (gat) got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                if (!got) {
+                    if (!gat || lane == 0) raise_abort(c, p);
+                    ok = false;
+                    break;
+                }
+                const uint32_t sA = smem_u32(base + (size_t)stage * S::STAGE_BYTES);
+                const uint32_t sB = sA + S::A_BYTES;
+                const uint32_t fb = smem_u32(&c.full[stage]);
+                const uint32_t fbc = PAIR ? mapa_rank(fb, 0) : fb;   // even CTA's barrier
+                const int nB = ti.nt * BN + rank * S::BN_CTA;      // first B column held here
+                // bytes: full boxes, except MN slabs lying wholly past the edge
+                uint32_t bytes = 0;
+                if (!VAR_K) {
+                    bytes += S::A_BYTES;
+                    bytes += S::B_BYTES;   // whole box (columns past N zero-filled)
+                } else {
+                    // whole boxes (slabs past the M / N edge are zero-filled); the
+                    // row-sum tile reads only A
+                    bytes = S::A_BYTES + (ti.ones ? 0 : S::B_BYTES);
+                }
+                // A segment's last K block (weight gradients) lands on a barrier
+                // of this CTA's own, for its relay warp to zero the rows past
+                // the segment before the MMAs read the stage: the odd CTA's
+                // stage barrier (which nothing else completes), the even or
+                // single CTA's tail barrier.
+                const int kvalid = VAR_K ? (MULTI ? cur.valid() : ti.rows - kb * BK) : BK;
+                const bool relay = VAR_K && kvalid < BK;
+                const uint32_t rb = (PAIR && !leader) ? fb : smem_u32(&c.tail[stage]);
+                if (!gat || lane == 0) {
                     if (relay) mbar_arrive_expect_tx(rb, bytes);
                     else if (PAIR && !leader) mbar_arrive_expect_tx_cluster(fbc, bytes);
                     else mbar_arrive_expect_tx(fb, bytes);
-                    const uint32_t lb = relay ? rb : fb;   // barrier of a CTA-local copy
-                    auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
-                        if (PAIR && !relay) tma2_load_2d(dst, m, fbc, c0, c1);
-                        else tma_load_2d(dst, m, lb, c0, c1);
-                    };
-                    auto load3 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2) {
-                        if (PAIR && !relay) tma2_load_3d(dst, m, fbc, c0, c1, c2);
-                        else tma_load_3d(dst, m, lb, c0, c1, c2);
-                    };
-                    if (!VAR_K) {
-                        load2(sA, &mapA, kb * BK, ti.row0);
+                }
+                if (gat) __syncwarp();
+                const uint32_t lb = relay ? rb : fb;   // barrier of a CTA-local copy
+                auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+                    if (PAIR && !relay) tma2_load_2d(dst, m, fbc, c0, c1);
+                    else tma_load_2d(dst, m, lb, c0, c1);
+                };
+                auto load3 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2) {
+                    if (PAIR && !relay) tma2_load_3d(dst, m, fbc, c0, c1, c2);
+                    else tma_load_3d(dst, m, lb, c0, c1, c2);
+                };
+                auto gather4 = [&](uint32_t dst, const CUtensorMap* m, int c0, const int (&rows)[4]) {
+                    if (PAIR && !relay) tma2_gather4(dst, m, fbc, c0, rows);
+                    else tma_gather4(dst, m, lb, c0, rows);
+                };
+                if (!VAR_K) {
+                    if (gat) gather4(sA + (uint32_t)lane * 512u, &mapA, kb * BK, arow);
+                    else if (lane == 0) load2(sA, &mapA, kb * BK, ti.row0);
+                    if (lane == 0) {
                         if (!B_MN) {
                             load3(sB, &mapB, kb * BK, nB, ti.e);
                         } else {
@@ -766,38 +848,62 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
                             if (PAIR && !relay) tma2_load_4d(sB, &mapB, fbc, 0, kb * BK, nB / 64, ti.e);
                             else tma_load_4d(sB, &mapB, lb, 0, kb * BK, nB / 64, ti.e);
                         }
-                    } else {
-                        // one box per operand: this CTA's 64-column slabs of BK rows
-                        // (maps: {column in slab, row, slab})
-                        const int r = MULTI ? cur.row() : ti.row0 + kb * BK;
-                        const int mA = ti.mt * S::TILE_M + rank * BM;
-                        load3(sA, &mapA, 0, r, mA / 64);
-                        if (!ti.ones) load3(sB, &mapB, 0, r, nB / 64);
-                        if (MULTI) cur.advance(p, ti.e);
                     }
-                    if (relay && (!PAIR || leader)) {
-                        issued_tail[stage] = (int)((tail_phase >> stage) & 1u);
-                        issued_parity[stage] = -1;
-                        tail_phase ^= 1u << stage;
-                    } else {
-                        issued_parity[stage] = (int)phase;
-                        issued_tail[stage] = -1;
+                } else {
+                    // one box per operand: this CTA's 64-column slabs of BK rows
+                    // (maps: {column in slab, row, slab}); gathered B: BK / 4
+                    // four-row loads per slab
+                    const int r = MULTI ? cur.row() : ti.row0 + kb * BK;
+                    const int mA = ti.mt * S::TILE_M + rank * BM;
+                    if (lane == 0) load3(sA, &mapA, 0, r, mA / 64);
+                    if (!ti.ones) {
+                        if (!gat) {
+                            if (lane == 0) load3(sB, &mapB, 0, r, nB / 64);
+                        } else {
+                            #pragma unroll
+                            for (int j = 0; j < kGatherJ; ++j) {
+                                const int jj = lane + 32 * j;
+                                const int slab = jj / (BK / 4), g = jj % (BK / 4);
+                                // a slab past N (its columns are never stored)
+                                // reads the last real slab instead
+                                const int col = nB + slab * 64 < p.N ? nB + slab * 64 : p.N - 64;
+                                gather4(sB + (uint32_t)(slab * SLAB_BYTES + g * 512), &mapB, col,
+                                        brow[j]);
+                            }
+                        }
                     }
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (MULTI) cur.advance(p, ti.e);
+                    if (gat && !ti.ones && kb + 1 < ti.num_kb) fetch_b(kb + 1);
                 }
-            }
-            if (!ok && (!PAIR || leader)) {
-                // wait (bounded) for every copy this CTA's barriers are counting
-                for (int s = 0; s < STAGES; ++s) {
-                    if (issued_parity[s] >= 0)
-                        mbar_wait_bounded(smem_u32(&c.full[s]), (uint32_t)issued_parity[s],
-                                          p.limit_ns, nullptr);
-                    if (issued_tail[s] >= 0)
-                        mbar_wait_bounded(smem_u32(&c.tail[s]), (uint32_t)issued_tail[s],
-                                          p.limit_ns, nullptr);
+                if (relay && (!PAIR || leader)) {
+                    issued_tail[stage] = (int)((tail_phase >> stage) & 1u);
+                    issued_parity[stage] = -1;
+                    tail_phase ^= 1u << stage;
+                } else {
+                    issued_parity[stage] = (int)phase;
+                    issued_tail[stage] = -1;
                 }
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
         }
+        if (!ok && (!PAIR || leader) && (!gat || lane == 0)) {
+            // wait (bounded) for every copy this CTA's barriers are counting
+            for (int s = 0; s < STAGES; ++s) {
+                if (issued_parity[s] >= 0)
+                    mbar_wait_bounded(smem_u32(&c.full[s]), (uint32_t)issued_parity[s],
+                                      p.limit_ns, nullptr);
+                if (issued_tail[s] >= 0)
+                    mbar_wait_bounded(smem_u32(&c.tail[s]), (uint32_t)issued_tail[s],
+                                      p.limit_ns, nullptr);
+            }
+        }
+        };
+        if (p.gather == nullptr) {
+            if (lane == 0) producer(BoolTag<false>{});
+        } else {
+            producer(BoolTag<true>{});
+        }
+        __syncwarp();
     } else if (warp == 1 || (VAR_K && warp == 2 + ES::WARPS)) {
         // ---- weight gradients: tail relay ---------------------------------------------
         // A segment's last K block holds rows of the next segment (or past the
@@ -1509,7 +1615,15 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     const bool pair = use_pairs();
     const uint32_t bn_cta = pair ? BN / 2 : BN;
     CUtensorMap ma, mb;
-    {
+    if (g.gather) {
+        // the unpermuted rows, one-row boxes for tile::gather4
+        if (logits || g.gather_k < 1 || g.gather_rows < 1 || g.gather_rows >= ((int64_t)1 << 31))
+            return cudaErrorInvalidValue;
+        const uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.gather_rows};
+        const uint64_t strides[1] = {(uint64_t)g.K * 2};
+        const uint32_t box[2] = {BK, 1};
+        if (!make_map(&ma, g.act, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    } else {
         const uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.P};
         const uint64_t strides[1] = {(uint64_t)g.K * 2};
         const uint32_t box[2] = {BK, BM};
@@ -1533,6 +1647,8 @@ cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t
     p.offsets = g.offsets; p.bias = g.bias; p.aux = g.aux; p.out0 = g.out0; p.out1 = g.out1;
     p.outf = nullptr; p.accumulate = 0; p.status = status; p.limit_ns = wait_limit_ns();
     withhold_hook(p);
+    p.gather = g.gather;
+    p.gk = g.gather_k;
     const bool colsum = g.epi == Epi::ScaleAux && g.colsum != nullptr;
     if (colsum && !g.colsum_partial) return cudaErrorInvalidValue;
     p.cpart = colsum ? g.colsum_partial : nullptr;
@@ -1613,7 +1729,15 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
         const uint32_t box[3] = {64, BK, BM / 64};
         if (!make_map(&ma, g.act_a, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    {
+    if (g.gather_b) {
+        // the unpermuted rows, one-row boxes of one 64-column slab for tile::gather4
+        if (g.gather_k < 1 || g.gather_rows < 1 || g.gather_rows >= ((int64_t)1 << 31))
+            return cudaErrorInvalidValue;
+        const uint64_t dims[2] = {(uint64_t)g.N, (uint64_t)g.gather_rows};
+        const uint64_t strides[1] = {(uint64_t)g.N * 2};
+        const uint32_t box[2] = {64, 1};
+        if (!make_map(&mb, g.act_b, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    } else {
         const uint64_t dims[3] = {64, (uint64_t)g.P, (uint64_t)g.N / 64};
         const uint64_t strides[2] = {(uint64_t)g.N * 2, 128};
         const uint32_t box[3] = {64, BK, (uint32_t)(pair ? BN / 2 : BN) / 64};
@@ -1626,6 +1750,10 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
     p.offsets = g.offsets; p.outf = g.out; p.accumulate = g.accumulate;
     p.nseg = g.nseg; p.ostride = g.ostride;
     for (int i = 0; i < g.nseg; ++i) p.seg_base[i] = g.seg_base[i];
+    p.gather = g.gather_b;
+    p.gk = g.gather_k;
+    p.gstride = g.gather_stride;
+    for (int i = 0; i < g.nseg; ++i) p.gbase[i] = g.gather_base[i];
     p.status = status; p.limit_ns = wait_limit_ns();
     withhold_hook(p);
     p.bsum = g.bsum;
@@ -1640,7 +1768,9 @@ cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t
     // The segment walk and the split are compiled into a kernel of their own
     // (MULTI): a one-segment call whose experts cannot exceed kKbPartMin K blocks
     // takes the lean kernel, without their code and set-up.
-    const bool multi = g.nseg > 1 || g.P > (int64_t)kKbPartMin * BK;
+    // (The lean kernel reads the rows at the chunk's own offsets: a group of
+    // chunks that does not start at row 0 takes the segment walk too.)
+    const bool multi = g.nseg > 1 || g.seg_base[0] != 0 || g.P > (int64_t)kKbPartMin * BK;
     // each partial tile's slot also reserves one row-sum row (tile_m floats)
     // after the tiles; the row sums of a split need at most one per N tiles
     int64_t cap = (multi && g.part) ? (int64_t)(g.part_bytes / (size_t)(slot_bytes + tile_m * 4))

@@ -100,6 +100,12 @@ struct GemmVarM {
     float* colsum = nullptr;
     float* colsum_partial = nullptr;
     int colsum_accumulate = 0;
+    // Row gather (the permute fused into the loads): when non-null, act is the
+    // unpermuted source [gather_rows, K] and row r of the operand is
+    // act[gather[r] / gather_k] (gather = the dispatch's perm, gather_k = k).
+    const int32_t* gather = nullptr;
+    int gather_k = 1;
+    int64_t gather_rows = 0;
 };
 // Bytes of GemmVarM::colsum_partial for P rows, E experts, N columns.
 size_t gemm_colsum_workspace(int64_t P, int E, int N);
@@ -124,6 +130,14 @@ struct GemmVarK {
     // into parts (none when null or too small for one tile)
     float* part = nullptr;
     size_t part_bytes = 0;
+    // Row gather of act_b: when non-null, act_b is the unpermuted source
+    // [gather_rows, N] and row r of chunk s's rows (r counted from seg_base[s])
+    // is act_b[gather_base[s] + gather_b[s * gather_stride + r] / gather_k].
+    const int32_t* gather_b = nullptr;
+    int gather_k = 1;
+    int64_t gather_stride = 0;
+    int64_t gather_base[kMaxWgradChunks] = {};
+    int64_t gather_rows = 0;
 };
 // Scratch bytes that let the weight-gradient GEMMs over `rows` rows split their
 // long reductions as finely as they would (parts of >= 512 K blocks of 64 rows).

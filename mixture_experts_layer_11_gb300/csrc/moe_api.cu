@@ -166,21 +166,32 @@ moe_status moe_permute(const moe_shape* s, const void* x, const int32_t* pos, vo
     return cuda_status(launch_permute(*s, x, pos, x_perm, (cudaStream_t)stream));
 }
 
-moe_status moe_expert_ffn_fwd(const moe_shape* s, const void* x_perm, const int32_t* offsets,
-                              const void* W1, const void* b1, const void* W2, const void* b2,
-                              void* G, void* A, void* y_perm, void* ws, int32_t* dev_status,
-                              moe_stream_t stream) {
-    (void)ws;
+}  // extern "C"
+
+namespace {
+
+// A5 (perm == nullptr: act is X_perm) or A4 + A5 with the permute fused into
+// the first GEMM's loads (act is x, row r of X_perm read as x[perm[r] / k]).
+moe_status ffn_fwd(const moe_shape* s, const void* act, const int32_t* perm,
+                   const int32_t* offsets, const void* W1, const void* b1, const void* W2,
+                   const void* b2, void* G, void* A, void* y_perm, int32_t* dev_status,
+                   moe_stream_t stream) {
     moe_status r = check_gemm_shape(s);
     if (r != MOE_OK) return r;
     if (s->T == 0) return MOE_OK;
-    if (!ok_ptr(x_perm) || !ok_ptr(offsets) || !ok_ptr(W1) || !ok_ptr(W2) || !ok_opt(b1) ||
-        !ok_opt(b2) || !ok_ptr(G) || !ok_ptr(A) || !ok_ptr(y_perm) || !ok_status(dev_status))
+    if (!ok_ptr(act) || !ok_ptr(offsets) || !ok_ptr(W1) || !ok_ptr(W2) || !ok_opt(b1) ||
+        !ok_opt(b2) || !ok_ptr(G) || !ok_ptr(A) || !ok_ptr(y_perm) || !ok_status(dev_status) ||
+        !ok_opt(perm))
         return MOE_ERR_INVALID;
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t P = s->T * s->k;
-    GemmVarM g1{s->E, s->f, s->d, P, offsets, x_perm, W1, true, Epi::BiasGelu, b1, nullptr, G, A};
+    GemmVarM g1{s->E, s->f, s->d, P, offsets, act, W1, true, Epi::BiasGelu, b1, nullptr, G, A};
     GemmVarM g2{s->E, s->d, s->f, P, offsets, A, W2, true, Epi::Bias, b2, nullptr, y_perm, nullptr};
+    if (perm) {
+        g1.gather = perm;
+        g1.gather_k = s->k;
+        g1.gather_rows = s->T;
+    }
     cudaError_t e;
     if (s->dtype == MOE_BF16) {
         e = launch_gemm_varm_tc(g1, dev_status, st);
@@ -190,6 +201,28 @@ moe_status moe_expert_ffn_fwd(const moe_shape* s, const void* x_perm, const int3
         if (e == cudaSuccess) e = launch_gemm_varm_simt(g2, st);
     }
     return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_expert_ffn_fwd(const moe_shape* s, const void* x_perm, const int32_t* offsets,
+                              const void* W1, const void* b1, const void* W2, const void* b2,
+                              void* G, void* A, void* y_perm, void* ws, int32_t* dev_status,
+                              moe_stream_t stream) {
+    (void)ws;
+    return ffn_fwd(s, x_perm, nullptr, offsets, W1, b1, W2, b2, G, A, y_perm, dev_status, stream);
+}
+
+moe_status moe_expert_ffn_fwd_gather(const moe_shape* s, const void* x, const int32_t* perm,
+                                     const int32_t* offsets, const void* W1, const void* b1,
+                                     const void* W2, const void* b2, void* G, void* A,
+                                     void* y_perm, void* ws, int32_t* dev_status,
+                                     moe_stream_t stream) {
+    (void)ws;
+    if (s && s->T > 0 && !ok_ptr(perm)) return MOE_ERR_INVALID;
+    return ffn_fwd(s, x, perm, offsets, W1, b1, W2, b2, G, A, y_perm, dev_status, stream);
 }
 
 moe_status moe_combine_fwd(const moe_shape* s, const void* y_perm, const int32_t* pos,
@@ -251,16 +284,23 @@ cudaError_t ffn_bwd_data(const moe_shape& s, const void* dy_perm, const void* G,
 // summed over every chunk's rows of expert e.  Chunks beyond what one launch
 // walks go to further launches that accumulate.  `partial`: column-sum
 // partial rows of the fp32 path (ffn_partial_bytes of the largest chunk).
+// perm != nullptr: x_perm is the unpermuted x of all chunks (chunk c's tokens
+// after those of chunks < c) and chunk c's rows of X_perm are read through its
+// perm (at perm + c * perm_stride): row r is x[token base + perm[r] / k].
 cudaError_t ffn_bwd_weights(const moe_shape& s, int nchunks, const int64_t* chunk_T,
                             const int32_t* offsets, int ostride, const void* dy_perm,
                             const void* x_perm, const void* dH, const void* A, float* dW1,
                             float* dW2, float* db2, int accumulate, float* partial,
-                            void* split, size_t split_size, int32_t* status, cudaStream_t st) {
+                            void* split, size_t split_size, int32_t* status, cudaStream_t st,
+                            const int32_t* perm = nullptr, int64_t perm_stride = 0) {
     const int E = s.E, d = s.d, f = s.f, k = s.k;
     const bool tc = s.dtype == MOE_BF16;
-    int64_t P = 0;
-    for (int c = 0; c < nchunks; ++c) P += chunk_T[c] * k;
-    int64_t base = 0;
+    int64_t P = 0, Ttot = 0;
+    for (int c = 0; c < nchunks; ++c) {
+        P += chunk_T[c] * k;
+        Ttot += chunk_T[c];
+    }
+    int64_t base = 0, tbase = 0;
     for (int c0 = 0; c0 < nchunks; c0 += kMaxWgradChunks) {
         const int n = nchunks - c0 < kMaxWgradChunks ? nchunks - c0 : kMaxWgradChunks;
         const int acc = accumulate || c0 > 0;
@@ -268,10 +308,18 @@ cudaError_t ffn_bwd_weights(const moe_shape& s, int nchunks, const int64_t* chun
         GemmVarK g_w2{E, d, f, P, offsets + (int64_t)c0 * ostride, dy_perm, A, dW2, acc};
         if (tc) g_w2.bsum = db2;   // db2 = column sums of dY_perm, by the dW2 GEMM
         GemmVarK g_w1{E, f, d, P, offsets + (int64_t)c0 * ostride, dH, x_perm, dW1, acc};
-        int64_t b = base;
+        int64_t b = base, tb = tbase;
         for (int i = 0; i < n; ++i) {
             g_w2.seg_base[i] = g_w1.seg_base[i] = b;
+            g_w1.gather_base[i] = tb;
             b += chunk_T[c0 + i] * k;
+            tb += chunk_T[c0 + i];
+        }
+        if (perm) {
+            g_w1.gather_b = perm + (int64_t)c0 * perm_stride;
+            g_w1.gather_k = k;
+            g_w1.gather_stride = perm_stride;
+            g_w1.gather_rows = Ttot;
         }
         g_w2.nseg = g_w1.nseg = n;
         g_w2.ostride = g_w1.ostride = ostride;
@@ -294,6 +342,7 @@ cudaError_t ffn_bwd_weights(const moe_shape& s, int nchunks, const int64_t* chun
             }
         }
         base = b;
+        tbase = tb;
     }
     return cudaSuccess;
 }
@@ -381,12 +430,18 @@ size_t moe_expert_ffn_bwd_weights_workspace_size(const moe_shape* s, int nchunks
     return n > 0 ? n : 256;
 }
 
-moe_status moe_expert_ffn_bwd_weights(const moe_shape* s, int nchunks, const int64_t* chunk_T,
-                                      const int32_t* offsets, int offsets_stride,
-                                      const void* dy_perm, const void* x_perm, const void* dH,
-                                      const void* A, float* dW1, float* dW2, float* db2,
-                                      int accumulate, void* ws, size_t ws_bytes,
-                                      int32_t* dev_status, moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The weight half's checks and dispatch; perm != nullptr: X rows gathered (see
+// ffn_bwd_weights).
+moe_status bwd_weights_entry(const moe_shape* s, int nchunks, const int64_t* chunk_T,
+                             const int32_t* offsets, int offsets_stride, const void* dy_perm,
+                             const void* xs, const int32_t* perm, int64_t perm_stride,
+                             const void* dH, const void* A, float* dW1, float* dW2, float* db2,
+                             int accumulate, void* ws, size_t ws_bytes, int32_t* dev_status,
+                             moe_stream_t stream) {
     moe_status r = check_gemm_shape(s);
     if (r != MOE_OK) return r;
     if (nchunks < 1 || chunk_T == nullptr || offsets_stride < s->E + 1 || offsets_stride % 4)
@@ -407,8 +462,11 @@ moe_status moe_expert_ffn_bwd_weights(const moe_shape* s, int nchunks, const int
         if (e == cudaSuccess) e = zero_grads(*s, db2, (size_t)E * d, nullptr, 0, st);
         return cuda_status(e);
     }
-    if (!ok_ptr(dy_perm) || !ok_ptr(x_perm) || !ok_ptr(dH) || !ok_ptr(A) || !ok_ptr(offsets) ||
+    if (!ok_ptr(dy_perm) || !ok_ptr(xs) || !ok_ptr(dH) || !ok_ptr(A) || !ok_ptr(offsets) ||
         !ok_status(dev_status) || !ok_opt(ws) || (ws == nullptr && ws_bytes != 0))
+        return MOE_ERR_INVALID;
+    // a gather reads chunk c's perm entries [c * perm_stride, + chunk_T[c] * k)
+    if (perm && (!ok_ptr(perm) || perm_stride < Tmax * s->k))
         return MOE_ERR_INVALID;
     moe_shape big = *s;
     big.T = Tmax;
@@ -416,12 +474,41 @@ moe_status moe_expert_ffn_bwd_weights(const moe_shape* s, int nchunks, const int
         // fp32: the column-sum partials of db2 (no split)
         if (ws == nullptr || ws_bytes < ffn_partial_bytes(big)) return MOE_ERR_INVALID;
         return cuda_status(ffn_bwd_weights(*s, nchunks, chunk_T, offsets, offsets_stride, dy_perm,
-                                           x_perm, dH, A, dW1, dW2, db2, accumulate, (float*)ws,
-                                           nullptr, 0, dev_status, st));
+                                           xs, dH, A, dW1, dW2, db2, accumulate, (float*)ws,
+                                           nullptr, 0, dev_status, st, perm, perm_stride));
     }
     return cuda_status(ffn_bwd_weights(*s, nchunks, chunk_T, offsets, offsets_stride, dy_perm,
-                                       x_perm, dH, A, dW1, dW2, db2, accumulate, nullptr, ws,
-                                       ws_bytes, dev_status, st));
+                                       xs, dH, A, dW1, dW2, db2, accumulate, nullptr, ws,
+                                       ws_bytes, dev_status, st, perm, perm_stride));
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_expert_ffn_bwd_weights(const moe_shape* s, int nchunks, const int64_t* chunk_T,
+                                      const int32_t* offsets, int offsets_stride,
+                                      const void* dy_perm, const void* x_perm, const void* dH,
+                                      const void* A, float* dW1, float* dW2, float* db2,
+                                      int accumulate, void* ws, size_t ws_bytes,
+                                      int32_t* dev_status, moe_stream_t stream) {
+    return bwd_weights_entry(s, nchunks, chunk_T, offsets, offsets_stride, dy_perm, x_perm,
+                             nullptr, 0, dH, A, dW1, dW2, db2, accumulate, ws, ws_bytes,
+                             dev_status, stream);
+}
+
+moe_status moe_expert_ffn_bwd_weights_gather(const moe_shape* s, int nchunks,
+                                             const int64_t* chunk_T, const int32_t* offsets,
+                                             int offsets_stride, const void* dy_perm,
+                                             const void* x, const int32_t* perm,
+                                             int64_t perm_stride, const void* dH, const void* A,
+                                             float* dW1, float* dW2, float* db2, int accumulate,
+                                             void* ws, size_t ws_bytes, int32_t* dev_status,
+                                             moe_stream_t stream) {
+    if (perm == nullptr) return MOE_ERR_INVALID;
+    return bwd_weights_entry(s, nchunks, chunk_T, offsets, offsets_stride, dy_perm, x, perm,
+                             perm_stride, dH, A, dW1, dW2, db2, accumulate, ws, ws_bytes,
+                             dev_status, stream);
 }
 
 moe_status moe_route_bwd(const moe_shape* s, const float* dw, const float* logits,

@@ -2,12 +2,20 @@
 points in the layer's order (route, permute, expert FFN, combine; then combine
 backward, expert FFN backward, permute backward, router backward).
 
+With ``gather`` the permute is fused into the expert GEMMs: the first GEMM of
+the forward and the dW1 GEMM of the backward load the rows of x that the
+dispatch's perm names (row r of the expert-sorted activations is
+x[perm[r] / k]) instead of reading a permuted copy, so X_perm is never written
+or kept.  The results are those of the unfused sequence, bit for bit.  It is
+not the default: each TMA tile::gather4 load moves four 128-byte rows, and at
+that rate the loads, not the tensor cores, bound those GEMMs.
+
 Tokens are processed in consecutive dispatch chunks of at most ``chunk``
 tokens, the bounded dispatch chunk of PipelinedLLEP ("Flattening Every Memory
 Peak in Long-Context Mixture-of-Experts Training", abstract): routing is per
 token, the histogram / offsets / positions are per chunk, and the weight
 gradients accumulate over chunks in fp32 in chunk order.  The activations a
-chunk's backward needs (X_perm, G = GELU'(h), A, Y_perm) stay resident in HBM between
+chunk's backward needs (G = GELU'(h), A, Y_perm; X_perm when unfused) stay resident in HBM between
 the forward and the backward; the backward's transient buffers (dY_perm,
 dX_perm and the library workspace) are shared by all chunks.
 
@@ -65,12 +73,15 @@ class LayerPass:
     recompute (keep only the routing between forward and backward and re-run
     each chunk's permute and expert forward in the backward; one stream),
     defer_wgrad (one weight-gradient pass over all chunks after the last
-    chunk's backward; default: with more than one chunk, unless recompute)."""
+    chunk's backward; default: with more than one chunk, unless recompute),
+    gather (the permute fused into the expert GEMMs' operand loads: no X_perm
+    is written; the first GEMM and the dW1 GEMM read x through the dispatch's
+    perm.  False: moe_permute writes X_perm and the GEMMs read it)."""
 
     def __init__(self, T: int, d: int, f: int, E: int, k: int, dtype: torch.dtype,
                  renorm: int, chunk: Optional[int] = None, device="cuda",
                  pipeline: bool = True, recompute: bool = False,
-                 defer_wgrad: Optional[bool] = None):
+                 defer_wgrad: Optional[bool] = None, gather: bool = False):
         self.T, self.d, self.f, self.E, self.k = T, d, f, E, k
         self.dtype, self.renorm = dtype, int(renorm)
         C = chunk if chunk else T
@@ -84,6 +95,7 @@ class LayerPass:
         if defer_wgrad is None:
             defer_wgrad = nch > 1
         self.defer_wgrad = bool(defer_wgrad) and not self.recompute
+        self.gather = bool(gather)
         dev = torch.device(device)
         f32, i32 = torch.float32, torch.int32
         z = lambda *s, dt=dtype: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
@@ -99,7 +111,7 @@ class LayerPass:
         # activations: of every chunk (kept for the backward), or of one chunk
         # (recompute)
         R = C * k if self.recompute else T * k
-        self.X_perm = z(R, d)
+        self.X_perm = None if self.gather else z(R, d)
         self.G = z(R, f)
         self.A = z(R, f)
         self.Y_perm = z(R, d)
@@ -120,6 +132,14 @@ class LayerPass:
             self.wws = torch.empty(max(wn, 256), dtype=torch.uint8, device=dev)
         else:
             self.dY_perm = z(nbuf, C * k, d)
+            if self.gather:
+                # per chunk: dH for the weight half, which reads x through perm
+                self.dH = z(nbuf, C * k, f)
+                self.wshapes = [ops.make_shape(c1 - c0, d, f, E, k, dtype, renorm)
+                                for c0, c1 in self.chunks]
+                wn = max(ops.moe_expert_ffn_bwd_weights_workspace_size(
+                    ws_, [c1 - c0]) for ws_, (c0, c1) in zip(self.wshapes, self.chunks))
+                self.wws = torch.empty(max(wn, 256), dtype=torch.uint8, device=dev)
         self.dX_perm = z(nbuf, C * k, d)
         self.dW1 = z(E, f, d, dt=f32)
         self.db1 = z(E, f, dt=f32)
@@ -168,7 +188,6 @@ class LayerPass:
             pos = self._rows(self.pos, c0, c1)
             perm = self._rows(self.perm, c0, c1, k)
             offs = self.offsets[ci]
-            Xp = self._act(self.X_perm, c0, c1)
             # routing and permute of this chunk: on the side stream when
             # pipelined (chunks are independent there: own rows, own workspace)
             with torch.cuda.stream(self.side if self.pipeline else main):
@@ -176,14 +195,21 @@ class LayerPass:
                               int(compute_logits), self._rows(self.idx, c0, c1),
                               self._rows(self.w, c0, c1), self.counts[ci], offs, pos, perm,
                               self.ws2 if self.pipeline else self.ws, self.status)
-                ops.moe_permute(s, xc, pos, Xp)
+                if not self.gather:
+                    ops.moe_permute(s, xc, pos, self._act(self.X_perm, c0, c1))
                 if self.pipeline:
                     self._ev_routed[ci].record(self.side)
             if self.pipeline:
                 main.wait_event(self._ev_routed[ci])
             Yp = self._act(self.Y_perm, c0, c1)
-            ops.moe_expert_ffn_fwd(s, Xp, offs, W1, b1, W2, b2, self._act(self.G, c0, c1),
-                                   self._act(self.A, c0, c1), Yp, self.ws, self.status)
+            if self.gather:   # A4 fused into A5: x rows through perm
+                ops.moe_expert_ffn_fwd_gather(s, xc, perm, offs, W1, b1, W2, b2,
+                                              self._act(self.G, c0, c1), self._act(self.A, c0, c1),
+                                              Yp, self.ws, self.status)
+            else:
+                ops.moe_expert_ffn_fwd(s, self._act(self.X_perm, c0, c1), offs, W1, b1, W2, b2,
+                                       self._act(self.G, c0, c1), self._act(self.A, c0, c1), Yp,
+                                       self.ws, self.status)
             ops.moe_combine_fwd(s, Yp, pos, self._rows(self.w, c0, c1), self._rows(self.y, c0, c1))
         if self.pipeline:
             self._ev_join.record(self.side)
@@ -217,6 +243,17 @@ class LayerPass:
                                             self.offsets[ci], W1, W2, self.dH[c0 * k:c1 * k],
                                             dXp, self.db1, int(ci > 0), self.ws, self.status)
                 return
+            if self.gather:   # data half, then the weight half reading x through perm
+                dH = self.dH[ci % 2 if self.pipeline else 0, :(c1 - c0) * k]
+                ops.moe_expert_ffn_bwd_data(self.shapes[ci], dYp, self._act(self.G, c0, c1),
+                                            self.offsets[ci], W1, W2, dH, dXp, self.db1,
+                                            int(ci > 0), self.ws, self.status)
+                ops.moe_expert_ffn_bwd_weights_gather(
+                    self.wshapes[ci], [c1 - c0], self.offsets[ci:ci + 1], dYp,
+                    self._rows(x, c0, c1), self._rows(self.perm, c0, c1, k), (c1 - c0) * k, dH,
+                    self._act(self.A, c0, c1), self.dW1, self.dW2, self.db2, int(ci > 0),
+                    self.wws, self.status)
+                return
             ops.moe_expert_ffn_bwd(self.shapes[ci], dYp, self._act(self.X_perm, c0, c1),
                                    self._act(self.G, c0, c1), self._act(self.A, c0, c1),
                                    self.offsets[ci], W1, W2, dXp, self.dW1, self.db1, self.dW2,
@@ -235,6 +272,14 @@ class LayerPass:
             c0, c1 = self.chunks[ci]
             W1_, b1_, W2_, b2_ = self._params
             s = self.shapes[ci]
+            if self.gather:
+                ops.moe_expert_ffn_fwd_gather(s, self._rows(x, c0, c1),
+                                              self._rows(self.perm, c0, c1, k), self.offsets[ci],
+                                              W1_, b1_, W2_, b2_, self._act(self.G, c0, c1),
+                                              self._act(self.A, c0, c1),
+                                              self._act(self.Y_perm, c0, c1), self.ws,
+                                              self.status)
+                return
             Xp = self._act(self.X_perm, c0, c1)
             ops.moe_permute(s, self._rows(x, c0, c1), self._rows(self.pos, c0, c1), Xp)
             ops.moe_expert_ffn_fwd(s, Xp, self.offsets[ci], W1_, b1_, W2_, b2_,
@@ -244,7 +289,12 @@ class LayerPass:
         if self.recompute and self._params is None:
             raise RuntimeError("recompute: backward needs the forward's parameters")
         def weights():         # A8, weight half: every chunk's rows in one pass
-            if self.defer_wgrad:
+            if self.defer_wgrad and self.gather:   # X through each chunk's perm
+                ops.moe_expert_ffn_bwd_weights_gather(self.wshape, self.chunk_T, self.offsets,
+                                                      self.dY_perm, x, self.perm, self.C * k,
+                                                      self.dH, self.A, self.dW1, self.dW2,
+                                                      self.db2, 0, self.wws, self.status)
+            elif self.defer_wgrad:
                 ops.moe_expert_ffn_bwd_weights(self.wshape, self.chunk_T, self.offsets,
                                                self.dY_perm, self.X_perm, self.dH, self.A,
                                                self.dW1, self.dW2, self.db2, 0, self.wws,

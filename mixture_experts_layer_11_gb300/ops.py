@@ -25,7 +25,9 @@ ENTRY_POINTS = ("moe_status_string", "moe_workspace_size", "moe_route", "moe_per
                 "moe_expert_ffn_fwd", "moe_combine_fwd", "moe_combine_bwd",
                 "moe_expert_ffn_bwd", "moe_route_bwd", "moe_debug_bounded_wait",
                 "moe_debug_gelu", "moe_route_noalloc", "moe_expert_ffn_bwd_data",
-                "moe_expert_ffn_bwd_weights", "moe_expert_ffn_bwd_weights_workspace_size")
+                "moe_expert_ffn_bwd_weights", "moe_expert_ffn_fwd_gather",
+                "moe_expert_ffn_bwd_weights_gather",
+                "moe_expert_ffn_bwd_weights_workspace_size")
 
 
 class MoEError(RuntimeError):
@@ -91,6 +93,11 @@ def lib() -> ctypes.CDLL:
                                                      ctypes.POINTER(ctypes.c_int64), _P,
                                                      ctypes.c_int, _P, _P, _P, _P, _P, _P, _P,
                                                      ctypes.c_int, _P, ctypes.c_size_t, _P, _P]
+            L.moe_expert_ffn_fwd_gather.argtypes = [_SP] + [_P] * 13
+            L.moe_expert_ffn_bwd_weights_gather.argtypes = [
+                _SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64), _P, ctypes.c_int, _P, _P,
+                _P, ctypes.c_int64, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P,
+                _P]
             L.moe_expert_ffn_bwd_weights_workspace_size.restype = ctypes.c_size_t
             L.moe_expert_ffn_bwd_weights_workspace_size.argtypes = [
                 _SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64)]
@@ -169,6 +176,17 @@ def moe_expert_ffn_fwd(s, x_perm, offsets, W1, b1, W2, b2, G, A, y_perm, ws, dev
         _stream(stream)))
 
 
+def moe_expert_ffn_fwd_gather(s, x, perm, offsets, W1, b1, W2, b2, G, A, y_perm, ws,
+                              dev_status, stream=None):
+    """moe_expert_ffn_fwd with the permute fused in: x [T,d] and the dispatch's
+    perm [T*k] instead of X_perm."""
+    _check("moe_expert_ffn_fwd_gather", lib().moe_expert_ffn_fwd_gather(
+        ctypes.byref(s), _ptr(x, _act(s)), _ptr(perm, _I32), _ptr(offsets, _I32),
+        _ptr(W1, _act(s)), _ptr(b1, _act(s)), _ptr(W2, _act(s)), _ptr(b2, _act(s)),
+        _ptr(G, _act(s)), _ptr(A, _act(s)), _ptr(y_perm, _act(s)), _ptr(ws),
+        _ptr(dev_status, _I32), _stream(stream)))
+
+
 def moe_combine_fwd(s, y_perm, pos, w, y, stream=None):
     _check("moe_combine_fwd", lib().moe_combine_fwd(
         ctypes.byref(s), _ptr(y_perm, _act(s)), _ptr(pos, _I32), _ptr(w, _F32), _ptr(y, _act(s)),
@@ -214,17 +232,39 @@ def moe_expert_ffn_bwd_weights(s, chunk_T, offsets, dy_perm, x_perm, dH, A, dW1,
     n = len(chunk_T)
     arr = (ctypes.c_int64 * n)(*[int(t) for t in chunk_T])
     fn = "moe_expert_ffn_bwd_weights"
-    if not isinstance(offsets, torch.Tensor) or offsets.dim() != 2 or offsets.shape[0] != n:
-        raise MoEError(fn, MOE_ERR_INVALID, "offsets must be a [nchunks, stride] tensor")
-    if not offsets.is_cuda or offsets.dtype != _I32 or offsets.stride(1) != 1:
-        raise MoEError(fn, MOE_ERR_INVALID, "offsets must be int32 CUDA rows")
-    stride = int(offsets.stride(0)) if n > 1 else max(int(offsets.shape[1]) + 3 & ~3, 4)
+    stride = _offsets_stride(fn, offsets, n)
     _check(fn, lib().moe_expert_ffn_bwd_weights(
         ctypes.byref(s), n, arr, offsets.data_ptr(), stride, _ptr(dy_perm, _act(s)),
         _ptr(x_perm, _act(s)), _ptr(dH, _act(s)), _ptr(A, _act(s)), _ptr(dW1, _F32),
         _ptr(dW2, _F32), _ptr(db2, _F32), int(accumulate), _ptr(ws),
         0 if ws is None else int(ws.numel() * ws.element_size()), _ptr(dev_status, _I32),
         _stream(stream)))
+
+
+def _offsets_stride(fn, offsets, n):
+    if not isinstance(offsets, torch.Tensor) or offsets.dim() != 2 or offsets.shape[0] != n:
+        raise MoEError(fn, MOE_ERR_INVALID, "offsets must be a [nchunks, stride] tensor")
+    if not offsets.is_cuda or offsets.dtype != _I32 or offsets.stride(1) != 1:
+        raise MoEError(fn, MOE_ERR_INVALID, "offsets must be int32 CUDA rows")
+    return int(offsets.stride(0)) if n > 1 else max(int(offsets.shape[1]) + 3 & ~3, 4)
+
+
+def moe_expert_ffn_bwd_weights_gather(s, chunk_T, offsets, dy_perm, x, perm, perm_stride, dH,
+                                      A, dW1, dW2, db2, accumulate, ws, dev_status,
+                                      stream=None):
+    """moe_expert_ffn_bwd_weights reading X through each chunk's perm: x holds
+    the chunks' tokens one chunk after the other; chunk c's perm starts at
+    element c * perm_stride of ``perm``."""
+    n = len(chunk_T)
+    arr = (ctypes.c_int64 * n)(*[int(t) for t in chunk_T])
+    fn = "moe_expert_ffn_bwd_weights_gather"
+    stride = _offsets_stride(fn, offsets, n)
+    _check(fn, lib().moe_expert_ffn_bwd_weights_gather(
+        ctypes.byref(s), n, arr, offsets.data_ptr(), stride, _ptr(dy_perm, _act(s)),
+        _ptr(x, _act(s)), _ptr(perm, _I32), ctypes.c_int64(int(perm_stride)), _ptr(dH, _act(s)),
+        _ptr(A, _act(s)), _ptr(dW1, _F32), _ptr(dW2, _F32), _ptr(db2, _F32), int(accumulate),
+        _ptr(ws), 0 if ws is None else int(ws.numel() * ws.element_size()),
+        _ptr(dev_status, _I32), _stream(stream)))
 
 
 def moe_route_bwd(s, dw, logits, idx, w, perm, offsets, x, Wg, dx_perm, pos, dx, dWg,
