@@ -76,6 +76,16 @@ def launches_per_step(cfg, nchunks: int, router_tc: bool, recompute: bool, defer
     bf = cfg.dtype == "bf16"
     tc = router_tc and bf and cfg.d % 64 == 0
     route = 4 if (tc or cfg.E > 32) else 3
+    if not tc and cfg.E > 32:
+        # CUDA-core logits in 128-row tiles of 64 (E <= 64) or 128 experts, two or
+        # three blocks per SM; a stream-K split (and its fix-up kernel) when the
+        # tiles do not fill whole waves
+        Tc = min(cfg.T, cfg.chunk or cfg.T)
+        bn = 64 if cfg.E <= 64 else 128
+        tiles = -(-Tc // 128) * -(-cfg.E // bn)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count \
+            if torch.cuda.is_available() else 152
+        route += 1 if tiles % (sms * (3 if bn == 64 else 2)) else 0
     permute = 0 if gather else 1
     data = 3 if bf else 4
     chunk_rows = min(cfg.T, cfg.chunk or cfg.T) * cfg.k
