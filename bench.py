@@ -105,13 +105,22 @@ def count_library_kernels(step) -> Optional[int]:
     try:
         from torch.profiler import ProfilerActivity, profile
         torch.cuda.synchronize()
-        # (kernel activity is attributed through the CPU-side launch records)
-        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
+        acts = [ProfilerActivity.CPU, ProfilerActivity.CUDA]
+        # a first session sets the activity tracing up (its records can miss kernels)
+        with profile(activities=acts):
             step()
             torch.cuda.synchronize()
-        n = sum(1 for e in prof.events()
+        with profile(activities=acts) as prof:
+            step()
+            torch.cuda.synchronize()
+        ev = prof.events()
+        n = sum(1 for e in ev
                 if e.device_type == torch.autograd.DeviceType.CUDA and "moe::" in e.name)
-    except Exception:
+        if n == 0:
+            print(f"kernel count: no library kernel among {len(ev)} profiler events",
+                  file=sys.stderr)
+    except Exception as exc:   # e.g. another tool holds the profiling interface
+        print(f"kernel count: profiler unavailable ({exc!r})", file=sys.stderr)
         return None
     return n or None
 
