@@ -395,7 +395,7 @@ def _sum_ms(marks):
 
 def measure(cfg, dev, steps, warmup, *, pipeline=True, graph=True, router_tc=False,
             recompute=False, defer_wgrad=None, sampler=None, e2e=False, dist=None, seed=0,
-            gather=False):
+            gather=False, gemm_units=None):
     """Times `steps` layer steps of one workload.  Returns a dict of measured
     values; with e2e also the end-to-end rate through host buffers."""
     from mixture_experts_layer_11_gb300.layer import LayerPass
@@ -406,7 +406,7 @@ def measure(cfg, dev, steps, warmup, *, pipeline=True, graph=True, router_tc=Fal
         os.environ.pop(ROUTER_TC_ENV, None)
     try:
         return _measure(cfg, dev, steps, warmup, pipeline, graph, router_tc, recompute,
-                        defer_wgrad, sampler, e2e, dist, seed, LayerPass, gather)
+                        defer_wgrad, sampler, e2e, dist, seed, LayerPass, gather, gemm_units)
     finally:
         if prev is None:
             os.environ.pop(ROUTER_TC_ENV, None)
@@ -415,12 +415,12 @@ def measure(cfg, dev, steps, warmup, *, pipeline=True, graph=True, router_tc=Fal
 
 
 def _measure(cfg, dev, steps, warmup, pipeline, graph_on, router_tc, recompute, defer_wgrad,
-             sampler, e2e, dist, seed, LayerPass, gather):
+             sampler, e2e, dist, seed, LayerPass, gather, gemm_units):
     torch.cuda.reset_peak_memory_stats(dev)
     inp = synth.make_inputs(cfg, seed=seed, device=str(dev))
     lp = LayerPass(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.torch_dtype, cfg.renorm,
                    chunk=cfg.chunk, device=dev, pipeline=pipeline, recompute=recompute,
-                   defer_wgrad=defer_wgrad, gather=gather)
+                   defer_wgrad=defer_wgrad, gather=gather, gemm_units=gemm_units)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     x_buf, dy_buf = inp["x"], inp["dy"]
@@ -488,6 +488,7 @@ def _measure(cfg, dev, steps, warmup, pipeline, graph_on, router_tc, recompute, 
                calls={n: (ms / steps, tok // steps) for n, (ms, tok) in calls.items()},
                device_memory_gib=torch.cuda.max_memory_allocated(dev) / 2**30,
                pipelined=lp.pipeline, defer_wgrad=lp.defer_wgrad, gather=lp.gather,
+               gemm_units=lp.gemm_units,
                launches_formula=launches_per_step(cfg, len(lp.chunks), router_tc, recompute,
                                                   lp.defer_wgrad, lp.gather) * steps,
                launches=(graph_kernels * steps if graph_kernels
@@ -714,6 +715,7 @@ def run_ours(args, cfg):
     sampler = ClockSampler(local)
     main = measure(cfg, dev, args.steps, args.warmup, sampler=sampler, e2e=True, dist=dist,
                    seed=rank, graph=not args.no_graph, recompute=args.recompute,
+                   gemm_units=args.gemm_units,
                    defer_wgrad=False if args.per_chunk_wgrad else None)
     total_ms, e2e_ms = max_over_ranks([main["total_ms"], main["e2e_ms"]], dist, dev)
     if rank != 0:
@@ -784,8 +786,9 @@ def run_ours(args, cfg):
                    "router": "CUDA cores (fp32 FMA); tensor cores only for the expert GEMMs",
                    "l2": "flushed between steps (256 MiB write, outside the step timing)",
                    "launch": "eager" if args.no_graph else "one CUDA graph per step",
-                   "chunks": (f"{main['chunks']}, pipelined on two streams" if main["pipelined"]
-                              else f"{main['chunks']}, one stream"),
+                   "chunks": (f"{main['chunks']}, pipelined on two streams, per-chunk expert "
+                              f"GEMMs on {main['gemm_units'] or 'all'} CTA pairs"
+                              if main["pipelined"] else f"{main['chunks']}, one stream"),
                    "activations": ("recomputed in the backward (routing kept)" if args.recompute
                                    else "kept from the forward for the backward"),
                    "weight_gradients": ("one pass over all chunks after the backward"
@@ -887,6 +890,9 @@ def main():
                          "the GPU one group of experts at a time")
     ap.add_argument("--group", type=int, default=16,
                     help="experts per streamed group (--weights-on-host)")
+    ap.add_argument("--gemm-units", type=int, default=None,
+                    help="CTA pairs of the per-chunk expert GEMMs when chunks are pipelined "
+                         "(default: the layer's choice; 0 = every pair)")
     ap.add_argument("--no-sub-configs", action="store_true",
                     help="time only the chosen workload (no per-workload table, no router "
                          "variant)")

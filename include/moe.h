@@ -368,6 +368,21 @@ MOE_API moe_status moe_route_noalloc(const moe_shape* s, const void* x, const vo
 MOE_API moe_status moe_debug_bounded_wait(uint64_t limit_ns, int32_t* dev_status,
                                   moe_stream_t stream);
 
+/* Launch option: the tensor-core expert GEMMs (moe_expert_ffn_* calls, bf16)
+ * that the calling host thread launches from now on use at most `units` CTA
+ * pairs (single CTAs with MOE_GEMM_PAIR=0); 0 restores the default, every
+ * pair the GPU holds at once.  Capturing a CUDA graph records the launch as
+ * made.  For overlapping other kernels with the GEMMs: a persistent GEMM grid
+ * holds every SM, so kernels on another stream otherwise run only in its
+ * gaps (the chunk pipeline of "MPipeMoE", "research method", and the
+ * overlap of "ES-MoE", review, section 3, leave SMs to the side stream this
+ * way).  The data-path GEMMs' results do not depend on it; the weight
+ * gradients' split reductions do (their parts follow the grid), so callers
+ * that want run-to-run identical weight gradients keep one setting for them.
+ * MOE_GEMM_MAX_UNITS in the environment, when set, takes precedence.  Returns
+ * MOE_ERR_INVALID for units < 0. */
+MOE_API moe_status moe_set_gemm_max_units(int units);
+
 /* Diagnostics: GELU(x) = x Phi(x) and GELU'(x) = Phi(x) + x phi(x) of n fp32
  * values, as the kernels evaluate them: fast != 0 selects the approximation
  * the bf16 expert-GEMM epilogues use (erf by Abramowitz & Stegun, "Handbook

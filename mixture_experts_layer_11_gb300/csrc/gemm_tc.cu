@@ -1394,11 +1394,14 @@ bool use_pairs() {
     return !(s && s[0] == '0');
 }
 
+// The caller's cap (moe_set_gemm_max_units), per host thread; 0: none.
+thread_local int64_t t_units_cap = 0;
+
 int64_t max_units_override() {
     const char* s = getenv("MOE_GEMM_MAX_UNITS");
-    if (!s || !*s) return 0;
+    if (!s || !*s) return t_units_cap;
     const long long v = strtoll(s, nullptr, 10);
-    return v > 0 ? (int64_t)v : 0;
+    return v > 0 ? (int64_t)v : t_units_cap;
 }
 
 void withhold_hook(TcParams& p) {
@@ -1607,6 +1610,8 @@ bool make_out_map(CUtensorMap* m, void* ptr, int64_t P, int N, int CW) {
 }
 
 }  // namespace
+
+void set_gemm_units_cap(int64_t units) { t_units_cap = units > 0 ? units : 0; }
 
 cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t st) {
     const bool logits = g.epi == Epi::Logits;

@@ -143,6 +143,9 @@ struct GemmVarK {
 // long reductions as finely as they would (parts of >= 512 K blocks of 64 rows).
 size_t vark_split_workspace(int64_t rows, int E, int M, int N);
 
+// Cap on the tensor-core GEMMs' CTA pairs (single CTAs) per launch for the
+// calling host thread; 0 = the co-resident maximum.
+void set_gemm_units_cap(int64_t units);
 cudaError_t launch_gemm_varm_tc(const GemmVarM& g, int32_t* status, cudaStream_t st);
 cudaError_t launch_gemm_vark_tc(const GemmVarK& g, int32_t* status, cudaStream_t st);
 cudaError_t launch_gemm_varm_simt(const GemmVarM& g, cudaStream_t st);

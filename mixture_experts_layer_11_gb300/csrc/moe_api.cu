@@ -633,6 +633,12 @@ moe_status moe_debug_bounded_wait(uint64_t limit_ns, int32_t* dev_status, moe_st
     return cuda_status(launch_bounded_wait(limit_ns, dev_status, (cudaStream_t)stream));
 }
 
+moe_status moe_set_gemm_max_units(int units) {
+    if (units < 0) return MOE_ERR_INVALID;
+    set_gemm_units_cap(units);
+    return MOE_OK;
+}
+
 moe_status moe_debug_gelu(int64_t n, const float* x, float* gelu, float* gelu_grad, int fast,
                           moe_stream_t stream) {
     if (n < 0) return MOE_ERR_INVALID;

@@ -63,6 +63,13 @@ def _pad4(n: int) -> int:
     return (n + 3) // 4 * 4
 
 
+# CTA pairs of the per-chunk expert GEMMs when the chunks are pipelined; 0 =
+# every pair the GPU holds.  A cap leaves SMs to the side stream (on the
+# long-context workload 64 of the 76 pairs made the step 3% faster), but one
+# capped run did not finish, for a reason not found; so no cap by default.
+GEMM_UNITS_PIPELINED = 0
+
+
 class LayerPass:
     """Preallocated buffers and launch sequence for one layer configuration.
 
@@ -76,12 +83,18 @@ class LayerPass:
     chunk's backward; default: with more than one chunk, unless recompute),
     gather (the permute fused into the expert GEMMs' operand loads: no X_perm
     is written; the first GEMM and the dW1 GEMM read x through the dispatch's
-    perm.  False: moe_permute writes X_perm and the GEMMs read it)."""
+    perm.  False: moe_permute writes X_perm and the GEMMs read it),
+    gemm_units (with the chunk pipeline: the CTA pairs the per-chunk expert
+    GEMMs of the forward and of the backward's data half may use, leaving the
+    other SMs to the side stream's routing, permute, combine backward and
+    router backward; None = GEMM_UNITS_PIPELINED, 0 = all.  The weight
+    gradients always use every pair)."""
 
     def __init__(self, T: int, d: int, f: int, E: int, k: int, dtype: torch.dtype,
                  renorm: int, chunk: Optional[int] = None, device="cuda",
                  pipeline: bool = True, recompute: bool = False,
-                 defer_wgrad: Optional[bool] = None, gather: bool = False):
+                 defer_wgrad: Optional[bool] = None, gather: bool = False,
+                 gemm_units: Optional[int] = None):
         self.T, self.d, self.f, self.E, self.k = T, d, f, E, k
         self.dtype, self.renorm = dtype, int(renorm)
         C = chunk if chunk else T
@@ -96,6 +109,9 @@ class LayerPass:
             defer_wgrad = nch > 1
         self.defer_wgrad = bool(defer_wgrad) and not self.recompute
         self.gather = bool(gather)
+        if gemm_units is None:
+            gemm_units = GEMM_UNITS_PIPELINED if self.pipeline else 0
+        self.gemm_units = int(gemm_units) if self.pipeline else 0
         dev = torch.device(device)
         f32, i32 = torch.float32, torch.int32
         z = lambda *s, dt=dtype: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
@@ -202,6 +218,7 @@ class LayerPass:
             if self.pipeline:
                 main.wait_event(self._ev_routed[ci])
             Yp = self._act(self.Y_perm, c0, c1)
+            ops.moe_set_gemm_max_units(self.gemm_units)
             if self.gather:   # A4 fused into A5: x rows through perm
                 ops.moe_expert_ffn_fwd_gather(s, xc, perm, offs, W1, b1, W2, b2,
                                               self._act(self.G, c0, c1), self._act(self.A, c0, c1),
@@ -210,6 +227,7 @@ class LayerPass:
                 ops.moe_expert_ffn_fwd(s, self._act(self.X_perm, c0, c1), offs, W1, b1, W2, b2,
                                        self._act(self.G, c0, c1), self._act(self.A, c0, c1), Yp,
                                        self.ws, self.status)
+            ops.moe_set_gemm_max_units(0)
             ops.moe_combine_fwd(s, Yp, pos, self._rows(self.w, c0, c1), self._rows(self.y, c0, c1))
         if self.pipeline:
             self._ev_join.record(self.side)
@@ -239,15 +257,19 @@ class LayerPass:
         def ffn_bwd(ci):       # A8: dX_perm of chunk ci; dW1, db1, dW2, db2 accumulate
             c0, c1, dYp, dXp = views(ci)
             if self.defer_wgrad:   # the activation half; db1 accumulates here
+                ops.moe_set_gemm_max_units(self.gemm_units)
                 ops.moe_expert_ffn_bwd_data(self.shapes[ci], dYp, self._act(self.G, c0, c1),
                                             self.offsets[ci], W1, W2, self.dH[c0 * k:c1 * k],
                                             dXp, self.db1, int(ci > 0), self.ws, self.status)
+                ops.moe_set_gemm_max_units(0)
                 return
             if self.gather:   # data half, then the weight half reading x through perm
                 dH = self.dH[ci % 2 if self.pipeline else 0, :(c1 - c0) * k]
+                ops.moe_set_gemm_max_units(self.gemm_units)
                 ops.moe_expert_ffn_bwd_data(self.shapes[ci], dYp, self._act(self.G, c0, c1),
                                             self.offsets[ci], W1, W2, dH, dXp, self.db1,
                                             int(ci > 0), self.ws, self.status)
+                ops.moe_set_gemm_max_units(0)
                 ops.moe_expert_ffn_bwd_weights_gather(
                     self.wshapes[ci], [c1 - c0], self.offsets[ci:ci + 1], dYp,
                     self._rows(x, c0, c1), self._rows(self.perm, c0, c1, k), (c1 - c0) * k, dH,

@@ -26,7 +26,7 @@ ENTRY_POINTS = ("moe_status_string", "moe_workspace_size", "moe_route", "moe_per
                 "moe_expert_ffn_bwd", "moe_route_bwd", "moe_debug_bounded_wait",
                 "moe_debug_gelu", "moe_route_noalloc", "moe_expert_ffn_bwd_data",
                 "moe_expert_ffn_bwd_weights", "moe_expert_ffn_fwd_gather",
-                "moe_expert_ffn_bwd_weights_gather",
+                "moe_expert_ffn_bwd_weights_gather", "moe_set_gemm_max_units",
                 "moe_expert_ffn_bwd_weights_workspace_size")
 
 
@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
                                                      ctypes.POINTER(ctypes.c_int64), _P,
                                                      ctypes.c_int, _P, _P, _P, _P, _P, _P, _P,
                                                      ctypes.c_int, _P, ctypes.c_size_t, _P, _P]
+            L.moe_set_gemm_max_units.argtypes = [ctypes.c_int]
             L.moe_expert_ffn_fwd_gather.argtypes = [_SP] + [_P] * 13
             L.moe_expert_ffn_bwd_weights_gather.argtypes = [
                 _SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64), _P, ctypes.c_int, _P, _P,
@@ -274,6 +275,12 @@ def moe_route_bwd(s, dw, logits, idx, w, perm, offsets, x, Wg, dx_perm, pos, dx,
         _ptr(perm, _I32), _ptr(offsets, _I32), _ptr(x, _act(s)), _ptr(Wg, _act(s)),
         _ptr(dx_perm, _act(s)), _ptr(pos, _I32), _ptr(dx, _act(s)), _ptr(dWg, _F32),
         int(accumulate), _ptr(ws), _ptr(dev_status, _I32), _stream(stream)))
+
+
+def moe_set_gemm_max_units(units: int):
+    """Cap the CTA pairs of the tensor-core GEMMs this host thread launches
+    (0 = no cap); see include/moe.h."""
+    _check("moe_set_gemm_max_units", lib().moe_set_gemm_max_units(int(units)))
 
 
 def moe_debug_bounded_wait(limit_ns: int, dev_status, stream=None):
