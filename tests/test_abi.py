@@ -97,3 +97,27 @@ def test_empty_calls_do_nothing(lib):
     assert lib.moe_permute(ctypes.byref(s), 16, 16, 16, None) == ops.MOE_OK
     assert lib.moe_combine_fwd(ctypes.byref(s), 16, 16, None, 16, None) == ops.MOE_OK
     assert lib.moe_combine_bwd(ctypes.byref(s), 16, 16, 16, 16, 16, 16, None) == ops.MOE_OK
+
+
+def test_gather_entry_points_reject_bad_arguments(lib):
+    """The fused-permute calls check their extra arguments on the host: a null
+    perm, a perm stride shorter than a chunk's entries."""
+    s = _shape()
+    assert lib.moe_expert_ffn_fwd_gather(ctypes.byref(s), 16, None, 16, 16, None, 16, None,
+                                         16, 16, 16, 16, 16, None) == ops.MOE_ERR_INVALID
+    T = ctypes.c_int64(int(s.T))
+    arr = (ctypes.c_int64 * 1)(T.value)
+    short = int(s.T) * int(s.k) - 1
+    args = [16, 16, ctypes.c_int64(short), 16, 16, 16, 16, 16, 0, 16, 4096, 16, None]
+    assert lib.moe_expert_ffn_bwd_weights_gather(ctypes.byref(s), 1, arr, 16, 12, 16, *args) \
+        == ops.MOE_ERR_INVALID
+    args[1] = None   # no perm
+    args[2] = ctypes.c_int64(int(s.T) * int(s.k))
+    assert lib.moe_expert_ffn_bwd_weights_gather(ctypes.byref(s), 1, arr, 16, 12, 16, *args) \
+        == ops.MOE_ERR_INVALID
+
+
+def test_gemm_max_units_option(lib):
+    assert lib.moe_set_gemm_max_units(-1) == ops.MOE_ERR_INVALID
+    assert lib.moe_set_gemm_max_units(8) == ops.MOE_OK
+    assert lib.moe_set_gemm_max_units(0) == ops.MOE_OK
