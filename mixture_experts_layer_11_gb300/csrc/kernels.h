@@ -140,7 +140,7 @@ struct GemmVarK {
     int64_t gather_rows = 0;
 };
 // Scratch bytes that let the weight-gradient GEMMs over `rows` rows split their
-// long reductions as finely as they would (parts of >= 512 K blocks of 64 rows).
+// long reductions as finely as they would (parts of >= 256 K blocks of 64 rows).
 size_t vark_split_workspace(int64_t rows, int E, int M, int N);
 
 // Cap on the tensor-core GEMMs' CTA pairs (single CTAs) per launch for the

@@ -112,7 +112,7 @@ def test_ffn_gather_equals_unfused(dtype, T, d, f, E, k, zipf, shape, monkeypatc
 @pytest.mark.parametrize("dtype,nchunks,T,d,f,E,k", [
     ("bf16", 3, 700, 256, 384, 8, 2),
     ("bf16", 17, 90, 128, 192, 16, 3),     # 16 + 1 chunks: the second launch has one chunk
-    ("bf16", 2, 40000, 128, 128, 2, 1),    # > 512 K blocks per expert: split parts
+    ("bf16", 2, 40000, 128, 128, 2, 1),    # > 256 K blocks per expert: split parts
     ("f32", 4, 150, 64, 96, 6, 2),
 ])
 def test_bwd_weights_gather_over_chunks(dtype, nchunks, T, d, f, E, k):
