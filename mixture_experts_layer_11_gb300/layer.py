@@ -63,11 +63,12 @@ def _pad4(n: int) -> int:
     return (n + 3) // 4 * 4
 
 
-# CTA pairs of the per-chunk expert GEMMs when the chunks are pipelined; 0 =
-# every pair the GPU holds.  A cap leaves SMs to the side stream (on the
-# long-context workload 64 of the 76 pairs made the step 3% faster), but one
-# capped run did not finish, for a reason not found; so no cap by default.
-GEMM_UNITS_PIPELINED = 0
+# CTA pairs of the per-chunk expert GEMMs when the chunks are pipelined (of the
+# 76 a GB300 holds; 0 = all): the cap leaves SMs to the side stream's routing,
+# permute, combine backward and router backward.  On the long-context workload
+# 64 gave 88.3-88.6 ms per step against 90.0 ms with every pair (56: 92.2,
+# 68: 88.7), on one box.
+GEMM_UNITS_PIPELINED = 64
 
 
 class LayerPass:
