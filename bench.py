@@ -29,6 +29,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -95,6 +96,26 @@ def launches_per_step(cfg, nchunks: int, router_tc: bool, recompute: bool, defer
     multi = nchunks > 1 or cfg.T * cfg.k > VARK_LEAN_MAX_ROWS
     per_step = ((4 if multi else 2) if bf else 4 * nchunks) if defer else 0
     return per_chunk * nchunks + per_step
+
+
+def gemm_traffic(cfg):
+    """DRAM bytes per step of all expert GEMM launches, from the committed ncu
+    summary of this workload, while the GEMM source is the one it was taken
+    on; else None."""
+    path = os.path.join(ROOT, "profiles", f"dram_gemm_{cfg.name}.md")
+    src = os.path.join(ROOT, "mixture_experts_layer_11_gb300", "csrc", "gemm_tc.cu")
+    try:
+        import hashlib
+        text = open(path).read()
+        want = re.search(r"gemm_tc\.cu sha256: ([0-9a-f]{64})", text).group(1)
+        n = int(re.search(r"traffic_bytes_per_step: (\d+)", text).group(1))
+        have = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except Exception:
+        return None, "no DRAM counter capture of this workload's GEMMs"
+    if have != want:
+        return None, "the GEMM source changed since its DRAM counters were taken"
+    return n, ("dram__bytes_read.sum + dram__bytes_write.sum of one step's expert GEMM launches "
+               "(bytes per step, from one ncu pass over the step's launches)")
 
 
 def workload_desc(cfg) -> str:
@@ -733,6 +754,7 @@ def run_ours(args, cfg):
                 "dispatch_gbs": d["achieved"], "dispatch_frac_of_hbm": d["frac"],
                 "steps": sub_steps}
 
+    traffic, traffic_note = gemm_traffic(cfg)
     value = whole_job_rate(cfg.T, args.steps, world, total_ms)
     flops = cfg.expert_flops() + cfg.router_flops()
     gemm = head.get("gemm", {})
@@ -768,8 +790,8 @@ def run_ours(args, cfg):
             "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak if achieved else None,
             "peak_kind": f"bf16 dense cuBLAS burst ({pk_kind}): each step lasts well under 1 s",
-            "traffic": None,
-            "traffic_note": "no DRAM counter capture of this kernel at this workload's size",
+            "traffic": traffic,
+            "traffic_note": traffic_note,
             "algorithmic_flops_per_step": cfg.expert_flops(),
             "gemm_ms_per_step": gemm.get("ms_per_step"),
         },
