@@ -736,6 +736,7 @@ def run_ours(args, cfg):
     serial = measure(cfg, dev, sub_steps, sub_warm, pipeline=False,
                      defer_wgrad=False if args.per_chunk_wgrad else None)
     disp = dispatch_roofline(cfg, serial, pk)
+    serial_gemm = summarize(cfg, serial, pk).get("gemm", {})
     disp["serial_step_ms"] = serial["total_ms"] / serial["steps"]
     disp["serial_calls_ms_per_step"] = {n: v[0] for n, v in serial["calls"].items()}
     # ---- the other workloads
@@ -794,6 +795,13 @@ def run_ours(args, cfg):
             "traffic_note": traffic_note,
             "algorithmic_flops_per_step": cfg.expert_flops(),
             "gemm_ms_per_step": gemm.get("ms_per_step"),
+            "timing": ("CUDA events around the expert GEMM calls of the timed (pipelined) steps; "
+                       "there they share the GPU with the side stream's dispatch kernels"),
+            "one_stream": {"achieved": serial_gemm.get("tflops"),
+                           "frac": (serial_gemm["tflops"] / peak
+                                    if serial_gemm.get("tflops") else None),
+                           "gemm_ms_per_step": serial_gemm.get("ms_per_step"),
+                           "timing": "the same calls in a one-stream pass (nothing beside them)"},
         },
         "dispatch_roofline": disp,
         "router_tensor_cores_variant": tc,
