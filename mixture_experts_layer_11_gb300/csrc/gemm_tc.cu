@@ -739,171 +739,171 @@ __global__ void __launch_bounds__(EpiShape<EPI, VAR_K>::THREADS, 1)
             tma_prefetch_map(&mapB);
         }
         auto producer = [&](auto gather_tag) {
-        constexpr bool gat = decltype(gather_tag)::value;
-        // VarK gather: (slab, four-row group) assignments per lane
-        constexpr int kGatherJ = (S::B_BYTES / SLAB_BYTES) * (BK / 4) / 32;
-        int stage = 0, ecur = 0;
-        uint32_t phase = 0;
-        // per stage, the parity of the last phase this CTA's copies count on
-        // (of full[], or of tail[] for a segment's last K block), else -1
-        int issued_parity[STAGES], issued_tail[STAGES];
-        for (int s = 0; s < STAGES; ++s) issued_parity[s] = issued_tail[s] = -1;
-        uint32_t tail_phase = 0;   // bit s: parity of tail[s]'s next phase
-        bool ok = true;
-        // source row of gathered operand row r of segment seg (r clamped to the
-        // segment's last row: rows past it are never used, or zeroed by the relay)
-        auto gsrc = [&](int seg, int r, int rlast) -> int {
-            const int rr = r < rlast ? r : rlast;
-            const int32_t v =
-                __ldg(p.gather + (int64_t)seg * p.gstride + (rr - p.seg_base[seg]));
-            return (int)(p.gbase[seg] + v / p.gk);
-        };
-        for (int t = unit0; t < num_units && ok; t += nunits) {
-            const Tile ti = get_tile<VAR_K, PAIR, MULTI>(c, p, t, ecur, rank);
-            SegCursor cur;
-            if (VAR_K && MULTI) cur.start(p, ti.e, ti.kb0, c.off);
-            int arow[4];                 // VarM gather: this lane's four A rows
-            int brow[kGatherJ][4];       // VarK gather: this lane's B rows, next K block
-            if (gat && !VAR_K) {
-                // the CTA's part may start past the expert's rows (then no row is used)
-                const int rlast = c.off[ti.e + 1] - 1;
-                #pragma unroll
-                for (int q = 0; q < 4; ++q) arow[q] = gsrc(0, ti.row0 + 4 * lane + q, rlast);
-            }
-            // VarK gather: the rows of the K block the cursor is at
-            auto fetch_b = [&](int kb) {
-                const int seg = MULTI ? cur.seg : 0;
-                const int r0 = MULTI ? cur.row() : ti.row0 + kb * BK;
-                const int rlast = MULTI ? cur.row0 + cur.rows - 1 : ti.row0 + ti.rows - 1;
-                #pragma unroll
-                for (int j = 0; j < kGatherJ; ++j) {
-                    const int g = (lane + 32 * j) & (BK / 4 - 1);
-                    #pragma unroll
-                    for (int q = 0; q < 4; ++q) brow[j][q] = gsrc(seg, r0 + 4 * g + q, rlast);
-                }
+            constexpr bool gat = decltype(gather_tag)::value;
+            // VarK gather: (slab, four-row group) assignments per lane
+            constexpr int kGatherJ = (S::B_BYTES / SLAB_BYTES) * (BK / 4) / 32;
+            int stage = 0, ecur = 0;
+            uint32_t phase = 0;
+            // per stage, the parity of the last phase this CTA's copies count on
+            // (of full[], or of tail[] for a segment's last K block), else -1
+            int issued_parity[STAGES], issued_tail[STAGES];
+            for (int s = 0; s < STAGES; ++s) issued_parity[s] = issued_tail[s] = -1;
+            uint32_t tail_phase = 0;   // bit s: parity of tail[s]'s next phase
+            bool ok = true;
+            // source row of gathered operand row r of segment seg (r clamped to the
+            // segment's last row: rows past it are never used, or zeroed by the relay)
+            auto gsrc = [&](int seg, int r, int rlast) -> int {
+                const int rr = r < rlast ? r : rlast;
+                const int32_t v =
+                    __ldg(p.gather + (int64_t)seg * p.gstride + (rr - p.seg_base[seg]));
+                return (int)(p.gbase[seg] + v / p.gk);
             };
-            if (gat && VAR_K && !ti.ones && ti.num_kb > 0) fetch_b(0);
-            for (int kb = 0; kb < ti.num_kb; ++kb) {
-                if (leader && t == p.withhold_unit && kb == p.withhold_kb) {
-                    // test hook: issue nothing more (no copy is left in
-                    // flight for this stage); the copies already issued are
-                    // waited for below
-                    ok = false;
-                    break;
+            for (int t = unit0; t < num_units && ok; t += nunits) {
+                const Tile ti = get_tile<VAR_K, PAIR, MULTI>(c, p, t, ecur, rank);
+                SegCursor cur;
+                if (VAR_K && MULTI) cur.start(p, ti.e, ti.kb0, c.off);
+                int arow[4];                 // VarM gather: this lane's four A rows
+                int brow[kGatherJ][4];       // VarK gather: this lane's B rows, next K block
+                if (gat && !VAR_K) {
+                    // the CTA's part may start past the expert's rows (then no row is used)
+                    const int rlast = c.off[ti.e + 1] - 1;
+                    #pragma unroll
+                    for (int q = 0; q < 4; ++q) arow[q] = gsrc(0, ti.row0 + 4 * lane + q, rlast);
                 }
-                bool got = true;
-                if (!gat || lane == 0)
-                    got = mbar_wait_bounded(smem_u32(&c.empty[stage]), phase ^ 1, p.limit_ns,
-                                            &c.abort_flag);
-                if (gat) got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-                if (!got) {
-                    if (!gat || lane == 0) raise_abort(c, p);
-                    ok = false;
-                    break;
-                }
-                const uint32_t sA = smem_u32(base + (size_t)stage * S::STAGE_BYTES);
-                const uint32_t sB = sA + S::A_BYTES;
-                const uint32_t fb = smem_u32(&c.full[stage]);
-                const uint32_t fbc = PAIR ? mapa_rank(fb, 0) : fb;   // even CTA's barrier
-                const int nB = ti.nt * BN + rank * S::BN_CTA;      // first B column held here
-                // bytes: full boxes, except MN slabs lying wholly past the edge
-                uint32_t bytes = 0;
-                if (!VAR_K) {
-                    bytes += S::A_BYTES;
-                    bytes += S::B_BYTES;   // whole box (columns past N zero-filled)
-                } else {
-                    // whole boxes (slabs past the M / N edge are zero-filled); the
-                    // row-sum tile reads only A
-                    bytes = S::A_BYTES + (ti.ones ? 0 : S::B_BYTES);
-                }
-                // A segment's last K block (weight gradients) lands on a barrier
-                // of this CTA's own, for its relay warp to zero the rows past
-                // the segment before the MMAs read the stage: the odd CTA's
-                // stage barrier (which nothing else completes), the even or
-                // single CTA's tail barrier.
-                const int kvalid = VAR_K ? (MULTI ? cur.valid() : ti.rows - kb * BK) : BK;
-                const bool relay = VAR_K && kvalid < BK;
-                const uint32_t rb = (PAIR && !leader) ? fb : smem_u32(&c.tail[stage]);
-                if (!gat || lane == 0) {
-                    if (relay) mbar_arrive_expect_tx(rb, bytes);
-                    else if (PAIR && !leader) mbar_arrive_expect_tx_cluster(fbc, bytes);
-                    else mbar_arrive_expect_tx(fb, bytes);
-                }
-                if (gat) __syncwarp();
-                const uint32_t lb = relay ? rb : fb;   // barrier of a CTA-local copy
-                auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
-                    if (PAIR && !relay) tma2_load_2d(dst, m, fbc, c0, c1);
-                    else tma_load_2d(dst, m, lb, c0, c1);
-                };
-                auto load3 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2) {
-                    if (PAIR && !relay) tma2_load_3d(dst, m, fbc, c0, c1, c2);
-                    else tma_load_3d(dst, m, lb, c0, c1, c2);
-                };
-                auto gather4 = [&](uint32_t dst, const CUtensorMap* m, int c0, const int (&rows)[4]) {
-                    if (PAIR && !relay) tma2_gather4(dst, m, fbc, c0, rows);
-                    else tma_gather4(dst, m, lb, c0, rows);
-                };
-                if (!VAR_K) {
-                    if (gat) gather4(sA + (uint32_t)lane * 512u, &mapA, kb * BK, arow);
-                    else if (lane == 0) load2(sA, &mapA, kb * BK, ti.row0);
-                    if (lane == 0) {
-                        if (!B_MN) {
-                            load3(sB, &mapB, kb * BK, nB, ti.e);
-                        } else {
-                            // this CTA's 64-column slabs of BK rows in one box
-                            // (map: {column in slab, K row, slab, expert})
-                            if (PAIR && !relay) tma2_load_4d(sB, &mapB, fbc, 0, kb * BK, nB / 64, ti.e);
-                            else tma_load_4d(sB, &mapB, lb, 0, kb * BK, nB / 64, ti.e);
-                        }
+                // VarK gather: the rows of the K block the cursor is at
+                auto fetch_b = [&](int kb) {
+                    const int seg = MULTI ? cur.seg : 0;
+                    const int r0 = MULTI ? cur.row() : ti.row0 + kb * BK;
+                    const int rlast = MULTI ? cur.row0 + cur.rows - 1 : ti.row0 + ti.rows - 1;
+                    #pragma unroll
+                    for (int j = 0; j < kGatherJ; ++j) {
+                        const int g = (lane + 32 * j) & (BK / 4 - 1);
+                        #pragma unroll
+                        for (int q = 0; q < 4; ++q) brow[j][q] = gsrc(seg, r0 + 4 * g + q, rlast);
                     }
-                } else {
-                    // one box per operand: this CTA's 64-column slabs of BK rows
-                    // (maps: {column in slab, row, slab}); gathered B: BK / 4
-                    // four-row loads per slab
-                    const int r = MULTI ? cur.row() : ti.row0 + kb * BK;
-                    const int mA = ti.mt * S::TILE_M + rank * BM;
-                    if (lane == 0) load3(sA, &mapA, 0, r, mA / 64);
-                    if (!ti.ones) {
-                        if (!gat) {
-                            if (lane == 0) load3(sB, &mapB, 0, r, nB / 64);
-                        } else {
-                            #pragma unroll
-                            for (int j = 0; j < kGatherJ; ++j) {
-                                const int jj = lane + 32 * j;
-                                const int slab = jj / (BK / 4), g = jj % (BK / 4);
-                                // a slab past N (its columns are never stored)
-                                // reads the last real slab instead
-                                const int col = nB + slab * 64 < p.N ? nB + slab * 64 : p.N - 64;
-                                gather4(sB + (uint32_t)(slab * SLAB_BYTES + g * 512), &mapB, col,
-                                        brow[j]);
+                };
+                if (gat && VAR_K && !ti.ones && ti.num_kb > 0) fetch_b(0);
+                for (int kb = 0; kb < ti.num_kb; ++kb) {
+                    if (leader && t == p.withhold_unit && kb == p.withhold_kb) {
+                        // test hook: issue nothing more (no copy is left in
+                        // flight for this stage); the copies already issued are
+                        // waited for below
+                        ok = false;
+                        break;
+                    }
+                    bool got = true;
+                    if (!gat || lane == 0)
+                        got = mbar_wait_bounded(smem_u32(&c.empty[stage]), phase ^ 1, p.limit_ns,
+                                                &c.abort_flag);
+                    if (gat) got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                    if (!got) {
+                        if (!gat || lane == 0) raise_abort(c, p);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sA = smem_u32(base + (size_t)stage * S::STAGE_BYTES);
+                    const uint32_t sB = sA + S::A_BYTES;
+                    const uint32_t fb = smem_u32(&c.full[stage]);
+                    const uint32_t fbc = PAIR ? mapa_rank(fb, 0) : fb;   // even CTA's barrier
+                    const int nB = ti.nt * BN + rank * S::BN_CTA;      // first B column held here
+                    // bytes: full boxes, except MN slabs lying wholly past the edge
+                    uint32_t bytes = 0;
+                    if (!VAR_K) {
+                        bytes += S::A_BYTES;
+                        bytes += S::B_BYTES;   // whole box (columns past N zero-filled)
+                    } else {
+                        // whole boxes (slabs past the M / N edge are zero-filled); the
+                        // row-sum tile reads only A
+                        bytes = S::A_BYTES + (ti.ones ? 0 : S::B_BYTES);
+                    }
+                    // A segment's last K block (weight gradients) lands on a barrier
+                    // of this CTA's own, for its relay warp to zero the rows past
+                    // the segment before the MMAs read the stage: the odd CTA's
+                    // stage barrier (which nothing else completes), the even or
+                    // single CTA's tail barrier.
+                    const int kvalid = VAR_K ? (MULTI ? cur.valid() : ti.rows - kb * BK) : BK;
+                    const bool relay = VAR_K && kvalid < BK;
+                    const uint32_t rb = (PAIR && !leader) ? fb : smem_u32(&c.tail[stage]);
+                    if (!gat || lane == 0) {
+                        if (relay) mbar_arrive_expect_tx(rb, bytes);
+                        else if (PAIR && !leader) mbar_arrive_expect_tx_cluster(fbc, bytes);
+                        else mbar_arrive_expect_tx(fb, bytes);
+                    }
+                    if (gat) __syncwarp();
+                    const uint32_t lb = relay ? rb : fb;   // barrier of a CTA-local copy
+                    auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+                        if (PAIR && !relay) tma2_load_2d(dst, m, fbc, c0, c1);
+                        else tma_load_2d(dst, m, lb, c0, c1);
+                    };
+                    auto load3 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2) {
+                        if (PAIR && !relay) tma2_load_3d(dst, m, fbc, c0, c1, c2);
+                        else tma_load_3d(dst, m, lb, c0, c1, c2);
+                    };
+                    auto gather4 = [&](uint32_t dst, const CUtensorMap* m, int c0, const int (&rows)[4]) {
+                        if (PAIR && !relay) tma2_gather4(dst, m, fbc, c0, rows);
+                        else tma_gather4(dst, m, lb, c0, rows);
+                    };
+                    if (!VAR_K) {
+                        if (gat) gather4(sA + (uint32_t)lane * 512u, &mapA, kb * BK, arow);
+                        else if (lane == 0) load2(sA, &mapA, kb * BK, ti.row0);
+                        if (lane == 0) {
+                            if (!B_MN) {
+                                load3(sB, &mapB, kb * BK, nB, ti.e);
+                            } else {
+                                // this CTA's 64-column slabs of BK rows in one box
+                                // (map: {column in slab, K row, slab, expert})
+                                if (PAIR && !relay) tma2_load_4d(sB, &mapB, fbc, 0, kb * BK, nB / 64, ti.e);
+                                else tma_load_4d(sB, &mapB, lb, 0, kb * BK, nB / 64, ti.e);
                             }
                         }
+                    } else {
+                        // one box per operand: this CTA's 64-column slabs of BK rows
+                        // (maps: {column in slab, row, slab}); gathered B: BK / 4
+                        // four-row loads per slab
+                        const int r = MULTI ? cur.row() : ti.row0 + kb * BK;
+                        const int mA = ti.mt * S::TILE_M + rank * BM;
+                        if (lane == 0) load3(sA, &mapA, 0, r, mA / 64);
+                        if (!ti.ones) {
+                            if (!gat) {
+                                if (lane == 0) load3(sB, &mapB, 0, r, nB / 64);
+                            } else {
+                                #pragma unroll
+                                for (int j = 0; j < kGatherJ; ++j) {
+                                    const int jj = lane + 32 * j;
+                                    const int slab = jj / (BK / 4), g = jj % (BK / 4);
+                                    // a slab past N (its columns are never stored)
+                                    // reads the last real slab instead
+                                    const int col = nB + slab * 64 < p.N ? nB + slab * 64 : p.N - 64;
+                                    gather4(sB + (uint32_t)(slab * SLAB_BYTES + g * 512), &mapB, col,
+                                            brow[j]);
+                                }
+                            }
+                        }
+                        if (MULTI) cur.advance(p, ti.e);
+                        if (gat && !ti.ones && kb + 1 < ti.num_kb) fetch_b(kb + 1);
                     }
-                    if (MULTI) cur.advance(p, ti.e);
-                    if (gat && !ti.ones && kb + 1 < ti.num_kb) fetch_b(kb + 1);
+                    if (relay && (!PAIR || leader)) {
+                        issued_tail[stage] = (int)((tail_phase >> stage) & 1u);
+                        issued_parity[stage] = -1;
+                        tail_phase ^= 1u << stage;
+                    } else {
+                        issued_parity[stage] = (int)phase;
+                        issued_tail[stage] = -1;
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
-                if (relay && (!PAIR || leader)) {
-                    issued_tail[stage] = (int)((tail_phase >> stage) & 1u);
-                    issued_parity[stage] = -1;
-                    tail_phase ^= 1u << stage;
-                } else {
-                    issued_parity[stage] = (int)phase;
-                    issued_tail[stage] = -1;
+            }
+            if (!ok && (!PAIR || leader) && (!gat || lane == 0)) {
+                // wait (bounded) for every copy this CTA's barriers are counting
+                for (int s = 0; s < STAGES; ++s) {
+                    if (issued_parity[s] >= 0)
+                        mbar_wait_bounded(smem_u32(&c.full[s]), (uint32_t)issued_parity[s],
+                                          p.limit_ns, nullptr);
+                    if (issued_tail[s] >= 0)
+                        mbar_wait_bounded(smem_u32(&c.tail[s]), (uint32_t)issued_tail[s],
+                                          p.limit_ns, nullptr);
                 }
-                if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
-        }
-        if (!ok && (!PAIR || leader) && (!gat || lane == 0)) {
-            // wait (bounded) for every copy this CTA's barriers are counting
-            for (int s = 0; s < STAGES; ++s) {
-                if (issued_parity[s] >= 0)
-                    mbar_wait_bounded(smem_u32(&c.full[s]), (uint32_t)issued_parity[s],
-                                      p.limit_ns, nullptr);
-                if (issued_tail[s] >= 0)
-                    mbar_wait_bounded(smem_u32(&c.tail[s]), (uint32_t)issued_tail[s],
-                                      p.limit_ns, nullptr);
-            }
-        }
         };
         if (p.gather == nullptr) {
             if (lane == 0) producer(BoolTag<false>{});
