@@ -22,7 +22,9 @@ dX_perm and the library workspace) are shared by all chunks.
 With more than one chunk the chunks are pipelined on two streams (the
 micro-batch overlap of MPipeMoE, "research method", and ES-MoE's overlap of
 the permutation with compute): a side stream routes and permutes chunk i+1
-while the current stream runs chunk i's expert GEMMs, and in the backward it
+and combines chunk i-1 while the current stream runs chunk i's expert GEMMs
+(on 64 of the GPU's 76 CTA pairs, so that it has SMs of its own), and in the
+backward it
 runs chunk i+1's combine backward and chunk i's router backward next to chunk
 i's expert backward.  The side stream has its own library workspace, dY_perm
 and dX_perm are double-buffered, and events order every reuse.  Each fp32
@@ -171,6 +173,7 @@ class LayerPass:
             self.ws2 = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
             ev = lambda: [torch.cuda.Event() for _ in range(nch)]  # noqa: E731
             self._ev_routed, self._ev_cb, self._ev_ffn, self._ev_rb = ev(), ev(), ev(), ev()
+            self._ev_fwd = ev()
             self._ev_fork, self._ev_join = torch.cuda.Event(), torch.cuda.Event()
 
     # -- per-chunk views ------------------------------------------------------------
@@ -198,6 +201,14 @@ class LayerPass:
         if self.pipeline:
             self._ev_fork.record(main)
             self.side.wait_event(self._ev_fork)
+
+        def combine(ci):       # A6 of chunk ci
+            c0, c1 = self.chunks[ci]
+            ops.moe_combine_fwd(self.shapes[ci], self._act(self.Y_perm, c0, c1),
+                                self._rows(self.pos, c0, c1), self._rows(self.w, c0, c1),
+                                self._rows(self.y, c0, c1))
+
+        prev = None            # pipelined: the chunk whose combine is still due
         for ci, ((c0, c1), s) in enumerate(zip(self.chunks, self.shapes)):
             if c1 == c0:
                 continue
@@ -216,6 +227,11 @@ class LayerPass:
                     ops.moe_permute(s, xc, pos, self._act(self.X_perm, c0, c1))
                 if self.pipeline:
                     self._ev_routed[ci].record(self.side)
+                    # the previous chunk's combine, after its expert GEMMs and
+                    # after this chunk's routing (which runs beside them)
+                    if prev is not None:
+                        self.side.wait_event(self._ev_fwd[prev])
+                        combine(prev)
             if self.pipeline:
                 main.wait_event(self._ev_routed[ci])
             Yp = self._act(self.Y_perm, c0, c1)
@@ -229,8 +245,16 @@ class LayerPass:
                                        self._act(self.G, c0, c1), self._act(self.A, c0, c1), Yp,
                                        self.ws, self.status)
             ops.moe_set_gemm_max_units(0)
-            ops.moe_combine_fwd(s, Yp, pos, self._rows(self.w, c0, c1), self._rows(self.y, c0, c1))
+            if self.pipeline:
+                self._ev_fwd[ci].record(main)
+                prev = ci
+            else:
+                combine(ci)
         if self.pipeline:
+            if prev is not None:
+                with torch.cuda.stream(self.side):
+                    self.side.wait_event(self._ev_fwd[prev])
+                    combine(prev)
             self._ev_join.record(self.side)
             main.wait_event(self._ev_join)
         return self.y
