@@ -157,3 +157,67 @@ def test_expert_ffn_bwd_data_and_weights_over_chunks(dtype, nchunks, T, d, f, E,
     assert int(st.item()) == 0
     for n, t in (("dW1", dW1), ("db1", db1_dev), ("dW2", dW2), ("db2", db2)):
         assert_close(n, t, grads[n], dtype)
+
+
+_WIDE_CACHE = {}
+
+
+def _wide_case(nchunks, T, E, k):
+    """Inputs of test_weights_wide_tiles and the oracle's weight gradients,
+    computed once per routing case (the oracle's backward of d = f = 1024 is
+    the slow part)."""
+    key = (nchunks, T, E, k)
+    if key in _WIDE_CACHE:
+        return _WIDE_CACHE[key]
+    d = f = 1024
+    tdt = torch.bfloat16
+    cfg = synth.MoEConfig("t", T=T, d=d, f=f, E=E, k=k, renorm=1, dtype="bf16")
+    inp = synth.make_inputs(cfg, seed=E + nchunks + T, random_bias=True)
+    P = T * k
+    stride = (E + 1 + 3) // 4 * 4
+    offs_all = torch.zeros(nchunks, stride, dtype=torch.int32)
+    g = torch.Generator().manual_seed(T + nchunks)
+    Xs, dYs, dHs, As = [], [], [], []
+    grads = None
+    for c in range(nchunks):
+        _, offsets = _segments(T, E, k, 1.0 + 0.2 * c, seed=300 + c)
+        offs_all[c, :E + 1] = torch.from_numpy(offsets)
+        X = torch.randn(P, d, generator=g).to(tdt)
+        dY = torch.randn(P, d, generator=g).to(tdt)
+        G = torch.rand(P, f, generator=g).to(tdt)
+        A = torch.randn(P, f, generator=g).to(tdt)
+        # the oracle's backward of this chunk (dH = (dY W2) * G, stored in
+        # bf16), its weight gradients accumulated over the chunks; the GPU's
+        # weight pass gets the oracle's dH
+        res = oracle.expert_ffn_bwd(dY, X, G, A, offsets, inp["W1"], inp["W2"], True, grads)
+        grads = dict(zip(("dW1", "db1", "dW2", "db2"), res[2:]))
+        Xs.append(X); dYs.append(dY); As.append(A)
+        dHs.append(torch.from_numpy(res[0]).to(tdt))
+    case = (offs_all, [torch.cat(t) for t in (dYs, Xs, dHs, As)], grads)
+    _WIDE_CACHE[key] = case
+    return case
+
+
+@pytest.mark.parametrize("units", [None, "20", "17"])
+@pytest.mark.parametrize("nchunks,T,E,k", [(2, 600, 4, 2), (2, 9000, 1, 1)])
+def test_weights_wide_tiles(nchunks, T, E, k, units, monkeypatch):
+    """Weight gradients of d = f = 1024 (4 x 4 tiles of 256 x 256 per expert)
+    over two chunks, on all pairs and with the pairs capped at 20 and 17,
+    against the oracle.  The second case has one expert of 18000 rows over
+    the chunks: 282 K blocks, split into two parts."""
+    if units:
+        monkeypatch.setenv("MOE_GEMM_MAX_UNITS", units)
+    d = f = 1024
+    offs_all, data, grads = _wide_case(nchunks, T, E, k)
+    s = ops.make_shape(T, d, f, E, k, "bf16", 1)
+    chunk_T = [T] * nchunks
+    wn = ops.moe_expert_ffn_bwd_weights_workspace_size(s, chunk_T)
+    wws = torch.empty(max(wn, 256), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = [torch.full(sh, float("nan"), device=DEV) for sh in ((E, f, d), (E, d, f), (E, d))]
+    ops.moe_expert_ffn_bwd_weights(s, chunk_T, offs_all.to(DEV), *[t.to(DEV) for t in data],
+                                   *out, 0, wws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for n, t in zip(("dW1", "dW2", "db2"), out):
+        assert_close(n, t, grads[n], "bf16")
