@@ -42,3 +42,49 @@ def test_reference_arm_other_ranks_print_nothing():
     r = _bench({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not r.stdout.strip()
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test",
+                                                  os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_launch_count_matches_profiled_steps():
+    """gpu_launches comes from launches_per_step(); its value for the two
+    steps whose launch lists were profiled: 16 library kernels for a
+    moe_s_bf16 step (one chunk, per-chunk weight gradients) and 132 for a
+    long-context step (8 chunks of 32768 tokens, deferred weight gradients,
+    stream-K router logits with their fix-up kernel on 152 SMs)."""
+    b = _bench_module()
+    from mixture_experts_layer_11_gb300 import synth
+    assert b.launches_per_step(synth.CONFIGS["moe_s_bf16"], 1, False, False, False) == 16
+    assert b.launches_per_step(synth.CONFIGS["longctx128_bf16"], 8, False, False, True) == 132
+    # the permute fused into the GEMM loads removes one kernel per chunk
+    assert b.launches_per_step(synth.CONFIGS["longctx128_bf16"], 8, False, False, True,
+                               gather=True) == 124
+
+
+def test_gemm_traffic_follows_the_source_hash(tmp_path, monkeypatch):
+    """roofline.traffic is read from the committed DRAM capture only while
+    gemm_tc.cu is the source it was taken on (whitespace aside)."""
+    import shutil
+    b = _bench_module()
+    from mixture_experts_layer_11_gb300 import synth
+    cfg = synth.CONFIGS["longctx128_bf16"]
+    n, note = b.gemm_traffic(cfg)
+    assert n is not None and n > 0, note
+    assert b.gemm_traffic(synth.CONFIGS["tiny_f32"])[0] is None   # no capture of it
+    csrc = tmp_path / "mixture_experts_layer_11_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    shutil.copytree(os.path.join(ROOT, "profiles"), tmp_path / "profiles")
+    src = open(os.path.join(ROOT, "mixture_experts_layer_11_gb300", "csrc", "gemm_tc.cu")).read()
+    monkeypatch.setattr(b, "ROOT", str(tmp_path))
+    (csrc / "gemm_tc.cu").write_text("\n\n  " + src.replace("\n", "\n ") + "\n")
+    assert b.gemm_traffic(cfg)[0] == n                            # layout only
+    (csrc / "gemm_tc.cu").write_text(src + "\n// changed\n")
+    m, note = b.gemm_traffic(cfg)
+    assert m is None and "changed" in note
