@@ -211,15 +211,25 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int64_t Tn, int nv, in
 // wgt = 1, row = p for the column sums of a permuted matrix (bias gradients);
 // with perm given, slot s = perm[p], wgt = wsel[s], row = s / k (the router
 // weight gradient of the selected experts, summed over their tokens).
-// Phase 1: one partial per (expert, chunk of kDwgChunk segment rows) and
-// column tile; the block's 8 warps take every 8th row of the chunk, lanes
-// consecutive 16-byte column vectors, and are added in warp order through
-// shared memory.  Phase 2: per expert and 32 or 128 columns (1 or 4 per lane), 8
-// warps take every 8th partial, added in warp order.  Deterministic.
+// Phase 1: one partial per (expert, run of segment rows) and column tile; the
+// block walks its rows kDwgChunk at a time, its 8 warps taking every 8th row,
+// lanes consecutive 16-byte column vectors, and the warps' sums are added in
+// warp order through shared memory.  A run is either a chunk of kDwgChunk rows
+// (blocks in expert order), or, when the rows are gathered from a source larger
+// than kSegPieceMinBytes, piece q of `pieces` equal pieces of the segment, with
+// the blocks in piece-major order: pieces x E partials instead of one per
+// kDwgChunk rows (a quarter of the partial bytes on a 32768-token, top-8 chunk
+// of 128 experts), and, as a segment lists its slots in token order, the blocks
+// that run together read the rows of one window of tokens for every expert, so
+// a token's row, read once per selected expert, mostly comes from L2.  Phase 2:
+// per expert and 32 or 128 columns (1 or 4 per lane), 8 warps take every 8th
+// partial, added in warp order.  Deterministic.
 constexpr int kSegCPL = 4;   // 16-byte vectors per lane in a column tile
+constexpr int kSegPieces = 16;
+constexpr int64_t kSegPieceMinBytes = 64ll << 20;
 
 template <typename T>
-__global__ void __launch_bounds__(256) seg_partial_kernel(int n, int E, int k,
+__global__ void __launch_bounds__(256) seg_partial_kernel(int n, int E, int k, int pieces,
                                                           const int32_t* __restrict__ offsets,
                                                           const int32_t* __restrict__ perm,
                                                           const float* __restrict__ wsel,
@@ -232,62 +242,76 @@ __global__ void __launch_bounds__(256) seg_partial_kernel(int n, int E, int k,
     // the segment bounds, loaded in one step (not a chain of dependent loads)
     for (int i = threadIdx.x; i <= E; i += 256) off_s[i] = offsets[i];
     __syncthreads();
-    int e = 0, acc = 0, sub = -1;
-    for (; e < E; ++e) {
+    int p0, p1;   // the block's rows
+    if (pieces > 0) {
+        // block x = q * E + e: piece q of expert e's segment (empty pieces
+        // still write their zero partial, which phase 2 adds)
+        const int e = blockIdx.x % E, q = blockIdx.x / E;
         const int cnt = off_s[e + 1] - off_s[e];
-        const int nc = (cnt + kDwgChunk - 1) / kDwgChunk;
-        if ((int)blockIdx.x < acc + nc) { sub = blockIdx.x - acc; break; }
-        acc += nc;
+        const int len = (cnt + pieces - 1) / pieces;
+        p0 = off_s[e] + min(cnt, q * len);
+        p1 = off_s[e] + min(cnt, (q + 1) * len);
+    } else {
+        int e = 0, acc = 0, sub = -1;
+        for (; e < E; ++e) {
+            const int cnt = off_s[e + 1] - off_s[e];
+            const int nc = (cnt + kDwgChunk - 1) / kDwgChunk;
+            if ((int)blockIdx.x < acc + nc) { sub = blockIdx.x - acc; break; }
+            acc += nc;
+        }
+        if (sub < 0) return;   // block-uniform
+        p0 = off_s[e] + sub * kDwgChunk;
+        p1 = min(off_s[e + 1], p0 + kDwgChunk);
     }
-    if (sub < 0) return;   // block-uniform
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ct0 = blockIdx.y * TILE;
-    const int p0 = off_s[e] + sub * kDwgChunk;
-    const int p1 = min(off_s[e + 1], p0 + kDwgChunk);
     float a[kSegCPL][V::N];
     #pragma unroll
     for (int i = 0; i < kSegCPL; ++i)
         #pragma unroll
         for (int u = 0; u < V::N; ++u) a[i][u] = 0.f;
-    // The warp's rows p0 + warp + 8 j (j < kDwgChunk / 8): their slot, weight
-    // and source row are fetched by lane j in one step, then every row's
-    // vectors are requested before the first is used.
-    constexpr int RPW = kDwgChunk / 8;   // rows per warp
+    constexpr int RPW = kDwgChunk / 8;   // rows per warp and step
     static_assert(RPW <= 32, "one lane per row");
-    int my_row = 0;
-    float my_g = 1.f;
-    {
-        const int r = p0 + warp + 8 * lane;
-        if (lane < RPW && r < p1) {
-            my_row = r;
-            if (perm) {
-                const int sl = __ldg(perm + r);
-                my_g = __ldg(wsel + sl);
-                my_row = sl / k;
+    for (int pb = p0; pb < p1; pb += kDwgChunk) {
+        const int pe = min(p1, pb + kDwgChunk);
+        // The warp's rows pb + warp + 8 j (j < RPW): their slot, weight and
+        // source row are fetched by lane j in one step, then every row's
+        // vectors are requested before the first is used.
+        int my_row = 0;
+        float my_g = 1.f;
+        {
+            const int r = pb + warp + 8 * lane;
+            if (lane < RPW && r < pe) {
+                my_row = r;
+                if (perm) {
+                    const int sl = __ldg(perm + r);
+                    my_g = __ldg(wsel + sl);
+                    my_row = sl / k;
+                }
             }
         }
-    }
-    uint4 raw[RPW][kSegCPL];
-    #pragma unroll
-    for (int j = 0; j < RPW; ++j) {
-        const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
-        const bool in = p0 + warp + 8 * j < p1;
+        uint4 raw[RPW][kSegCPL];
         #pragma unroll
-        for (int i = 0; i < kSegCPL; ++i) {
-            const int c = ct0 + (lane + 32 * i) * V::N;
-            raw[j][i] = (in && c < n) ? ldg16(src + row * n + c) : make_uint4(0, 0, 0, 0);
-        }
-    }
-    #pragma unroll
-    for (int j = 0; j < RPW; ++j) {
-        const float g = __shfl_sync(0xffffffffu, my_g, j);
-        if (p0 + warp + 8 * j >= p1) break;   // warp-uniform
-        #pragma unroll
-        for (int i = 0; i < kSegCPL; ++i) {
-            float v[V::N];
-            V::unpack(raw[j][i], v);
+        for (int j = 0; j < RPW; ++j) {
+            const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
+            const bool in = pb + warp + 8 * j < pe;
             #pragma unroll
-            for (int u = 0; u < V::N; ++u) a[i][u] = fmaf(g, v[u], a[i][u]);
+            for (int i = 0; i < kSegCPL; ++i) {
+                const int c = ct0 + (lane + 32 * i) * V::N;
+                raw[j][i] = (in && c < n) ? ldg16(src + row * n + c) : make_uint4(0, 0, 0, 0);
+            }
+        }
+        #pragma unroll
+        for (int j = 0; j < RPW; ++j) {
+            const float g = __shfl_sync(0xffffffffu, my_g, j);
+            if (pb + warp + 8 * j >= pe) break;   // warp-uniform
+            #pragma unroll
+            for (int i = 0; i < kSegCPL; ++i) {
+                float v[V::N];
+                V::unpack(raw[j][i], v);
+                #pragma unroll
+                for (int u = 0; u < V::N; ++u) a[i][u] = fmaf(g, v[u], a[i][u]);
+            }
         }
     }
     #pragma unroll
@@ -309,7 +333,7 @@ __global__ void __launch_bounds__(256) seg_partial_kernel(int n, int E, int k,
 
 // VL consecutive columns per lane (1, or 4 when n % 4 == 0), 32 * VL per block
 template <int VL>
-__global__ void __launch_bounds__(256) seg_reduce_kernel(int n, int E,
+__global__ void __launch_bounds__(256) seg_reduce_kernel(int n, int E, int pieces,
                                                          const int32_t* __restrict__ offsets,
                                                          const float* __restrict__ partial,
                                                          float* __restrict__ out, int accumulate) {
@@ -320,13 +344,20 @@ __global__ void __launch_bounds__(256) seg_reduce_kernel(int n, int E,
     const int c = (blockIdx.y * 32 + lane) * VL;
     for (int i = threadIdx.x; i <= e + 1; i += 256) off_s[i] = offsets[i];
     __syncthreads();
-    int start = 0;
-    for (int q = 0; q < e; ++q) {
-        const int cnt = off_s[q + 1] - off_s[q];
-        start += (cnt + kDwgChunk - 1) / kDwgChunk;
+    // expert e's partials: start, start + stride, ... (nc of them)
+    int start = 0, nc, stride = 1;
+    if (pieces > 0) {
+        start = e;
+        nc = pieces;
+        stride = E;
+    } else {
+        for (int q = 0; q < e; ++q) {
+            const int cnt = off_s[q + 1] - off_s[q];
+            start += (cnt + kDwgChunk - 1) / kDwgChunk;
+        }
+        const int cnt = off_s[e + 1] - off_s[e];
+        nc = (cnt + kDwgChunk - 1) / kDwgChunk;
     }
-    const int cnt = off_s[e + 1] - off_s[e];
-    const int nc = (cnt + kDwgChunk - 1) / kDwgChunk;
     float sum[VL];
     #pragma unroll
     for (int x = 0; x < VL; ++x) sum[x] = 0.f;
@@ -338,7 +369,7 @@ __global__ void __launch_bounds__(256) seg_reduce_kernel(int n, int E,
             #pragma unroll
             for (int u = 0; u < UN; ++u) {
                 const int i = i0 + 8 * u;
-                const float* src = partial + (int64_t)(start + i) * n + c;
+                const float* src = partial + ((int64_t)start + (int64_t)i * stride) * n + c;
                 if (VL == 4) {
                     const float4 f = i < nc ? *reinterpret_cast<const float4*>(src)
                                             : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -440,22 +471,29 @@ cudaError_t launch_segment_rowsum(const moe_shape& s, const void* src, int n,
                                   const float* wsel, float* out, int accumulate, float* partial,
                                   cudaStream_t st) {
     const int64_t nchunks = (s.T * s.k + kDwgChunk - 1) / kDwgChunk + s.E;
-    const int tile = 32 * kSegCPL * (s.dtype == MOE_BF16 ? 8 : 4);
-    const dim3 grid((unsigned)nchunks, (unsigned)((n + tile - 1) / tile));
+    const int esz = s.dtype == MOE_BF16 ? 2 : 4;
+    const int tile = 32 * kSegCPL * (16 / esz);
+    // pieces: rows gathered from a source well beyond what L2 keeps; no more
+    // partials than the chunked runs' (the workspace holds nchunks of them)
+    int pieces = 0;
+    if (perm != nullptr && (int64_t)s.T * n * esz >= kSegPieceMinBytes)
+        pieces = (int)std::min<int64_t>(kSegPieces, nchunks / s.E);
+    const dim3 grid((unsigned)(pieces > 0 ? (int64_t)pieces * s.E : nchunks),
+                    (unsigned)((n + tile - 1) / tile));
     if (s.dtype == MOE_BF16)
         seg_partial_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-            n, s.E, s.k, offsets, perm, wsel, (const __nv_bfloat16*)src, partial);
+            n, s.E, s.k, pieces, offsets, perm, wsel, (const __nv_bfloat16*)src, partial);
     else
-        seg_partial_kernel<float><<<grid, 256, 0, st>>>(n, s.E, s.k, offsets, perm, wsel,
+        seg_partial_kernel<float><<<grid, 256, 0, st>>>(n, s.E, s.k, pieces, offsets, perm, wsel,
                                                         (const float*)src, partial);
     // 4 columns per lane when that still leaves two blocks per SM (wide
     // outputs, many experts), else 1 (more blocks for small problems)
     if (n % 4 == 0 && (int64_t)s.E * ((n + 127) / 128) >= 2 * (int64_t)device_sm_count())
         seg_reduce_kernel<4><<<dim3(s.E, (unsigned)((n + 127) / 128)), 256, 0, st>>>(
-            n, s.E, offsets, partial, out, accumulate);
+            n, s.E, pieces, offsets, partial, out, accumulate);
     else
         seg_reduce_kernel<1><<<dim3(s.E, (unsigned)((n + 31) / 32)), 256, 0, st>>>(
-            n, s.E, offsets, partial, out, accumulate);
+            n, s.E, pieces, offsets, partial, out, accumulate);
     return cudaGetLastError();
 }
 

@@ -21,11 +21,32 @@ CASES = [("f32", 256, 64, 4, 1, 0), ("bf16", 1000, 768, 8, 2, 1), ("bf16", 777, 
 @pytest.mark.parametrize("dtype,T,d,E,k,renorm", CASES)
 @pytest.mark.parametrize("fused", [True, False])
 def test_route_bwd(dtype, T, d, E, k, renorm, fused):
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    rb = dtype == "bf16"
     cfg = synth.MoEConfig("t", T=T, d=d, f=64, E=E, k=k, renorm=renorm, dtype=dtype)
     inp = synth.make_inputs(cfg, seed=T + E)
     L = torch.from_numpy(oracle.router_logits(inp["x"], inp["Wg"])).float()
+    _check(cfg, inp, L, fused)
+
+
+@pytest.mark.parametrize("zipf", [None, 1.2])
+def test_route_bwd_large_source(zipf):
+    """x of 64 MB (T = 8192, d = 4096, bf16), beyond what L2 keeps: dWg sums
+    its gathered rows in token-window pieces of every expert's segment.  With
+    a Zipf logit shift the hot experts' pieces are long and some experts get
+    no rows (empty pieces).  Seeded logits stand in for x Wg^T (the backward
+    only needs the same logits on both sides)."""
+    T, d, E, k = 8192, 4096, 128, 8
+    cfg = synth.MoEConfig("t", T=T, d=d, f=64, E=E, k=k, renorm=1, dtype="bf16")
+    inp = synth.make_inputs(cfg, seed=17)
+    L = synth.make_logits(T, E, seed=19).float()
+    if zipf:
+        L = L + synth.zipf_logit_bias(E, zipf, 2.0).float()
+    _check(cfg, inp, L, True)
+
+
+def _check(cfg, inp, L, fused):
+    dtype, T, d, E, k, renorm = cfg.dtype, cfg.T, cfg.d, cfg.E, cfg.k, cfg.renorm
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    rb = dtype == "bf16"
     idx, w = oracle.gate(L.double().numpy(), k, renorm)
     counts, offsets, pos, perm = oracle.dispatch(idx, E)
     g = torch.Generator().manual_seed(T)
